@@ -1,0 +1,484 @@
+/*
+ * hg_oracle.c -- TEST INFRASTRUCTURE, not part of the product path.
+ *
+ * A plain, slow, obviously-correct fp64 CPU evaluation of the multiresolution
+ * hash-grid encoding: the gradient-augmented cubic-Hermite variant
+ * (Hermite-NGP) and its degenerate d-linear case (Instant-NGP).  Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg may load this
+ * file's shared library.  It shares no code with the CUDA library.
+ *
+ * Sources (page title, section):
+ *  - "Hermite-NGP: Gradient-Augmented Hash Encoding for Learning PDEs",
+ *    section "整体框架" (pipeline: per-level hash lookup of Hermite
+ *    coefficients bucketed by derivative order, tensor-product Hermite
+ *    reconstruction of gamma, grad gamma and the Laplacian in one pass);
+ *    section "关键设计 1" (the encoding equation
+ *        gamma^l(x) = sum_g sum_alpha theta^(alpha)_{l,h(g)}
+ *                     H^(alpha)((x - x_g)/dx_l) dx_l^{|alpha|},
+ *     H^(alpha) = prod_i h^(alpha_i), the value basis h^(0) = -2t^3 + 3t^2
+ *     and the derivative basis h^(1) = t^3 - t^2, and the order-bucketed
+ *     tables);
+ *    section "关键设计 2" (the factorised derivative
+ *        d/dx_i H^(alpha) = d/dx_i h^(alpha_i)(y_i) prod_{k!=i} h^(alpha_k)(y_k)
+ *     and the second derivative of the bases).
+ *  - "SIGGRAPH 2022｜InstantNGP 与多分辨率哈希编码", section
+ *    "InstantNGP 与多分辨率哈希编码流程与原理" (steps 1-3: the cell's corner
+ *    features, hashed lookup, d-linear interpolation; one-to-one indexing when
+ *    a level's vertices fit the table, hashing otherwise).
+ *
+ * Readings where the pages are silent (each one is listed in the design
+ * notes of the repository):
+ *  - Only the bases of the cell's high-side vertex are printed.  The oracle
+ *    uses the standard cubic Hermite pair as functions of the signed offset
+ *    s = (x - x_g)/dx from the vertex: phi0(s) = (1-|s|)^2 (1+2|s|),
+ *    phi1(s) = s (1-|s|)^2.  For the high-side vertex (s = t - 1) these are the
+ *    printed h^(0)(t), h^(1)(t).  Derivatives are the one-sided ones from inside
+ *    the cell that contains x.
+ *  - The hash is the XOR of g_i * pi_i (mod 2^32), pi = (1, 2654435761,
+ *    805459861), then mod T.  A level whose (N+1)^d vertices fit in T is
+ *    indexed one-to-one as sum_i g_i (N+1)^i.
+ *  - x is clamped to [0,1] (NaN to 0); pos = fl32(x * N) (one fp32 multiply,
+ *    rounded to nearest); c = min(floor(pos), N-1); t = pos - c.  Everything
+ *    after that is fp64.
+ *  - Tables are bucketed by derivative order k = |alpha| (d+1 tables); table k
+ *    holds C(d,k) * F values per entry, alpha in lexicographic axis order
+ *    (k=1: x,y,z; k=2: xy,xz,yz; k=3: xyz), then the feature index.
+ *  - "grad^2 gamma" is the Laplacian (trace of the Hessian), one value per
+ *    (level, feature).
+ *  - Inactive levels (bit l of the mask clear) output zero and receive no
+ *    gradient.
+ *
+ * Each floating output is returned together with its condition magnitude:
+ * the same sum with every factor replaced by its absolute value.  Tests use
+ * it to scale the tolerance.
+ *
+ * Build: gcc -O2 -fopenmp -ffp-contract=off -fPIC -shared
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OR_MAXD 3
+
+static const uint32_t OR_PRIMES[OR_MAXD] = {1u, 2654435761u, 805459861u};
+
+/* ------------------------------------------------------------------ */
+/* small combinatorics                                                  */
+/* ------------------------------------------------------------------ */
+
+static int popcount_small(int m) {
+    int c = 0;
+    while (m) { c += m & 1; m >>= 1; }
+    return c;
+}
+
+static int binom(int n, int k) {
+    int r = 1;
+    for (int i = 0; i < k; ++i) r = r * (n - i) / (i + 1);
+    return r;
+}
+
+/* Position of the multi-index alpha (bit i set = derivative along axis i)
+ * inside its order bucket |alpha|, counting the same-order multi-indices in
+ * lexicographic axis order: k=1 -> x,y,z; k=2 -> xy,xz,yz; k=3 -> xyz.      */
+static int slot_in_bucket(int d, int alpha) {
+    int k = popcount_small(alpha), slot = 0;
+    /* enumerate same-order masks in lexicographic order of their axis lists */
+    int lists[8][OR_MAXD], nl = 0;
+    for (int m = 0; m < (1 << d); ++m) {
+        if (popcount_small(m) != k) continue;
+        int p = 0;
+        for (int i = 0; i < d; ++i) if (m >> i & 1) lists[nl][p++] = i;
+        for (int q = p; q < OR_MAXD; ++q) lists[nl][q] = 99;
+        nl++;
+    }
+    /* rank of alpha's axis list among them */
+    int mine[OR_MAXD], p = 0;
+    for (int i = 0; i < d; ++i) if (alpha >> i & 1) mine[p++] = i;
+    for (int q = p; q < OR_MAXD; ++q) mine[q] = 99;
+    for (int j = 0; j < nl; ++j) {
+        int less = 0;
+        for (int q = 0; q < OR_MAXD; ++q) {
+            if (lists[j][q] != mine[q]) { less = lists[j][q] < mine[q]; break; }
+        }
+        if (less) slot++;
+    }
+    return slot;
+}
+
+/* ------------------------------------------------------------------ */
+/* cell location and vertex indexing                                    */
+/* ------------------------------------------------------------------ */
+
+/* Clamp to [0,1] (NaN -> 0), scale by N in one fp32 multiply, split into the
+ * cell index and the local coordinate.                                     */
+static void locate(float x, int32_t N, int64_t* c, double* t) {
+    float xc = x;
+    if (!(xc >= 0.0f)) xc = 0.0f;
+    if (xc > 1.0f) xc = 1.0f;
+    volatile float pos = xc * (float)N;
+    float pf = pos;
+    int64_t ci = (int64_t)floorf(pf);
+    if (ci > (int64_t)N - 1) ci = (int64_t)N - 1;
+    *c = ci;
+    *t = (double)pf - (double)ci;
+}
+
+/* Index of grid vertex g in an order table of 2^log2T entries at resolution N. */
+static uint32_t vertex_index(int d, const int64_t* g, int32_t N, int log2T) {
+    uint64_t T = (uint64_t)1 << log2T;
+    uint64_t side = (uint64_t)N + 1, nvert = 1;
+    for (int i = 0; i < d; ++i) nvert *= side;
+    if (nvert <= T) {
+        uint64_t idx = 0, mul = 1;
+        for (int i = 0; i < d; ++i) { idx += (uint64_t)g[i] * mul; mul *= side; }
+        return (uint32_t)idx;
+    }
+    uint32_t h = 0;
+    for (int i = 0; i < d; ++i) h ^= (uint32_t)(((uint64_t)g[i] * OR_PRIMES[i]) & 0xffffffffu);
+    return (uint32_t)((uint64_t)h % T);
+}
+
+/* ------------------------------------------------------------------ */
+/* 1D cubic Hermite bases of a vertex, as functions of the signed offset     */
+/* s = (x - x_g)/dx.  sigma = +1 for the cell's low-side vertex and -1 for   */
+/* its high-side vertex, so that a = sigma*s = |s| and the derivatives are   */
+/* the one-sided ones from inside the cell.  out = {phi, dphi/ds, d2phi/ds2}. */
+/* ------------------------------------------------------------------ */
+static void hermite_1d(int order, double s, double sigma, double out[3]) {
+    double a = sigma * s;
+    if (order == 0) {
+        out[0] = (1.0 - a) * (1.0 - a) * (1.0 + 2.0 * a);
+        out[1] = sigma * (-6.0 * a * (1.0 - a));
+        out[2] = -6.0 + 12.0 * a;
+    } else {
+        out[0] = s * (1.0 - a) * (1.0 - a);
+        out[1] = (1.0 - a) * (1.0 - 3.0 * a);
+        out[2] = sigma * (6.0 * a - 4.0);
+    }
+}
+
+/* Exposed for the basis pins: the basis of the vertex on side v (0 = low,
+ * 1 = high) of a cell, at local coordinate t.                              */
+void oracle_basis_1d(int v, int order, double t, double out[3]) {
+    double s = t - (double)v;
+    double sigma = v ? -1.0 : 1.0;
+    hermite_1d(order, s, sigma, out);
+}
+
+/* ------------------------------------------------------------------ */
+/* Hermite: one cell of one level                                       */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    int d, F;
+    int32_t N;
+    const int32_t* log2T;         /* [d+1] */
+    const double* const* tab;     /* [d+1]: this level's table k, [T_k][C(d,k)][F] */
+} or_level;
+
+/* Evaluate the cell with corner c at local coordinate t (fp64), writing
+ * gamma[F], dgamma[d][F] (d/dx), lap[F], and the condition magnitudes.
+ * Any output pointer may be NULL.                                           */
+static void hermite_cell(const or_level* lv, const int64_t* c, const double* t,
+                         double* gamma, double* dgamma, double* lap,
+                         double* mg, double* md, double* ml) {
+    const int d = lv->d, F = lv->F;
+    const double N = (double)lv->N;
+    const double dx = 1.0 / N;
+    for (int f = 0; f < F; ++f) {
+        if (gamma) gamma[f] = 0.0;
+        if (mg) mg[f] = 0.0;
+        if (lap) lap[f] = 0.0;
+        if (ml) ml[f] = 0.0;
+        for (int j = 0; j < d; ++j) {
+            if (dgamma) dgamma[j * F + f] = 0.0;
+            if (md) md[j * F + f] = 0.0;
+        }
+    }
+    for (int v = 0; v < (1 << d); ++v) {
+        int64_t g[OR_MAXD];
+        double s[OR_MAXD], sigma[OR_MAXD];
+        for (int i = 0; i < d; ++i) {
+            int vi = v >> i & 1;
+            g[i] = c[i] + vi;
+            s[i] = t[i] - (double)vi;         /* (x - x_g)/dx */
+            sigma[i] = vi ? -1.0 : 1.0;
+        }
+        for (int alpha = 0; alpha < (1 << d); ++alpha) {
+            int k = popcount_small(alpha);
+            int slot = slot_in_bucket(d, alpha);
+            uint32_t idx = vertex_index(d, g, lv->N, lv->log2T[k]);
+            const double* theta = lv->tab[k] + ((size_t)idx * binom(d, k) + slot) * F;
+            double scale = pow(dx, (double)k);  /* dx^{|alpha|} */
+            double h[OR_MAXD][3];
+            for (int i = 0; i < d; ++i) hermite_1d(alpha >> i & 1, s[i], sigma[i], h[i]);
+            /* H, dH/dy_j, d2H/dy_j^2 */
+            double H = 1.0;
+            for (int i = 0; i < d; ++i) H *= h[i][0];
+            double dH[OR_MAXD], d2H[OR_MAXD];
+            for (int j = 0; j < d; ++j) {
+                dH[j] = 1.0; d2H[j] = 1.0;
+                for (int i = 0; i < d; ++i) {
+                    dH[j] *= (i == j) ? h[i][1] : h[i][0];
+                    d2H[j] *= (i == j) ? h[i][2] : h[i][0];
+                }
+            }
+            for (int f = 0; f < F; ++f) {
+                double th = theta[f];
+                if (gamma) gamma[f] += th * H * scale;
+                if (mg) mg[f] += fabs(th) * fabs(H) * scale;
+                for (int j = 0; j < d; ++j) {
+                    /* d/dx_j = N d/dy_j */
+                    if (dgamma) dgamma[j * F + f] += th * scale * N * dH[j];
+                    if (md) md[j * F + f] += fabs(th) * scale * N * fabs(dH[j]);
+                    if (lap) lap[f] += th * scale * N * N * d2H[j];
+                    if (ml) ml[f] += fabs(th) * scale * N * N * fabs(d2H[j]);
+                }
+            }
+        }
+    }
+}
+
+/* Exposed for the continuity and finite-difference pins: evaluate one cell
+ * of one level at an arbitrary fp64 local coordinate.                      */
+int oracle_eval_cell(int d, int F, int32_t N, const int32_t* log2T,
+                     const double* const* tables, const int64_t* c, const double* t,
+                     double* gamma, double* dgamma, double* lap) {
+    if (d < 1 || d > OR_MAXD) return 1;
+    or_level lv = {d, F, N, log2T, tables};
+    hermite_cell(&lv, c, t, gamma, dgamma, lap, NULL, NULL, NULL);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Public oracle entry points                                            */
+/* ------------------------------------------------------------------ */
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+/* idx[N][L][d+1][2^d]: vertex index of corner v (bit i = axis i) in order
+ * table k, for every level (the mask does not apply).                       */
+int oracle_hash_indices(int d, int L, const int32_t* res, const int32_t* log2T,
+                        int64_t n_pts, const float* coords, uint32_t* idx, int nthreads) {
+    if (d < 1 || d > OR_MAXD) return 1;
+    set_threads(nthreads);
+    const int V = 1 << d;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < n_pts; ++n) {
+        for (int l = 0; l < L; ++l) {
+            int64_t c[OR_MAXD];
+            double t[OR_MAXD];
+            for (int i = 0; i < d; ++i) locate(coords[n * d + i], res[l], &c[i], &t[i]);
+            for (int k = 0; k <= d; ++k) {
+                for (int v = 0; v < V; ++v) {
+                    int64_t g[OR_MAXD];
+                    for (int i = 0; i < d; ++i) g[i] = c[i] + (v >> i & 1);
+                    idx[((n * L + l) * (d + 1) + k) * V + v] = vertex_index(d, g, res[l], log2T[k]);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Forward.  tables[k] is table k for all levels, [L][T_k][C(d,k)][F]
+ * contiguous.  Outputs are point-major: gamma[N][L][F], dgamma[N][d][L][F],
+ * lap[N][L][F], with magnitudes in the same shapes.  dgamma/lap and the
+ * magnitude arrays may be NULL.                                           */
+int oracle_encode_fwd(int d, int L, int F, const int32_t* res, const int32_t* log2T,
+                      uint32_t level_mask, const double* const* tables,
+                      int64_t n_pts, const float* coords,
+                      double* gamma, double* dgamma, double* lap,
+                      double* mgamma, double* mdgamma, double* mlap, int nthreads) {
+    if (d < 1 || d > OR_MAXD || L < 1 || F < 1 || F > 8) return 1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 256)
+    for (int64_t n = 0; n < n_pts; ++n) {
+        double g_[8], dg_[OR_MAXD * 8], lp_[8], mg_[8], md_[OR_MAXD * 8], ml_[8];
+        for (int l = 0; l < L; ++l) {
+            const int active = (level_mask >> l) & 1u;
+            if (active) {
+                const double* tab_l[OR_MAXD + 1];
+                for (int k = 0; k <= d; ++k)
+                    tab_l[k] = tables[k] + (size_t)l * ((size_t)1 << log2T[k]) * binom(d, k) * F;
+                or_level lv = {d, F, res[l], log2T, tab_l};
+                int64_t c[OR_MAXD];
+                double t[OR_MAXD];
+                for (int i = 0; i < d; ++i) locate(coords[n * d + i], res[l], &c[i], &t[i]);
+                hermite_cell(&lv, c, t, g_, dg_, lp_, mg_, md_, ml_);
+            } else {
+                for (int f = 0; f < F; ++f) {
+                    g_[f] = lp_[f] = mg_[f] = ml_[f] = 0.0;
+                    for (int j = 0; j < d; ++j) dg_[j * F + f] = md_[j * F + f] = 0.0;
+                }
+            }
+            for (int f = 0; f < F; ++f) {
+                size_t o = ((size_t)n * L + l) * F + f;
+                gamma[o] = g_[f];
+                if (mgamma) mgamma[o] = mg_[f];
+                if (lap) lap[o] = lp_[f];
+                if (mlap) mlap[o] = ml_[f];
+                for (int j = 0; j < d; ++j) {
+                    size_t od = (((size_t)n * d + j) * L + l) * F + f;
+                    if (dgamma) dgamma[od] = dg_[j * F + f];
+                    if (mdgamma) mdgamma[od] = md_[j * F + f];
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Backward for ONE level l: accumulate into grads[k] ([T_k][C(d,k)][F],
+ * this level only, caller-zeroed) the transpose of the forward applied to
+ * the upstream gradients (point-major layouts as in the forward; g_dgamma
+ * and g_lap may be NULL).  mags[k] receives the condition magnitudes.
+ * Colliding vertices sum their contributions.  Serial over points.         */
+int oracle_encode_bwd_level(int d, int L, int F, int l, const int32_t* res, const int32_t* log2T,
+                            int64_t n_pts, const float* coords,
+                            const double* g_gamma, const double* g_dgamma, const double* g_lap,
+                            double* const* grads, double* const* mags) {
+    if (d < 1 || d > OR_MAXD || l < 0 || l >= L) return 1;
+    const double N = (double)res[l];
+    const double dx = 1.0 / N;
+    for (int64_t n = 0; n < n_pts; ++n) {
+        int64_t c[OR_MAXD];
+        double t[OR_MAXD];
+        for (int i = 0; i < d; ++i) locate(coords[n * d + i], res[l], &c[i], &t[i]);
+        for (int v = 0; v < (1 << d); ++v) {
+            int64_t g[OR_MAXD];
+            double s[OR_MAXD], sigma[OR_MAXD];
+            for (int i = 0; i < d; ++i) {
+                int vi = v >> i & 1;
+                g[i] = c[i] + vi;
+                s[i] = t[i] - (double)vi;
+                sigma[i] = vi ? -1.0 : 1.0;
+            }
+            for (int alpha = 0; alpha < (1 << d); ++alpha) {
+                int k = popcount_small(alpha);
+                int slot = slot_in_bucket(d, alpha);
+                uint32_t idx = vertex_index(d, g, res[l], log2T[k]);
+                double scale = pow(dx, (double)k);
+                double h[OR_MAXD][3];
+                for (int i = 0; i < d; ++i) hermite_1d(alpha >> i & 1, s[i], sigma[i], h[i]);
+                double H = 1.0;
+                for (int i = 0; i < d; ++i) H *= h[i][0];
+                double dH[OR_MAXD], d2H[OR_MAXD];
+                for (int j = 0; j < d; ++j) {
+                    dH[j] = 1.0; d2H[j] = 1.0;
+                    for (int i = 0; i < d; ++i) {
+                        dH[j] *= (i == j) ? h[i][1] : h[i][0];
+                        d2H[j] *= (i == j) ? h[i][2] : h[i][0];
+                    }
+                }
+                double* gk = grads[k] + ((size_t)idx * binom(d, k) + slot) * F;
+                double* mk = mags ? mags[k] + ((size_t)idx * binom(d, k) + slot) * F : NULL;
+                for (int f = 0; f < F; ++f) {
+                    double up = g_gamma[((size_t)n * L + l) * F + f];
+                    double w = up * H * scale;
+                    double m = fabs(up) * fabs(H) * scale;
+                    for (int j = 0; j < d; ++j) {
+                        if (g_dgamma) {
+                            double ud = g_dgamma[(((size_t)n * d + j) * L + l) * F + f];
+                            w += ud * scale * N * dH[j];
+                            m += fabs(ud) * scale * N * fabs(dH[j]);
+                        }
+                        if (g_lap) {
+                            double ul = g_lap[((size_t)n * L + l) * F + f];
+                            w += ul * scale * N * N * d2H[j];
+                            m += fabs(ul) * scale * N * N * fabs(d2H[j]);
+                        }
+                    }
+                    gk[f] += w;
+                    if (mk) mk[f] += m;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* d-linear (Instant-NGP)                                                */
+/* ------------------------------------------------------------------ */
+
+/* gamma[N][L][F] = sum over the cell's corners of w_v * table[l][idx][f],
+ * w_v = prod_i (v_i ? t_i : 1 - t_i); table is [L][T][F] contiguous.        */
+int oracle_linear_fwd(int d, int L, int F, const int32_t* res, int log2T, uint32_t level_mask,
+                      const double* table, int64_t n_pts, const float* coords,
+                      double* gamma, double* mgamma, int nthreads) {
+    if (d < 1 || d > OR_MAXD) return 1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 256)
+    for (int64_t n = 0; n < n_pts; ++n) {
+        for (int l = 0; l < L; ++l) {
+            for (int f = 0; f < F; ++f) {
+                gamma[((size_t)n * L + l) * F + f] = 0.0;
+                if (mgamma) mgamma[((size_t)n * L + l) * F + f] = 0.0;
+            }
+            if (!((level_mask >> l) & 1u)) continue;
+            int64_t c[OR_MAXD];
+            double t[OR_MAXD];
+            for (int i = 0; i < d; ++i) locate(coords[n * d + i], res[l], &c[i], &t[i]);
+            for (int v = 0; v < (1 << d); ++v) {
+                int64_t g[OR_MAXD];
+                double w = 1.0;
+                for (int i = 0; i < d; ++i) {
+                    int vi = v >> i & 1;
+                    g[i] = c[i] + vi;
+                    w *= vi ? t[i] : 1.0 - t[i];
+                }
+                uint32_t idx = vertex_index(d, g, res[l], log2T);
+                const double* th = table + ((size_t)l * ((size_t)1 << log2T) + idx) * F;
+                for (int f = 0; f < F; ++f) {
+                    gamma[((size_t)n * L + l) * F + f] += w * th[f];
+                    if (mgamma) mgamma[((size_t)n * L + l) * F + f] += fabs(w) * fabs(th[f]);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Backward of the d-linear forward for ONE level l into grad[T][F] (this
+ * level only, caller-zeroed); mag may be NULL.  Serial over points.        */
+int oracle_linear_bwd_level(int d, int L, int F, int l, const int32_t* res, int log2T,
+                            int64_t n_pts, const float* coords, const double* g_gamma,
+                            double* grad, double* mag) {
+    if (d < 1 || d > OR_MAXD || l < 0 || l >= L) return 1;
+    for (int64_t n = 0; n < n_pts; ++n) {
+        int64_t c[OR_MAXD];
+        double t[OR_MAXD];
+        for (int i = 0; i < d; ++i) locate(coords[n * d + i], res[l], &c[i], &t[i]);
+        for (int v = 0; v < (1 << d); ++v) {
+            int64_t g[OR_MAXD];
+            double w = 1.0;
+            for (int i = 0; i < d; ++i) {
+                int vi = v >> i & 1;
+                g[i] = c[i] + vi;
+                w *= vi ? t[i] : 1.0 - t[i];
+            }
+            uint32_t idx = vertex_index(d, g, res[l], log2T);
+            for (int f = 0; f < F; ++f) {
+                double up = g_gamma[((size_t)n * L + l) * F + f];
+                grad[(size_t)idx * F + f] += w * up;
+                if (mag) mag[(size_t)idx * F + f] += fabs(w) * fabs(up);
+            }
+        }
+    }
+    return 0;
+}
+
+/* The bucket slot of alpha, exposed so tests can check the ordering rule. */
+int oracle_slot_in_bucket(int d, int alpha) { return slot_in_bucket(d, alpha); }
