@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Benchmark of the multiresolution hash-grid encoding on one B300 per rank.
+
+A step is one full pass of the hot path over one batch of synthetic points:
+zero the gradient table, Hermite forward (gamma, grad gamma, Laplacian of
+every point and level) and Hermite backward (scatter of the coefficient
+gradients).  The default workload is the 3D Hermite grid: N = 2^21 points in
+[0,1]^3, L = 16 levels from N_min = 16 to N_max = 512, F = 2, 2^19 entries
+per order table (packed layout), fp32 coefficients U[-1e-2, 1e-2], N(0,1)
+upstream gradients.  ``--config`` picks another of the five workloads.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+a bounded sample of the same workload instead (the oracle is a deliberately
+slow fp64 program; the ratio against it is context, not a target).
+
+Multi-GPU (torchrun): every rank runs its own replica on its own shard of
+points (the forward and backward of different points are independent); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "encoded points/s (Hermite fwd γ,∇γ,∇²γ + bwd) at 1 B300; % of L2/HBM gather roofline"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--config", type=int, default=4, help="workload 1..5 (default 4: 3D Hermite, 2^21 points)")
+    p.add_argument("--level-mask", type=lambda s: int(s, 0), default=None)
+    p.add_argument("--layout", choices=["feature", "point"], default="feature")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample", type=int, default=1 << 14, help="points in the oracle's timed sample")
+    p.add_argument("--points", type=int, default=None, help="override the workload's point count (profiling)")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# workload description and algorithmic byte counts
+# ---------------------------------------------------------------------------
+
+def describe(w, mask, layout):
+    res_note = f"N_min={w.n_min}, N_max={w.n_max}"
+    lt = w.log2_T[0]
+    return {
+        "workload": w.name,
+        "n_points": w.n_points,
+        "d": w.d, "L": w.L, "F": w.F, "log2_T": lt, "n_min": w.n_min, "n_max": w.n_max,
+        "table_dtype": w.dtype,
+        "table_layout": "packed [L][T][2^d][F]" if w.kind == "hermite" else "[L][T][F]",
+        "output_layout": layout + "-major",
+        "active_levels": bin(mask).count("1"),
+        "coords": w.coords,
+        "description": f"{w.kind} d={w.d}: N={w.n_points} pts, L={w.L}, F={w.F}, T=2^{lt}, {res_note}, {w.dtype}",
+        "l2_flush": "inputs larger than L2 (tables + upstream gradients + outputs exceed 126 MB per step)",
+        "parallelism": "replicas",
+    }
+
+
+def algorithmic_bytes(w, mask):
+    """Per-launch algorithmic quantities (one launch covers all N points).
+
+    fwd: compulsory coefficient bytes gathered = N * L_active * 2^d corners *
+         (2^d slots * F * elem) for Hermite, N * L_active * 2^d * F * elem for
+         d-linear.
+    bwd: RED payload bytes = the same count of fp32 gradient values * 4 B.
+    """
+    La = bin(mask).count("1")
+    es = 2 if w.dtype == "f16" else 4
+    slots = (1 << w.d) if w.kind == "hermite" else 1
+    per_pt_level_vals = (1 << w.d) * slots * w.F
+    gather = w.n_points * La * per_pt_level_vals * es
+    red = w.n_points * La * per_pt_level_vals * 4
+    return gather, red
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_setup(w, inputs):
+    import oracle
+    from multiresolution_hash_grid_02_b300 import workloads as W
+    oracle.build()
+    res = oracle.level_resolutions(w.L, w.n_min, w.n_max)
+    if w.kind == "hermite":
+        tabs = [np.ascontiguousarray(t, np.float64) for t in W.split_orders(inputs["table"], w.d)]
+    else:
+        tabs = np.ascontiguousarray(inputs["table"], np.float64)
+    return oracle, res, tabs
+
+
+def oracle_step(oracle, w, res, tabs, inputs, lo, hi, mask, threads):
+    """Oracle forward + backward on points [lo, hi) of the workload."""
+    x = inputs["coords"][lo:hi]
+    if w.kind == "hermite":
+        oracle.encode_fwd(w.d, w.F, res, w.log2_T, tabs, x, level_mask=mask, nthreads=threads, with_mags=False)
+        oracle.encode_bwd(w.d, w.F, res, w.log2_T, x, inputs["g_gamma"][lo:hi], inputs["g_dgamma"][lo:hi],
+                          inputs["g_lap"][lo:hi], level_mask=mask, with_mags=False, nthreads=threads)
+    else:
+        oracle.linear_fwd(w.d, w.F, res, w.log2_T[0], tabs, x, level_mask=mask, nthreads=threads, with_mags=False)
+        oracle.linear_bwd(w.d, w.F, res, w.log2_T[0], x, inputs["g_gamma"][lo:hi], level_mask=mask,
+                          with_mags=False, nthreads=threads)
+
+
+def cpu_baseline(w, inputs, mask, sample):
+    oracle, res, tabs = oracle_setup(w, inputs)
+    threads = len(os.sched_getaffinity(0))
+    sample = min(sample, w.n_points)
+    oracle_step(oracle, w, res, tabs, inputs, 0, min(256, sample), mask, threads)  # warm the code path
+    t0 = time.perf_counter()
+    oracle_step(oracle, w, res, tabs, inputs, 0, sample, mask, threads)
+    dt = time.perf_counter() - t0
+    return {"value": sample / dt, "unit": "points/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {sample} of the {w.n_points} points, all {bin(mask).count('1')} active levels, "
+                      f"fwd + bwd, fp64, {dt:.1f} s"}
+
+
+def run_reference(args):
+    from multiresolution_hash_grid_02_b300 import workloads as W
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.config]
+    mask = args.level_mask if args.level_mask is not None else (1 << w.L) - 1
+    inputs = W.make(w)
+    oracle, res, tabs = oracle_setup(w, inputs)
+    threads = len(os.sched_getaffinity(0))
+    per_step = min(max(256, args.cpu_sample // 8), w.n_points)
+    times = []
+    for i in range(args.warmup + args.steps):
+        lo = (i * per_step) % max(1, w.n_points - per_step)
+        t0 = time.perf_counter()
+        oracle_step(oracle, w, res, tabs, inputs, lo, lo + per_step, mask, threads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t = sum(times)
+    value = per_step * len(times) / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "points/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy)", "config": describe(w, mask, args.layout),
+            "cpu_baseline": {"value": value, "unit": "points/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{per_step} points per step (of {w.n_points}), fwd + bwd, all active levels"},
+            "e2e": {"value": value, "unit": "points/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# native (CUDA) arm
+# ---------------------------------------------------------------------------
+
+def probe_peaks(torch, hg):
+    """Measured L2 ceilings: random 64-byte row gather and random 16-byte
+    vector RED, each on a 32 MiB buffer (L2-resident); best of 5."""
+    buf = torch.zeros(1 << 23, dtype=torch.float32, device="cuda")   # 32 MiB
+    n_threads = 148 * 2048 * 4
+    sink = torch.empty(n_threads, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    best_g = best_r = 0.0
+    rows, per = 1 << 19, 64
+    for i in range(6):
+        ev[0].record()
+        hg.hg_probe_l2_gather(buf, 19, 64, n_threads, per, i, sink)
+        ev[1].record()
+        torch.cuda.synchronize()
+        if i:
+            best_g = max(best_g, n_threads * per * 64 / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9)
+    for i in range(6):
+        ev[0].record()
+        hg.hg_probe_l2_red(buf, 21, n_threads, 32, i)
+        ev[1].record()
+        torch.cuda.synchronize()
+        if i:
+            best_r = max(best_r, n_threads * 32 * 16 / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9)
+    assert rows
+    return best_g, best_r
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import torch.distributed as dist
+    from multiresolution_hash_grid_02_b300 import hg, workloads as W
+    import multiresolution_hash_grid_02_b300 as M
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    w = W.WORKLOADS[args.config]
+    if args.points:
+        w = w.scaled(args.points)
+    mask = args.level_mask if args.level_mask is not None else (1 << w.L) - 1
+    layout = M.HG_FEATURE_MAJOR if args.layout == "feature" else M.HG_POINT_MAJOR
+    fm = layout == M.HG_FEATURE_MAJOR
+    inputs = W.make(w, seed=w.seed + rank)
+    n, d, L, F = w.n_points, w.d, w.L, w.F
+    desc = M.GridDesc(d=d, L=L, F=F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T * (d + 1) if w.kind == "linear"
+                      else w.log2_T, level_mask=mask, dtype=M.HG_F16 if w.dtype == "f16" else M.HG_F32, layout=layout)
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    coords = dev(inputs["coords"])
+    table = dev(inputs["table"])
+    hermite = w.kind == "hermite"
+    conv = (lambda a, ax: W.to_feature_major(a, ax)) if fm else (lambda a, ax: a)
+    gg = dev(conv(inputs["g_gamma"], False))
+    gd = dev(conv(inputs["g_dgamma"], True)) if hermite else None
+    gl = dev(conv(inputs["g_lap"], False)) if hermite else None
+    shape_g = (L, F, n) if fm else (n, L, F)
+    shape_d = (d, L, F, n) if fm else (n, d, L, F)
+    gamma = torch.empty(shape_g, device="cuda")
+    dgamma = torch.empty(shape_d, device="cuda") if hermite else None
+    lap = torch.empty(shape_g, device="cuda") if hermite else None
+    grad = torch.zeros(table.shape, dtype=torch.float32, device="cuda")
+    if hermite:
+        tviews, gviews = M.packed_views(table, d), M.packed_views(grad, d)
+    else:
+        tviews, gviews = M.linear_view(table), M.linear_view(grad)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        if hermite:
+            hg.hg_encode_fwd(desc, n, coords, tviews, gamma, dgamma, lap, stream)
+        else:
+            hg.hg_linear_fwd(desc, n, coords, tviews, gamma, stream)
+
+    def bwd():
+        if hermite:
+            hg.hg_encode_bwd(desc, n, coords, gg, gd, gl, gviews, stream)
+        else:
+            hg.hg_linear_bwd(desc, n, coords, gg, gviews, stream)
+
+    launches_per_step = 2
+    ev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+
+    def step(rec=None):
+        grad.zero_()
+        if rec:
+            rec[0].record(stream)
+        fwd()
+        if rec:
+            rec[1].record(stream)
+        bwd()
+        if rec:
+            rec[2].record(stream)
+
+    gather_peak, red_peak = probe_peaks(torch, hg)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(ev_f[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev_f]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev_f]
+    t_fwd = statistics.mean(fwd_ms)
+    t_bwd = statistics.mean(bwd_ms)
+
+    total_points = n * world * args.steps
+    value = total_points / (elapsed_ms * 1e-3)
+
+    gather_bytes, red_bytes = algorithmic_bytes(w, mask)
+    fwd_gbs = gather_bytes / (t_fwd * 1e-3) / 1e9
+    bwd_gbs = red_bytes / (t_bwd * 1e-3) / 1e9
+    t_bound = gather_bytes / (gather_peak * 1e9) + red_bytes / (red_peak * 1e9)
+    combined = t_bound / ((t_fwd + t_bwd) * 1e-3)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    hbm = None
+    if os.path.exists(peaks_path):
+        with open(peaks_path) as f:
+            hbm = json.load(f).get("hbm_gbs")
+    kernels = {
+        "fwd": {"ms": t_fwd, "bound": "l2", "achieved": fwd_gbs, "peak": gather_peak, "unit": "GB/s",
+                "frac": fwd_gbs / gather_peak, "algorithmic_bytes": gather_bytes,
+                "what": "compulsory coefficient bytes gathered / launch time vs the measured random-gather L2 peak"},
+        "bwd": {"ms": t_bwd, "bound": "l2", "achieved": bwd_gbs, "peak": red_peak, "unit": "GB/s",
+                "frac": bwd_gbs / red_peak, "algorithmic_bytes": red_bytes,
+                "what": "fp32 gradient RED payload bytes / launch time vs the measured random-RED L2 peak"},
+    }
+    dom = "bwd" if t_bwd >= t_fwd else "fwd"
+    k = kernels[dom]
+    roofline = {"bound": "l2", "kernel": dom, "achieved": k["achieved"], "peak": k["peak"], "unit": "GB/s",
+                "frac": k["frac"], "traffic": None,
+                "peak_source": "measured live by this run's L2 probes (hg_probe_l2_gather / hg_probe_l2_red)",
+                "combined_frac": combined, "hbm_peak_gbs": hbm}
+
+    e2e = None
+    if not args.no_e2e and rank == 0:
+        e2e = run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, hermite, grad,
+                      stream, fwd_fn=None)
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        cpu = cpu_baseline(w, inputs, mask, args.cpu_sample)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "points/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded numpy: uniform coords, uniform coefficients, N(0,1) upstream gradients)",
+            "config": describe(w, mask, args.layout),
+            "roofline": roofline, "kernels": kernels,
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, hermite, grad, stream,
+            fwd_fn=None, steps=5):
+    """Same step through the C ABI with inputs starting in pinned host memory:
+    H2D of the step's coordinates and upstream gradients, zero the gradient
+    table, forward, backward, D2H of the forward's outputs."""
+    n = w.n_points
+
+    def pinned(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return t.pin_memory()
+
+    h_coords = pinned(inputs["coords"])
+    h_gg = pinned(conv(inputs["g_gamma"], False))
+    h_gd = pinned(conv(inputs["g_dgamma"], True)) if hermite else None
+    h_gl = pinned(conv(inputs["g_lap"], False)) if hermite else None
+    d_coords = torch.empty_like(h_coords, device="cuda")
+    d_gg = torch.empty_like(h_gg, device="cuda")
+    d_gd = torch.empty_like(h_gd, device="cuda") if hermite else None
+    d_gl = torch.empty_like(h_gl, device="cuda") if hermite else None
+    d_gamma = torch.empty(shape_g, device="cuda")
+    d_dgamma = torch.empty(shape_d, device="cuda") if hermite else None
+    d_lap = torch.empty(shape_g, device="cuda") if hermite else None
+    o_gamma = torch.empty(shape_g).pin_memory()
+    o_dgamma = torch.empty(shape_d).pin_memory() if hermite else None
+    o_lap = torch.empty(shape_g).pin_memory() if hermite else None
+    h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_gg, h_gd, h_gl) if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in (o_gamma, o_dgamma, o_lap) if t is not None)
+
+    def one():
+        d_coords.copy_(h_coords, non_blocking=True)
+        d_gg.copy_(h_gg, non_blocking=True)
+        if hermite:
+            d_gd.copy_(h_gd, non_blocking=True)
+            d_gl.copy_(h_gl, non_blocking=True)
+        grad.zero_()
+        if hermite:
+            hg.hg_encode_fwd(desc, n, d_coords, tviews, d_gamma, d_dgamma, d_lap, stream)
+            hg.hg_encode_bwd(desc, n, d_coords, d_gg, d_gd, d_gl, gviews, stream)
+        else:
+            hg.hg_linear_fwd(desc, n, d_coords, tviews, d_gamma, stream)
+            hg.hg_linear_bwd(desc, n, d_coords, d_gg, gviews, stream)
+        o_gamma.copy_(d_gamma, non_blocking=True)
+        if hermite:
+            o_dgamma.copy_(d_dgamma, non_blocking=True)
+            o_lap.copy_(d_lap, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": n / (ms * 1e-3), "unit": "points/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": steps,
+            "note": "pinned host buffers; coordinates and upstream gradients in, gamma/grad gamma/Laplacian out; "
+                    "gradient tables stay on the device"}
+
+
+if __name__ == "__main__":
+    main()

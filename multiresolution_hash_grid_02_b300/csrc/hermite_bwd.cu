@@ -1,0 +1,167 @@
+// Hermite-NGP backward: scatter-add the coefficient gradients of every
+// (point, level) into the order-bucketed gradient tables.
+//
+// "Hermite-NGP: Gradient-Augmented Hash Encoding for Learning PDEs",
+// 整体框架 (the flowchart's backward pass updates the hash coefficients theta)
+// and 关键设计 1 (the encoding is linear in theta, so the backward is the
+// transpose of the forward's blend).  Colliding entries add their gradients
+// ("英偉達將訓練 NeRF 模型從 5 小時縮至 5 秒", the hashed levels).
+//
+// Mapping as in the forward (one thread per (point, level), grid.y = level,
+// so a level's gradient table stays resident in L2 while it is accumulated).
+// The transpose runs the separable blend backwards (axis 2, then 1, then 0)
+// and yields all 2^d x 2^d coefficient gradients of a feature in registers;
+// the packed layout then issues one 16-byte vector RED per four floats.
+#include <cuda_runtime.h>
+
+#include "hg_device.cuh"
+
+namespace hg {
+namespace {
+
+constexpr int kBlock = 256;
+
+// Transposed 2D blend: upstream (gg, gd[0..1], gl) -> qb[corner][alpha].
+__device__ __forceinline__ void blend2_t(float gg, const float (&gd)[3], float gl, const Basis1& b0,
+                                         const Basis1& b1, float (&qb)[4][4]) {
+#pragma unroll
+    for (int v1 = 0; v1 < 2; ++v1)
+#pragma unroll
+        for (int a1 = 0; a1 < 2; ++a1) {
+            const float s = fmaf(gg, b1.w[v1][a1], fmaf(gd[1], b1.d1[v1][a1], gl * b1.d2[v1][a1]));
+            const float s1 = gd[0] * b1.w[v1][a1];
+            const float s2 = gl * b1.w[v1][a1];
+#pragma unroll
+            for (int v0 = 0; v0 < 2; ++v0)
+#pragma unroll
+                for (int a0 = 0; a0 < 2; ++a0)
+                    qb[v0 + 2 * v1][a0 + 2 * a1] = fmaf(s, b0.w[v0][a0], fmaf(s1, b0.d1[v0][a0], s2 * b0.d2[v0][a0]));
+        }
+}
+
+// Transposed 3D blend.
+__device__ __forceinline__ void blend3_t(float gg, const float (&gd)[3], float gl, const Basis1& b0,
+                                         const Basis1& b1, const Basis1& b2, float (&qb)[8][8]) {
+#pragma unroll
+    for (int v2 = 0; v2 < 2; ++v2)
+#pragma unroll
+        for (int a2 = 0; a2 < 2; ++a2) {
+            const float A = fmaf(gg, b2.w[v2][a2], fmaf(gd[2], b2.d1[v2][a2], gl * b2.d2[v2][a2]));
+            const float B = gd[0] * b2.w[v2][a2];
+            const float C = gd[1] * b2.w[v2][a2];
+            const float Dl = gl * b2.w[v2][a2];
+#pragma unroll
+            for (int v1 = 0; v1 < 2; ++v1)
+#pragma unroll
+                for (int a1 = 0; a1 < 2; ++a1) {
+                    const float s = fmaf(A, b1.w[v1][a1], fmaf(C, b1.d1[v1][a1], Dl * b1.d2[v1][a1]));
+                    const float s1 = B * b1.w[v1][a1];
+                    const float s2 = Dl * b1.w[v1][a1];
+#pragma unroll
+                    for (int v0 = 0; v0 < 2; ++v0)
+#pragma unroll
+                        for (int a0 = 0; a0 < 2; ++a0)
+                            qb[v0 + 2 * v1 + 4 * v2][a0 + 2 * a1 + 4 * a2] =
+                                fmaf(s, b0.w[v0][a0], fmaf(s1, b0.d1[v0][a0], s2 * b0.d2[v0][a0]));
+                }
+        }
+}
+
+template <int D, int FC, bool VEC>
+__global__ void __launch_bounds__(kBlock) hermite_bwd_kernel(const __grid_constant__ BwdParams p) {
+    constexpr int V = 1 << D;
+    const int l = blockIdx.y;
+    if (!((p.c.level_mask >> l) & 1u)) return;
+    const int64_t n = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    if (n >= p.c.n) return;
+    const int F = p.c.F;
+    const Level& lv = p.c.lv[l];
+
+    uint32_t c[D];
+    float t[D];
+    Basis1 B[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+        locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
+        B[i] = hermite_basis(t[i], lv);
+    }
+
+    constexpr int NK = VEC ? 1 : D + 1;
+    uint32_t idx[NK][V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        uint32_t g[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) g[i] = c[i] + ((v >> i) & 1u);
+#pragma unroll
+        for (int k = 0; k < NK; ++k) idx[k][v] = vertex_index<D>(g, lv, (lv.dense >> k) & 1u, p.c.tmask[k]);
+    }
+
+    for (int f0 = 0; f0 < F; f0 += FC) {
+        float qb[FC][V][V];
+#pragma unroll
+        for (int f = 0; f < FC; ++f) {
+            const int64_t lf = static_cast<int64_t>(l) * F + f0 + f;
+            const float gg = p.g_gamma ? __ldcs(p.g_gamma + n * p.c.sn + lf * p.c.sf) : 0.f;
+            const float gl = p.g_lap ? __ldcs(p.g_lap + n * p.c.sn + lf * p.c.sf) : 0.f;
+            float gd[3] = {0.f, 0.f, 0.f};
+            if (p.g_dgamma) {
+#pragma unroll
+                for (int j = 0; j < D; ++j) gd[j] = __ldcs(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf);
+            }
+            if constexpr (D == 2) {
+                blend2_t(gg, gd, gl, B[0], B[1], qb[f]);
+            } else {
+                blend3_t(gg, gd, gl, B[0], B[1], B[D - 1], qb[f]);
+            }
+        }
+        if constexpr (VEC) {
+            // packed row: [slot][FC] floats, 16-byte aligned, length V*FC (a multiple of 4)
+            float* row0 = p.grad.ptr[0] + l * p.grad.ls[0];
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                float r[V * FC];
+#pragma unroll
+                for (int a = 0; a < V; ++a)
+#pragma unroll
+                    for (int f = 0; f < FC; ++f) r[packed_slot<D>(a) * FC + f] = qb[f][v][a];
+                float* dst = row0 + static_cast<int64_t>(idx[0][v]) * p.grad.rs[0];
+#pragma unroll
+                for (int i = 0; i < V * FC; i += 4) red_add_v4(dst + i, r[i], r[i + 1], r[i + 2], r[i + 3]);
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+#pragma unroll
+                for (int a = 0; a < V; ++a) {
+                    const int k = alpha_order(a);
+                    float* e = p.grad.ptr[k] + l * p.grad.ls[k] + static_cast<int64_t>(idx[k][v]) * p.grad.rs[k] +
+                               bucket_slot<D>(a) * F + f0;
+#pragma unroll
+                    for (int f = 0; f < FC; ++f) red_add_f32(e + f, qb[f][v][a]);
+                }
+        }
+    }
+}
+
+template <int D, int FC, bool VEC>
+cudaError_t launch(const BwdParams& p, cudaStream_t s) {
+    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
+    hermite_bwd_kernel<D, FC, VEC><<<grid, kBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t pick(const BwdParams& p, int fc, bool vec, cudaStream_t s) {
+    if (fc == 2) return vec ? launch<D, 2, true>(p, s) : launch<D, 2, false>(p, s);
+    return vec ? launch<D, 1, true>(p, s) : launch<D, 1, false>(p, s);
+}
+
+}  // namespace
+
+int launch_hermite_bwd(const BwdParams& p, int fc, bool vec, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return p.c.d == 2 ? pick<2>(p, fc, vec, s) : pick<3>(p, fc, vec, s);
+}
+
+}  // namespace hg

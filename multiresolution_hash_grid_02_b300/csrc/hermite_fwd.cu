@@ -1,0 +1,198 @@
+// Hermite-NGP forward: gamma, grad gamma and the Laplacian of every
+// (point, level) in one pass.
+//
+// "Hermite-NGP: Gradient-Augmented Hash Encoding for Learning PDEs",
+// 关键设计 1 (the encoding equation with tensor-product Hermite bases and the
+// dx^|alpha| scaling) and 关键设计 2 (the factorised derivative and the
+// second derivative of the bases).
+//
+// Mapping: one thread per (point, level); grid.y = level, so the blocks of
+// one level run together and that level's table stays resident in L2 while
+// every point gathers from it.  The blend is separable: contract axis 0, then
+// axis 1 (then axis 2), carrying value, d/dx_0 and d2/dx_0^2 partial sums, so
+// a 3D level costs ~600 FMA for F = 2 instead of ~1300 for the direct sum.
+#include <cuda_runtime.h>
+
+#include "hg_device.cuh"
+
+namespace hg {
+namespace {
+
+constexpr int kBlock = 256;
+
+// Separable 2D blend of one feature: q[corner][alpha].
+__device__ __forceinline__ void blend2(const float (&q)[4][4], const Basis1& b0, const Basis1& b1, float& g,
+                                       float (&dg)[3], float& lap) {
+    g = 0.f, dg[0] = 0.f, dg[1] = 0.f, lap = 0.f;
+#pragma unroll
+    for (int v1 = 0; v1 < 2; ++v1)
+#pragma unroll
+        for (int a1 = 0; a1 < 2; ++a1) {
+            float s = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll
+            for (int v0 = 0; v0 < 2; ++v0)
+#pragma unroll
+                for (int a0 = 0; a0 < 2; ++a0) {
+                    const float c = q[v0 + 2 * v1][a0 + 2 * a1];
+                    s = fmaf(c, b0.w[v0][a0], s);
+                    s1 = fmaf(c, b0.d1[v0][a0], s1);
+                    s2 = fmaf(c, b0.d2[v0][a0], s2);
+                }
+            g = fmaf(s, b1.w[v1][a1], g);
+            dg[0] = fmaf(s1, b1.w[v1][a1], dg[0]);
+            dg[1] = fmaf(s, b1.d1[v1][a1], dg[1]);
+            lap = fmaf(s2, b1.w[v1][a1], lap);
+            lap = fmaf(s, b1.d2[v1][a1], lap);
+        }
+}
+
+// Separable 3D blend of one feature.
+__device__ __forceinline__ void blend3(const float (&q)[8][8], const Basis1& b0, const Basis1& b1,
+                                       const Basis1& b2, float& g, float (&dg)[3], float& lap) {
+    g = 0.f, dg[0] = 0.f, dg[1] = 0.f, dg[2] = 0.f, lap = 0.f;
+#pragma unroll
+    for (int v2 = 0; v2 < 2; ++v2)
+#pragma unroll
+        for (int a2 = 0; a2 < 2; ++a2) {
+            float A = 0.f, B = 0.f, C = 0.f, Dl = 0.f;
+#pragma unroll
+            for (int v1 = 0; v1 < 2; ++v1)
+#pragma unroll
+                for (int a1 = 0; a1 < 2; ++a1) {
+                    float s = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll
+                    for (int v0 = 0; v0 < 2; ++v0)
+#pragma unroll
+                        for (int a0 = 0; a0 < 2; ++a0) {
+                            const float c = q[v0 + 2 * v1 + 4 * v2][a0 + 2 * a1 + 4 * a2];
+                            s = fmaf(c, b0.w[v0][a0], s);
+                            s1 = fmaf(c, b0.d1[v0][a0], s1);
+                            s2 = fmaf(c, b0.d2[v0][a0], s2);
+                        }
+                    A = fmaf(s, b1.w[v1][a1], A);
+                    B = fmaf(s1, b1.w[v1][a1], B);
+                    C = fmaf(s, b1.d1[v1][a1], C);
+                    Dl = fmaf(s2, b1.w[v1][a1], Dl);
+                    Dl = fmaf(s, b1.d2[v1][a1], Dl);
+                }
+            g = fmaf(A, b2.w[v2][a2], g);
+            dg[0] = fmaf(B, b2.w[v2][a2], dg[0]);
+            dg[1] = fmaf(C, b2.w[v2][a2], dg[1]);
+            dg[2] = fmaf(A, b2.d1[v2][a2], dg[2]);
+            lap = fmaf(Dl, b2.w[v2][a2], lap);
+            lap = fmaf(A, b2.d2[v2][a2], lap);
+        }
+}
+
+// Kernel: D dims, FC features per pass, TT table element type, VEC = packed
+// interleaved rows read whole with vector loads (requires F == FC).
+template <int D, int FC, typename TT, bool VEC>
+__global__ void __launch_bounds__(kBlock) hermite_fwd_kernel(const __grid_constant__ FwdParams p) {
+    constexpr int V = 1 << D;
+    const int l = blockIdx.y;
+    const int64_t n = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    if (n >= p.c.n) return;
+    const int F = p.c.F;
+    const Level& lv = p.c.lv[l];
+    const bool active = (p.c.level_mask >> l) & 1u;
+
+    float x[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) x[i] = __ldg(p.coords + n * D + i);
+
+    uint32_t c[D];
+    float t[D];
+    Basis1 B[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+        locate(x[i], lv, c[i], t[i]);
+        B[i] = hermite_basis(t[i], lv);
+    }
+
+    // vertex indices: one per corner (VEC) or one per (order, corner)
+    constexpr int NK = VEC ? 1 : D + 1;
+    uint32_t idx[NK][V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        uint32_t g[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) g[i] = c[i] + ((v >> i) & 1u);
+#pragma unroll
+        for (int k = 0; k < NK; ++k) idx[k][v] = vertex_index<D>(g, lv, (lv.dense >> k) & 1u, p.c.tmask[k]);
+    }
+
+    for (int f0 = 0; f0 < F; f0 += FC) {
+        float q[FC][V][V];
+        if (active) {
+            if constexpr (VEC) {
+                constexpr int ROW = V * FC * static_cast<int>(sizeof(TT));
+                const TT* base = static_cast<const TT*>(p.tab.ptr[0]) + l * p.tab.ls[0];
+                RowRegs<ROW> rows[V];
+#pragma unroll
+                for (int v = 0; v < V; ++v) load_row<ROW>(base + static_cast<int64_t>(idx[0][v]) * p.tab.rs[0], rows[v]);
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+#pragma unroll
+                    for (int a = 0; a < V; ++a)
+#pragma unroll
+                        for (int f = 0; f < FC; ++f) q[f][v][a] = row_elem<TT, ROW>(rows[v], packed_slot<D>(a) * FC + f);
+            } else {
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+#pragma unroll
+                    for (int a = 0; a < V; ++a) {
+                        const int k = alpha_order(a);
+                        const TT* e = static_cast<const TT*>(p.tab.ptr[k]) + l * p.tab.ls[k] +
+                                      static_cast<int64_t>(idx[k][v]) * p.tab.rs[k] + bucket_slot<D>(a) * F + f0;
+#pragma unroll
+                        for (int f = 0; f < FC; ++f) q[f][v][a] = to_f32<TT>(e[f]);
+                    }
+            }
+        }
+#pragma unroll
+        for (int f = 0; f < FC; ++f) {
+            float g = 0.f, dg[3] = {0.f, 0.f, 0.f}, lap = 0.f;
+            if (active) {
+                if constexpr (D == 2) {
+                    blend2(q[f], B[0], B[1], g, dg, lap);
+                } else {
+                    blend3(q[f], B[0], B[1], B[D - 1], g, dg, lap);
+                }
+            }
+            const int64_t lf = static_cast<int64_t>(l) * F + f0 + f;
+            __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, g);
+            if (p.dgamma) {
+#pragma unroll
+                for (int j = 0; j < D; ++j) __stcs(p.dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf, dg[j]);
+            }
+            if (p.lap) __stcs(p.lap + n * p.c.sn + lf * p.c.sf, lap);
+        }
+    }
+}
+
+template <int D, int FC, typename TT, bool VEC>
+cudaError_t launch(const FwdParams& p, cudaStream_t s) {
+    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
+    hermite_fwd_kernel<D, FC, TT, VEC><<<grid, kBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, int FC, typename TT>
+cudaError_t pick_vec(const FwdParams& p, bool vec, cudaStream_t s) {
+    return vec ? launch<D, FC, TT, true>(p, s) : launch<D, FC, TT, false>(p, s);
+}
+
+template <int D, typename TT>
+cudaError_t pick_fc(const FwdParams& p, int fc, bool vec, cudaStream_t s) {
+    return fc == 2 ? pick_vec<D, 2, TT>(p, vec, s) : pick_vec<D, 1, TT>(p, vec, s);
+}
+
+}  // namespace
+
+int launch_hermite_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.c.d == 2) return dtype == HG_F16 ? pick_fc<2, __half>(p, fc, vec, s) : pick_fc<2, float>(p, fc, vec, s);
+    return dtype == HG_F16 ? pick_fc<3, __half>(p, fc, vec, s) : pick_fc<3, float>(p, fc, vec, s);
+}
+
+}  // namespace hg

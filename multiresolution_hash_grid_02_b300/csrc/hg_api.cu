@@ -1,0 +1,410 @@
+// C ABI of libhg.so: argument checking, the level schedule, per-level
+// constants, layout detection, and dispatch to the kernels.  Declared in
+// include/hg.h, which also documents every entry point.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "hg_params.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+hg_status fail(hg_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+hg_status ok() {
+    g_err[0] = '\0';
+    return HG_OK;
+}
+
+int binom(int n, int k) {
+    int r = 1;
+    for (int i = 0; i < k; ++i) r = r * (n - i) / (i + 1);
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// Level schedule: N_l = floor(n_min * (n_max/n_min)^(l/(L-1))).  A double
+// estimate is corrected with an exact integer test
+//     n^(L-1) <= n_max^l * n_min^(L-1-l)
+// evaluated on little-endian base-2^32 big integers.
+// ---------------------------------------------------------------------------
+struct Big {
+    uint32_t w[48];
+    int n;
+};
+
+void big_set(Big& b, uint32_t v) {
+    b.w[0] = v;
+    b.n = 1;
+}
+
+void big_mul(Big& b, uint32_t m) {
+    uint64_t carry = 0;
+    for (int i = 0; i < b.n; ++i) {
+        const uint64_t cur = static_cast<uint64_t>(b.w[i]) * m + carry;
+        b.w[i] = static_cast<uint32_t>(cur);
+        carry = cur >> 32;
+    }
+    if (carry) b.w[b.n++] = static_cast<uint32_t>(carry);
+    while (b.n > 1 && b.w[b.n - 1] == 0) --b.n;
+}
+
+int big_cmp(const Big& a, const Big& b) {
+    if (a.n != b.n) return a.n < b.n ? -1 : 1;
+    for (int i = a.n - 1; i >= 0; --i)
+        if (a.w[i] != b.w[i]) return a.w[i] < b.w[i] ? -1 : 1;
+    return 0;
+}
+
+// n^(L-1) <= n_max^l * n_min^(L-1-l)
+bool at_most_exact(uint32_t n, int L, int l, uint32_t n_min, uint32_t n_max) {
+    Big lhs, rhs;
+    big_set(lhs, 1);
+    big_set(rhs, 1);
+    for (int i = 0; i < L - 1; ++i) big_mul(lhs, n);
+    for (int i = 0; i < l; ++i) big_mul(rhs, n_max);
+    for (int i = 0; i < L - 1 - l; ++i) big_mul(rhs, n_min);
+    return big_cmp(lhs, rhs) <= 0;
+}
+
+hg_status compute_resolutions(const hg_grid_desc* desc, int32_t* res) {
+    const int L = desc->L;
+    if (desc->res) {
+        for (int l = 0; l < L; ++l) {
+            if (desc->res[l] < 1 || desc->res[l] > HG_MAX_RESOLUTION)
+                return fail(HG_ERR_INVALID_ARG, "res[%d] = %d is outside 1..%d", l, desc->res[l], HG_MAX_RESOLUTION);
+            res[l] = desc->res[l];
+        }
+        return HG_OK;
+    }
+    const int64_t n_min = desc->n_min, n_max = desc->n_max;
+    if (n_min < 1 || n_max < n_min || n_max > HG_MAX_RESOLUTION)
+        return fail(HG_ERR_INVALID_ARG, "need 1 <= n_min (%lld) <= n_max (%lld) <= %d", (long long)n_min,
+                    (long long)n_max, HG_MAX_RESOLUTION);
+    if (L == 1) {
+        res[0] = static_cast<int32_t>(n_min);
+        return HG_OK;
+    }
+    const double lb = std::log(static_cast<double>(n_max) / static_cast<double>(n_min)) / (L - 1);
+    for (int l = 0; l < L; ++l) {
+        int64_t est = static_cast<int64_t>(std::floor(static_cast<double>(n_min) * std::exp(lb * l)));
+        est = est < n_min ? n_min : (est > n_max ? n_max : est);
+        while (est > n_min && !at_most_exact(static_cast<uint32_t>(est), L, l, n_min, n_max)) --est;
+        while (est < n_max && at_most_exact(static_cast<uint32_t>(est + 1), L, l, n_min, n_max)) ++est;
+        res[l] = static_cast<int32_t>(est);
+    }
+    return HG_OK;
+}
+
+// ---------------------------------------------------------------------------
+// common checks and parameter blocks
+// ---------------------------------------------------------------------------
+size_t dtype_size(int dtype) { return dtype == HG_F16 ? 2 : 4; }
+
+hg_status check_desc(const hg_grid_desc* desc, int n_orders) {
+    if (!desc) return fail(HG_ERR_INVALID_ARG, "desc is NULL");
+    if (desc->d != 2 && desc->d != 3) return fail(HG_ERR_INVALID_ARG, "d = %d; must be 2 or 3", desc->d);
+    if (desc->L < 1 || desc->L > HG_MAX_LEVELS)
+        return fail(HG_ERR_INVALID_ARG, "L = %d; must be in 1..%d", desc->L, HG_MAX_LEVELS);
+    if (desc->F != 1 && desc->F != 2 && desc->F != 4 && desc->F != 8)
+        return fail(HG_ERR_INVALID_ARG, "F = %d; must be 1, 2, 4 or 8", desc->F);
+    if (desc->dtype != HG_F32 && desc->dtype != HG_F16) return fail(HG_ERR_INVALID_ARG, "unknown dtype %d", desc->dtype);
+    if (desc->layout != HG_POINT_MAJOR && desc->layout != HG_FEATURE_MAJOR)
+        return fail(HG_ERR_INVALID_ARG, "unknown layout %d", desc->layout);
+    for (int k = 0; k < n_orders; ++k)
+        if (desc->log2_T[k] < 0 || desc->log2_T[k] > HG_MAX_LOG2_T)
+            return fail(HG_ERR_INVALID_ARG, "log2_T[%d] = %d; must be in 0..%d", k, desc->log2_T[k], HG_MAX_LOG2_T);
+    if (desc->L < 32 && (desc->level_mask >> desc->L) != 0)
+        return fail(HG_ERR_INVALID_ARG, "level_mask 0x%x has bits at or above L = %d", desc->level_mask, desc->L);
+    return HG_OK;
+}
+
+hg_status check_n(int64_t n) {
+    if (n < 0 || n > INT32_MAX) return fail(HG_ERR_INVALID_ARG, "n = %lld; must be in 0..2^31-1", (long long)n);
+    return HG_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Fills c from desc (orders 0..n_orders-1 decide the dense flags).
+hg_status make_common(const hg_grid_desc* desc, int n_orders, int64_t n, hg::Common& c) {
+    memset(&c, 0, sizeof(c));
+    c.d = desc->d;
+    c.L = desc->L;
+    c.F = desc->F;
+    c.level_mask = desc->level_mask;
+    c.n = n;
+    int32_t res[HG_MAX_LEVELS];
+    hg_status st = compute_resolutions(desc, res);
+    if (st != HG_OK) return st;
+    for (int k = 0; k < 4; ++k) c.tmask[k] = k < n_orders ? (1u << desc->log2_T[k]) - 1u : 0u;
+    for (int l = 0; l < desc->L; ++l) {
+        hg::Level& lv = c.lv[l];
+        const uint32_t N = static_cast<uint32_t>(res[l]);
+        lv.N = N;
+        lv.side = N + 1;
+        lv.side2 = (N + 1) * (N + 1);  // only used when the level is one-to-one (fits 2^30)
+        lv.fN = static_cast<float>(N);
+        lv.fN2 = static_cast<float>(static_cast<double>(N) * N);
+        lv.dx = static_cast<float>(1.0 / N);
+        lv.dense = 0;
+        for (int k = 0; k < n_orders; ++k) {
+            const uint64_t T = uint64_t(1) << desc->log2_T[k];
+            uint64_t verts = 1;
+            bool fits = true;
+            for (int i = 0; i < desc->d; ++i) {
+                verts *= (uint64_t)N + 1;
+                if (verts > T) {
+                    fits = false;
+                    break;
+                }
+            }
+            if (fits) lv.dense |= 1u << k;
+        }
+    }
+    const int64_t LF = static_cast<int64_t>(desc->L) * desc->F;
+    if (desc->layout == HG_POINT_MAJOR) {
+        c.sn = LF;
+        c.sf = 1;
+        c.dsn = desc->d * LF;
+        c.dsj = LF;
+        c.dsf = 1;
+    } else {
+        c.sn = 1;
+        c.sf = n;
+        c.dsn = 1;
+        c.dsj = LF * n;
+        c.dsf = n;
+    }
+    return HG_OK;
+}
+
+// A table view: non-NULL, element-aligned, rows that do not overlap.
+hg_status check_view(const char* what, int k, const void* ptr, int64_t ls, int64_t rs, int64_t width, int64_t T,
+                     int L, size_t esize) {
+    if (!ptr) return fail(HG_ERR_INVALID_ARG, "%s[%d].ptr is NULL", what, k);
+    if (!aligned(ptr, esize)) return fail(HG_ERR_INVALID_ARG, "%s[%d].ptr is not %zu-byte aligned", what, k, esize);
+    if (rs < width)
+        return fail(HG_ERR_INVALID_ARG, "%s[%d].row_stride = %lld < %lld values per entry", what, k, (long long)rs,
+                    (long long)width);
+    if (L > 1 && ls < T * rs)
+        return fail(HG_ERR_INVALID_ARG, "%s[%d].level_stride = %lld < T * row_stride = %lld", what, k, (long long)ls,
+                    (long long)(T * rs));
+    if (ls < 0) return fail(HG_ERR_INVALID_ARG, "%s[%d].level_stride is negative", what, k);
+    return HG_OK;
+}
+
+// True when the d+1 views are the interleaved [L][T][2^d][F] buffer.
+bool is_packed(const hg_grid_desc* desc, const void* const* ptrs, const int64_t* ls, const int64_t* rs, size_t esize) {
+    const int d = desc->d, F = desc->F, V = 1 << d;
+    int off = 0;
+    for (int k = 0; k <= d; ++k) {
+        if (desc->log2_T[k] != desc->log2_T[0]) return false;
+        if (rs[k] != static_cast<int64_t>(V) * F || ls[k] != ls[0]) return false;
+        const char* want = static_cast<const char*>(ptrs[0]) + static_cast<size_t>(off) * F * esize;
+        if (static_cast<const char*>(ptrs[k]) != want) return false;
+        off += binom(d, k);
+    }
+    return true;
+}
+
+hg_status launch_status(int err, const char* what) {
+    if (err != cudaSuccess)
+        return fail(HG_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(static_cast<cudaError_t>(err)));
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t hg_abi_version(void) { return HG_ABI_VERSION; }
+
+const char* hg_status_string(hg_status s) {
+    switch (s) {
+        case HG_OK: return "HG_OK";
+        case HG_ERR_INVALID_ARG: return "HG_ERR_INVALID_ARG";
+        case HG_ERR_UNSUPPORTED: return "HG_ERR_UNSUPPORTED";
+        case HG_ERR_CUDA: return "HG_ERR_CUDA";
+    }
+    return "HG_UNKNOWN_STATUS";
+}
+
+const char* hg_last_error(void) { return g_err; }
+
+hg_status hg_level_resolutions(const hg_grid_desc* desc, int32_t* res_out) {
+    if (!desc) return fail(HG_ERR_INVALID_ARG, "desc is NULL");
+    if (!res_out) return fail(HG_ERR_INVALID_ARG, "res_out is NULL");
+    if (desc->L < 1 || desc->L > HG_MAX_LEVELS)
+        return fail(HG_ERR_INVALID_ARG, "L = %d; must be in 1..%d", desc->L, HG_MAX_LEVELS);
+    hg_status st = compute_resolutions(desc, res_out);
+    return st == HG_OK ? ok() : st;
+}
+
+hg_status hg_encode_fwd(const hg_grid_desc* desc, int64_t n, const float* coords, const hg_table* tables,
+                        float* gamma, float* dgamma, float* lap, hg_stream stream) {
+    hg_status st = check_desc(desc, desc ? desc->d + 1 : 0);
+    if (st != HG_OK) return st;
+    if ((st = check_n(n)) != HG_OK) return st;
+    if (!tables) return fail(HG_ERR_INVALID_ARG, "tables is NULL");
+    const int d = desc->d, F = desc->F, V = 1 << d;
+    const size_t es = dtype_size(desc->dtype);
+    const void* ptrs[4];
+    int64_t ls[4], rs[4];
+    for (int k = 0; k <= d; ++k) {
+        ptrs[k] = tables[k].ptr;
+        ls[k] = tables[k].level_stride;
+        rs[k] = tables[k].row_stride;
+        st = check_view("tables", k, ptrs[k], ls[k], rs[k], static_cast<int64_t>(binom(d, k)) * F,
+                        int64_t(1) << desc->log2_T[k], desc->L, es);
+        if (st != HG_OK) return st;
+    }
+    hg::FwdParams p;
+    if ((st = make_common(desc, d + 1, n, p.c)) != HG_OK) return st;
+    if (n == 0) return ok();
+    if (!coords || !gamma) return fail(HG_ERR_INVALID_ARG, "coords and gamma must not be NULL");
+    if (!aligned(coords, 4) || !aligned(gamma, 4) || (dgamma && !aligned(dgamma, 4)) || (lap && !aligned(lap, 4)))
+        return fail(HG_ERR_INVALID_ARG, "coords and outputs must be 4-byte aligned");
+    for (int k = 0; k <= d; ++k) {
+        p.tab.ptr[k] = ptrs[k];
+        p.tab.ls[k] = ls[k];
+        p.tab.rs[k] = rs[k];
+    }
+    p.coords = coords;
+    p.gamma = gamma;
+    p.dgamma = dgamma;
+    p.lap = lap;
+    const int fc = (F % 2 == 0) ? 2 : 1;
+    bool vec = fc == F && is_packed(desc, ptrs, ls, rs, es);
+    if (vec) {
+        const size_t row = static_cast<size_t>(V) * F * es;
+        const size_t al = row < 16 ? row : 16;
+        vec = aligned(ptrs[0], al) && (static_cast<size_t>(ls[0]) * es) % al == 0;
+    }
+    return launch_status(hg::launch_hermite_fwd(p, fc, vec, desc->dtype, stream), "hermite forward");
+}
+
+hg_status hg_encode_bwd(const hg_grid_desc* desc, int64_t n, const float* coords, const float* g_gamma,
+                        const float* g_dgamma, const float* g_lap, const hg_grad_table* grads, hg_stream stream) {
+    hg_status st = check_desc(desc, desc ? desc->d + 1 : 0);
+    if (st != HG_OK) return st;
+    if ((st = check_n(n)) != HG_OK) return st;
+    if (!grads) return fail(HG_ERR_INVALID_ARG, "grads is NULL");
+    const int d = desc->d, F = desc->F, V = 1 << d;
+    const void* ptrs[4];
+    int64_t ls[4], rs[4];
+    for (int k = 0; k <= d; ++k) {
+        ptrs[k] = grads[k].ptr;
+        ls[k] = grads[k].level_stride;
+        rs[k] = grads[k].row_stride;
+        st = check_view("grads", k, ptrs[k], ls[k], rs[k], static_cast<int64_t>(binom(d, k)) * F,
+                        int64_t(1) << desc->log2_T[k], desc->L, 4);
+        if (st != HG_OK) return st;
+    }
+    hg::BwdParams p;
+    if ((st = make_common(desc, d + 1, n, p.c)) != HG_OK) return st;
+    if (n == 0 || (!g_gamma && !g_dgamma && !g_lap)) return ok();
+    if (!coords) return fail(HG_ERR_INVALID_ARG, "coords must not be NULL");
+    if (!aligned(coords, 4) || (g_gamma && !aligned(g_gamma, 4)) || (g_dgamma && !aligned(g_dgamma, 4)) ||
+        (g_lap && !aligned(g_lap, 4)))
+        return fail(HG_ERR_INVALID_ARG, "coords and upstream gradients must be 4-byte aligned");
+    for (int k = 0; k <= d; ++k) {
+        p.grad.ptr[k] = const_cast<float*>(static_cast<const float*>(ptrs[k]));
+        p.grad.ls[k] = ls[k];
+        p.grad.rs[k] = rs[k];
+    }
+    p.coords = coords;
+    p.g_gamma = g_gamma;
+    p.g_dgamma = g_dgamma;
+    p.g_lap = g_lap;
+    const int fc = (F % 2 == 0) ? 2 : 1;
+    bool vec = fc == F && is_packed(desc, ptrs, ls, rs, 4);
+    if (vec) vec = aligned(ptrs[0], 16) && (static_cast<size_t>(ls[0]) * 4) % 16 == 0 && (V * F) % 4 == 0;
+    return launch_status(hg::launch_hermite_bwd(p, fc, vec, stream), "hermite backward");
+}
+
+hg_status hg_linear_fwd(const hg_grid_desc* desc, int64_t n, const float* coords, const hg_table* table,
+                        float* gamma, hg_stream stream) {
+    hg_status st = check_desc(desc, 1);
+    if (st != HG_OK) return st;
+    if ((st = check_n(n)) != HG_OK) return st;
+    if (!table) return fail(HG_ERR_INVALID_ARG, "table is NULL");
+    const int F = desc->F;
+    const size_t es = dtype_size(desc->dtype);
+    st = check_view("table", 0, table->ptr, table->level_stride, table->row_stride, F, int64_t(1) << desc->log2_T[0],
+                    desc->L, es);
+    if (st != HG_OK) return st;
+    hg::FwdParams p;
+    if ((st = make_common(desc, 1, n, p.c)) != HG_OK) return st;
+    if (n == 0) return ok();
+    if (!coords || !gamma) return fail(HG_ERR_INVALID_ARG, "coords and gamma must not be NULL");
+    if (!aligned(coords, 4) || !aligned(gamma, 4)) return fail(HG_ERR_INVALID_ARG, "coords and gamma must be 4-byte aligned");
+    memset(&p.tab, 0, sizeof(p.tab));
+    p.tab.ptr[0] = table->ptr;
+    p.tab.ls[0] = table->level_stride;
+    p.tab.rs[0] = table->row_stride;
+    p.coords = coords;
+    p.gamma = gamma;
+    p.dgamma = nullptr;
+    p.lap = nullptr;
+    const int fc = (F % 2 == 0) ? 2 : 1;
+    const bool vec = fc == 2 && aligned(table->ptr, 2 * es) && table->row_stride % 2 == 0 && table->level_stride % 2 == 0;
+    return launch_status(hg::launch_linear_fwd(p, fc, vec, desc->dtype, stream), "linear forward");
+}
+
+hg_status hg_linear_bwd(const hg_grid_desc* desc, int64_t n, const float* coords, const float* g_gamma,
+                        const hg_grad_table* grad, hg_stream stream) {
+    hg_status st = check_desc(desc, 1);
+    if (st != HG_OK) return st;
+    if ((st = check_n(n)) != HG_OK) return st;
+    if (!grad) return fail(HG_ERR_INVALID_ARG, "grad is NULL");
+    const int F = desc->F;
+    st = check_view("grad", 0, grad->ptr, grad->level_stride, grad->row_stride, F, int64_t(1) << desc->log2_T[0],
+                    desc->L, 4);
+    if (st != HG_OK) return st;
+    hg::BwdParams p;
+    if ((st = make_common(desc, 1, n, p.c)) != HG_OK) return st;
+    if (n == 0 || !g_gamma) return ok();
+    if (!coords) return fail(HG_ERR_INVALID_ARG, "coords must not be NULL");
+    if (!aligned(coords, 4) || !aligned(g_gamma, 4))
+        return fail(HG_ERR_INVALID_ARG, "coords and g_gamma must be 4-byte aligned");
+    memset(&p.grad, 0, sizeof(p.grad));
+    p.grad.ptr[0] = grad->ptr;
+    p.grad.ls[0] = grad->level_stride;
+    p.grad.rs[0] = grad->row_stride;
+    p.coords = coords;
+    p.g_gamma = g_gamma;
+    p.g_dgamma = nullptr;
+    p.g_lap = nullptr;
+    const int fc = (F % 2 == 0) ? 2 : 1;
+    const bool vec = fc == 2 && aligned(grad->ptr, 8) && grad->row_stride % 2 == 0 && grad->level_stride % 2 == 0;
+    return launch_status(hg::launch_linear_bwd(p, fc, vec, stream), "linear backward");
+}
+
+hg_status hg_hash_indices(const hg_grid_desc* desc, int64_t n, const float* coords, uint32_t* idx, hg_stream stream) {
+    hg_status st = check_desc(desc, desc ? desc->d + 1 : 0);
+    if (st != HG_OK) return st;
+    if ((st = check_n(n)) != HG_OK) return st;
+    hg::IdxParams p;
+    if ((st = make_common(desc, desc->d + 1, n, p.c)) != HG_OK) return st;
+    if (n == 0) return ok();
+    if (!coords || !idx) return fail(HG_ERR_INVALID_ARG, "coords and idx must not be NULL");
+    if (!aligned(coords, 4) || !aligned(idx, 4)) return fail(HG_ERR_INVALID_ARG, "coords and idx must be 4-byte aligned");
+    p.coords = coords;
+    p.idx = idx;
+    return launch_status(hg::launch_indices(p, stream), "vertex indices");
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// Kernel parameter blocks shared by the C-ABI layer and the kernels.
+// Passed by value as __grid_constant__ kernel parameters.
+#pragma once
+
+#include <stdint.h>
+
+#include "../../include/hg.h"
+
+namespace hg {
+
+// Per-level constants, computed once per call on the host.
+struct Level {
+    uint32_t N;       // resolution N_l
+    uint32_t side;    // N_l + 1 (vertices per axis)
+    uint32_t side2;   // (N_l + 1)^2
+    uint32_t dense;   // bit k: order-k table is indexed one-to-one at this level
+    float fN;         // (float)N_l      -- d/dx = N d/dt
+    float fN2;        // (float)N_l^2
+    float dx;         // fp32(1/N_l)     -- the dx^|alpha| scaling
+    float pad;
+};
+
+struct Common {
+    int32_t d, L, F;
+    uint32_t level_mask;
+    int64_t n;
+    uint32_t tmask[4];          // T_k - 1
+    // output / upstream-gradient addressing, in elements:
+    //   gamma, lap:  n*sn  + (l*F + f)*sf
+    //   dgamma:      n*dsn + j*dsj + (l*F + f)*dsf
+    int64_t sn, sf, dsn, dsj, dsf;
+    Level lv[HG_MAX_LEVELS];
+};
+
+struct Tables {
+    const void* ptr[4];         // order table k (for the vector path: ptr[0] is the packed row base)
+    int64_t ls[4], rs[4];       // level / row strides in elements
+};
+
+struct Grads {
+    float* ptr[4];
+    int64_t ls[4], rs[4];
+};
+
+struct FwdParams {
+    Common c;
+    Tables tab;
+    const float* coords;
+    float* gamma;
+    float* dgamma;
+    float* lap;
+};
+
+struct BwdParams {
+    Common c;
+    Grads grad;
+    const float* coords;
+    const float* g_gamma;
+    const float* g_dgamma;
+    const float* g_lap;
+};
+
+struct IdxParams {
+    Common c;
+    const float* coords;
+    uint32_t* idx;
+};
+
+// Launchers (one per kernel family); return the cudaError_t of the launch.
+// fc: features per pass (1 or 2); vec: whole-row vector access (packed layout).
+int launch_hermite_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream);
+int launch_hermite_bwd(const BwdParams& p, int fc, bool vec, void* stream);
+int launch_linear_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream);
+int launch_linear_bwd(const BwdParams& p, int fc, bool vec, void* stream);
+int launch_indices(const IdxParams& p, void* stream);
+
+}  // namespace hg

@@ -226,45 +226,60 @@ def encode_fwd(d: int, F: int, res, log2T, tables, coords: np.ndarray,
     return out
 
 
-def encode_bwd(d: int, F: int, res, log2T, coords: np.ndarray, g_gamma: np.ndarray,
-               g_dgamma: np.ndarray | None = None, g_lap: np.ndarray | None = None,
-               level_mask: int | None = None, levels=None, with_mags: bool = True,
-               nthreads: int | None = None):
-    """Hermite backward: the transpose of :func:`encode_fwd` applied to the
-    upstream gradients (point-major layouts).  Colliding vertices sum.
+def encode_bwd_levels(d: int, F: int, res, log2T, coords: np.ndarray, g_gamma: np.ndarray | None,
+                      g_dgamma: np.ndarray | None = None, g_lap: np.ndarray | None = None,
+                      levels=None, with_mags: bool = True, nthreads: int | None = None):
+    """Hermite backward for the listed levels: the transpose of
+    :func:`encode_fwd` applied to the upstream gradients (float32,
+    point-major layouts; any may be None).  Colliding vertices sum.
 
-    Returns (grads, mags): lists over order k of fp64 [L][T_k][C(d,k)][F]
-    arrays.  Only levels that are active in ``level_mask`` and listed in
-    ``levels`` (default: all) are computed; the others stay zero.  Levels run
-    in parallel threads (each level owns its slice, so the result does not
-    depend on the thread count).
+    Returns {level: (grads, mags)} with grads[k] / mags[k] fp64 arrays
+    [T_k][C(d,k)][F] (mags None unless ``with_mags``).  Levels run in parallel
+    threads, each on its own arrays, so the result does not depend on the
+    thread count.
     """
     from concurrent.futures import ThreadPoolExecutor
     lib = _load()
     L = len(res)
-    if level_mask is None:
-        level_mask = (1 << L) - 1
+    levels = list(range(L)) if levels is None else list(levels)
     coords = np.ascontiguousarray(coords, np.float32)
     n = coords.shape[0]
     r = np.asarray(res, np.int32)
     lt = np.asarray(log2T, np.int32)
-    gg = np.ascontiguousarray(g_gamma, np.float64)
-    gd = None if g_dgamma is None else np.ascontiguousarray(g_dgamma, np.float64)
-    gl = None if g_lap is None else np.ascontiguousarray(g_lap, np.float64)
+    f32 = lambda a: None if a is None else np.ascontiguousarray(a, np.float32)
+    gg, gd, gl = f32(g_gamma), f32(g_dgamma), f32(g_lap)
+    shapes = [(1 << int(log2T[k]), comb(d, k), F) for k in range(d + 1)]
+    out = {l: ([np.zeros(s) for s in shapes], [np.zeros(s) for s in shapes] if with_mags else None) for l in levels}
+
+    def one(l):
+        grads, mags = out[l]
+        return lib.oracle_encode_bwd_level(d, L, F, l, _ptr(r), _ptr(lt), n, _ptr(coords), _ptr(gg), _ptr(gd),
+                                           _ptr(gl), _ptr_array(grads), _ptr_array(mags) if with_mags else None)
+
+    with ThreadPoolExecutor(max_workers=max(1, min(len(levels) or 1, nthreads or default_threads()))) as ex:
+        for rc in ex.map(one, levels):
+            _check(rc, "encode_bwd")
+    return out
+
+
+def encode_bwd(d: int, F: int, res, log2T, coords: np.ndarray, g_gamma: np.ndarray | None,
+               g_dgamma: np.ndarray | None = None, g_lap: np.ndarray | None = None,
+               level_mask: int | None = None, with_mags: bool = True, nthreads: int | None = None):
+    """Hermite backward over all levels: (grads, mags), lists over order k of
+    fp64 [L][T_k][C(d,k)][F] arrays; inactive levels stay zero."""
+    L = len(res)
+    if level_mask is None:
+        level_mask = (1 << L) - 1
+    active = [l for l in range(L) if (level_mask >> l) & 1]
+    per = encode_bwd_levels(d, F, res, log2T, coords, g_gamma, g_dgamma, g_lap, active, with_mags, nthreads)
     shapes = order_table_shapes(d, L, F, log2T)
     grads = [np.zeros(s) for s in shapes]
     mags = [np.zeros(s) for s in shapes] if with_mags else None
-    todo = [l for l in (range(L) if levels is None else levels) if (level_mask >> l) & 1]
-
-    def one(l):
-        gs = _ptr_array([g[l] for g in grads])
-        ms = _ptr_array([m[l] for m in mags]) if with_mags else None
-        return lib.oracle_encode_bwd_level(d, L, F, l, _ptr(r), _ptr(lt), n, _ptr(coords),
-                                           _ptr(gg), _ptr(gd), _ptr(gl), gs, ms)
-
-    with ThreadPoolExecutor(max_workers=max(1, min(len(todo) or 1, nthreads or default_threads()))) as ex:
-        for rc in ex.map(one, todo):
-            _check(rc, "encode_bwd")
+    for l, (g, m) in per.items():
+        for k in range(d + 1):
+            grads[k][l] = g[k]
+            if with_mags:
+                mags[k][l] = m[k]
     return grads, mags
 
 
@@ -288,28 +303,42 @@ def linear_fwd(d: int, F: int, res, log2T: int, table: np.ndarray, coords: np.nd
     return (g, m) if with_mags else g
 
 
-def linear_bwd(d: int, F: int, res, log2T: int, coords: np.ndarray, g_gamma: np.ndarray,
-               level_mask: int | None = None, levels=None, with_mags: bool = True,
-               nthreads: int | None = None):
-    """d-linear backward: fp64 grad [L][T][F] (and magnitude), colliding vertices summed."""
+def linear_bwd_levels(d: int, F: int, res, log2T: int, coords: np.ndarray, g_gamma: np.ndarray,
+                      levels=None, with_mags: bool = True, nthreads: int | None = None):
+    """d-linear backward for the listed levels: {level: (grad [T][F], mag)}."""
     from concurrent.futures import ThreadPoolExecutor
     lib = _load()
     L = len(res)
-    if level_mask is None:
-        level_mask = (1 << L) - 1
+    levels = list(range(L)) if levels is None else list(levels)
     coords = np.ascontiguousarray(coords, np.float32)
     n = coords.shape[0]
     r = np.asarray(res, np.int32)
-    gg = np.ascontiguousarray(g_gamma, np.float64)
-    grad = np.zeros((L, 1 << int(log2T), F))
-    mag = np.zeros_like(grad) if with_mags else None
-    todo = [l for l in (range(L) if levels is None else levels) if (level_mask >> l) & 1]
+    gg = np.ascontiguousarray(g_gamma, np.float32)
+    out = {l: (np.zeros((1 << int(log2T), F)), np.zeros((1 << int(log2T), F)) if with_mags else None) for l in levels}
 
     def one(l):
-        return lib.oracle_linear_bwd_level(d, L, F, l, _ptr(r), int(log2T), n, _ptr(coords), _ptr(gg),
-                                           _ptr(grad[l]), None if mag is None else _ptr(mag[l]))
+        g, m = out[l]
+        return lib.oracle_linear_bwd_level(d, L, F, l, _ptr(r), int(log2T), n, _ptr(coords), _ptr(gg), _ptr(g),
+                                           _ptr(m))
 
-    with ThreadPoolExecutor(max_workers=max(1, min(len(todo) or 1, nthreads or default_threads()))) as ex:
-        for rc in ex.map(one, todo):
+    with ThreadPoolExecutor(max_workers=max(1, min(len(levels) or 1, nthreads or default_threads()))) as ex:
+        for rc in ex.map(one, levels):
             _check(rc, "linear_bwd")
+    return out
+
+
+def linear_bwd(d: int, F: int, res, log2T: int, coords: np.ndarray, g_gamma: np.ndarray,
+               level_mask: int | None = None, with_mags: bool = True, nthreads: int | None = None):
+    """d-linear backward over all levels: fp64 grad [L][T][F] (and magnitude)."""
+    L = len(res)
+    if level_mask is None:
+        level_mask = (1 << L) - 1
+    active = [l for l in range(L) if (level_mask >> l) & 1]
+    per = linear_bwd_levels(d, F, res, log2T, coords, g_gamma, active, with_mags, nthreads)
+    grad = np.zeros((L, 1 << int(log2T), F))
+    mag = np.zeros_like(grad) if with_mags else None
+    for l, (g, m) in per.items():
+        grad[l] = g
+        if with_mags:
+            mag[l] = m
     return (grad, mag) if with_mags else grad

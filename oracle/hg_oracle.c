@@ -200,44 +200,46 @@ static void hermite_cell(const or_level* lv, const int64_t* c, const double* t,
             if (md) md[j * F + f] = 0.0;
         }
     }
+    double scale[OR_MAXD + 1];
+    for (int k = 0; k <= d; ++k) scale[k] = pow(dx, (double)k);   /* dx^{|alpha|} */
+    /* bases of axis i for the corner on side vi, basis order a: {phi, phi', phi''} in y */
+    double hb[OR_MAXD][2][2][3];
+    for (int i = 0; i < d; ++i)
+        for (int vi = 0; vi < 2; ++vi)
+            for (int a = 0; a < 2; ++a)
+                hermite_1d(a, t[i] - (double)vi, vi ? -1.0 : 1.0, hb[i][vi][a]);
     for (int v = 0; v < (1 << d); ++v) {
         int64_t g[OR_MAXD];
-        double s[OR_MAXD], sigma[OR_MAXD];
-        for (int i = 0; i < d; ++i) {
-            int vi = v >> i & 1;
-            g[i] = c[i] + vi;
-            s[i] = t[i] - (double)vi;         /* (x - x_g)/dx */
-            sigma[i] = vi ? -1.0 : 1.0;
-        }
+        for (int i = 0; i < d; ++i) g[i] = c[i] + (v >> i & 1);     /* corner vertex */
+        uint32_t idx[OR_MAXD + 1];
+        for (int k = 0; k <= d; ++k) idx[k] = vertex_index(d, g, lv->N, lv->log2T[k]);
         for (int alpha = 0; alpha < (1 << d); ++alpha) {
             int k = popcount_small(alpha);
             int slot = slot_in_bucket(d, alpha);
-            uint32_t idx = vertex_index(d, g, lv->N, lv->log2T[k]);
-            const double* theta = lv->tab[k] + ((size_t)idx * binom(d, k) + slot) * F;
-            double scale = pow(dx, (double)k);  /* dx^{|alpha|} */
-            double h[OR_MAXD][3];
-            for (int i = 0; i < d; ++i) hermite_1d(alpha >> i & 1, s[i], sigma[i], h[i]);
+            const double* theta = lv->tab[k] + ((size_t)idx[k] * binom(d, k) + slot) * F;
+            const double (*h[OR_MAXD])[3];
+            for (int i = 0; i < d; ++i) h[i] = &hb[i][v >> i & 1][alpha >> i & 1];
             /* H, dH/dy_j, d2H/dy_j^2 */
             double H = 1.0;
-            for (int i = 0; i < d; ++i) H *= h[i][0];
+            for (int i = 0; i < d; ++i) H *= (*h[i])[0];
             double dH[OR_MAXD], d2H[OR_MAXD];
             for (int j = 0; j < d; ++j) {
                 dH[j] = 1.0; d2H[j] = 1.0;
                 for (int i = 0; i < d; ++i) {
-                    dH[j] *= (i == j) ? h[i][1] : h[i][0];
-                    d2H[j] *= (i == j) ? h[i][2] : h[i][0];
+                    dH[j] *= (i == j) ? (*h[i])[1] : (*h[i])[0];
+                    d2H[j] *= (i == j) ? (*h[i])[2] : (*h[i])[0];
                 }
             }
             for (int f = 0; f < F; ++f) {
                 double th = theta[f];
-                if (gamma) gamma[f] += th * H * scale;
-                if (mg) mg[f] += fabs(th) * fabs(H) * scale;
+                if (gamma) gamma[f] += th * H * scale[k];
+                if (mg) mg[f] += fabs(th) * fabs(H) * scale[k];
                 for (int j = 0; j < d; ++j) {
                     /* d/dx_j = N d/dy_j */
-                    if (dgamma) dgamma[j * F + f] += th * scale * N * dH[j];
-                    if (md) md[j * F + f] += fabs(th) * scale * N * fabs(dH[j]);
-                    if (lap) lap[f] += th * scale * N * N * d2H[j];
-                    if (ml) ml[f] += fabs(th) * scale * N * N * fabs(d2H[j]);
+                    if (dgamma) dgamma[j * F + f] += th * scale[k] * N * dH[j];
+                    if (md) md[j * F + f] += fabs(th) * scale[k] * N * fabs(dH[j]);
+                    if (lap) lap[f] += th * scale[k] * N * N * d2H[j];
+                    if (ml) ml[f] += fabs(th) * scale[k] * N * N * fabs(d2H[j]);
                 }
             }
         }
@@ -342,62 +344,68 @@ int oracle_encode_fwd(int d, int L, int F, const int32_t* res, const int32_t* lo
 
 /* Backward for ONE level l: accumulate into grads[k] ([T_k][C(d,k)][F],
  * this level only, caller-zeroed) the transpose of the forward applied to
- * the upstream gradients (point-major layouts as in the forward; g_dgamma
- * and g_lap may be NULL).  mags[k] receives the condition magnitudes.
+ * the upstream gradients (float32 inputs, widened exactly; point-major
+ * layouts as in the forward; any of them may be NULL).  mags[k] receives the condition magnitudes.
  * Colliding vertices sum their contributions.  Serial over points.         */
 int oracle_encode_bwd_level(int d, int L, int F, int l, const int32_t* res, const int32_t* log2T,
                             int64_t n_pts, const float* coords,
-                            const double* g_gamma, const double* g_dgamma, const double* g_lap,
+                            const float* g_gamma, const float* g_dgamma, const float* g_lap,
                             double* const* grads, double* const* mags) {
     if (d < 1 || d > OR_MAXD || l < 0 || l >= L) return 1;
     const double N = (double)res[l];
     const double dx = 1.0 / N;
+    double scale[OR_MAXD + 1];
+    for (int k = 0; k <= d; ++k) scale[k] = pow(dx, (double)k);   /* dx^{|alpha|} */
+    int slot_of[8], order_of[8];
+    for (int alpha = 0; alpha < (1 << d); ++alpha) {
+        slot_of[alpha] = slot_in_bucket(d, alpha);
+        order_of[alpha] = popcount_small(alpha);
+    }
     for (int64_t n = 0; n < n_pts; ++n) {
         int64_t c[OR_MAXD];
         double t[OR_MAXD];
         for (int i = 0; i < d; ++i) locate(coords[n * d + i], res[l], &c[i], &t[i]);
+        double hb[OR_MAXD][2][2][3];
+        for (int i = 0; i < d; ++i)
+            for (int vi = 0; vi < 2; ++vi)
+                for (int a = 0; a < 2; ++a)
+                    hermite_1d(a, t[i] - (double)vi, vi ? -1.0 : 1.0, hb[i][vi][a]);
         for (int v = 0; v < (1 << d); ++v) {
             int64_t g[OR_MAXD];
-            double s[OR_MAXD], sigma[OR_MAXD];
-            for (int i = 0; i < d; ++i) {
-                int vi = v >> i & 1;
-                g[i] = c[i] + vi;
-                s[i] = t[i] - (double)vi;
-                sigma[i] = vi ? -1.0 : 1.0;
-            }
+            for (int i = 0; i < d; ++i) g[i] = c[i] + (v >> i & 1);
+            uint32_t idx[OR_MAXD + 1];
+            for (int k = 0; k <= d; ++k) idx[k] = vertex_index(d, g, res[l], log2T[k]);
             for (int alpha = 0; alpha < (1 << d); ++alpha) {
-                int k = popcount_small(alpha);
-                int slot = slot_in_bucket(d, alpha);
-                uint32_t idx = vertex_index(d, g, res[l], log2T[k]);
-                double scale = pow(dx, (double)k);
-                double h[OR_MAXD][3];
-                for (int i = 0; i < d; ++i) hermite_1d(alpha >> i & 1, s[i], sigma[i], h[i]);
+                int k = order_of[alpha];
+                const double (*h[OR_MAXD])[3];
+                for (int i = 0; i < d; ++i) h[i] = &hb[i][v >> i & 1][alpha >> i & 1];
                 double H = 1.0;
-                for (int i = 0; i < d; ++i) H *= h[i][0];
+                for (int i = 0; i < d; ++i) H *= (*h[i])[0];
                 double dH[OR_MAXD], d2H[OR_MAXD];
                 for (int j = 0; j < d; ++j) {
                     dH[j] = 1.0; d2H[j] = 1.0;
                     for (int i = 0; i < d; ++i) {
-                        dH[j] *= (i == j) ? h[i][1] : h[i][0];
-                        d2H[j] *= (i == j) ? h[i][2] : h[i][0];
+                        dH[j] *= (i == j) ? (*h[i])[1] : (*h[i])[0];
+                        d2H[j] *= (i == j) ? (*h[i])[2] : (*h[i])[0];
                     }
                 }
-                double* gk = grads[k] + ((size_t)idx * binom(d, k) + slot) * F;
-                double* mk = mags ? mags[k] + ((size_t)idx * binom(d, k) + slot) * F : NULL;
+                size_t off = ((size_t)idx[k] * binom(d, k) + slot_of[alpha]) * F;
+                double* gk = grads[k] + off;
+                double* mk = mags ? mags[k] + off : NULL;
                 for (int f = 0; f < F; ++f) {
-                    double up = g_gamma[((size_t)n * L + l) * F + f];
-                    double w = up * H * scale;
-                    double m = fabs(up) * fabs(H) * scale;
+                    double up = g_gamma ? (double)g_gamma[((size_t)n * L + l) * F + f] : 0.0;
+                    double w = up * H * scale[k];
+                    double m = fabs(up) * fabs(H) * scale[k];
                     for (int j = 0; j < d; ++j) {
                         if (g_dgamma) {
-                            double ud = g_dgamma[(((size_t)n * d + j) * L + l) * F + f];
-                            w += ud * scale * N * dH[j];
-                            m += fabs(ud) * scale * N * fabs(dH[j]);
+                            double ud = (double)g_dgamma[(((size_t)n * d + j) * L + l) * F + f];
+                            w += ud * scale[k] * N * dH[j];
+                            m += fabs(ud) * scale[k] * N * fabs(dH[j]);
                         }
                         if (g_lap) {
-                            double ul = g_lap[((size_t)n * L + l) * F + f];
-                            w += ul * scale * N * N * d2H[j];
-                            m += fabs(ul) * scale * N * N * fabs(d2H[j]);
+                            double ul = (double)g_lap[((size_t)n * L + l) * F + f];
+                            w += ul * scale[k] * N * N * d2H[j];
+                            m += fabs(ul) * scale[k] * N * N * fabs(d2H[j]);
                         }
                     }
                     gk[f] += w;
@@ -454,7 +462,7 @@ int oracle_linear_fwd(int d, int L, int F, const int32_t* res, int log2T, uint32
 /* Backward of the d-linear forward for ONE level l into grad[T][F] (this
  * level only, caller-zeroed); mag may be NULL.  Serial over points.        */
 int oracle_linear_bwd_level(int d, int L, int F, int l, const int32_t* res, int log2T,
-                            int64_t n_pts, const float* coords, const double* g_gamma,
+                            int64_t n_pts, const float* coords, const float* g_gamma,
                             double* grad, double* mag) {
     if (d < 1 || d > OR_MAXD || l < 0 || l >= L) return 1;
     for (int64_t n = 0; n < n_pts; ++n) {
@@ -471,7 +479,7 @@ int oracle_linear_bwd_level(int d, int L, int F, int l, const int32_t* res, int 
             }
             uint32_t idx = vertex_index(d, g, res[l], log2T);
             for (int f = 0; f < F; ++f) {
-                double up = g_gamma[((size_t)n * L + l) * F + f];
+                double up = (double)g_gamma[((size_t)n * L + l) * F + f];
                 grad[(size_t)idx * F + f] += w * up;
                 if (mag) mag[(size_t)idx * F + f] += fabs(w) * fabs(up);
             }

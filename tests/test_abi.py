@@ -1,0 +1,163 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/hg.h declares, computes the level schedule on the
+host, and rejects bad arguments with a status code before touching the GPU.
+
+Every call here either fails argument checking or has n = 0, so no kernel
+is ever launched.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def m():
+    import multiresolution_hash_grid_02_b300 as pkg
+    from multiresolution_hash_grid_02_b300 import build
+    build.build()
+    return pkg
+
+
+def _declared(header):
+    with open(os.path.join(ROOT, "include", header)) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hg_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(m):
+    lib = m.hg.lib()
+    names = _declared("hg.h") + _declared("hg_probe.h")
+    assert {"hg_encode_fwd", "hg_encode_bwd", "hg_linear_fwd", "hg_linear_bwd", "hg_level_resolutions",
+            "hg_hash_indices", "hg_status_string", "hg_last_error", "hg_abi_version"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_matches_header(m):
+    with open(os.path.join(ROOT, "include", "hg.h")) as f:
+        v = int(re.search(r"#define HG_ABI_VERSION (\d+)", f.read()).group(1))
+    assert m.hg.hg_abi_version() == v
+
+
+def test_status_strings(m):
+    assert [m.hg.hg_status_string(s) for s in range(4)] == ["HG_OK", "HG_ERR_INVALID_ARG", "HG_ERR_UNSUPPORTED",
+                                                            "HG_ERR_CUDA"]
+
+
+@pytest.mark.parametrize("L,n_min,n_max", [(4, 4, 32), (16, 16, 2048), (16, 16, 1024), (16, 16, 512),
+                                           (1, 7, 7), (2, 1, 1), (32, 2, 1 << 22), (9, 3, 1000), (31, 5, 4000000),
+                                           (16, 1, 65536), (24, 16, 1 << 19)])
+def test_level_schedule_equals_oracle(m, oracle_mod, L, n_min, n_max):
+    got = m.hg.hg_level_resolutions(m.GridDesc(d=2, L=L, F=2, n_min=n_min, n_max=n_max))
+    assert got == oracle_mod.level_resolutions(L, n_min, n_max)
+
+
+def test_level_schedule_sweep(m, oracle_mod):
+    import random
+    rnd = random.Random(3)
+    for _ in range(300):
+        L = rnd.randint(1, 32)
+        a = rnd.randint(1, 5000)
+        b = rnd.randint(a, 1 << 22)
+        got = m.hg.hg_level_resolutions(m.GridDesc(d=3, L=L, F=1, n_min=a, n_max=b))
+        assert got == oracle_mod.level_resolutions(L, a, b), (L, a, b)
+
+
+def test_explicit_resolutions(m):
+    assert m.hg.hg_level_resolutions(m.GridDesc(d=2, L=3, F=2, res=[5, 9, 700])) == [5, 9, 700]
+    with pytest.raises(m.HGError):
+        m.hg.hg_level_resolutions(m.GridDesc(d=2, L=2, F=2, res=[0, 9]))
+
+
+def _fwd_status(m, desc, n=5, coords=16, tables=None, gamma=16):
+    if tables is None:
+        tables = m.hg.packed_views(_FakeTable((desc.L, 1 << desc.log2_T[0], 1 << desc.d, desc.F)), desc.d)
+    return m.hg.hg_encode_fwd(desc, n, coords, tables, gamma, None, None, stream=0, check=False)
+
+
+class _FakeTable:
+    """Shape-only stand-in for a tensor: address 0 (so every call that gets
+    past the shape checks fails on the NULL pointer, before any launch)."""
+
+    def __init__(self, shape, addr=0, esize=4):
+        self.shape = shape
+        self._addr = addr
+        self._esize = esize
+
+    def data_ptr(self):
+        return self._addr
+
+    def element_size(self):
+        return self._esize
+
+
+@pytest.mark.parametrize("field,value", [("d", 1), ("d", 4), ("L", 0), ("L", 33), ("F", 3), ("F", 16),
+                                         ("dtype", 2), ("layout", 7), ("n_min", 0), ("n_max", 1 << 23)])
+def test_bad_descriptor_is_rejected(m, field, value):
+    desc = m.GridDesc(d=3, L=4, F=2, n_min=4, n_max=32, log2_T=(8, 8, 8, 8))
+    setattr(desc, field, value)
+    t = _FakeTable((4, 256, 8, 2), addr=1 << 20)
+    views = m.hg.packed_views(t, 3) if field != "d" else []
+    st = m.hg.hg_encode_fwd(desc, 5, 16, views or m.hg.packed_views(t, 3), 1 << 21, None, None, stream=0,
+                            check=False)
+    assert st == m.hg.HG_ERR_INVALID_ARG
+    assert m.hg.hg_last_error() != ""
+
+
+def test_bad_arguments_are_rejected(m):
+    hg = m.hg
+    ok_desc = lambda: m.GridDesc(d=3, L=4, F=2, n_min=4, n_max=32, log2_T=(8, 8, 8, 8))
+    t = _FakeTable((4, 256, 8, 2), addr=1 << 20)
+    views = hg.packed_views(t, 3)
+    E = hg.HG_ERR_INVALID_ARG
+    # level mask above L, table size out of range
+    d = ok_desc(); d.level_mask = 1 << 4
+    assert hg.hg_encode_fwd(d, 5, 16, views, 32, stream=0, check=False) == E
+    d = ok_desc(); d.log2_T = (31, 8, 8, 8)
+    assert hg.hg_encode_fwd(d, 5, 16, views, 32, stream=0, check=False) == E
+    # n out of range
+    assert hg.hg_encode_fwd(ok_desc(), -1, 16, views, 32, stream=0, check=False) == E
+    assert hg.hg_encode_fwd(ok_desc(), 1 << 31, 16, views, 32, stream=0, check=False) == E
+    # NULL coords / gamma with n > 0
+    assert hg.hg_encode_fwd(ok_desc(), 5, 0, views, 32, stream=0, check=False) == E
+    assert hg.hg_encode_fwd(ok_desc(), 5, 16, views, 0, stream=0, check=False) == E
+    # NULL and misaligned table pointers
+    nul = hg.packed_views(_FakeTable((4, 256, 8, 2), addr=0), 3)
+    assert hg.hg_encode_fwd(ok_desc(), 5, 16, nul, 32, stream=0, check=False) == E
+    odd = hg.packed_views(_FakeTable((4, 256, 8, 2), addr=(1 << 20) + 1), 3)
+    assert hg.hg_encode_fwd(ok_desc(), 5, 16, odd, 32, stream=0, check=False) == E
+    # rows that overlap: row stride below the values per entry, level stride below T * row stride
+    bad = [hg.TableView(t, 256 * 8 * 2, 1, 0)] + views[1:]
+    assert hg.hg_encode_fwd(ok_desc(), 5, 16, bad, 32, stream=0, check=False) == E
+    bad = [hg.TableView(t, 100, 16, 0)] + views[1:]
+    assert hg.hg_encode_fwd(ok_desc(), 5, 16, bad, 32, stream=0, check=False) == E
+    # misaligned coordinates / outputs
+    assert hg.hg_encode_fwd(ok_desc(), 5, 18, views, 32, stream=0, check=False) == E
+    assert hg.hg_encode_fwd(ok_desc(), 5, 16, views, 33, stream=0, check=False) == E
+    # backward: misaligned upstream gradient, NULL coords
+    assert hg.hg_encode_bwd(ok_desc(), 5, 16, 18, None, None, views, stream=0, check=False) == E
+    assert hg.hg_encode_bwd(ok_desc(), 5, 0, 16, None, None, views, stream=0, check=False) == E
+    # d-linear and indices
+    lv = hg.linear_view(_FakeTable((4, 256, 2), addr=1 << 20))
+    assert hg.hg_linear_fwd(ok_desc(), 5, 0, lv, 32, stream=0, check=False) == E
+    assert hg.hg_linear_bwd(ok_desc(), 5, 0, 16, lv, stream=0, check=False) == E
+    assert hg.hg_hash_indices(ok_desc(), 5, 16, 0, stream=0, check=False) == E
+    # NULL descriptor / table array at the C level
+    lib = hg.lib()
+    assert lib.hg_encode_fwd(None, 5, 16, None, 32, None, None, None) == E
+    assert lib.hg_level_resolutions(None, None) == E
+
+
+def test_zero_points_touch_nothing(m):
+    """n = 0 with a valid descriptor succeeds without a launch (no GPU here)."""
+    hg = m.hg
+    desc = m.GridDesc(d=2, L=3, F=2, n_min=4, n_max=16, log2_T=(8, 8, 8))
+    t = _FakeTable((3, 256, 4, 2), addr=1 << 20)
+    assert hg.hg_encode_fwd(desc, 0, 0, hg.packed_views(t, 2), 0, stream=0, check=False) == hg.HG_OK
+    assert hg.hg_encode_bwd(desc, 0, 0, 0, 0, 0, hg.packed_views(t, 2), stream=0, check=False) == hg.HG_OK
+    assert hg.hg_last_error() == ""

@@ -457,13 +457,13 @@ def test_backward_adjoint_identity(oracle_mod, d, res, log2T):
     L = len(res)
     tabs = [rng.uniform(-1, 1, size=(L, 1 << log2T[k], comb(d, k), F)) for k in range(d + 1)]
     xs = rng.random((n, d), dtype=np.float32)
-    gg = rng.standard_normal((n, L, F))
-    gd = rng.standard_normal((n, d, L, F))
-    gl = rng.standard_normal((n, L, F))
+    gg = rng.standard_normal((n, L, F), dtype=np.float32)
+    gd = rng.standard_normal((n, d, L, F), dtype=np.float32)
+    gl = rng.standard_normal((n, L, F), dtype=np.float32)
     out = oracle_mod.encode_fwd(d, F, res, log2T, tabs, xs)
     grads, mags = oracle_mod.encode_bwd(d, F, res, log2T, xs, gg, gd, gl)
     lhs = _inner_tables(grads, tabs)
-    rhs = float((gg * out["gamma"]).sum() + (gd * out["dgamma"]).sum() + (gl * out["lap"]).sum())
+    rhs = float((gg * out["gamma"]).sum() + (gd * out["dgamma"]).sum() + (gl * out["lap"]).sum())  # fp64 products
     scale = _inner_tables(mags, [np.abs(t) for t in tabs])
     assert abs(lhs - rhs) <= 1e-12 * scale
 
@@ -476,9 +476,9 @@ def test_backward_equals_bruteforce_jacobian(oracle_mod):
     L = len(res)
     shapes = [(L, 1 << log2T[k], comb(d, k), F) for k in range(d + 1)]
     xs = rng.random((25, d), dtype=np.float32)
-    gg = rng.standard_normal((25, L, F))
-    gd = rng.standard_normal((25, d, L, F))
-    gl = rng.standard_normal((25, L, F))
+    gg = rng.standard_normal((25, L, F), dtype=np.float32)
+    gd = rng.standard_normal((25, d, L, F), dtype=np.float32)
+    gl = rng.standard_normal((25, L, F), dtype=np.float32)
     grads, _ = oracle_mod.encode_bwd(d, F, res, log2T, xs, gg, gd, gl)
     for k, shp in enumerate(shapes):
         for e in np.ndindex(*shp):
@@ -494,7 +494,7 @@ def test_linear_backward_adjoint_and_jacobian(oracle_mod):
     d, F, res, log2T = 3, 2, [2, 5], 4
     L = len(res)
     xs = rng.random((40, d), dtype=np.float32)
-    gg = rng.standard_normal((40, L, F))
+    gg = rng.standard_normal((40, L, F), dtype=np.float32)
     grad, _ = oracle_mod.linear_bwd(d, F, res, log2T, xs, gg)
     for e in np.ndindex(L, 1 << log2T, F):
         table = np.zeros((L, 1 << log2T, F))
@@ -516,7 +516,7 @@ def test_level_mask(oracle_mod):
     full = oracle_mod.encode_fwd(d, F, res, log2T, tabs, xs)
     mask = 0b0101
     part = oracle_mod.encode_fwd(d, F, res, log2T, tabs, xs, level_mask=mask)
-    gg = rng.standard_normal((100, L, F))
+    gg = rng.standard_normal((100, L, F), dtype=np.float32)
     gfull, _ = oracle_mod.encode_bwd(d, F, res, log2T, xs, gg)
     gpart, _ = oracle_mod.encode_bwd(d, F, res, log2T, xs, gg, level_mask=mask)
     for l in range(L):
