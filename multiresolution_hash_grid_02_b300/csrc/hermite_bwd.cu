@@ -144,6 +144,109 @@ __global__ void __launch_bounds__(kBlock) hermite_bwd_kernel(const __grid_consta
     }
 }
 
+// Transposed blend of one packed slot (one alpha, weights W0..W1[..W2]) of
+// one feature: qb[v] = d(loss)/d theta at corner v, from the upstream
+// gradients (gg, gd[], gl).  The same separable order as blend3_t / blend2_t,
+// restricted to one alpha.
+template <int D>
+__device__ __forceinline__ void unit_blend_t(float gg, const float (&gd)[3], float gl, const AxisW& W0,
+                                             const AxisW& W1, const AxisW& W2, float (&qb)[1 << D]) {
+    if constexpr (D == 3) {
+#pragma unroll
+        for (int v2 = 0; v2 < 2; ++v2) {
+            const float A = fmaf(gg, W2.w[v2], fmaf(gd[2], W2.d1[v2], gl * W2.d2[v2]));
+            const float B = gd[0] * W2.w[v2];
+            const float C = gd[1] * W2.w[v2];
+            const float Dl = gl * W2.w[v2];
+#pragma unroll
+            for (int v1 = 0; v1 < 2; ++v1) {
+                const float s = fmaf(A, W1.w[v1], fmaf(C, W1.d1[v1], Dl * W1.d2[v1]));
+                const float s1 = B * W1.w[v1];
+                const float s2 = Dl * W1.w[v1];
+#pragma unroll
+                for (int v0 = 0; v0 < 2; ++v0)
+                    qb[v0 + 2 * v1 + 4 * v2] = fmaf(s, W0.w[v0], fmaf(s1, W0.d1[v0], s2 * W0.d2[v0]));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int v1 = 0; v1 < 2; ++v1) {
+            const float s = fmaf(gg, W1.w[v1], fmaf(gd[1], W1.d1[v1], gl * W1.d2[v1]));
+            const float s1 = gd[0] * W1.w[v1];
+            const float s2 = gl * W1.w[v1];
+#pragma unroll
+            for (int v0 = 0; v0 < 2; ++v0) qb[v0 + 2 * v1] = fmaf(s, W0.w[v0], fmaf(s1, W0.d1[v0], s2 * W0.d2[v0]));
+        }
+    }
+}
+
+// Lane-split backward for packed fp32 gradient rows of 32 or 64 bytes: G
+// lanes share one (point, level); lane g owns the 16-byte chunk g of every
+// corner row (S = 2^D/G slots x FC features = 4 floats), computes the
+// gradients of those slots, and issues one red.global.add.v4.f32 per corner,
+// so one warp instruction reduces into whole rows.
+template <int D, int FC, int G>
+__global__ void __launch_bounds__(kBlock) hermite_bwd_split_kernel(const __grid_constant__ BwdParams p) {
+    constexpr int V = 1 << D, S = V / G;
+    static_assert(S * FC == 4, "one 16-byte chunk per lane");
+    const int l = blockIdx.y;
+    if (!((p.c.level_mask >> l) & 1u)) return;
+    const int64_t n = (static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x) / G;
+    const int lane = threadIdx.x % G;
+    if (n >= p.c.n) return;
+    const int F = p.c.F;
+    const Level& lv = p.c.lv[l];
+
+    uint32_t c[D];
+    float t[D];
+    Basis1 B[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+        locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
+        B[i] = hermite_basis(t[i], lv);
+    }
+    float gg[FC], gl[FC], gd[FC][3];
+#pragma unroll
+    for (int f = 0; f < FC; ++f) {
+        const int64_t lf = static_cast<int64_t>(l) * F + f;
+        gg[f] = p.g_gamma ? __ldg(p.g_gamma + n * p.c.sn + lf * p.c.sf) : 0.f;
+        gl[f] = p.g_lap ? __ldg(p.g_lap + n * p.c.sn + lf * p.c.sf) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+            gd[f][j] = (p.g_dgamma && j < D) ? __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf) : 0.f;
+    }
+    float r[V][4];
+#pragma unroll
+    for (int u = 0; u < S; ++u) {
+        const AxisW W0 = unit_axis<D, G>(B[0], lane, u, 0);
+        const AxisW W1 = unit_axis<D, G>(B[1], lane, u, 1);
+        const AxisW W2 = unit_axis<D, G>(B[D - 1], lane, u, D - 1);
+#pragma unroll
+        for (int f = 0; f < FC; ++f) {
+            float qb[V];
+            unit_blend_t<D>(gg[f], gd[f], gl[f], W0, W1, W2, qb);
+#pragma unroll
+            for (int v = 0; v < V; ++v) r[v][u * FC + f] = qb[v];
+        }
+    }
+    float* row0 = p.grad.ptr[0] + l * p.grad.ls[0] + lane * 4;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        uint32_t g[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) g[i] = c[i] + ((v >> i) & 1u);
+        const uint32_t id = vertex_index<D>(g, lv, lv.dense & 1u, p.c.tmask[0]);
+        red_add_v4(row0 + static_cast<int64_t>(id) * p.grad.rs[0], r[v][0], r[v][1], r[v][2], r[v][3]);
+    }
+}
+
+template <int D, int FC, int G>
+cudaError_t launch_split(const BwdParams& p, cudaStream_t s) {
+    dim3 grid(static_cast<unsigned>((p.c.n * G + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
+    hermite_bwd_split_kernel<D, FC, G><<<grid, kBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <int D, int FC, bool VEC>
 cudaError_t launch(const BwdParams& p, cudaStream_t s) {
     dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
@@ -161,6 +264,12 @@ cudaError_t pick(const BwdParams& p, int fc, bool vec, cudaStream_t s) {
 
 int launch_hermite_bwd(const BwdParams& p, int fc, bool vec, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (vec && fc == p.c.F) {
+        // packed rows of 2^d * F floats: 32 bytes -> lane pairs, 64 bytes -> quads
+        if (p.c.d == 2 && p.c.F == 2) return launch_split<2, 2, 2>(p, s);
+        if (p.c.d == 3 && p.c.F == 1) return launch_split<3, 1, 2>(p, s);
+        if (p.c.d == 3 && p.c.F == 2) return launch_split<3, 2, 4>(p, s);
+    }
     return p.c.d == 2 ? pick<2>(p, fc, vec, s) : pick<3>(p, fc, vec, s);
 }
 

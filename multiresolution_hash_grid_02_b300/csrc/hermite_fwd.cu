@@ -170,6 +170,112 @@ __global__ void __launch_bounds__(kBlock) hermite_fwd_kernel(const __grid_consta
     }
 }
 
+// Contribution of one packed slot (multi-index alpha, weights W0..W2 picked
+// for its per-axis orders) of one feature to the 3D outputs; c[v] holds that
+// slot's coefficient at corner v = v0 + 2 v1 + 4 v2.  The same separable
+// order as blend3, restricted to one alpha.
+__device__ __forceinline__ void unit_blend3(const float (&c)[8], const AxisW& W0, const AxisW& W1, const AxisW& W2,
+                                            float (&o)[5]) {
+#pragma unroll
+    for (int v2 = 0; v2 < 2; ++v2) {
+        float A = 0.f, B = 0.f, C = 0.f, Dl = 0.f;
+#pragma unroll
+        for (int v1 = 0; v1 < 2; ++v1) {
+            const float c0 = c[2 * v1 + 4 * v2], c1 = c[1 + 2 * v1 + 4 * v2];
+            const float s = fmaf(c0, W0.w[0], c1 * W0.w[1]);
+            const float s1 = fmaf(c0, W0.d1[0], c1 * W0.d1[1]);
+            const float s2 = fmaf(c0, W0.d2[0], c1 * W0.d2[1]);
+            A = fmaf(s, W1.w[v1], A);
+            B = fmaf(s1, W1.w[v1], B);
+            C = fmaf(s, W1.d1[v1], C);
+            Dl = fmaf(s2, W1.w[v1], Dl);
+            Dl = fmaf(s, W1.d2[v1], Dl);
+        }
+        o[0] = fmaf(A, W2.w[v2], o[0]);
+        o[1] = fmaf(B, W2.w[v2], o[1]);
+        o[2] = fmaf(C, W2.w[v2], o[2]);
+        o[3] = fmaf(A, W2.d1[v2], o[3]);
+        o[4] = fmaf(Dl, W2.w[v2], o[4]);
+        o[4] = fmaf(A, W2.d2[v2], o[4]);
+    }
+}
+
+// Lane-pair split for 64-byte packed rows (3D, F = 2, fp32).  Lane h of a
+// pair reads the 32-byte half h of every corner row with one 256-bit load, so
+// one warp instruction covers whole rows (one L1 wavefront per row), and
+// blends the four slots of that half for both features; the encoding is
+// linear in theta, so the pair's partial outputs add up.  A reduce-scatter
+// leaves feature h's outputs on lane h, which stores them.
+__global__ void __launch_bounds__(kBlock) hermite_fwd_pair3_kernel(const __grid_constant__ FwdParams p) {
+    constexpr int D = 3, V = 8, G = 2, S = 4, FC = 2;
+    const int l = blockIdx.y;
+    const int64_t n = (static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x) >> 1;
+    const int lane = threadIdx.x & 1;
+    if (n >= p.c.n) return;  // both lanes of a pair share n
+    const int F = p.c.F;
+    const Level& lv = p.c.lv[l];
+    const int64_t lf = static_cast<int64_t>(l) * F + lane;
+    if (!((p.c.level_mask >> l) & 1u)) {
+        __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, 0.f);
+        if (p.dgamma) {
+#pragma unroll
+            for (int j = 0; j < D; ++j) __stcs(p.dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf, 0.f);
+        }
+        if (p.lap) __stcs(p.lap + n * p.c.sn + lf * p.c.sf, 0.f);
+        return;
+    }
+
+    uint32_t c[D];
+    float t[D];
+    Basis1 B[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+        locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
+        B[i] = hermite_basis(t[i], lv);
+    }
+    const float* base = static_cast<const float*>(p.tab.ptr[0]) + l * p.tab.ls[0] + lane * (S * FC);
+    uint32_t q[V][8];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const uint32_t g[D] = {c[0] + (v & 1u), c[1] + ((v >> 1) & 1u), c[2] + ((v >> 2) & 1u)};
+        const uint32_t id = vertex_index<D>(g, lv, lv.dense & 1u, p.c.tmask[0]);
+        ld_nc_v8(base + static_cast<int64_t>(id) * p.tab.rs[0], q[v]);
+    }
+    float o[FC][5];
+#pragma unroll
+    for (int f = 0; f < FC; ++f)
+#pragma unroll
+        for (int k = 0; k < 5; ++k) o[f][k] = 0.f;
+#pragma unroll
+    for (int u = 0; u < S; ++u) {
+        const AxisW W0 = unit_axis<D, G>(B[0], lane, u, 0);
+        const AxisW W1 = unit_axis<D, G>(B[1], lane, u, 1);
+        const AxisW W2 = unit_axis<D, G>(B[2], lane, u, 2);
+#pragma unroll
+        for (int f = 0; f < FC; ++f) {
+            float cv[V];
+#pragma unroll
+            for (int v = 0; v < V; ++v) cv[v] = __uint_as_float(q[v][u * FC + f]);
+            unit_blend3(cv, W0, W1, W2, o[f]);
+        }
+    }
+    // reduce-scatter across the pair: lane h keeps feature h
+    const unsigned mask = __activemask();
+    float r[5];
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const float mine = lane ? o[1][k] : o[0][k];
+        const float other = lane ? o[0][k] : o[1][k];
+        r[k] = mine + __shfl_xor_sync(mask, other, 1);
+    }
+    __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, r[0]);
+    if (p.dgamma) {
+#pragma unroll
+        for (int j = 0; j < D; ++j) __stcs(p.dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf, r[1 + j]);
+    }
+    if (p.lap) __stcs(p.lap + n * p.c.sn + lf * p.c.sf, r[4]);
+}
+
 template <int D, int FC, typename TT, bool VEC>
 cudaError_t launch(const FwdParams& p, cudaStream_t s) {
     dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
@@ -191,6 +297,11 @@ cudaError_t pick_fc(const FwdParams& p, int fc, bool vec, cudaStream_t s) {
 
 int launch_hermite_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (vec && p.c.d == 3 && p.c.F == 2 && dtype == HG_F32) {
+        dim3 grid(static_cast<unsigned>((p.c.n * 2 + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
+        hermite_fwd_pair3_kernel<<<grid, kBlock, 0, s>>>(p);
+        return cudaGetLastError();
+    }
     if (p.c.d == 2) return dtype == HG_F16 ? pick_fc<2, __half>(p, fc, vec, s) : pick_fc<2, float>(p, fc, vec, s);
     return dtype == HG_F16 ? pick_fc<3, __half>(p, fc, vec, s) : pick_fc<3, float>(p, fc, vec, s);
 }

@@ -290,7 +290,7 @@ hg_status hg_encode_fwd(const hg_grid_desc* desc, int64_t n, const float* coords
     bool vec = fc == F && is_packed(desc, ptrs, ls, rs, es);
     if (vec) {
         const size_t row = static_cast<size_t>(V) * F * es;
-        const size_t al = row < 16 ? row : 16;
+        const size_t al = row < 32 ? row : 32;  // 256-bit loads of 32-byte rows / half-rows
         vec = aligned(ptrs[0], al) && (static_cast<size_t>(ls[0]) * es) % al == 0;
     }
     return launch_status(hg::launch_hermite_fwd(p, fc, vec, desc->dtype, stream), "hermite forward");

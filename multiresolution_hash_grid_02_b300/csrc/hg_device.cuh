@@ -100,16 +100,27 @@ template <>
 __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
 
 // Read-only loads of ROW_BYTES contiguous bytes (ROW_BYTES in {8,16,32,64},
-// address aligned to min(16, ROW_BYTES)) into registers.
+// address aligned to min(32, ROW_BYTES)) into registers.
 template <int ROW_BYTES>
 struct RowRegs {
     static constexpr int kWords = ROW_BYTES / 4;
     uint32_t w[kWords];
 };
 
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t (&r)[8]);
+
 template <int ROW_BYTES>
 __device__ __forceinline__ void load_row(const void* p, RowRegs<ROW_BYTES>& r) {
-    if constexpr (ROW_BYTES >= 16) {
+    if constexpr (ROW_BYTES >= 32) {
+        // one 256-bit load per 32 bytes: a single L1 wavefront per sector pair
+#pragma unroll
+        for (int i = 0; i < ROW_BYTES / 32; ++i) {
+            uint32_t q[8];
+            ld_nc_v8(static_cast<const char*>(p) + 32 * i, q);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r.w[8 * i + j] = q[j];
+        }
+    } else if constexpr (ROW_BYTES == 16) {
         const uint4* q = reinterpret_cast<const uint4*>(p);
 #pragma unroll
         for (int i = 0; i < ROW_BYTES / 16; ++i) {
@@ -147,6 +158,63 @@ __device__ __forceinline__ void red_add_v2(float* a, float x, float y) {
 __device__ __forceinline__ void red_add_v4(float* a, float x, float y, float z, float w) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(a), "f"(x), "f"(y), "f"(z), "f"(w)
                  : "memory");
+}
+
+}  // namespace hg
+
+namespace hg {
+
+// Multi-index alpha held by packed slot s (inverse of packed_slot).
+template <int D>
+__host__ __device__ constexpr int slot_alpha(int s) {
+    return D == 2 ? s : (s == 3 ? 4 : (s == 4 ? 3 : s));
+}
+
+// Lane-split rows: G lanes share one (point, level); lane g owns the S = 2^D/G
+// consecutive packed slots g*S .. g*S+S-1 of every corner row.  Bit i of the
+// multi-index of unit u is the same in every lane when !split_bit_varies.
+template <int D, int G>
+__host__ __device__ constexpr bool split_bit_varies(int u, int i) {
+    constexpr int S = (1 << D) / G;
+    const int b0 = (slot_alpha<D>(u) >> i) & 1;
+    for (int g = 1; g < G; ++g)
+        if (((slot_alpha<D>(g * S + u) >> i) & 1) != b0) return true;
+    return false;
+}
+
+// One axis' weights of the two corners for one basis order.
+struct AxisW {
+    float w[2], d1[2], d2[2];
+};
+
+__device__ __forceinline__ AxisW axis_pick(const Basis1& b, bool slope) {
+    AxisW r;
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+        r.w[v] = slope ? b.w[v][1] : b.w[v][0];
+        r.d1[v] = slope ? b.d1[v][1] : b.d1[v][0];
+        r.d2[v] = slope ? b.d2[v][1] : b.d2[v][0];
+    }
+    return r;
+}
+
+// Weights of axis i for unit u of a G-lane split (compile-time when the bit
+// does not vary across lanes).
+template <int D, int G>
+__device__ __forceinline__ AxisW unit_axis(const Basis1& b, int lane, int u, int i) {
+    constexpr int S = (1 << D) / G;
+    if (split_bit_varies<D, G>(u, i)) return axis_pick(b, (slot_alpha<D>(lane * S + u) >> i) & 1);
+    return axis_pick(b, (slot_alpha<D>(u) >> i) & 1);
+}
+
+// 256-bit read-only load (sm_100+): 32 bytes, 32-byte aligned.
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t (&r)[8]) {
+    float f[8];
+    asm("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]), "=f"(f[4]), "=f"(f[5]), "=f"(f[6]), "=f"(f[7])
+        : "l"(p));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = __float_as_uint(f[i]);
 }
 
 }  // namespace hg
