@@ -219,31 +219,49 @@ def run_reference(args):
 # native (CUDA) arm
 # ---------------------------------------------------------------------------
 
-def probe_peaks(torch, hg):
-    """Measured L2 ceilings: random 64-byte row gather and random 16-byte
-    vector RED, each on a 32 MiB buffer (L2-resident); best of 5."""
+def kernel_patterns(w):
+    """(row bytes, lanes per row) of the forward gather and the backward RED
+    the kernels issue for this workload (packed layout)."""
+    es = 2 if w.dtype == "f16" else 4
+    slots = (1 << w.d) if w.kind == "hermite" else 1
+    trow = slots * w.F * es
+    grow = slots * w.F * 4
+    g = (64, 2) if trow == 64 else (32, 1)
+    r = {64: (64, 4), 32: (32, 2)}.get(grow, (16, 1))
+    return g, r
+
+
+def probe_peaks(torch, hg, gather_pat, red_pat):
+    """Measured L2 ceilings for the kernels' own access patterns: random
+    whole-row gathers and random 16-byte vector REDs on a 32 MiB buffer
+    (L2-resident), rows split across lanes as the kernels split them; best of 5
+    after one warm-up launch."""
     buf = torch.zeros(1 << 23, dtype=torch.float32, device="cuda")   # 32 MiB
     n_threads = 148 * 2048 * 4
     sink = torch.empty(n_threads, device="cuda")
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    best_g = best_r = 0.0
-    rows, per = 1 << 19, 64
-    for i in range(6):
-        ev[0].record()
-        hg.hg_probe_l2_gather(buf, 19, 64, n_threads, per, i, sink)
-        ev[1].record()
-        torch.cuda.synchronize()
-        if i:
-            best_g = max(best_g, n_threads * per * 64 / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9)
-    for i in range(6):
-        ev[0].record()
-        hg.hg_probe_l2_red(buf, 21, n_threads, 32, i)
-        ev[1].record()
-        torch.cuda.synchronize()
-        if i:
-            best_r = max(best_r, n_threads * 32 * 16 / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9)
-    assert rows
-    return best_g, best_r
+
+    def best(fn, nbytes):
+        b = 0.0
+        for i in range(6):
+            ev[0].record()
+            fn(i)
+            ev[1].record()
+            torch.cuda.synchronize()
+            if i:
+                b = max(b, nbytes / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9)
+        return b
+
+    grow, glanes = gather_pat
+    rrow, rlanes = red_pat
+    gl2 = {64: 19, 32: 20}[grow]
+    rl2 = {64: 19, 32: 20, 16: 21}[rrow]
+    per_g, per_r = 64, 64
+    g = best(lambda i: hg.hg_probe_l2_gather(buf, gl2, grow, glanes, n_threads, per_g, i, sink),
+             n_threads // glanes * per_g * grow)
+    r = best(lambda i: hg.hg_probe_l2_red(buf, rl2, rrow, rlanes, n_threads, per_r, i),
+             n_threads // rlanes * per_r * rrow)
+    return g, r
 
 
 def main():
@@ -322,7 +340,8 @@ def main():
         if rec:
             rec[2].record(stream)
 
-    gather_peak, red_peak = probe_peaks(torch, hg)
+    gather_pat, red_pat = kernel_patterns(w)
+    gather_peak, red_peak = probe_peaks(torch, hg, gather_pat, red_pat)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -369,9 +388,11 @@ def main():
     kernels = {
         "fwd": {"ms": t_fwd, "bound": "l2", "achieved": fwd_gbs, "peak": gather_peak, "unit": "GB/s",
                 "frac": fwd_gbs / gather_peak, "algorithmic_bytes": gather_bytes,
+                "probe": f"{gather_pat[0]}-byte rows, {gather_pat[1]} lane(s) per row",
                 "what": "compulsory coefficient bytes gathered / launch time vs the measured random-gather L2 peak"},
         "bwd": {"ms": t_bwd, "bound": "l2", "achieved": bwd_gbs, "peak": red_peak, "unit": "GB/s",
                 "frac": bwd_gbs / red_peak, "algorithmic_bytes": red_bytes,
+                "probe": f"{red_pat[0]}-byte rows, {red_pat[1]} lane(s) per row",
                 "what": "fp32 gradient RED payload bytes / launch time vs the measured random-RED L2 peak"},
     }
     dom = "bwd" if t_bwd >= t_fwd else "fwd"

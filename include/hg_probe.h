@@ -18,25 +18,31 @@
 extern "C" {
 #endif
 
-/* Random-row gather: n_threads threads each read `rows_per_thread` rows of
- * row_bytes (32 or 64) bytes, chosen by an integer hash among the
- * 2^log2_rows rows of `buf` (device, 16-byte aligned, 2^log2_rows * row_bytes
- * bytes), with 16-byte vector loads, and write one float each to `sink`
- * (device float [n_threads]).  Bytes moved = n_threads * rows_per_thread *
- * row_bytes.  Errors: HG_ERR_INVALID_ARG for NULL / misaligned pointers,
- * row_bytes not 32 or 64, log2_rows outside 4..30, rows_per_thread not a
- * positive multiple of 8, n_threads < 1; HG_ERR_CUDA on launch failure. */
-hg_status hg_probe_l2_gather(const void* buf, int32_t log2_rows, int32_t row_bytes, int64_t n_threads,
-                             int32_t rows_per_thread, uint32_t seed, float* sink, hg_stream stream);
+/* Random-row gather: groups of `lanes_per_row` consecutive lanes (1, 2 or 4)
+ * read whole rows of row_bytes (32 or 64) bytes, each lane its
+ * row_bytes/lanes_per_row-byte chunk (256-bit loads for 32-byte chunks,
+ * 128-bit loads otherwise), so that one warp instruction covers whole rows.
+ * Each group reads `rows_per_group` rows chosen by an integer hash among the
+ * 2^log2_rows rows of `buf` (device, 32-byte aligned, 2^log2_rows * row_bytes
+ * bytes); every lane writes one float to `sink` (device float [n_threads]).
+ * Bytes moved = n_threads / lanes_per_row * rows_per_group * row_bytes.
+ * Errors: HG_ERR_INVALID_ARG for NULL / misaligned pointers, row_bytes not 32
+ * or 64, lanes_per_row not 1, 2 or 4 (or a 64-byte row split one way), log2_rows
+ * outside 4..30, rows_per_group not a positive multiple of 8, n_threads not a
+ * positive multiple of lanes_per_row; HG_ERR_CUDA on launch failure. */
+hg_status hg_probe_l2_gather(const void* buf, int32_t log2_rows, int32_t row_bytes, int32_t lanes_per_row,
+                             int64_t n_threads, int32_t rows_per_group, uint32_t seed, float* sink, hg_stream stream);
 
-/* Random vector reduction: n_threads threads each issue `ops_per_thread`
- * red.global.add.v4.f32 (16 bytes of payload) at 16-byte slots chosen by an
- * integer hash among the 2^log2_slots slots of `buf` (device float,
- * 4 * 2^log2_slots floats, 16-byte aligned), adding 1.0 to each lane.
- * Payload bytes = n_threads * ops_per_thread * 16.  Errors: as above
- * (log2_slots in 4..30, ops_per_thread >= 1). */
-hg_status hg_probe_l2_red(float* buf, int32_t log2_slots, int64_t n_threads, int32_t ops_per_thread, uint32_t seed,
-                          hg_stream stream);
+/* Random vector reduction: groups of `lanes_per_row` lanes (1, 2 or 4) add
+ * 1.0 to every float of whole rows of row_bytes (16, 32 or 64) bytes, each
+ * lane issuing red.global.add.v4.f32 (16 bytes of payload) on its
+ * row_bytes/lanes_per_row-byte chunk, at rows chosen by an integer hash among
+ * the 2^log2_rows rows of `buf` (device float, 16-byte aligned).  Payload
+ * bytes = n_threads / lanes_per_row * rows_per_group * row_bytes.  Errors: as
+ * above (row_bytes 16, 32 or 64 with chunks of at least 16 bytes,
+ * rows_per_group >= 1). */
+hg_status hg_probe_l2_red(float* buf, int32_t log2_rows, int32_t row_bytes, int32_t lanes_per_row, int64_t n_threads,
+                          int32_t rows_per_group, uint32_t seed, hg_stream stream);
 
 #ifdef __cplusplus
 }

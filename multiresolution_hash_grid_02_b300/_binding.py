@@ -257,18 +257,19 @@ def hg_hash_indices(desc: GridDesc, n: int, coords, idx, stream=None, check: boo
 # hardware probes (include/hg_probe.h)
 # ---------------------------------------------------------------------------
 
-def hg_probe_l2_gather(buf, log2_rows: int, row_bytes: int, n_threads: int, rows_per_thread: int, seed: int,
-                       sink, stream=None) -> None:
+def hg_probe_l2_gather(buf, log2_rows: int, row_bytes: int, lanes_per_row: int, n_threads: int,
+                       rows_per_group: int, seed: int, sink, stream=None) -> None:
     L = lib()
-    L.hg_probe_l2_gather.argtypes = [c_vp, c_i32, c_i32, c_i64, c_i32, c_u32, c_vp, c_vp]
+    L.hg_probe_l2_gather.argtypes = [c_vp, c_i32, c_i32, c_i32, c_i64, c_i32, c_u32, c_vp, c_vp]
     L.hg_probe_l2_gather.restype = ctypes.c_int
-    _check(L.hg_probe_l2_gather(_addr(buf), log2_rows, row_bytes, n_threads, rows_per_thread, seed & 0xffffffff,
-                                _addr(sink), _stream(stream)), "hg_probe_l2_gather")
+    _check(L.hg_probe_l2_gather(_addr(buf), log2_rows, row_bytes, lanes_per_row, n_threads, rows_per_group,
+                                seed & 0xffffffff, _addr(sink), _stream(stream)), "hg_probe_l2_gather")
 
 
-def hg_probe_l2_red(buf, log2_slots: int, n_threads: int, ops_per_thread: int, seed: int, stream=None) -> None:
+def hg_probe_l2_red(buf, log2_rows: int, row_bytes: int, lanes_per_row: int, n_threads: int, rows_per_group: int,
+                    seed: int, stream=None) -> None:
     L = lib()
-    L.hg_probe_l2_red.argtypes = [c_vp, c_i32, c_i64, c_i32, c_u32, c_vp]
+    L.hg_probe_l2_red.argtypes = [c_vp, c_i32, c_i32, c_i32, c_i64, c_i32, c_u32, c_vp]
     L.hg_probe_l2_red.restype = ctypes.c_int
-    _check(L.hg_probe_l2_red(_addr(buf), log2_slots, n_threads, ops_per_thread, seed & 0xffffffff, _stream(stream)),
-           "hg_probe_l2_red")
+    _check(L.hg_probe_l2_red(_addr(buf), log2_rows, row_bytes, lanes_per_row, n_threads, rows_per_group,
+                             seed & 0xffffffff, _stream(stream)), "hg_probe_l2_red")

@@ -70,7 +70,7 @@ __device__ __forceinline__ void blend3_t(float gg, const float (&gd)[3], float g
 template <int D, int FC, bool VEC>
 __global__ void __launch_bounds__(kBlock) hermite_bwd_kernel(const __grid_constant__ BwdParams p) {
     constexpr int V = 1 << D;
-    const int l = blockIdx.y;
+    const int l = p.c.lvl[blockIdx.y];
     if (!((p.c.level_mask >> l) & 1u)) return;
     const int64_t n = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
     if (n >= p.c.n) return;
@@ -189,7 +189,7 @@ template <int D, int FC, int G>
 __global__ void __launch_bounds__(kBlock) hermite_bwd_split_kernel(const __grid_constant__ BwdParams p) {
     constexpr int V = 1 << D, S = V / G;
     static_assert(S * FC == 4, "one 16-byte chunk per lane");
-    const int l = blockIdx.y;
+    const int l = p.c.lvl[blockIdx.y];
     if (!((p.c.level_mask >> l) & 1u)) return;
     const int64_t n = (static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x) / G;
     const int lane = threadIdx.x % G;
@@ -229,6 +229,10 @@ __global__ void __launch_bounds__(kBlock) hermite_bwd_split_kernel(const __grid_
             for (int v = 0; v < V; ++v) r[v][u * FC + f] = qb[v];
         }
     }
+    // consecutive points in one cell (coherent inputs) add up before the RED
+    const unsigned active =
+        item_lanes<G>((static_cast<int64_t>(blockIdx.x) * kBlock + (threadIdx.x & ~31u)) / G, p.c.n);
+    if (!run_aggregate<D, G, V * 4>(active, c, reinterpret_cast<float(&)[V * 4]>(r))) return;
     float* row0 = p.grad.ptr[0] + l * p.grad.ls[0] + lane * 4;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
@@ -240,16 +244,116 @@ __global__ void __launch_bounds__(kBlock) hermite_bwd_split_kernel(const __grid_
     }
 }
 
+constexpr int kPrivBlock = 512;
+
+// Privatised backward for small one-to-one levels.  A CTA owns (level, a
+// chunk of points, 16-byte row part g): it accumulates its points' gradients
+// for part g of every row of the level in shared memory (shared atomics,
+// contention resolved on chip), then adds the part into the gradient table
+// with one red.global.add.v4.f32 per row that received anything.  Without it
+// the coarsest levels -- a few hundred to a few thousand rows hit by millions
+// of points -- serialise on the same L2 addresses.  Each contribution is the
+// split kernel's (part g plays lane g).
+template <int D, int FC, int G>
+__global__ void __launch_bounds__(kPrivBlock) hermite_bwd_priv_kernel(const __grid_constant__ BwdParams p) {
+    constexpr int V = 1 << D, S = V / G;
+    static_assert(S * FC == 4, "one 16-byte part per row");
+    extern __shared__ float4 sacc[];
+    const int l = p.priv.lvl[blockIdx.y];
+    const uint32_t rows = p.priv.rows[blockIdx.y];
+    const int part = blockIdx.z;
+    for (uint32_t i = threadIdx.x; i < rows; i += kPrivBlock) sacc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncthreads();
+    const int F = p.c.F;
+    const Level& lv = p.c.lv[l];
+    float* sf = reinterpret_cast<float*>(sacc);
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * p.priv.chunk;
+    const int64_t n1 = min(n0 + p.priv.chunk, p.c.n);
+    for (int64_t n = n0 + threadIdx.x; n < n1; n += kPrivBlock) {
+        uint32_t c[D];
+        float t[D];
+        Basis1 B[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) {
+            locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
+            B[i] = hermite_basis(t[i], lv);
+        }
+        float gg[FC], gl[FC], gd[FC][3];
+#pragma unroll
+        for (int f = 0; f < FC; ++f) {
+            const int64_t lf = static_cast<int64_t>(l) * F + f;
+            gg[f] = p.g_gamma ? __ldg(p.g_gamma + n * p.c.sn + lf * p.c.sf) : 0.f;
+            gl[f] = p.g_lap ? __ldg(p.g_lap + n * p.c.sn + lf * p.c.sf) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+                gd[f][j] = (p.g_dgamma && j < D) ? __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf) : 0.f;
+        }
+        float r[V][4];
+#pragma unroll
+        for (int u = 0; u < S; ++u) {
+            const AxisW W0 = unit_axis<D, G>(B[0], part, u, 0);
+            const AxisW W1 = unit_axis<D, G>(B[1], part, u, 1);
+            const AxisW W2 = unit_axis<D, G>(B[D - 1], part, u, D - 1);
+#pragma unroll
+            for (int f = 0; f < FC; ++f) {
+                float qb[V];
+                unit_blend_t<D>(gg[f], gd[f], gl[f], W0, W1, W2, qb);
+#pragma unroll
+                for (int v = 0; v < V; ++v) r[v][u * FC + f] = qb[v];
+            }
+        }
+        const unsigned active = item_lanes<1>(n - (threadIdx.x & 31), n1);
+        if (run_aggregate<D, 1, V * 4>(active, c, reinterpret_cast<float(&)[V * 4]>(r))) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                uint32_t g[D];
+#pragma unroll
+                for (int i = 0; i < D; ++i) g[i] = c[i] + ((v >> i) & 1u);
+                float* a = sf + 4 * vertex_index<D>(g, lv, true, 0u);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) atomicAdd(a + j, r[v][j]);
+            }
+        }
+    }
+    __syncthreads();
+    float* row0 = p.grad.ptr[0] + l * p.grad.ls[0] + part * 4;
+    for (uint32_t i = threadIdx.x; i < rows; i += kPrivBlock) {
+        const float4 a = sacc[i];
+        if (a.x != 0.f || a.y != 0.f || a.z != 0.f || a.w != 0.f)
+            red_add_v4(row0 + static_cast<int64_t>(i) * p.grad.rs[0], a.x, a.y, a.z, a.w);
+    }
+}
+
+template <int D, int FC, int G>
+cudaError_t launch_priv(const BwdParams& p, cudaStream_t s) {
+    if (p.priv.n == 0) return cudaSuccess;
+    if (p.priv.smem_bytes > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(hermite_bwd_priv_kernel<D, FC, G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, p.priv.smem_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid(static_cast<unsigned>((p.c.n + p.priv.chunk - 1) / p.priv.chunk), static_cast<unsigned>(p.priv.n), G);
+    hermite_bwd_priv_kernel<D, FC, G><<<grid, kPrivBlock, p.priv.smem_bytes, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <int D, int FC, int G>
 cudaError_t launch_split(const BwdParams& p, cudaStream_t s) {
-    dim3 grid(static_cast<unsigned>((p.c.n * G + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
+    cudaError_t e = launch_priv<D, FC, G>(p, s);
+    if (e != cudaSuccess || p.c.nlvl == 0) return e;
+    dim3 grid(static_cast<unsigned>((p.c.n * G + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
     hermite_bwd_split_kernel<D, FC, G><<<grid, kBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
 
 template <int D, int FC, bool VEC>
 cudaError_t launch(const BwdParams& p, cudaStream_t s) {
-    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
+    if (VEC && D == 2 && FC == 1) {  // 16-byte rows: one part per row
+        cudaError_t e = launch_priv<2, 1, 1>(p, s);
+        if (e != cudaSuccess) return e;
+    }
+    if (p.c.nlvl == 0) return cudaSuccess;
+    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
     hermite_bwd_kernel<D, FC, VEC><<<grid, kBlock, 0, s>>>(p);
     return cudaGetLastError();
 }

@@ -89,7 +89,7 @@ __device__ __forceinline__ void blend3(const float (&q)[8][8], const Basis1& b0,
 template <int D, int FC, typename TT, bool VEC>
 __global__ void __launch_bounds__(kBlock) hermite_fwd_kernel(const __grid_constant__ FwdParams p) {
     constexpr int V = 1 << D;
-    const int l = blockIdx.y;
+    const int l = p.c.lvl[blockIdx.y];
     const int64_t n = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
     if (n >= p.c.n) return;
     const int F = p.c.F;
@@ -170,45 +170,73 @@ __global__ void __launch_bounds__(kBlock) hermite_fwd_kernel(const __grid_consta
     }
 }
 
-// Contribution of one packed slot (multi-index alpha, weights W0..W2 picked
-// for its per-axis orders) of one feature to the 3D outputs; c[v] holds that
-// slot's coefficient at corner v = v0 + 2 v1 + 4 v2.  The same separable
-// order as blend3, restricted to one alpha.
-__device__ __forceinline__ void unit_blend3(const float (&c)[8], const AxisW& W0, const AxisW& W1, const AxisW& W2,
-                                            float (&o)[5]) {
+// Contribution of one packed slot (multi-index alpha, with the weights
+// W0..W2 of its per-axis orders) to the 3D outputs, for both features at
+// once: c[v] is the slot's (feature 0, feature 1) coefficient pair at corner
+// v = v0 + 2 v1 + 4 v2; o[] accumulates (gamma, d/dx0, d/dx1, d/dx2, lap)
+// pairs.  The same separable order as blend3, restricted to one alpha.
+__device__ __forceinline__ void unit_blend3_f2(const uint64_t (&c)[8], const AxisW2& W0, const AxisW2& W1,
+                                               const AxisW2& W2, uint64_t (&o)[5]) {
 #pragma unroll
     for (int v2 = 0; v2 < 2; ++v2) {
-        float A = 0.f, B = 0.f, C = 0.f, Dl = 0.f;
+        uint64_t A, B, C, Dl;
 #pragma unroll
         for (int v1 = 0; v1 < 2; ++v1) {
-            const float c0 = c[2 * v1 + 4 * v2], c1 = c[1 + 2 * v1 + 4 * v2];
-            const float s = fmaf(c0, W0.w[0], c1 * W0.w[1]);
-            const float s1 = fmaf(c0, W0.d1[0], c1 * W0.d1[1]);
-            const float s2 = fmaf(c0, W0.d2[0], c1 * W0.d2[1]);
-            A = fmaf(s, W1.w[v1], A);
-            B = fmaf(s1, W1.w[v1], B);
-            C = fmaf(s, W1.d1[v1], C);
-            Dl = fmaf(s2, W1.w[v1], Dl);
-            Dl = fmaf(s, W1.d2[v1], Dl);
+            const uint64_t c0 = c[2 * v1 + 4 * v2], c1 = c[1 + 2 * v1 + 4 * v2];
+            const uint64_t s = f2_fma(c0, W0.w[0], f2_mul(c1, W0.w[1]));
+            const uint64_t s1 = f2_fma(c0, W0.d1[0], f2_mul(c1, W0.d1[1]));
+            const uint64_t s2 = f2_fma(c0, W0.d2[0], f2_mul(c1, W0.d2[1]));
+            if (v1 == 0) {
+                A = f2_mul(s, W1.w[0]);
+                B = f2_mul(s1, W1.w[0]);
+                C = f2_mul(s, W1.d1[0]);
+                Dl = f2_fma(s, W1.d2[0], f2_mul(s2, W1.w[0]));
+            } else {
+                A = f2_fma(s, W1.w[1], A);
+                B = f2_fma(s1, W1.w[1], B);
+                C = f2_fma(s, W1.d1[1], C);
+                Dl = f2_fma(s2, W1.w[1], Dl);
+                Dl = f2_fma(s, W1.d2[1], Dl);
+            }
         }
-        o[0] = fmaf(A, W2.w[v2], o[0]);
-        o[1] = fmaf(B, W2.w[v2], o[1]);
-        o[2] = fmaf(C, W2.w[v2], o[2]);
-        o[3] = fmaf(A, W2.d1[v2], o[3]);
-        o[4] = fmaf(Dl, W2.w[v2], o[4]);
-        o[4] = fmaf(A, W2.d2[v2], o[4]);
+        o[0] = f2_fma(A, W2.w[v2], o[0]);
+        o[1] = f2_fma(B, W2.w[v2], o[1]);
+        o[2] = f2_fma(C, W2.w[v2], o[2]);
+        o[3] = f2_fma(A, W2.d1[v2], o[3]);
+        o[4] = f2_fma(Dl, W2.w[v2], o[4]);
+        o[4] = f2_fma(A, W2.d2[v2], o[4]);
     }
 }
 
-// Lane-pair split for 64-byte packed rows (3D, F = 2, fp32).  Lane h of a
-// pair reads the 32-byte half h of every corner row with one 256-bit load, so
+// Half-row h of a packed 3D F = 2 row (slots 4h..4h+3, both features) as
+// four (feature 0, feature 1) pairs: one 256-bit load for fp32 rows, one
+// 128-bit load widened exactly for fp16 rows.
+template <typename TT>
+__device__ __forceinline__ void load_half_row(const TT* e, uint64_t (&q)[4]) {
+    if constexpr (sizeof(TT) == 4) {
+        ld_nc_v4b64(e, q);
+    } else {
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(e));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            q[i] = f2_pack(f.x, f.y);
+        }
+    }
+}
+
+// Lane-pair split for packed 3D F = 2 rows (64 bytes fp32, 32 bytes fp16).
+// Lane h of a pair reads the half h of every corner row with one load, so
 // one warp instruction covers whole rows (one L1 wavefront per row), and
-// blends the four slots of that half for both features; the encoding is
-// linear in theta, so the pair's partial outputs add up.  A reduce-scatter
-// leaves feature h's outputs on lane h, which stores them.
+// blends the four slots of that half.  The two features travel as packed
+// pairs through f32x2 FMAs (the weights are shared).  The encoding is linear
+// in theta, so the pair's partial outputs add up: a reduce-scatter leaves
+// feature h's outputs on lane h, which stores them.
+template <typename TT>
 __global__ void __launch_bounds__(kBlock) hermite_fwd_pair3_kernel(const __grid_constant__ FwdParams p) {
-    constexpr int D = 3, V = 8, G = 2, S = 4, FC = 2;
-    const int l = blockIdx.y;
+    constexpr int D = 3, V = 8, G = 2, S = 4;
+    const int l = p.c.lvl[blockIdx.y];
     const int64_t n = (static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x) >> 1;
     const int lane = threadIdx.x & 1;
     if (n >= p.c.n) return;  // both lanes of a pair share n
@@ -233,39 +261,37 @@ __global__ void __launch_bounds__(kBlock) hermite_fwd_pair3_kernel(const __grid_
         locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
         B[i] = hermite_basis(t[i], lv);
     }
-    const float* base = static_cast<const float*>(p.tab.ptr[0]) + l * p.tab.ls[0] + lane * (S * FC);
-    uint32_t q[V][8];
+    // half-row h of corner v: 4 slots x (f0, f1) = four 64-bit pairs
+    const TT* base = static_cast<const TT*>(p.tab.ptr[0]) + l * p.tab.ls[0] + lane * (S * 2);
+    uint64_t q[V][S];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const uint32_t g[D] = {c[0] + (v & 1u), c[1] + ((v >> 1) & 1u), c[2] + ((v >> 2) & 1u)};
         const uint32_t id = vertex_index<D>(g, lv, lv.dense & 1u, p.c.tmask[0]);
-        ld_nc_v8(base + static_cast<int64_t>(id) * p.tab.rs[0], q[v]);
+        load_half_row<TT>(base + static_cast<int64_t>(id) * p.tab.rs[0], q[v]);
     }
-    float o[FC][5];
+    uint64_t o[5];
 #pragma unroll
-    for (int f = 0; f < FC; ++f)
-#pragma unroll
-        for (int k = 0; k < 5; ++k) o[f][k] = 0.f;
+    for (int k = 0; k < 5; ++k) o[k] = 0ull;  // (+0.0f, +0.0f)
 #pragma unroll
     for (int u = 0; u < S; ++u) {
-        const AxisW W0 = unit_axis<D, G>(B[0], lane, u, 0);
-        const AxisW W1 = unit_axis<D, G>(B[1], lane, u, 1);
-        const AxisW W2 = unit_axis<D, G>(B[2], lane, u, 2);
+        const AxisW2 W0 = axis_dup(unit_axis<D, G>(B[0], lane, u, 0));
+        const AxisW2 W1 = axis_dup(unit_axis<D, G>(B[1], lane, u, 1));
+        const AxisW2 W2 = axis_dup(unit_axis<D, G>(B[2], lane, u, 2));
+        uint64_t cv[V];
 #pragma unroll
-        for (int f = 0; f < FC; ++f) {
-            float cv[V];
-#pragma unroll
-            for (int v = 0; v < V; ++v) cv[v] = __uint_as_float(q[v][u * FC + f]);
-            unit_blend3(cv, W0, W1, W2, o[f]);
-        }
+        for (int v = 0; v < V; ++v) cv[v] = q[v][u];
+        unit_blend3_f2(cv, W0, W1, W2, o);
     }
     // reduce-scatter across the pair: lane h keeps feature h
     const unsigned mask = __activemask();
     float r[5];
 #pragma unroll
     for (int k = 0; k < 5; ++k) {
-        const float mine = lane ? o[1][k] : o[0][k];
-        const float other = lane ? o[0][k] : o[1][k];
+        float x, y;
+        f2_unpack(o[k], x, y);
+        const float mine = lane ? y : x;
+        const float other = lane ? x : y;
         r[k] = mine + __shfl_xor_sync(mask, other, 1);
     }
     __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, r[0]);
@@ -278,7 +304,7 @@ __global__ void __launch_bounds__(kBlock) hermite_fwd_pair3_kernel(const __grid_
 
 template <int D, int FC, typename TT, bool VEC>
 cudaError_t launch(const FwdParams& p, cudaStream_t s) {
-    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
+    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
     hermite_fwd_kernel<D, FC, TT, VEC><<<grid, kBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
@@ -297,9 +323,12 @@ cudaError_t pick_fc(const FwdParams& p, int fc, bool vec, cudaStream_t s) {
 
 int launch_hermite_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (vec && p.c.d == 3 && p.c.F == 2 && dtype == HG_F32) {
-        dim3 grid(static_cast<unsigned>((p.c.n * 2 + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
-        hermite_fwd_pair3_kernel<<<grid, kBlock, 0, s>>>(p);
+    if (vec && p.c.d == 3 && p.c.F == 2) {
+        dim3 grid(static_cast<unsigned>((p.c.n * 2 + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
+        if (dtype == HG_F16)
+            hermite_fwd_pair3_kernel<__half><<<grid, kBlock, 0, s>>>(p);
+        else
+            hermite_fwd_pair3_kernel<float><<<grid, kBlock, 0, s>>>(p);
         return cudaGetLastError();
     }
     if (p.c.d == 2) return dtype == HG_F16 ? pick_fc<2, __half>(p, fc, vec, s) : pick_fc<2, float>(p, fc, vec, s);

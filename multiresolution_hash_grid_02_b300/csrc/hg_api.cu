@@ -220,6 +220,84 @@ bool is_packed(const hg_grid_desc* desc, const void* const* ptrs, const int64_t*
     return true;
 }
 
+// Launches cover every level (the forwards write zeros for inactive ones).
+void all_levels(hg::Common& c) {
+    c.nlvl = c.L;
+    for (int l = 0; l < c.L; ++l) c.lvl[l] = static_cast<uint8_t>(l);
+}
+
+// Streaming multiprocessors of the current device (148 if it cannot be read).
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+        return sms;
+    return 148;
+}
+
+// Shared memory per CTA of the privatised backward, and the largest whole
+// level (all parts of its rows) the Hermite backward privatises.  Measured on
+// B300: a d-linear level of up to ~100 KB gains several times over direct
+// REDs (a few hundred hot rows serialise in L2), while Hermite levels gain
+// only when tiny -- 3D levels of hundreds of KB run at the full RED rate
+// directly, and the shared-memory pass then costs more than it saves.
+constexpr int64_t kPrivMaxBytes = 160 * 1024;
+constexpr int64_t kHermitePrivLevelBytes = 32 * 1024;
+
+// Splits the active levels of a backward between the privatised kernel
+// (one-to-one levels whose rows -- part_bytes per row and CTA -- fit in
+// shared memory, whose whole size is at most level_limit, and which receive
+// many contributions per row) and the direct kernel.  parts = CTAs sharing a
+// row (16-byte parts of a Hermite row).
+void plan_backward(hg::BwdParams& p, bool allow, int64_t part_bytes, int parts, int64_t level_limit) {
+    hg::Common& c = p.c;
+    const int V = 1 << c.d;
+    const int64_t target = 2 * static_cast<int64_t>(sm_count());
+    bool cand[HG_MAX_LEVELS] = {};
+    uint64_t rows[HG_MAX_LEVELS] = {};
+    int ncand = 0;
+    for (int l = 0; l < c.L; ++l) {
+        if (!((c.level_mask >> l) & 1u) || !allow || !(c.lv[l].dense & 1u)) continue;
+        rows[l] = 1;
+        for (int i = 0; i < c.d; ++i) rows[l] *= c.lv[l].side;
+        if (static_cast<int64_t>(rows[l]) * part_bytes <= kPrivMaxBytes &&
+            static_cast<int64_t>(rows[l]) * part_bytes * parts <= level_limit) {
+            cand[l] = true;
+            ++ncand;
+        }
+    }
+    // each privatised CTA flushes all its rows: keep a level only if its
+    // contributions outnumber the flushed rows severalfold
+    int64_t chunks = 1;
+    for (int pass = 0; pass < 2 && ncand > 0; ++pass) {
+        chunks = (target + static_cast<int64_t>(ncand) * parts - 1) / (static_cast<int64_t>(ncand) * parts);
+        if (chunks < 1) chunks = 1;
+        ncand = 0;
+        for (int l = 0; l < c.L; ++l) {
+            if (!cand[l]) continue;
+            if (c.n * V < 4 * static_cast<int64_t>(rows[l]) * chunks) cand[l] = false;
+            else ++ncand;
+        }
+    }
+    c.nlvl = 0;
+    p.priv.n = 0;
+    p.priv.smem_bytes = 0;
+    for (int l = 0; l < c.L; ++l) {
+        if (!((c.level_mask >> l) & 1u)) continue;
+        if (cand[l]) {
+            p.priv.lvl[p.priv.n] = static_cast<uint8_t>(l);
+            p.priv.rows[p.priv.n] = static_cast<uint32_t>(rows[l]);
+            const int64_t b = static_cast<int64_t>(rows[l]) * part_bytes;
+            if (b > p.priv.smem_bytes) p.priv.smem_bytes = static_cast<int32_t>(b);
+            ++p.priv.n;
+        } else {
+            c.lvl[c.nlvl++] = static_cast<uint8_t>(l);
+        }
+    }
+    p.priv.chunk = (c.n + chunks - 1) / chunks;
+    if (p.priv.chunk < 1) p.priv.chunk = 1;
+}
+
 hg_status launch_status(int err, const char* what) {
     if (err != cudaSuccess)
         return fail(HG_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(static_cast<cudaError_t>(err)));
@@ -293,6 +371,7 @@ hg_status hg_encode_fwd(const hg_grid_desc* desc, int64_t n, const float* coords
         const size_t al = row < 32 ? row : 32;  // 256-bit loads of 32-byte rows / half-rows
         vec = aligned(ptrs[0], al) && (static_cast<size_t>(ls[0]) * es) % al == 0;
     }
+    all_levels(p.c);
     return launch_status(hg::launch_hermite_fwd(p, fc, vec, desc->dtype, stream), "hermite forward");
 }
 
@@ -332,6 +411,7 @@ hg_status hg_encode_bwd(const hg_grid_desc* desc, int64_t n, const float* coords
     const int fc = (F % 2 == 0) ? 2 : 1;
     bool vec = fc == F && is_packed(desc, ptrs, ls, rs, 4);
     if (vec) vec = aligned(ptrs[0], 16) && (static_cast<size_t>(ls[0]) * 4) % 16 == 0 && (V * F) % 4 == 0;
+    plan_backward(p, vec, 16, vec ? V * F / 4 : 1, kHermitePrivLevelBytes);
     return launch_status(hg::launch_hermite_bwd(p, fc, vec, stream), "hermite backward");
 }
 
@@ -361,6 +441,7 @@ hg_status hg_linear_fwd(const hg_grid_desc* desc, int64_t n, const float* coords
     p.lap = nullptr;
     const int fc = (F % 2 == 0) ? 2 : 1;
     const bool vec = fc == 2 && aligned(table->ptr, 2 * es) && table->row_stride % 2 == 0 && table->level_stride % 2 == 0;
+    all_levels(p.c);
     return launch_status(hg::launch_linear_fwd(p, fc, vec, desc->dtype, stream), "linear forward");
 }
 
@@ -390,6 +471,7 @@ hg_status hg_linear_bwd(const hg_grid_desc* desc, int64_t n, const float* coords
     p.g_lap = nullptr;
     const int fc = (F % 2 == 0) ? 2 : 1;
     const bool vec = fc == 2 && aligned(grad->ptr, 8) && grad->row_stride % 2 == 0 && grad->level_stride % 2 == 0;
+    plan_backward(p, true, static_cast<int64_t>(F) * 4, 1, kPrivMaxBytes);
     return launch_status(hg::launch_linear_bwd(p, fc, vec, stream), "linear backward");
 }
 
@@ -404,6 +486,7 @@ hg_status hg_hash_indices(const hg_grid_desc* desc, int64_t n, const float* coor
     if (!aligned(coords, 4) || !aligned(idx, 4)) return fail(HG_ERR_INVALID_ARG, "coords and idx must be 4-byte aligned");
     p.coords = coords;
     p.idx = idx;
+    all_levels(p.c);
     return launch_status(hg::launch_indices(p, stream), "vertex indices");
 }
 

@@ -218,3 +218,105 @@ __device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t (&r)[8]) {
 }
 
 }  // namespace hg
+
+namespace hg {
+
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic): one 64-bit register holds the
+// same quantity for features 0 (low half) and 1 (high half).  Each f32x2
+// instruction is exactly two round-to-nearest fp32 operations.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_pack(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_dup(float x) { return f2_pack(x, x); }
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& x, float& y) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// One axis' weights broadcast to both halves of a pair.
+struct AxisW2 {
+    uint64_t w[2], d1[2], d2[2];
+};
+
+__device__ __forceinline__ AxisW2 axis_dup(const AxisW& a) {
+    AxisW2 r;
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+        r.w[v] = f2_dup(a.w[v]);
+        r.d1[v] = f2_dup(a.d1[v]);
+        r.d2[v] = f2_dup(a.d2[v]);
+    }
+    return r;
+}
+
+// 256-bit read-only load as four 64-bit words (32-byte aligned).
+__device__ __forceinline__ void ld_nc_v4b64(const void* p, uint64_t (&r)[4]) {
+    asm("ld.global.nc.v4.b64 {%0,%1,%2,%3}, [%4];" : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]) : "l"(p));
+}
+
+}  // namespace hg
+
+namespace hg {
+
+// Warp-level aggregation of scatter contributions for spatially coherent
+// points.  Items occupy G consecutive lanes each (lane = item * G + part);
+// consecutive items of the warp whose cells are equal form a run.  The values
+// x[] of every lane are summed over its run (same part) into the run's first
+// item, whose lanes return true and issue the reductions; the other lanes
+// return false.  When no run is longer than one item (random points), the
+// exchange is skipped for the whole warp.  `active` is the warp's lanes that
+// hold an item -- the low lanes (items beyond n sit at the end); every lane in
+// it must call this function.
+template <int D, int G, int NV>
+__device__ __forceinline__ bool run_aggregate(unsigned active, const uint32_t (&c)[D], float (&x)[NV]) {
+    const int wl = threadIdx.x & 31;
+    bool same = wl >= G;
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+        const uint32_t prev = __shfl_up_sync(active, c[i], G);
+        same = same && prev == c[i];
+    }
+    const bool head = !same;
+    const unsigned heads = __ballot_sync(active, head);
+    if (heads == active) return true;
+    // my run ends before the first head in a later item (or the last active lane)
+    const int last_of_item = wl | (G - 1);
+    const unsigned later = last_of_item >= 31 ? 0u : heads & ~((2u << last_of_item) - 1u);
+    const int end = later ? __ffs(later) - 1 : 32 - __clz(active);
+#pragma unroll
+    for (int off = G; off < 32; off <<= 1) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const float y = __shfl_down_sync(active, x[k], off);
+            if (wl + off < end) x[k] += y;
+        }
+    }
+    return head;
+}
+
+}  // namespace hg
+
+namespace hg {
+
+// Lanes of the calling warp that hold one of the n items when items are
+// numbered first_item + lane / G from lane 0 of the warp.
+template <int G>
+__device__ __forceinline__ unsigned item_lanes(int64_t first_item, int64_t n) {
+    const int64_t left = (n - first_item) * G;
+    return left >= 32 ? 0xffffffffu : (left <= 0 ? 0u : ((1u << left) - 1u));
+}
+
+}  // namespace hg

@@ -30,6 +30,19 @@ struct Common {
     //   dgamma:      n*dsn + j*dsj + (l*F + f)*dsf
     int64_t sn, sf, dsn, dsj, dsf;
     Level lv[HG_MAX_LEVELS];
+    // levels this launch covers: blockIdx.y -> level lvl[blockIdx.y], nlvl of them
+    int32_t nlvl;
+    uint8_t lvl[HG_MAX_LEVELS];
+};
+
+// Backward levels accumulated in shared memory first (privatised): small
+// one-to-one levels whose gradient rows fit one CTA's shared memory.
+struct Priv {
+    int32_t n;                       // number of privatised levels (grid.y)
+    uint8_t lvl[HG_MAX_LEVELS];      // their level indices
+    uint32_t rows[HG_MAX_LEVELS];    // (N_l + 1)^d rows each
+    int64_t chunk;                   // points per CTA (grid.x = ceil(n / chunk))
+    int32_t smem_bytes;              // dynamic shared memory per CTA
 };
 
 struct Tables {
@@ -53,6 +66,7 @@ struct FwdParams {
 
 struct BwdParams {
     Common c;
+    Priv priv;
     Grads grad;
     const float* coords;
     const float* g_gamma;

@@ -26,7 +26,7 @@ __device__ __forceinline__ float corner_weight(const float (&t)[D], int v) {
 template <int D, int FC, typename TT, bool VEC>
 __global__ void __launch_bounds__(kBlock) linear_fwd_kernel(const __grid_constant__ FwdParams p) {
     constexpr int V = 1 << D;
-    const int l = blockIdx.y;
+    const int l = p.c.lvl[blockIdx.y];
     const int64_t n = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
     if (n >= p.c.n) return;
     const int F = p.c.F;
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kBlock) linear_fwd_kernel(const __grid_constan
 template <int D, int FC, bool VEC>
 __global__ void __launch_bounds__(kBlock) linear_bwd_kernel(const __grid_constant__ BwdParams p) {
     constexpr int V = 1 << D;
-    const int l = blockIdx.y;
+    const int l = p.c.lvl[blockIdx.y];
     if (!((p.c.level_mask >> l) & 1u)) return;
     const int64_t n = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
     if (n >= p.c.n) return;
@@ -121,8 +121,72 @@ __global__ void __launch_bounds__(kBlock) linear_bwd_kernel(const __grid_constan
     }
 }
 
+constexpr int kPrivBlock = 512;
+
+// Privatised d-linear backward for small one-to-one levels (see the Hermite
+// version): a CTA accumulates a chunk of points into a shared-memory copy of
+// the level's gradient rows, then adds each row that received anything into
+// the table.
+template <int D, int FC>
+__global__ void __launch_bounds__(kPrivBlock) linear_bwd_priv_kernel(const __grid_constant__ BwdParams p) {
+    constexpr int V = 1 << D;
+    extern __shared__ float sacc[];
+    const int l = p.priv.lvl[blockIdx.y];
+    const uint32_t rows = p.priv.rows[blockIdx.y];
+    const int F = p.c.F;
+    const uint32_t vals = rows * static_cast<uint32_t>(F);
+    for (uint32_t i = threadIdx.x; i < vals; i += kPrivBlock) sacc[i] = 0.f;
+    __syncthreads();
+    const Level& lv = p.c.lv[l];
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * p.priv.chunk;
+    const int64_t n1 = min(n0 + p.priv.chunk, p.c.n);
+    for (int64_t n = n0 + threadIdx.x; n < n1; n += kPrivBlock) {
+        uint32_t c[D];
+        float t[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
+        for (int f0 = 0; f0 < F; f0 += FC) {
+            float up[FC];
+#pragma unroll
+            for (int f = 0; f < FC; ++f) {
+                const int64_t lf = static_cast<int64_t>(l) * F + f0 + f;
+                up[f] = __ldg(p.g_gamma + n * p.c.sn + lf * p.c.sf);
+            }
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                uint32_t g[D];
+#pragma unroll
+                for (int i = 0; i < D; ++i) g[i] = c[i] + ((v >> i) & 1u);
+                const float w = corner_weight<D>(t, v);
+                float* a = sacc + vertex_index<D>(g, lv, true, 0u) * F + f0;
+#pragma unroll
+                for (int f = 0; f < FC; ++f) atomicAdd(a + f, w * up[f]);
+            }
+        }
+    }
+    __syncthreads();
+    float* base = p.grad.ptr[0] + l * p.grad.ls[0];
+    for (uint32_t i = threadIdx.x; i < vals; i += kPrivBlock) {
+        const float a = sacc[i];
+        if (a != 0.f) red_add_f32(base + static_cast<int64_t>(i / F) * p.grad.rs[0] + i % F, a);
+    }
+}
+
+template <int D, int FC>
+cudaError_t launch_priv(const BwdParams& p, cudaStream_t s) {
+    if (p.priv.n == 0) return cudaSuccess;
+    if (p.priv.smem_bytes > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(linear_bwd_priv_kernel<D, FC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             p.priv.smem_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid(static_cast<unsigned>((p.c.n + p.priv.chunk - 1) / p.priv.chunk), static_cast<unsigned>(p.priv.n));
+    linear_bwd_priv_kernel<D, FC><<<grid, kPrivBlock, p.priv.smem_bytes, s>>>(p);
+    return cudaGetLastError();
+}
+
 __global__ void __launch_bounds__(kBlock) indices_kernel(const __grid_constant__ IdxParams p) {
-    const int l = blockIdx.y;
+    const int l = p.c.lvl[blockIdx.y];
     const int64_t n = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
     if (n >= p.c.n) return;
     const int d = p.c.d;
@@ -149,7 +213,7 @@ __global__ void __launch_bounds__(kBlock) indices_kernel(const __grid_constant__
 
 template <int D, int FC, typename TT, bool VEC>
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t s) {
-    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
+    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
     linear_fwd_kernel<D, FC, TT, VEC><<<grid, kBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
@@ -162,7 +226,9 @@ cudaError_t pick_fwd(const FwdParams& p, int fc, bool vec, cudaStream_t s) {
 
 template <int D, int FC, bool VEC>
 cudaError_t launch_bwd(const BwdParams& p, cudaStream_t s) {
-    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
+    cudaError_t e = launch_priv<D, FC>(p, s);
+    if (e != cudaSuccess || p.c.nlvl == 0) return e;
+    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
     linear_bwd_kernel<D, FC, VEC><<<grid, kBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
@@ -188,7 +254,7 @@ int launch_linear_bwd(const BwdParams& p, int fc, bool vec, void* stream) {
 
 int launch_indices(const IdxParams& p, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.L));
+    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
     indices_kernel<<<grid, kBlock, 0, s>>>(p);
     return cudaGetLastError();
 }

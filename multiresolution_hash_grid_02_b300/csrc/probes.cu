@@ -1,6 +1,7 @@
 // Hardware probes for the roofline of the encoding kernels (declared in
-// include/hg_probe.h): random 16-byte-vector row gathers from, and random
-// 16-byte vector REDs into, a buffer small enough to stay in L2.
+// include/hg_probe.h): random whole-row gathers from, and random 16-byte
+// vector REDs into, a buffer small enough to stay in L2, with the same
+// lanes-per-row split the encoding kernels use.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,73 +22,118 @@ __device__ __forceinline__ uint32_t mix(uint32_t x) {
     return x;
 }
 
-template <int ROW>
-__global__ void __launch_bounds__(kBlock) gather_kernel(const uint4* __restrict__ buf, uint32_t row_mask,
-                                                        int rows_per_thread, uint32_t seed, float* sink,
+// ROW bytes per row, LPR lanes per row; each lane reads CH = ROW/LPR bytes.
+template <int ROW, int LPR>
+__global__ void __launch_bounds__(kBlock) gather_kernel(const char* __restrict__ buf, uint32_t row_mask,
+                                                        int rows_per_group, uint32_t seed, float* sink,
                                                         int64_t n_threads) {
-    constexpr int Q = ROW / 16;
-    const uint32_t tid = blockIdx.x * kBlock + threadIdx.x;
+    constexpr int CH = ROW / LPR;
+    constexpr int W = CH / 4;  // 32-bit words per lane per row
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
     if (tid >= n_threads) return;
+    const uint32_t grp = static_cast<uint32_t>(tid / LPR), lane = static_cast<uint32_t>(tid % LPR);
     uint32_t acc = 0;
-    for (int r = 0; r < rows_per_thread; r += 8) {
-        uint4 v[8][Q];
+    for (int r = 0; r < rows_per_group; r += 8) {
+        uint32_t v[8][W];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const uint32_t row = mix(tid * 0x9e3779b9u + (r + j) * 0x85ebca6bu + seed) & row_mask;
+            const uint32_t row = mix(grp * 0x9e3779b9u + (r + j) * 0x85ebca6bu + seed) & row_mask;
+            const char* p = buf + static_cast<size_t>(row) * ROW + lane * CH;
+            if constexpr (CH % 32 == 0) {
 #pragma unroll
-            for (int q = 0; q < Q; ++q) v[j][q] = __ldg(buf + static_cast<size_t>(row) * Q + q);
+                for (int h = 0; h < CH / 32; ++h) {
+                    uint32_t q[8];
+                    hg::ld_nc_v8(p + 32 * h, q);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[j][8 * h + i] = q[i];
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < CH / 16; ++h) {
+                    const uint4 q = __ldg(reinterpret_cast<const uint4*>(p + 16 * h));
+                    v[j][4 * h + 0] = q.x;
+                    v[j][4 * h + 1] = q.y;
+                    v[j][4 * h + 2] = q.z;
+                    v[j][4 * h + 3] = q.w;
+                }
+            }
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j)
 #pragma unroll
-            for (int q = 0; q < Q; ++q) acc ^= v[j][q].x ^ v[j][q].y ^ v[j][q].z ^ v[j][q].w;
+            for (int i = 0; i < W; ++i) acc ^= v[j][i];
     }
     sink[tid] = __uint_as_float(acc & 0x007fffffu);
 }
 
-__global__ void __launch_bounds__(kBlock) red_kernel(float* buf, uint32_t slot_mask, int ops_per_thread,
-                                                     uint32_t seed, int64_t n_threads) {
-    const uint32_t tid = blockIdx.x * kBlock + threadIdx.x;
+template <int ROW, int LPR>
+__global__ void __launch_bounds__(kBlock) red_kernel(float* buf, uint32_t row_mask, int rows_per_group, uint32_t seed,
+                                                     int64_t n_threads) {
+    constexpr int CH = ROW / LPR;  // bytes per lane, a multiple of 16
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
     if (tid >= n_threads) return;
-    for (int r = 0; r < ops_per_thread; ++r) {
-        const uint32_t slot = mix(tid * 0x9e3779b9u + r * 0x85ebca6bu + seed) & slot_mask;
-        hg::red_add_v4(buf + static_cast<size_t>(slot) * 4, 1.f, 1.f, 1.f, 1.f);
+    const uint32_t grp = static_cast<uint32_t>(tid / LPR), lane = static_cast<uint32_t>(tid % LPR);
+    for (int r = 0; r < rows_per_group; ++r) {
+        const uint32_t row = mix(grp * 0x9e3779b9u + r * 0x85ebca6bu + seed) & row_mask;
+        float* p = buf + static_cast<size_t>(row) * (ROW / 4) + lane * (CH / 4);
+#pragma unroll
+        for (int h = 0; h < CH / 16; ++h) hg::red_add_v4(p + 4 * h, 1.f, 1.f, 1.f, 1.f);
     }
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+template <int ROW, int LPR>
+cudaError_t launch_gather(const void* buf, uint32_t mask, int rpg, uint32_t seed, float* sink, int64_t nt,
+                          cudaStream_t s) {
+    const unsigned blocks = static_cast<unsigned>((nt + kBlock - 1) / kBlock);
+    gather_kernel<ROW, LPR><<<blocks, kBlock, 0, s>>>(static_cast<const char*>(buf), mask, rpg, seed, sink, nt);
+    return cudaGetLastError();
+}
+
+template <int ROW, int LPR>
+cudaError_t launch_red(float* buf, uint32_t mask, int rpg, uint32_t seed, int64_t nt, cudaStream_t s) {
+    const unsigned blocks = static_cast<unsigned>((nt + kBlock - 1) / kBlock);
+    red_kernel<ROW, LPR><<<blocks, kBlock, 0, s>>>(buf, mask, rpg, seed, nt);
+    return cudaGetLastError();
+}
 
 }  // namespace
 
 extern "C" {
 
-hg_status hg_probe_l2_gather(const void* buf, int32_t log2_rows, int32_t row_bytes, int64_t n_threads,
-                             int32_t rows_per_thread, uint32_t seed, float* sink, hg_stream stream) {
-    if (!buf || !sink || !aligned16(buf) || (reinterpret_cast<uintptr_t>(sink) & 3u)) return HG_ERR_INVALID_ARG;
-    if ((row_bytes != 32 && row_bytes != 64) || log2_rows < 4 || log2_rows > 30) return HG_ERR_INVALID_ARG;
-    if (rows_per_thread < 8 || rows_per_thread % 8 || n_threads < 1) return HG_ERR_INVALID_ARG;
-    const int64_t blocks = (n_threads + kBlock - 1) / kBlock;
-    if (blocks > INT32_MAX / kBlock) return HG_ERR_INVALID_ARG;
+hg_status hg_probe_l2_gather(const void* buf, int32_t log2_rows, int32_t row_bytes, int32_t lanes_per_row,
+                             int64_t n_threads, int32_t rows_per_group, uint32_t seed, float* sink, hg_stream stream) {
+    if (!buf || !sink || !aligned(buf, 32) || !aligned(sink, 4)) return HG_ERR_INVALID_ARG;
+    if (log2_rows < 4 || log2_rows > 30 || rows_per_group < 8 || rows_per_group % 8) return HG_ERR_INVALID_ARG;
+    if (lanes_per_row != 1 && lanes_per_row != 2 && lanes_per_row != 4) return HG_ERR_INVALID_ARG;
+    if (n_threads < lanes_per_row || n_threads % lanes_per_row || n_threads > int64_t(INT32_MAX)) return HG_ERR_INVALID_ARG;
     const uint32_t mask = (1u << log2_rows) - 1u;
-    const uint4* b = static_cast<const uint4*>(buf);
-    if (row_bytes == 32)
-        gather_kernel<32><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(b, mask, rows_per_thread, seed, sink,
-                                                                               n_threads);
-    else
-        gather_kernel<64><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(b, mask, rows_per_thread, seed, sink,
-                                                                               n_threads);
-    return cudaGetLastError() == cudaSuccess ? HG_OK : HG_ERR_CUDA;
+    cudaError_t e;
+    if (row_bytes == 32 && lanes_per_row == 1) e = launch_gather<32, 1>(buf, mask, rows_per_group, seed, sink, n_threads, stream);
+    else if (row_bytes == 32 && lanes_per_row == 2) e = launch_gather<32, 2>(buf, mask, rows_per_group, seed, sink, n_threads, stream);
+    else if (row_bytes == 64 && lanes_per_row == 1) e = launch_gather<64, 1>(buf, mask, rows_per_group, seed, sink, n_threads, stream);
+    else if (row_bytes == 64 && lanes_per_row == 2) e = launch_gather<64, 2>(buf, mask, rows_per_group, seed, sink, n_threads, stream);
+    else if (row_bytes == 64 && lanes_per_row == 4) e = launch_gather<64, 4>(buf, mask, rows_per_group, seed, sink, n_threads, stream);
+    else return HG_ERR_INVALID_ARG;
+    return e == cudaSuccess ? HG_OK : HG_ERR_CUDA;
 }
 
-hg_status hg_probe_l2_red(float* buf, int32_t log2_slots, int64_t n_threads, int32_t ops_per_thread, uint32_t seed,
-                          hg_stream stream) {
-    if (!buf || !aligned16(buf) || log2_slots < 4 || log2_slots > 30 || ops_per_thread < 1 || n_threads < 1)
-        return HG_ERR_INVALID_ARG;
-    const int64_t blocks = (n_threads + kBlock - 1) / kBlock;
-    if (blocks > INT32_MAX / kBlock) return HG_ERR_INVALID_ARG;
-    red_kernel<<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(buf, (1u << log2_slots) - 1u, ops_per_thread,
-                                                                    seed, n_threads);
-    return cudaGetLastError() == cudaSuccess ? HG_OK : HG_ERR_CUDA;
+hg_status hg_probe_l2_red(float* buf, int32_t log2_rows, int32_t row_bytes, int32_t lanes_per_row, int64_t n_threads,
+                          int32_t rows_per_group, uint32_t seed, hg_stream stream) {
+    if (!buf || !aligned(buf, 16) || log2_rows < 4 || log2_rows > 30 || rows_per_group < 1) return HG_ERR_INVALID_ARG;
+    if (lanes_per_row != 1 && lanes_per_row != 2 && lanes_per_row != 4) return HG_ERR_INVALID_ARG;
+    if (n_threads < lanes_per_row || n_threads % lanes_per_row || n_threads > int64_t(INT32_MAX)) return HG_ERR_INVALID_ARG;
+    const uint32_t mask = (1u << log2_rows) - 1u;
+    cudaError_t e;
+    if (row_bytes == 16 && lanes_per_row == 1) e = launch_red<16, 1>(buf, mask, rows_per_group, seed, n_threads, stream);
+    else if (row_bytes == 32 && lanes_per_row == 1) e = launch_red<32, 1>(buf, mask, rows_per_group, seed, n_threads, stream);
+    else if (row_bytes == 32 && lanes_per_row == 2) e = launch_red<32, 2>(buf, mask, rows_per_group, seed, n_threads, stream);
+    else if (row_bytes == 64 && lanes_per_row == 1) e = launch_red<64, 1>(buf, mask, rows_per_group, seed, n_threads, stream);
+    else if (row_bytes == 64 && lanes_per_row == 2) e = launch_red<64, 2>(buf, mask, rows_per_group, seed, n_threads, stream);
+    else if (row_bytes == 64 && lanes_per_row == 4) e = launch_red<64, 4>(buf, mask, rows_per_group, seed, n_threads, stream);
+    else return HG_ERR_INVALID_ARG;
+    return e == cudaSuccess ? HG_OK : HG_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -37,7 +37,14 @@ def _mods():
 EDGE = [0.0, 1.0, 0.5, 0.25, 1.0 - 2 ** -24, 2 ** -24, -0.5, 1.5, float("nan"), float("inf"), float("-inf"), -0.0]
 
 
-def _coords(rng, n, d, res):
+def _coords(rng, n, d, res, stratified=False):
+    if stratified:
+        # one point per stratum, strata in row-major order: consecutive points
+        # are neighbours (coherent scatter, as the PINN collocation workload)
+        side = round(n ** (1.0 / d))
+        assert side ** d == n
+        cells = np.stack([(np.arange(n) // side ** i) % side for i in range(d)], axis=1)
+        return ((cells + rng.random((n, d))) / side).astype(np.float32)
     x = rng.random((n, d), dtype=np.float32)
     m = min(n, 64)
     if n >= 8:
@@ -69,6 +76,18 @@ CASES = [
     ("3d_mask_1010", 3, 4, 2, 4, 60, (10, 10, 10, 10), "f32", 1, True, 600, 0b1010),
     ("3d_one_point", 3, 4, 2, 4, 60, (10, 10, 10, 10), "f32", 1, True, 1, None),
     ("2d_32_levels_max_res", 2, 32, 2, 2, 1 << 22, (12, 12, 12), "f32", 1, True, 1500, None),
+    # many points per vertex on small one-to-one levels: the backward takes the
+    # shared-memory (privatised) path for these levels
+    ("2d_F1_coarse_many_points", 2, 3, 1, 4, 16, (10, 10, 10), "f32", 1, True, 20000, None),
+    ("2d_F2_coarse_many_points", 2, 3, 2, 4, 16, (10, 10, 10), "f32", 0, True, 20000, None),
+    ("3d_F1_coarse_many_points", 3, 3, 1, 2, 8, (10, 10, 10, 10), "f32", 0, True, 20000, None),
+    ("3d_F2_f16_coarse_many_points", 3, 3, 2, 2, 6, (9, 9, 9, 9), "f16", 1, True, 30000, 0b011),
+    # stratified (coherent) points: runs of points in one cell are summed in
+    # the warp before the scatter
+    ("2d_F2_stratified", 2, 5, 2, 4, 160, (11, 11, 11), "f32", 1, True, 16384, None),
+    ("2d_F1_stratified", 2, 4, 1, 4, 64, (10, 10, 10), "f32", 0, True, 10000, None),
+    ("3d_F2_stratified", 3, 4, 2, 2, 40, (12, 12, 12, 12), "f32", 1, True, 13824, None),
+    ("3d_F1_f16_stratified", 3, 3, 1, 2, 20, (10, 10, 10, 10), "f16", 1, True, 8000, None),
 ]
 
 
@@ -77,7 +96,7 @@ def _build_case(case, seed=0):
     cid, d, L, F, nmin, nmax, log2T, dt, layout, packed, n, mask = case
     rng = np.random.default_rng(zlib.crc32(cid.encode()) + seed)
     res = oracle.level_resolutions(L, nmin, nmax)
-    coords = _coords(rng, n, d, res)
+    coords = _coords(rng, n, d, res, stratified="stratified" in cid)
     npdt = np.float16 if dt == "f16" else np.float32
     if packed:
         assert len(set(log2T)) == 1
@@ -172,6 +191,9 @@ LIN_CASES = [
     ("3d_F2", 3, 8, 2, 4, 128, 12, "f32", 1, 2500, None),
     ("3d_F4_f16_mask", 3, 5, 4, 4, 64, 10, "f16", 0, 700, 0b10110),
     ("3d_F8", 3, 3, 8, 2, 16, 8, "f32", 1, 257, None),
+    ("2d_F1_coarse_many_points", 2, 3, 1, 4, 16, 10, "f32", 1, 30000, None),
+    ("3d_F4_f16_coarse_many_points", 3, 3, 4, 2, 8, 9, "f16", 0, 30000, 0b101),
+    ("2d_F2_stratified", 2, 6, 2, 4, 300, 12, "f32", 1, 16384, None),
 ]
 
 
@@ -182,7 +204,7 @@ def test_linear_parity(case):
     cid, d, L, F, nmin, nmax, log2T, dt, layout, n, mask = case
     rng = np.random.default_rng(zlib.crc32(cid.encode()))
     res = oracle.level_resolutions(L, nmin, nmax)
-    coords = _coords(rng, n, d, res)
+    coords = _coords(rng, n, d, res, stratified="stratified" in cid)
     npdt = np.float16 if dt == "f16" else np.float32
     table = (rng.random((L, 1 << log2T, F), dtype=np.float32) * 2 - 1).astype(npdt)
     gg = rng.standard_normal((n, L, F), dtype=np.float32)
