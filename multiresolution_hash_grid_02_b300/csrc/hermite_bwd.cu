@@ -185,8 +185,10 @@ __device__ __forceinline__ void unit_blend_t(float gg, const float (&gd)[3], flo
 // corner row (S = 2^D/G slots x FC features = 4 floats), computes the
 // gradients of those slots, and issues one red.global.add.v4.f32 per corner,
 // so one warp instruction reduces into whole rows.
+// Four 256-thread blocks per SM (64 registers): the run-aggregation branch,
+// rarely taken on random points, must not cost occupancy on the common path.
 template <int D, int FC, int G>
-__global__ void __launch_bounds__(kBlock) hermite_bwd_split_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kBlock, 4) hermite_bwd_split_kernel(const __grid_constant__ BwdParams p) {
     constexpr int V = 1 << D, S = V / G;
     static_assert(S * FC == 4, "one 16-byte chunk per lane");
     const int l = p.c.lvl[blockIdx.y];
