@@ -37,6 +37,7 @@ if ROOT not in sys.path:
 
 METRIC = "encoded points/s (Hermite fwd γ,∇γ,∇²γ + bwd) at 1 B300; % of L2/HBM gather roofline"
 L2_BYTES = 126 * 1024 * 1024
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def parse_args():
@@ -50,9 +51,97 @@ def parse_args():
     p.add_argument("--layout", choices=["feature", "point"], default="feature")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-sample", type=int, default=1 << 14, help="points in the oracle's timed sample")
+    p.add_argument("--cpu-sample", type=int, default=1 << 18, help="points in the oracle's timed sample")
     p.add_argument("--points", type=int, default=None, help="override the workload's point count (profiling)")
+    p.add_argument("--probe-patterns", action="store_true",
+                   help="print the L2 random-row gather / RED rates for 1, 2 and 4 lanes per row "
+                        "(32- and 64-byte rows) as one JSON line, then exit")
+    p.add_argument("--record-traffic", metavar="NCU_LOG", default=None,
+                   help="parse an ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum log of the benchmark "
+                        "command and record per-launch DRAM traffic (with the kernel-source hash) in "
+                        "profiles/dram_traffic.json, then exit")
     return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# DRAM traffic recorded from an ncu capture, valid while the kernels are unchanged
+# ---------------------------------------------------------------------------
+
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources and public headers of the library."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    pkg = os.path.join(ROOT, "multiresolution_hash_grid_02_b300", "csrc")
+    files = sorted(glob.glob(os.path.join(pkg, "*.cu")) + glob.glob(os.path.join(pkg, "*.cuh")) +
+                   glob.glob(os.path.join(pkg, "*.h")) + glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def parse_ncu_dram_log(path: str) -> dict:
+    """{kernel name: {"dram_read": B, "dram_write": B, "launches": k}} from ncu's
+    default text output (units Kbyte/Mbyte/Gbyte are decimal)."""
+    import re
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
+    out, cur = {}, None
+    with open(path) as f:
+        for line in f:
+            m = re.match(r"\s{2}(\S.*?)\s+\(\d+, \d+, \d+\)x\(\d+, \d+, \d+\)", line)
+            if m:
+                base = m.group(1).split("(")[0]
+                k = re.search(r"(\w+_kernel\b.*)$", base)
+                cur = (k.group(1) if k else base).strip()
+                out.setdefault(cur, {"dram_read": 0.0, "dram_write": 0.0, "launches": 0})
+                out[cur]["launches"] += 1
+                continue
+            m = re.match(r"\s+dram__bytes_(read|write)\.sum\s+(\S+)\s+([\d.,]+)", line)
+            if m and cur:
+                out[cur]["dram_" + m.group(1)] += float(m.group(3).replace(",", "")) * scale[m.group(2)]
+    for k, v in out.items():
+        n = max(1, v["launches"])
+        v["bytes_per_launch"] = (v["dram_read"] + v["dram_write"]) / n
+    return out
+
+
+def record_traffic(log_path: str, workload: str, command: str):
+    data = {"workload": workload, "source_sha256": kernel_source_hash(), "command": command,
+            "kernels": parse_ncu_dram_log(log_path)}
+    os.makedirs(os.path.dirname(TRAFFIC_FILE), exist_ok=True)
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(data, f, indent=1)
+    print(json.dumps(data))
+
+
+def recorded_traffic(workload: str, kernel_prefix: str):
+    """Per-launch DRAM bytes of the kernel from the recorded capture, or None
+    when there is none for this workload or the kernels changed since."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if data.get("workload") != workload or data.get("source_sha256") != kernel_source_hash():
+        return None
+    for name, v in data.get("kernels", {}).items():
+        if name.startswith(kernel_prefix):
+            return v["bytes_per_launch"]
+    return None
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value across ranks (the slowest rank's time); identity for
+    one rank.  Uses the default process group (NCCL on GPUs, gloo on CPU)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 # ---------------------------------------------------------------------------
@@ -264,8 +353,36 @@ def probe_peaks(torch, hg, gather_pat, red_pat):
     return g, r
 
 
+def probe_pattern_table():
+    """L2 random-row rates for every lanes-per-row split the probes support:
+    the measurement behind splitting each (point, level) across lanes."""
+    import torch
+    from multiresolution_hash_grid_02_b300 import hg
+    rows = {}
+    for kind, pats in (("gather", ((32, 1), (32, 2), (64, 1), (64, 2), (64, 4))),
+                       ("red", ((16, 1), (32, 1), (32, 2), (64, 1), (64, 2), (64, 4)))):
+        for pat in pats:
+            g, r = probe_peaks(torch, hg, pat if kind == "gather" else (64, 2), pat if kind == "red" else (64, 4))
+            rows[f"{kind} {pat[0]}-byte rows, {pat[1]} lane(s)/row"] = round(g if kind == "gather" else r, 1)
+    return rows
+
+
 def main():
     args = parse_args()
+    if args.probe_patterns:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        print(json.dumps({"probe_patterns_gbs": probe_pattern_table(), "buffer": "32 MiB (L2-resident)",
+                          "gpu": torch.cuda.get_device_name()}), flush=True)
+        return
+    if args.record_traffic:
+        from multiresolution_hash_grid_02_b300 import workloads as W
+        w = W.WORKLOADS[args.config]
+        record_traffic(args.record_traffic, w.name if not args.points else f"{w.name}@{args.points}",
+                       "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
+                       "--clock-control none -k regex:hermite -s 2 -c 2 python bench.py --steps 2 --warmup 1 "
+                       "--no-e2e --no-cpu-baseline")
+        return
     if args.impl == "reference":
         run_reference(args)
         return
@@ -362,11 +479,7 @@ def main():
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, "cuda")
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev_f]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in ev_f]
     t_fwd = statistics.mean(fwd_ms)
@@ -397,8 +510,11 @@ def main():
     }
     dom = "bwd" if t_bwd >= t_fwd else "fwd"
     k = kernels[dom]
+    kname = {"fwd": "hermite_fwd" if w.kind == "hermite" else "linear_fwd",
+             "bwd": "hermite_bwd" if w.kind == "hermite" else "linear_bwd"}[dom]
+    traffic = recorded_traffic(w.name if not args.points else f"{w.name}@{args.points}", kname)
     roofline = {"bound": "l2", "kernel": dom, "achieved": k["achieved"], "peak": k["peak"], "unit": "GB/s",
-                "frac": k["frac"], "traffic": None,
+                "frac": k["frac"], "traffic": traffic,
                 "peak_source": "measured live by this run's L2 probes (hg_probe_l2_gather / hg_probe_l2_red)",
                 "combined_frac": combined, "hbm_peak_gbs": hbm}
 
