@@ -51,7 +51,7 @@ def parse_args():
     p.add_argument("--layout", choices=["feature", "point"], default="feature")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-sample", type=int, default=1 << 18, help="points in the oracle's timed sample")
+    p.add_argument("--cpu-sample", type=int, default=1 << 20, help="points in the oracle's timed sample")
     p.add_argument("--points", type=int, default=None, help="override the workload's point count (profiling)")
     p.add_argument("--probe-patterns", action="store_true",
                    help="print the L2 random-row gather / RED rates for 1, 2 and 4 lanes per row "
@@ -521,7 +521,7 @@ def main():
     e2e = None
     if not args.no_e2e and rank == 0:
         e2e = run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, hermite, grad,
-                      stream, fwd_fn=None)
+                      stream)
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(w, inputs, mask, args.cpu_sample)
@@ -544,63 +544,75 @@ def main():
 
 
 def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, hermite, grad, stream,
-            fwd_fn=None, steps=5):
-    """Same step through the C ABI with inputs starting in pinned host memory:
-    H2D of the step's coordinates and upstream gradients, zero the gradient
-    table, forward, backward, D2H of the forward's outputs."""
+            steps=8, warmup=2):
+    """The step through the C ABI with inputs starting in pinned host memory,
+    pipelined over three streams as a streaming user would run it: the
+    host-to-device copy of step i+1's coordinates and upstream gradients and
+    the device-to-host read of step i-1's gamma / grad gamma / Laplacian
+    overlap the encode of step i (two device buffer sets).  Every step's
+    copies and kernels are inside the timed region."""
     n = w.n_points
 
     def pinned(a):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return t.pin_memory()
+        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
 
-    h_coords = pinned(inputs["coords"])
-    h_gg = pinned(conv(inputs["g_gamma"], False))
-    h_gd = pinned(conv(inputs["g_dgamma"], True)) if hermite else None
-    h_gl = pinned(conv(inputs["g_lap"], False)) if hermite else None
-    d_coords = torch.empty_like(h_coords, device="cuda")
-    d_gg = torch.empty_like(h_gg, device="cuda")
-    d_gd = torch.empty_like(h_gd, device="cuda") if hermite else None
-    d_gl = torch.empty_like(h_gl, device="cuda") if hermite else None
-    d_gamma = torch.empty(shape_g, device="cuda")
-    d_dgamma = torch.empty(shape_d, device="cuda") if hermite else None
-    d_lap = torch.empty(shape_g, device="cuda") if hermite else None
-    o_gamma = torch.empty(shape_g).pin_memory()
-    o_dgamma = torch.empty(shape_d).pin_memory() if hermite else None
-    o_lap = torch.empty(shape_g).pin_memory() if hermite else None
-    h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_gg, h_gd, h_gl) if t is not None)
-    d2h = sum(t.numel() * t.element_size() for t in (o_gamma, o_dgamma, o_lap) if t is not None)
+    h_in = [pinned(inputs["coords"]), pinned(conv(inputs["g_gamma"], False))]
+    if hermite:
+        h_in += [pinned(conv(inputs["g_dgamma"], True)), pinned(conv(inputs["g_lap"], False))]
+    out_shapes = [shape_g] + ([shape_d, shape_g] if hermite else [])
+    d_in = [[torch.empty_like(t, device="cuda") for t in h_in] for _ in range(2)]
+    d_out = [[torch.empty(sh, device="cuda") for sh in out_shapes] for _ in range(2)]
+    h_out = [[torch.empty(sh).pin_memory() for sh in out_shapes] for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    s_comp = stream
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    started = [False, False]
 
-    def one():
-        d_coords.copy_(h_coords, non_blocking=True)
-        d_gg.copy_(h_gg, non_blocking=True)
-        if hermite:
-            d_gd.copy_(h_gd, non_blocking=True)
-            d_gl.copy_(h_gl, non_blocking=True)
+    def step(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if started[b]:
+                s_in.wait_event(ev_comp[b])          # step i-2 has finished reading this input set
+            for d, h in zip(d_in[b], h_in):
+                d.copy_(h, non_blocking=True)
+            ev_in[b].record(s_in)
+        s_comp.wait_event(ev_in[b])
+        if started[b]:
+            s_comp.wait_event(ev_out[b])             # step i-2's outputs are on the host
         grad.zero_()
+        c, gg = d_in[b][0], d_in[b][1]
         if hermite:
-            hg.hg_encode_fwd(desc, n, d_coords, tviews, d_gamma, d_dgamma, d_lap, stream)
-            hg.hg_encode_bwd(desc, n, d_coords, d_gg, d_gd, d_gl, gviews, stream)
+            hg.hg_encode_fwd(desc, n, c, tviews, d_out[b][0], d_out[b][1], d_out[b][2], s_comp)
+            hg.hg_encode_bwd(desc, n, c, gg, d_in[b][2], d_in[b][3], gviews, s_comp)
         else:
-            hg.hg_linear_fwd(desc, n, d_coords, tviews, d_gamma, stream)
-            hg.hg_linear_bwd(desc, n, d_coords, d_gg, gviews, stream)
-        o_gamma.copy_(d_gamma, non_blocking=True)
-        if hermite:
-            o_dgamma.copy_(d_dgamma, non_blocking=True)
-            o_lap.copy_(d_lap, non_blocking=True)
+            hg.hg_linear_fwd(desc, n, c, tviews, d_out[b][0], s_comp)
+            hg.hg_linear_bwd(desc, n, c, gg, gviews, s_comp)
+        ev_comp[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[b])
+            for h, d in zip(h_out[b], d_out[b]):
+                h.copy_(d, non_blocking=True)
+            ev_out[b].record(s_out)
+        started[b] = True
 
-    one()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        one()
-    b.record(stream)
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_in)
+    for i in range(warmup, warmup + steps):
+        step(i)
+    e.record(s_out)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
+    ms = a.elapsed_time(e) / steps
     return {"value": n / (ms * 1e-3), "unit": "points/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms, "steps": steps,
-            "note": "pinned host buffers; coordinates and upstream gradients in, gamma/grad gamma/Laplacian out; "
+            "note": "pinned host buffers; coordinates and upstream gradients in, gamma/grad gamma/Laplacian out, "
+                    "every step; copies of neighbouring steps overlap the encode (3 streams, 2 buffer sets); "
                     "gradient tables stay on the device"}
 
 

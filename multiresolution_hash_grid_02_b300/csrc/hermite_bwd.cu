@@ -180,6 +180,42 @@ __device__ __forceinline__ void unit_blend_t(float gg, const float (&gd)[3], flo
     }
 }
 
+// The same transposed blend for both features at once (F = 2): the upstream
+// gradients are (feature 0, feature 1) pairs, the weights are shared, and
+// each f32x2 operation is exactly the two fp32 operations above.
+template <int D>
+__device__ __forceinline__ void unit_blend_t_f2(uint64_t gg, const uint64_t (&gd)[3], uint64_t gl, const AxisW2& W0,
+                                                const AxisW2& W1, const AxisW2& W2, uint64_t (&qb)[1 << D]) {
+    if constexpr (D == 3) {
+#pragma unroll
+        for (int v2 = 0; v2 < 2; ++v2) {
+            const uint64_t A = f2_fma(gg, W2.w[v2], f2_fma(gd[2], W2.d1[v2], f2_mul(gl, W2.d2[v2])));
+            const uint64_t B = f2_mul(gd[0], W2.w[v2]);
+            const uint64_t C = f2_mul(gd[1], W2.w[v2]);
+            const uint64_t Dl = f2_mul(gl, W2.w[v2]);
+#pragma unroll
+            for (int v1 = 0; v1 < 2; ++v1) {
+                const uint64_t s = f2_fma(A, W1.w[v1], f2_fma(C, W1.d1[v1], f2_mul(Dl, W1.d2[v1])));
+                const uint64_t s1 = f2_mul(B, W1.w[v1]);
+                const uint64_t s2 = f2_mul(Dl, W1.w[v1]);
+#pragma unroll
+                for (int v0 = 0; v0 < 2; ++v0)
+                    qb[v0 + 2 * v1 + 4 * v2] = f2_fma(s, W0.w[v0], f2_fma(s1, W0.d1[v0], f2_mul(s2, W0.d2[v0])));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int v1 = 0; v1 < 2; ++v1) {
+            const uint64_t s = f2_fma(gg, W1.w[v1], f2_fma(gd[1], W1.d1[v1], f2_mul(gl, W1.d2[v1])));
+            const uint64_t s1 = f2_mul(gd[0], W1.w[v1]);
+            const uint64_t s2 = f2_mul(gl, W1.w[v1]);
+#pragma unroll
+            for (int v0 = 0; v0 < 2; ++v0)
+                qb[v0 + 2 * v1] = f2_fma(s, W0.w[v0], f2_fma(s1, W0.d1[v0], f2_mul(s2, W0.d2[v0])));
+        }
+    }
+}
+
 // Lane-split backward for packed fp32 gradient rows of 32 or 64 bytes: G
 // lanes share one (point, level); lane g owns the 16-byte chunk g of every
 // corner row (S = 2^D/G slots x FC features = 4 floats), computes the
@@ -223,12 +259,22 @@ __global__ void __launch_bounds__(kBlock, 4) hermite_bwd_split_kernel(const __gr
         const AxisW W0 = unit_axis<D, G>(B[0], lane, u, 0);
         const AxisW W1 = unit_axis<D, G>(B[1], lane, u, 1);
         const AxisW W2 = unit_axis<D, G>(B[D - 1], lane, u, D - 1);
+        if constexpr (FC == 2) {
+            const uint64_t gd2[3] = {f2_pack(gd[0][0], gd[1][0]), f2_pack(gd[0][1], gd[1][1]),
+                                     f2_pack(gd[0][2], gd[1][2])};
+            uint64_t qb[V];
+            unit_blend_t_f2<D>(f2_pack(gg[0], gg[1]), gd2, f2_pack(gl[0], gl[1]), axis_dup(W0), axis_dup(W1),
+                               axis_dup(W2), qb);
 #pragma unroll
-        for (int f = 0; f < FC; ++f) {
-            float qb[V];
-            unit_blend_t<D>(gg[f], gd[f], gl[f], W0, W1, W2, qb);
+            for (int v = 0; v < V; ++v) f2_unpack(qb[v], r[v][u * FC], r[v][u * FC + 1]);
+        } else {
 #pragma unroll
-            for (int v = 0; v < V; ++v) r[v][u * FC + f] = qb[v];
+            for (int f = 0; f < FC; ++f) {
+                float qb[V];
+                unit_blend_t<D>(gg[f], gd[f], gl[f], W0, W1, W2, qb);
+#pragma unroll
+                for (int v = 0; v < V; ++v) r[v][u * FC + f] = qb[v];
+            }
         }
     }
     // consecutive points in one cell (coherent inputs) add up before the RED
