@@ -60,7 +60,10 @@ def _load():
     global _lib
     if _lib is not None:
         return _lib
-    lib = ctypes.CDLL(build())
+    # HG_ORACLE_LIB: load another build of hg_oracle.c instead (the mutation
+    # tests point it at copies with planted mistakes)
+    override = os.environ.get("HG_ORACLE_LIB")
+    lib = ctypes.CDLL(override if override else build())
     P = ctypes.c_void_p
     i32, i64, u32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
     lib.oracle_basis_1d.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, P]
