@@ -315,17 +315,18 @@ def kernel_patterns(w):
     slots = (1 << w.d) if w.kind == "hermite" else 1
     trow = slots * w.F * es
     grow = slots * w.F * 4
-    g = (64, 2) if trow == 64 else (32, 1)
+    # the lane-pair forward serves 3D F = 2 rows (64 B fp32, 32 B fp16); other rows: one thread per row
+    g = (trow, 2) if (w.kind == "hermite" and w.d == 3 and w.F == 2) else (32, 1)
     r = {64: (64, 4), 32: (32, 2)}.get(grow, (16, 1))
     return g, r
 
 
-def probe_peaks(torch, hg, gather_pat, red_pat):
-    """Measured L2 ceilings for the kernels' own access patterns: random
-    whole-row gathers and random 16-byte vector REDs on a 32 MiB buffer
-    (L2-resident), rows split across lanes as the kernels split them; best of 5
-    after one warm-up launch."""
-    buf = torch.zeros(1 << 23, dtype=torch.float32, device="cuda")   # 32 MiB
+def probe_peaks(torch, hg, gather_pat, red_pat, log2_bytes=25):
+    """Measured ceilings for the kernels' own access patterns: random
+    whole-row gathers and random 16-byte vector REDs on a 2^log2_bytes buffer
+    (32 MiB: L2-resident; 1 GiB: HBM), rows split across lanes as the kernels
+    split them; best of 5 after one warm-up launch."""
+    buf = torch.zeros(1 << (log2_bytes - 2), dtype=torch.float32, device="cuda")
     n_threads = 148 * 2048 * 4
     sink = torch.empty(n_threads, device="cuda")
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -343,8 +344,8 @@ def probe_peaks(torch, hg, gather_pat, red_pat):
 
     grow, glanes = gather_pat
     rrow, rlanes = red_pat
-    gl2 = {64: 19, 32: 20}[grow]
-    rl2 = {64: 19, 32: 20, 16: 21}[rrow]
+    gl2 = log2_bytes - {64: 6, 32: 5}[grow]
+    rl2 = log2_bytes - {64: 6, 32: 5, 16: 4}[rrow]
     per_g, per_r = 64, 64
     g = best(lambda i: hg.hg_probe_l2_gather(buf, gl2, grow, glanes, n_threads, per_g, i, sink),
              n_threads // glanes * per_g * grow)
@@ -359,11 +360,13 @@ def probe_pattern_table():
     import torch
     from multiresolution_hash_grid_02_b300 import hg
     rows = {}
-    for kind, pats in (("gather", ((32, 1), (32, 2), (64, 1), (64, 2), (64, 4))),
-                       ("red", ((16, 1), (32, 1), (32, 2), (64, 1), (64, 2), (64, 4)))):
-        for pat in pats:
-            g, r = probe_peaks(torch, hg, pat if kind == "gather" else (64, 2), pat if kind == "red" else (64, 4))
-            rows[f"{kind} {pat[0]}-byte rows, {pat[1]} lane(s)/row"] = round(g if kind == "gather" else r, 1)
+    for where, l2b in (("L2 (32 MiB)", 25), ("HBM (1 GiB)", 30)):
+        for kind, pats in (("gather", ((32, 1), (32, 2), (64, 1), (64, 2), (64, 4))),
+                           ("red", ((16, 1), (32, 1), (32, 2), (64, 1), (64, 2), (64, 4)))):
+            for pat in pats:
+                g, r = probe_peaks(torch, hg, pat if kind == "gather" else (64, 2), pat if kind == "red" else (64, 4),
+                                   l2b)
+                rows[f"{where} {kind} {pat[0]}-byte rows, {pat[1]} lane(s)/row"] = round(g if kind == "gather" else r, 1)
     return rows
 
 
@@ -372,8 +375,8 @@ def main():
     if args.probe_patterns:
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        print(json.dumps({"probe_patterns_gbs": probe_pattern_table(), "buffer": "32 MiB (L2-resident)",
-                          "gpu": torch.cuda.get_device_name()}), flush=True)
+        print(json.dumps({"probe_patterns_gbs": probe_pattern_table(), "gpu": torch.cuda.get_device_name()}),
+              flush=True)
         return
     if args.record_traffic:
         from multiresolution_hash_grid_02_b300 import workloads as W

@@ -74,7 +74,7 @@ def test_algorithmic_bytes_and_patterns():
     g5, r5 = bench.algorithmic_bytes(w5, (1 << 16) - 1)
     assert g5 == (1 << 23) * 16 * 8 * 32 and r5 == 2 * g5       # fp16 rows, fp32 gradients
     assert bench.kernel_patterns(w) == ((64, 2), (64, 4))
-    assert bench.kernel_patterns(w5) == ((32, 1), (64, 4))
+    assert bench.kernel_patterns(w5) == ((32, 2), (64, 4))
     w2 = W.WORKLOADS[2]
     assert bench.algorithmic_bytes(w2, (1 << 16) - 1) == ((1 << 20) * 16 * 4 * 8,) * 2
 
