@@ -79,9 +79,16 @@ def _load():
     lib.oracle_linear_bwd_level.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             P, ctypes.c_int, i64, P, P, P, P]
     lib.oracle_slot_in_bucket.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.oracle_hess_entries.argtypes = [ctypes.c_int]
+    lib.oracle_eval_cell_hessian.argtypes = [ctypes.c_int, ctypes.c_int, i32, P, P, P, P, P, P, P]
+    lib.oracle_encode_fwd_hessian.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, u32, P,
+                                              i64, P, P, P, P, P, P, P, ctypes.c_int]
+    lib.oracle_encode_bwd_hessian_level.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    P, P, i64, P, P, P, P, P, P]
     for name in ("oracle_eval_cell", "oracle_hash_indices", "oracle_encode_fwd",
                  "oracle_encode_bwd_level", "oracle_linear_fwd", "oracle_linear_bwd_level",
-                 "oracle_slot_in_bucket"):
+                 "oracle_slot_in_bucket", "oracle_hess_entries", "oracle_eval_cell_hessian",
+                 "oracle_encode_fwd_hessian", "oracle_encode_bwd_hessian_level"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -345,3 +352,91 @@ def linear_bwd(d: int, F: int, res, log2T: int, coords: np.ndarray, g_gamma: np.
         if with_mags:
             mag[l] = m
     return (grad, mag) if with_mags else grad
+
+
+# ---------------------------------------------------------------------------
+# full Hessian (upper triangle, row-major: 2D xx, xy, yy; 3D xx, xy, xz, yy, yz, zz)
+# ---------------------------------------------------------------------------
+
+def hess_entries(d: int) -> int:
+    return int(_load().oracle_hess_entries(d))
+
+
+def hess_pairs(d: int) -> list[tuple[int, int]]:
+    """(i, j) of each Hessian entry, in storage order."""
+    return [(i, j) for i in range(d) for j in range(i, d)]
+
+
+def eval_cell_hessian(d: int, F: int, N: int, log2T, level_tables, c, t):
+    """One cell at an fp64 local coordinate: (gamma[F], dgamma[d][F], hess[P][F])."""
+    lib = _load()
+    tabs = [np.ascontiguousarray(a, dtype=np.float64) for a in level_tables]
+    lt = np.asarray(log2T, np.int32)
+    cc = np.asarray(c, np.int64)
+    tt = np.asarray(t, np.float64)
+    P = hess_entries(d)
+    g, dg, h = np.zeros(F), np.zeros((d, F)), np.zeros((P, F))
+    _check(lib.oracle_eval_cell_hessian(d, F, int(N), _ptr(lt), _ptr_array(tabs), _ptr(cc), _ptr(tt), _ptr(g),
+                                        _ptr(dg), _ptr(h)), "eval_cell_hessian")
+    return g, dg, h
+
+
+def encode_fwd_hessian(d: int, F: int, res, log2T, tables, coords: np.ndarray, level_mask: int | None = None,
+                       nthreads: int | None = None, with_mags: bool = True):
+    """Hermite forward with the full Hessian: point-major fp64 gamma [N][L][F],
+    dgamma [N][d][L][F], hess [N][P][L][F] (+ magnitudes mgamma, mdgamma, mhess)."""
+    lib = _load()
+    L = len(res)
+    if level_mask is None:
+        level_mask = (1 << L) - 1
+    tabs = _as_f64_tables(tables)
+    for k, tb in enumerate(tabs):
+        if tb.shape != (L, 1 << int(log2T[k]), comb(d, k), F):
+            raise ValueError(f"order table {k} has shape {tb.shape}")
+    coords = np.ascontiguousarray(coords, np.float32)
+    n = coords.shape[0]
+    P = hess_entries(d)
+    r = np.asarray(res, np.int32)
+    lt = np.asarray(log2T, np.int32)
+    out = {"gamma": np.zeros((n, L, F)), "dgamma": np.zeros((n, d, L, F)), "hess": np.zeros((n, P, L, F))}
+    if with_mags:
+        out.update(mgamma=np.zeros((n, L, F)), mdgamma=np.zeros((n, d, L, F)), mhess=np.zeros((n, P, L, F)))
+    _check(lib.oracle_encode_fwd_hessian(d, L, F, _ptr(r), _ptr(lt), level_mask & 0xffffffff, _ptr_array(tabs), n,
+                                         _ptr(coords), _ptr(out["gamma"]), _ptr(out["dgamma"]), _ptr(out["hess"]),
+                                         _ptr(out.get("mgamma")), _ptr(out.get("mdgamma")), _ptr(out.get("mhess")),
+                                         nthreads or default_threads()), "encode_fwd_hessian")
+    return out
+
+
+def encode_bwd_hessian(d: int, F: int, res, log2T, coords: np.ndarray, g_gamma=None, g_dgamma=None, g_hess=None,
+                       level_mask: int | None = None, levels=None, with_mags: bool = True,
+                       nthreads: int | None = None):
+    """Backward of :func:`encode_fwd_hessian` (float32 upstream, point-major;
+    any may be None): (grads, mags) lists over order k of fp64
+    [L][T_k][C(d,k)][F]; levels outside ``levels`` / the mask stay zero."""
+    from concurrent.futures import ThreadPoolExecutor
+    lib = _load()
+    L = len(res)
+    if level_mask is None:
+        level_mask = (1 << L) - 1
+    todo = [l for l in (range(L) if levels is None else levels) if (level_mask >> l) & 1]
+    coords = np.ascontiguousarray(coords, np.float32)
+    n = coords.shape[0]
+    r = np.asarray(res, np.int32)
+    lt = np.asarray(log2T, np.int32)
+    f32 = lambda a: None if a is None else np.ascontiguousarray(a, np.float32)
+    gg, gd, gh = f32(g_gamma), f32(g_dgamma), f32(g_hess)
+    shapes = order_table_shapes(d, L, F, log2T)
+    grads = [np.zeros(s) for s in shapes]
+    mags = [np.zeros(s) for s in shapes] if with_mags else None
+
+    def one(l):
+        gs = _ptr_array([g[l] for g in grads])
+        ms = _ptr_array([m[l] for m in mags]) if with_mags else None
+        return lib.oracle_encode_bwd_hessian_level(d, L, F, l, _ptr(r), _ptr(lt), n, _ptr(coords), _ptr(gg),
+                                                   _ptr(gd), _ptr(gh), gs, ms)
+
+    with ThreadPoolExecutor(max_workers=max(1, min(len(todo) or 1, nthreads or default_threads()))) as ex:
+        for rc in ex.map(one, todo):
+            _check(rc, "encode_bwd_hessian")
+    return grads, mags

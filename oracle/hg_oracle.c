@@ -184,9 +184,36 @@ typedef struct {
 /* Evaluate the cell with corner c at local coordinate t (fp64), writing
  * gamma[F], dgamma[d][F] (d/dx), lap[F], and the condition magnitudes.
  * Any output pointer may be NULL.                                           */
+/* Number of entries of the upper triangle of a d x d Hessian (i <= j, row-major:
+ * 2D xx, xy, yy; 3D xx, xy, xz, yy, yz, zz) and the position of (i, j).   */
+static int hess_entries(int d) { return d * (d + 1) / 2; }
+static int hess_pos(int d, int i, int j) {
+    int p = 0;
+    for (int a = 0; a < d; ++a)
+        for (int b = a; b < d; ++b) {
+            if (a == i && b == j) return p;
+            ++p;
+        }
+    return -1;
+}
+
+static void hermite_cell_h(const or_level* lv, const int64_t* c, const double* t,
+                           double* gamma, double* dgamma, double* lap,
+                           double* mg, double* md, double* ml, double* hess, double* mh);
+
 static void hermite_cell(const or_level* lv, const int64_t* c, const double* t,
                          double* gamma, double* dgamma, double* lap,
                          double* mg, double* md, double* ml) {
+    hermite_cell_h(lv, c, t, gamma, dgamma, lap, mg, md, ml, NULL, NULL);
+}
+
+/* As hermite_cell, plus (when hess != NULL) the Hessian hess[P][F], P the
+ * upper-triangle entries: d2/dx_i dx_j = N^2 d2/dy_i dy_j, where the mixed
+ * derivative of H replaces factors i and j by their first derivatives and
+ * the pure one factor i by its second derivative.  mh: magnitudes.        */
+static void hermite_cell_h(const or_level* lv, const int64_t* c, const double* t,
+                           double* gamma, double* dgamma, double* lap,
+                           double* mg, double* md, double* ml, double* hess, double* mh) {
     const int d = lv->d, F = lv->F;
     const double N = (double)lv->N;
     const double dx = 1.0 / N;
@@ -198,6 +225,10 @@ static void hermite_cell(const or_level* lv, const int64_t* c, const double* t,
         for (int j = 0; j < d; ++j) {
             if (dgamma) dgamma[j * F + f] = 0.0;
             if (md) md[j * F + f] = 0.0;
+        }
+        for (int q = 0; q < hess_entries(d); ++q) {
+            if (hess) hess[q * F + f] = 0.0;
+            if (mh) mh[q * F + f] = 0.0;
         }
     }
     double scale[OR_MAXD + 1];
@@ -240,6 +271,19 @@ static void hermite_cell(const or_level* lv, const int64_t* c, const double* t,
                     if (md) md[j * F + f] += fabs(th) * scale[k] * N * fabs(dH[j]);
                     if (lap) lap[f] += th * scale[k] * N * N * d2H[j];
                     if (ml) ml[f] += fabs(th) * scale[k] * N * N * fabs(d2H[j]);
+                }
+                if (hess) {
+                    for (int i = 0; i < d; ++i)
+                        for (int j = i; j < d; ++j) {
+                            double hij = 1.0;
+                            for (int m = 0; m < d; ++m) {
+                                if (i == j) hij *= (m == i) ? (*h[m])[2] : (*h[m])[0];
+                                else hij *= (m == i || m == j) ? (*h[m])[1] : (*h[m])[0];
+                            }
+                            const int q = hess_pos(d, i, j);
+                            hess[q * F + f] += th * scale[k] * N * N * hij;
+                            if (mh) mh[q * F + f] += fabs(th) * scale[k] * N * N * fabs(hij);
+                        }
                 }
             }
         }
@@ -490,3 +534,143 @@ int oracle_linear_bwd_level(int d, int L, int F, int l, const int32_t* res, int 
 
 /* The bucket slot of alpha, exposed so tests can check the ordering rule. */
 int oracle_slot_in_bucket(int d, int alpha) { return slot_in_bucket(d, alpha); }
+
+/* ------------------------------------------------------------------ */
+/* Full Hessian (the upper triangle of d2 gamma / dx_i dx_j)            */
+/* ------------------------------------------------------------------ */
+
+int oracle_hess_entries(int d) { return hess_entries(d); }
+
+/* One cell at an fp64 local coordinate: gamma[F], dgamma[d][F], hess[P][F]. */
+int oracle_eval_cell_hessian(int d, int F, int32_t N, const int32_t* log2T,
+                             const double* const* tables, const int64_t* c, const double* t,
+                             double* gamma, double* dgamma, double* hess) {
+    if (d < 1 || d > OR_MAXD) return 1;
+    or_level lv = {d, F, N, log2T, tables};
+    hermite_cell_h(&lv, c, t, gamma, dgamma, NULL, NULL, NULL, NULL, hess, NULL);
+    return 0;
+}
+
+/* Forward with the Hessian: point-major gamma[N][L][F], dgamma[N][d][L][F],
+ * hess[N][P][L][F] and their magnitudes (any magnitude array may be NULL). */
+int oracle_encode_fwd_hessian(int d, int L, int F, const int32_t* res, const int32_t* log2T,
+                              uint32_t level_mask, const double* const* tables,
+                              int64_t n_pts, const float* coords,
+                              double* gamma, double* dgamma, double* hess,
+                              double* mgamma, double* mdgamma, double* mhess, int nthreads) {
+    if (d < 1 || d > OR_MAXD || L < 1 || F < 1 || F > 8) return 1;
+    set_threads(nthreads);
+    const int P = hess_entries(d);
+#pragma omp parallel for schedule(dynamic, 256)
+    for (int64_t n = 0; n < n_pts; ++n) {
+        double g_[8], dg_[OR_MAXD * 8], h_[6 * 8], mg_[8], md_[OR_MAXD * 8], mh_[6 * 8];
+        for (int l = 0; l < L; ++l) {
+            if ((level_mask >> l) & 1u) {
+                const double* tab_l[OR_MAXD + 1];
+                for (int k = 0; k <= d; ++k)
+                    tab_l[k] = tables[k] + (size_t)l * ((size_t)1 << log2T[k]) * binom(d, k) * F;
+                or_level lv = {d, F, res[l], log2T, tab_l};
+                int64_t c[OR_MAXD];
+                double t[OR_MAXD];
+                for (int i = 0; i < d; ++i) locate(coords[n * d + i], res[l], &c[i], &t[i]);
+                hermite_cell_h(&lv, c, t, g_, dg_, NULL, mg_, md_, NULL, h_, mh_);
+            } else {
+                for (int f = 0; f < F; ++f) {
+                    g_[f] = mg_[f] = 0.0;
+                    for (int j = 0; j < d; ++j) dg_[j * F + f] = md_[j * F + f] = 0.0;
+                    for (int q = 0; q < P; ++q) h_[q * F + f] = mh_[q * F + f] = 0.0;
+                }
+            }
+            for (int f = 0; f < F; ++f) {
+                size_t o = ((size_t)n * L + l) * F + f;
+                gamma[o] = g_[f];
+                if (mgamma) mgamma[o] = mg_[f];
+                for (int j = 0; j < d; ++j) {
+                    size_t od = (((size_t)n * d + j) * L + l) * F + f;
+                    if (dgamma) dgamma[od] = dg_[j * F + f];
+                    if (mdgamma) mdgamma[od] = md_[j * F + f];
+                }
+                for (int q = 0; q < P; ++q) {
+                    size_t oh = (((size_t)n * P + q) * L + l) * F + f;
+                    if (hess) hess[oh] = h_[q * F + f];
+                    if (mhess) mhess[oh] = mh_[q * F + f];
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Backward of the Hessian forward for ONE level l: grads[k] ([T_k][C][F],
+ * caller-zeroed) += the transpose applied to g_gamma [N][L][F],
+ * g_dgamma [N][d][L][F], g_hess [N][P][L][F] (float32, any may be NULL);
+ * mags[k] the condition magnitudes (may be NULL).  Serial over points.    */
+int oracle_encode_bwd_hessian_level(int d, int L, int F, int l, const int32_t* res, const int32_t* log2T,
+                                    int64_t n_pts, const float* coords,
+                                    const float* g_gamma, const float* g_dgamma, const float* g_hess,
+                                    double* const* grads, double* const* mags) {
+    if (d < 1 || d > OR_MAXD || l < 0 || l >= L) return 1;
+    const int P = hess_entries(d);
+    const double N = (double)res[l];
+    const double dx = 1.0 / N;
+    double scale[OR_MAXD + 1];
+    for (int k = 0; k <= d; ++k) scale[k] = pow(dx, (double)k);
+    for (int64_t n = 0; n < n_pts; ++n) {
+        int64_t c[OR_MAXD];
+        double t[OR_MAXD];
+        for (int i = 0; i < d; ++i) locate(coords[n * d + i], res[l], &c[i], &t[i]);
+        double hb[OR_MAXD][2][2][3];
+        for (int i = 0; i < d; ++i)
+            for (int vi = 0; vi < 2; ++vi)
+                for (int a = 0; a < 2; ++a)
+                    hermite_1d(a, t[i] - (double)vi, vi ? -1.0 : 1.0, hb[i][vi][a]);
+        for (int v = 0; v < (1 << d); ++v) {
+            int64_t g[OR_MAXD];
+            for (int i = 0; i < d; ++i) g[i] = c[i] + (v >> i & 1);
+            for (int alpha = 0; alpha < (1 << d); ++alpha) {
+                const int k = popcount_small(alpha);
+                const uint32_t idx = vertex_index(d, g, res[l], log2T[k]);
+                const double (*h[OR_MAXD])[3];
+                for (int i = 0; i < d; ++i) h[i] = &hb[i][v >> i & 1][alpha >> i & 1];
+                double H = 1.0;
+                for (int i = 0; i < d; ++i) H *= (*h[i])[0];
+                double dH[OR_MAXD], hij[6];
+                for (int j = 0; j < d; ++j) {
+                    dH[j] = 1.0;
+                    for (int i = 0; i < d; ++i) dH[j] *= (i == j) ? (*h[i])[1] : (*h[i])[0];
+                }
+                for (int i = 0; i < d; ++i)
+                    for (int j = i; j < d; ++j) {
+                        double x = 1.0;
+                        for (int m = 0; m < d; ++m) {
+                            if (i == j) x *= (m == i) ? (*h[m])[2] : (*h[m])[0];
+                            else x *= (m == i || m == j) ? (*h[m])[1] : (*h[m])[0];
+                        }
+                        hij[hess_pos(d, i, j)] = x;
+                    }
+                const size_t off = ((size_t)idx * binom(d, k) + slot_in_bucket(d, alpha)) * F;
+                for (int f = 0; f < F; ++f) {
+                    double w = 0.0, m = 0.0;
+                    if (g_gamma) {
+                        double up = (double)g_gamma[((size_t)n * L + l) * F + f];
+                        w += up * H * scale[k];
+                        m += fabs(up) * fabs(H) * scale[k];
+                    }
+                    for (int j = 0; j < d && g_dgamma; ++j) {
+                        double ud = (double)g_dgamma[(((size_t)n * d + j) * L + l) * F + f];
+                        w += ud * scale[k] * N * dH[j];
+                        m += fabs(ud) * scale[k] * N * fabs(dH[j]);
+                    }
+                    for (int q = 0; q < P && g_hess; ++q) {
+                        double uh = (double)g_hess[(((size_t)n * P + q) * L + l) * F + f];
+                        w += uh * scale[k] * N * N * hij[q];
+                        m += fabs(uh) * scale[k] * N * N * fabs(hij[q]);
+                    }
+                    grads[k][off + f] += w;
+                    if (mags) mags[k][off + f] += m;
+                }
+            }
+        }
+    }
+    return 0;
+}

@@ -33,6 +33,13 @@ MUTANTS = [
     ("d-linear weights swapped", "w *= vi ? t[i] : 1.0 - t[i];\n                }\n                uint32_t idx = vertex_index(d, g, res[l], log2T);\n                const double* th",
      "w *= vi ? 1.0 - t[i] : t[i];\n                }\n                uint32_t idx = vertex_index(d, g, res[l], log2T);\n                const double* th"),
     ("cell not clamped at x = 1", "if (ci > (int64_t)N - 1) ci = (int64_t)N - 1;\n    *c = ci;", "*c = ci;"),
+    ("mixed second derivative drops one factor",
+     "else hij *= (m == i || m == j) ? (*h[m])[1] : (*h[m])[0];",
+     "else hij *= (m == i) ? (*h[m])[1] : (*h[m])[0];"),
+    ("Hessian missing N^2", "hess[q * F + f] += th * scale[k] * N * N * hij;", "hess[q * F + f] += th * scale[k] * N * hij;"),
+    ("Hessian backward uses the pure derivative for mixed entries",
+     "else x *= (m == i || m == j) ? (*h[m])[1] : (*h[m])[0];",
+     "else x *= (m == i || m == j) ? (*h[m])[2] : (*h[m])[0];"),
 ]
 
 
@@ -48,9 +55,9 @@ def _build(src_text, out_dir, tag):
 
 def _pins_pass(lib_path):
     env = dict(os.environ, HG_ORACLE_LIB=lib_path)
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"), "-x",
-                        "-q", "-p", "no:cacheprovider"], env=env, cwd=ROOT, capture_output=True, text=True,
-                       timeout=600)
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_hessian_pins.py"), "-x", "-q", "-p",
+                        "no:cacheprovider"], env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     return r.returncode == 0, r.stdout[-400:]
 
 
