@@ -34,9 +34,10 @@ def check_close(name: str, got: np.ndarray, want: np.ndarray, mag: np.ndarray, r
     got = np.asarray(got, np.float64)
     err = np.abs(got - want)
     bound = rtol * mag
-    bad = err > bound
+    bad = ~(err <= bound)          # a NaN (an output never written) fails too
     if bad.any():
-        i = np.unravel_index(np.argmax(np.where(bad, err / np.maximum(mag, 1e-300), 0)), err.shape)
+        i = np.unravel_index(np.argmax(np.where(bad, np.nan_to_num(err / np.maximum(mag, 1e-300), nan=np.inf), 0)),
+                             err.shape)
         raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} elements outside {rtol:g} * magnitude; "
                              f"worst at {i}: got {got[i]!r}, oracle {want[i]!r}, magnitude {mag[i]!r}")
     nz = mag > 0
