@@ -36,6 +36,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "encoded points/s (Hermite fwd γ,∇γ,∇²γ + bwd) at 1 B300; % of L2/HBM gather roofline"
+METRIC_HESSIAN = "encoded points/s (Hermite fwd γ,∇γ, full Hessian + bwd) at 1 B300; % of L2 gather roofline"
 L2_BYTES = 126 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
@@ -53,6 +54,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=1 << 20, help="points in the oracle's timed sample")
     p.add_argument("--points", type=int, default=None, help="override the workload's point count (profiling)")
+    p.add_argument("--hessian", action="store_true",
+                   help="Hermite workloads: the full-Hessian entry points (every d2/dx_i dx_j) instead of the "
+                        "Laplacian ones")
     p.add_argument("--probe-patterns", action="store_true",
                    help="print the L2 random-row gather / RED rates for 1, 2 and 4 lanes per row "
                         "(32- and 64-byte rows) as one JSON line, then exit")
@@ -108,25 +112,38 @@ def parse_ncu_dram_log(path: str) -> dict:
 
 
 def record_traffic(log_path: str, workload: str, command: str):
-    data = {"workload": workload, "source_sha256": kernel_source_hash(), "command": command,
-            "kernels": parse_ncu_dram_log(log_path)}
+    """Store the per-launch DRAM traffic of one bench configuration (key
+    `workload`) beside those of the others captured from the same kernel
+    sources; a capture from changed sources starts the file afresh."""
+    sha = kernel_source_hash()
+    try:
+        with open(TRAFFIC_FILE) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        data = {}
+    if data.get("source_sha256") != sha or "entries" not in data:
+        data = {"source_sha256": sha, "entries": {}}
+    data["entries"][workload] = {"command": command, "kernels": parse_ncu_dram_log(log_path)}
     os.makedirs(os.path.dirname(TRAFFIC_FILE), exist_ok=True)
     with open(TRAFFIC_FILE, "w") as f:
         json.dump(data, f, indent=1)
-    print(json.dumps(data))
+    print(json.dumps(data["entries"][workload]))
 
 
 def recorded_traffic(workload: str, kernel_prefix: str):
     """Per-launch DRAM bytes of the kernel from the recorded capture, or None
-    when there is none for this workload or the kernels changed since."""
+    when there is none for this configuration or the kernels changed since."""
     try:
         with open(TRAFFIC_FILE) as f:
             data = json.load(f)
     except (OSError, ValueError):
         return None
-    if data.get("workload") != workload or data.get("source_sha256") != kernel_source_hash():
+    if data.get("source_sha256") != kernel_source_hash():
         return None
-    for name, v in data.get("kernels", {}).items():
+    entry = data.get("entries", {}).get(workload)
+    if not entry:
+        return None
+    for name, v in entry.get("kernels", {}).items():
         if name.startswith(kernel_prefix):
             return v["bytes_per_launch"]
     return None
@@ -148,7 +165,7 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
 # workload description and algorithmic byte counts
 # ---------------------------------------------------------------------------
 
-def describe(w, mask, layout):
+def describe(w, mask, layout, hessian=False):
     res_note = f"N_min={w.n_min}, N_max={w.n_max}"
     lt = w.log2_T[0]
     return {
@@ -163,6 +180,7 @@ def describe(w, mask, layout):
         "description": f"{w.kind} d={w.d}: N={w.n_points} pts, L={w.L}, F={w.F}, T=2^{lt}, {res_note}, {w.dtype}",
         "l2_flush": "inputs larger than L2 (tables + upstream gradients + outputs exceed 126 MB per step)",
         "parallelism": "replicas",
+        "second_order": ("full Hessian" if hessian else "Laplacian") if w.kind == "hermite" else None,
     }
 
 
@@ -236,6 +254,18 @@ class ClockSampler:
 # the CPU oracle (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
+def traffic_key(w, points=None, hessian=False):
+    """Name under which the DRAM traffic of a bench configuration is recorded."""
+    key = w.name if not points else f"{w.name}@{points}"
+    return key + "+hessian" if hessian and w.kind == "hermite" else key
+
+
+def add_hessian_upstream(w, inputs, rank=0):
+    """Seeded upstream gradient of the full Hessian (point-major)."""
+    from multiresolution_hash_grid_02_b300 import workloads as W
+    inputs["g_hess"] = W.draw_upstream_hessian(np.random.default_rng(w.seed + 1000 + rank), w)
+
+
 def oracle_setup(w, inputs):
     import oracle
     from multiresolution_hash_grid_02_b300 import workloads as W
@@ -248,10 +278,15 @@ def oracle_setup(w, inputs):
     return oracle, res, tabs
 
 
-def oracle_step(oracle, w, res, tabs, inputs, lo, hi, mask, threads):
+def oracle_step(oracle, w, res, tabs, inputs, lo, hi, mask, threads, hessian=False):
     """Oracle forward + backward on points [lo, hi) of the workload."""
     x = inputs["coords"][lo:hi]
-    if w.kind == "hermite":
+    if w.kind == "hermite" and hessian:
+        oracle.encode_fwd_hessian(w.d, w.F, res, w.log2_T, tabs, x, level_mask=mask, nthreads=threads,
+                                  with_mags=False)
+        oracle.encode_bwd_hessian(w.d, w.F, res, w.log2_T, x, inputs["g_gamma"][lo:hi], inputs["g_dgamma"][lo:hi],
+                                  inputs["g_hess"][lo:hi], level_mask=mask, with_mags=False, nthreads=threads)
+    elif w.kind == "hermite":
         oracle.encode_fwd(w.d, w.F, res, w.log2_T, tabs, x, level_mask=mask, nthreads=threads, with_mags=False)
         oracle.encode_bwd(w.d, w.F, res, w.log2_T, x, inputs["g_gamma"][lo:hi], inputs["g_dgamma"][lo:hi],
                           inputs["g_lap"][lo:hi], level_mask=mask, with_mags=False, nthreads=threads)
@@ -261,13 +296,13 @@ def oracle_step(oracle, w, res, tabs, inputs, lo, hi, mask, threads):
                           with_mags=False, nthreads=threads)
 
 
-def cpu_baseline(w, inputs, mask, sample):
+def cpu_baseline(w, inputs, mask, sample, hessian=False):
     oracle, res, tabs = oracle_setup(w, inputs)
     threads = len(os.sched_getaffinity(0))
     sample = min(sample, w.n_points)
-    oracle_step(oracle, w, res, tabs, inputs, 0, min(256, sample), mask, threads)  # warm the code path
+    oracle_step(oracle, w, res, tabs, inputs, 0, min(256, sample), mask, threads, hessian)  # warm the code path
     t0 = time.perf_counter()
-    oracle_step(oracle, w, res, tabs, inputs, 0, sample, mask, threads)
+    oracle_step(oracle, w, res, tabs, inputs, 0, sample, mask, threads, hessian)
     dt = time.perf_counter() - t0
     return {"value": sample / dt, "unit": "points/s", "cores": threads, "kind": "oracle",
             "sample": f"first {sample} of the {w.n_points} points, all {bin(mask).count('1')} active levels, "
@@ -282,6 +317,9 @@ def run_reference(args):
     w = W.WORKLOADS[args.config]
     mask = args.level_mask if args.level_mask is not None else (1 << w.L) - 1
     inputs = W.make(w)
+    hessian = args.hessian and w.kind == "hermite"
+    if hessian:
+        add_hessian_upstream(w, inputs)
     oracle, res, tabs = oracle_setup(w, inputs)
     threads = len(os.sched_getaffinity(0))
     per_step = min(max(256, args.cpu_sample // 8), w.n_points)
@@ -289,15 +327,15 @@ def run_reference(args):
     for i in range(args.warmup + args.steps):
         lo = (i * per_step) % max(1, w.n_points - per_step)
         t0 = time.perf_counter()
-        oracle_step(oracle, w, res, tabs, inputs, lo, lo + per_step, mask, threads)
+        oracle_step(oracle, w, res, tabs, inputs, lo, lo + per_step, mask, threads, hessian)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     t = sum(times)
     value = per_step * len(times) / t
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "points/s", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": METRIC_HESSIAN if hessian else METRIC, "value": value, "unit": "points/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded numpy)", "config": describe(w, mask, args.layout),
+            "data": "synthetic (seeded numpy)", "config": describe(w, mask, args.layout, hessian),
             "cpu_baseline": {"value": value, "unit": "points/s", "cores": threads, "kind": "oracle",
                              "sample": f"{per_step} points per step (of {w.n_points}), fwd + bwd, all active levels"},
             "e2e": {"value": value, "unit": "points/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -381,10 +419,12 @@ def main():
     if args.record_traffic:
         from multiresolution_hash_grid_02_b300 import workloads as W
         w = W.WORKLOADS[args.config]
-        record_traffic(args.record_traffic, w.name if not args.points else f"{w.name}@{args.points}",
+        extra = (f" --config {args.config}" if args.config != 4 else "") + (" --hessian" if args.hessian else "") + \
+            (f" --points {args.points}" if args.points else "")
+        record_traffic(args.record_traffic, traffic_key(w, args.points, args.hessian),
                        "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
                        "--clock-control none -k regex:hermite -s 2 -c 2 python bench.py --steps 2 --warmup 1 "
-                       "--no-e2e --no-cpu-baseline")
+                       "--no-e2e --no-cpu-baseline" + extra)
         return
     if args.impl == "reference":
         run_reference(args)
@@ -408,7 +448,11 @@ def main():
     layout = M.HG_FEATURE_MAJOR if args.layout == "feature" else M.HG_POINT_MAJOR
     fm = layout == M.HG_FEATURE_MAJOR
     inputs = W.make(w, seed=w.seed + rank)
+    hessian = args.hessian and w.kind == "hermite"
+    if hessian:
+        add_hessian_upstream(w, inputs, rank)
     n, d, L, F = w.n_points, w.d, w.L, w.F
+    P = d * (d + 1) // 2
     desc = M.GridDesc(d=d, L=L, F=F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T * (d + 1) if w.kind == "linear"
                       else w.log2_T, level_mask=mask, dtype=M.HG_F16 if w.dtype == "f16" else M.HG_F32, layout=layout)
 
@@ -421,12 +465,14 @@ def main():
     conv = (lambda a, ax: W.to_feature_major(a, ax)) if fm else (lambda a, ax: a)
     gg = dev(conv(inputs["g_gamma"], False))
     gd = dev(conv(inputs["g_dgamma"], True)) if hermite else None
-    gl = dev(conv(inputs["g_lap"], False)) if hermite else None
     shape_g = (L, F, n) if fm else (n, L, F)
     shape_d = (d, L, F, n) if fm else (n, d, L, F)
+    # second-order output and its upstream gradient: the Laplacian, or the full Hessian
+    shape_s = ((P, L, F, n) if fm else (n, P, L, F)) if hessian else shape_g
+    gl = (dev(conv(inputs["g_hess"], True)) if hessian else dev(conv(inputs["g_lap"], False))) if hermite else None
     gamma = torch.empty(shape_g, device="cuda")
     dgamma = torch.empty(shape_d, device="cuda") if hermite else None
-    lap = torch.empty(shape_g, device="cuda") if hermite else None
+    lap = torch.empty(shape_s, device="cuda") if hermite else None
     grad = torch.zeros(table.shape, dtype=torch.float32, device="cuda")
     if hermite:
         tviews, gviews = M.packed_views(table, d), M.packed_views(grad, d)
@@ -435,13 +481,17 @@ def main():
     stream = torch.cuda.current_stream()
 
     def fwd():
-        if hermite:
+        if hessian:
+            hg.hg_encode_fwd_hessian(desc, n, coords, tviews, gamma, dgamma, lap, stream)
+        elif hermite:
             hg.hg_encode_fwd(desc, n, coords, tviews, gamma, dgamma, lap, stream)
         else:
             hg.hg_linear_fwd(desc, n, coords, tviews, gamma, stream)
 
     def bwd():
-        if hermite:
+        if hessian:
+            hg.hg_encode_bwd_hessian(desc, n, coords, gg, gd, gl, gviews, stream)
+        elif hermite:
             hg.hg_encode_bwd(desc, n, coords, gg, gd, gl, gviews, stream)
         else:
             hg.hg_linear_bwd(desc, n, coords, gg, gviews, stream)
@@ -515,7 +565,7 @@ def main():
     k = kernels[dom]
     kname = {"fwd": "hermite_fwd" if w.kind == "hermite" else "linear_fwd",
              "bwd": "hermite_bwd" if w.kind == "hermite" else "linear_bwd"}[dom]
-    traffic = recorded_traffic(w.name if not args.points else f"{w.name}@{args.points}", kname)
+    traffic = recorded_traffic(traffic_key(w, args.points, hessian), kname)
     roofline = {"bound": "l2", "kernel": dom, "achieved": k["achieved"], "peak": k["peak"], "unit": "GB/s",
                 "frac": k["frac"], "traffic": traffic,
                 "peak_source": "measured live by this run's L2 probes (hg_probe_l2_gather / hg_probe_l2_red)",
@@ -523,19 +573,20 @@ def main():
 
     e2e = None
     if not args.no_e2e and rank == 0:
-        e2e = run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, hermite, grad,
-                      stream)
+        e2e = run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, shape_s, hermite,
+                      hessian, grad, stream)
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        cpu = cpu_baseline(w, inputs, mask, args.cpu_sample)
+        cpu = cpu_baseline(w, inputs, mask, args.cpu_sample, hessian)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "points/s", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC_HESSIAN if hessian else METRIC, "value": value, "unit": "points/s", "n_gpus": world,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded numpy: uniform coords, uniform coefficients, N(0,1) upstream gradients)",
-            "config": describe(w, mask, args.layout),
+            "config": describe(w, mask, args.layout, hessian),
             "roofline": roofline, "kernels": kernels,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
@@ -546,14 +597,15 @@ def main():
         dist.destroy_process_group()
 
 
-def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, hermite, grad, stream,
-            steps=8, warmup=2):
+def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, shape_s, hermite, hessian,
+            grad, stream, steps=8, warmup=2):
     """The step through the C ABI with inputs starting in pinned host memory,
     pipelined over three streams as a streaming user would run it: the
     host-to-device copy of step i+1's coordinates and upstream gradients and
     the device-to-host read of step i-1's gamma / grad gamma / Laplacian
     overlap the encode of step i (two device buffer sets).  Every step's
-    copies and kernels are inside the timed region."""
+    copies and kernels are inside the timed region.  With `hessian` the
+    second-order output and upstream are the full Hessian's (shape_s)."""
     n = w.n_points
 
     def pinned(a):
@@ -561,8 +613,9 @@ def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, sha
 
     h_in = [pinned(inputs["coords"]), pinned(conv(inputs["g_gamma"], False))]
     if hermite:
-        h_in += [pinned(conv(inputs["g_dgamma"], True)), pinned(conv(inputs["g_lap"], False))]
-    out_shapes = [shape_g] + ([shape_d, shape_g] if hermite else [])
+        second = conv(inputs["g_hess"], True) if hessian else conv(inputs["g_lap"], False)
+        h_in += [pinned(conv(inputs["g_dgamma"], True)), pinned(second)]
+    out_shapes = [shape_g] + ([shape_d, shape_s] if hermite else [])
     d_in = [[torch.empty_like(t, device="cuda") for t in h_in] for _ in range(2)]
     d_out = [[torch.empty(sh, device="cuda") for sh in out_shapes] for _ in range(2)]
     h_out = [[torch.empty(sh).pin_memory() for sh in out_shapes] for _ in range(2)]
@@ -588,7 +641,10 @@ def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, sha
             s_comp.wait_event(ev_out[b])             # step i-2's outputs are on the host
         grad.zero_()
         c, gg = d_in[b][0], d_in[b][1]
-        if hermite:
+        if hessian:
+            hg.hg_encode_fwd_hessian(desc, n, c, tviews, d_out[b][0], d_out[b][1], d_out[b][2], s_comp)
+            hg.hg_encode_bwd_hessian(desc, n, c, gg, d_in[b][2], d_in[b][3], gviews, s_comp)
+        elif hermite:
             hg.hg_encode_fwd(desc, n, c, tviews, d_out[b][0], d_out[b][1], d_out[b][2], s_comp)
             hg.hg_encode_bwd(desc, n, c, gg, d_in[b][2], d_in[b][3], gviews, s_comp)
         else:
@@ -614,7 +670,8 @@ def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, sha
     ms = a.elapsed_time(e) / steps
     return {"value": n / (ms * 1e-3), "unit": "points/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms, "steps": steps,
-            "note": "pinned host buffers; coordinates and upstream gradients in, gamma/grad gamma/Laplacian out, "
+            "note": "pinned host buffers; coordinates and upstream gradients in, gamma/grad gamma/"
+                    + ("Hessian" if hessian else "Laplacian") + " out, "
                     "every step; copies of neighbouring steps overlap the encode (3 streams, 2 buffer sets); "
                     "gradient tables stay on the device"}
 

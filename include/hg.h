@@ -179,6 +179,31 @@ hg_status hg_encode_bwd(const hg_grid_desc* desc, int64_t n, const float* coords
                         const float* g_gamma, const float* g_dgamma, const float* g_lap,
                         const hg_grad_table* grads, hg_stream stream);
 
+/* Hermite forward with the full Hessian: the second derivatives of the
+ * encoding's bases [HNGP 关键设计 2] give every d2 gamma / dx_i dx_j, not only
+ * their sum (the Laplacian), for PDEs with mixed derivatives.  For each point
+ * and active level the P = d(d+1)/2 entries of the upper triangle, row-major
+ * (2D xx, xy, yy; 3D xx, xy, xz, yy, yz, zz), are
+ *   hess_ij = sum_g sum_alpha theta^(alpha)[idx_k(g)] dx^|alpha| d2H/dx_i dx_j.
+ *   gamma, dgamma: as hg_encode_fwd (dgamma may be NULL)
+ *   hess:   device float32 output (required when n > 0):
+ *           HG_POINT_MAJOR [n][P][L][F], HG_FEATURE_MAJOR [P][L][F][n]
+ * The trace of hess equals hg_encode_fwd's lap to rounding.
+ * Errors: as hg_encode_fwd. */
+hg_status hg_encode_fwd_hessian(const hg_grid_desc* desc, int64_t n, const float* coords,
+                                const hg_table* tables, float* gamma, float* dgamma, float* hess,
+                                hg_stream stream);
+
+/* Backward of hg_encode_fwd_hessian: as hg_encode_bwd with the upstream
+ * gradient of the Hessian (g_hess, the layout of hess, may be NULL) in place
+ * of that of the Laplacian:
+ *   grad_k[l][idx_k(g)][slot(alpha)][f] += dx^|alpha| * ( g_gamma * H
+ *       + sum_j g_dgamma_j * dH/dx_j + sum_{i<=j} g_hess_ij * d2H/dx_i dx_j ).
+ * Errors: as hg_encode_fwd. */
+hg_status hg_encode_bwd_hessian(const hg_grid_desc* desc, int64_t n, const float* coords,
+                                const float* g_gamma, const float* g_dgamma, const float* g_hess,
+                                const hg_grad_table* grads, hg_stream stream);
+
 /* d-linear forward (Instant-NGP) [INGP 流程与原理 steps 1-3]:
  *   gamma[l][f] = sum_{corner v} w_v * table[l][idx_0(c+v)][f],
  *   w_v = prod_i (v_i ? t_i : 1 - t_i),

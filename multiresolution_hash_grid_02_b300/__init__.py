@@ -2,8 +2,8 @@
 Instant-NGP) -- Python side of the C-ABI library ``libhg.so``.
 
 ``from multiresolution_hash_grid_02_b300 import hg`` gives the binding with the
-C entry-point names (``hg.hg_encode_fwd`` ...); ``encoding`` holds the
-autograd wrapper; ``workloads`` the seeded synthetic inputs.  Importing the
+C entry-point names (``hg.hg_encode_fwd`` ...); ``workloads`` holds the
+seeded synthetic inputs.  Importing the
 package does not load the CUDA library; the first call does, and raises if it
 is missing.
 """

@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         "hg_level_resolutions": [D, ctypes.POINTER(c_i32)],
         "hg_encode_fwd": [D, c_i64, c_vp, T, c_vp, c_vp, c_vp, c_vp],
         "hg_encode_bwd": [D, c_i64, c_vp, c_vp, c_vp, c_vp, G, c_vp],
+        "hg_encode_fwd_hessian": [D, c_i64, c_vp, T, c_vp, c_vp, c_vp, c_vp],
+        "hg_encode_bwd_hessian": [D, c_i64, c_vp, c_vp, c_vp, c_vp, G, c_vp],
         "hg_linear_fwd": [D, c_i64, c_vp, T, c_vp, c_vp],
         "hg_linear_bwd": [D, c_i64, c_vp, c_vp, G, c_vp],
         "hg_hash_indices": [D, c_i64, c_vp, c_vp, c_vp],
@@ -224,6 +226,26 @@ def hg_encode_bwd(desc: GridDesc, n: int, coords, g_gamma, g_dgamma, g_lap, grad
                              _tables_c(grads, hg_grad_table), _stream(stream) if n else 0)
     if check:
         _check(st, "hg_encode_bwd")
+    return st
+
+
+def hg_encode_fwd_hessian(desc: GridDesc, n: int, coords, tables: Sequence[TableView], gamma, dgamma=None,
+                          hess=None, stream=None, check: bool = True) -> int:
+    c = desc.as_c()
+    st = lib().hg_encode_fwd_hessian(ctypes.byref(c), int(n), _addr(coords), _tables_c(tables, hg_table),
+                                     _addr(gamma), _addr(dgamma), _addr(hess), _stream(stream) if n else 0)
+    if check:
+        _check(st, "hg_encode_fwd_hessian")
+    return st
+
+
+def hg_encode_bwd_hessian(desc: GridDesc, n: int, coords, g_gamma, g_dgamma, g_hess, grads: Sequence[TableView],
+                          stream=None, check: bool = True) -> int:
+    c = desc.as_c()
+    st = lib().hg_encode_bwd_hessian(ctypes.byref(c), int(n), _addr(coords), _addr(g_gamma), _addr(g_dgamma),
+                                     _addr(g_hess), _tables_c(grads, hg_grad_table), _stream(stream) if n else 0)
+    if check:
+        _check(st, "hg_encode_bwd_hessian")
     return st
 
 

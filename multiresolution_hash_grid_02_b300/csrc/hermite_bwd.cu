@@ -12,6 +12,9 @@
 // The transpose runs the separable blend backwards (axis 2, then 1, then 0)
 // and yields all 2^d x 2^d coefficient gradients of a feature in registers;
 // the packed layout then issues one 16-byte vector RED per four floats.
+// The full-Hessian variant (HESS) takes the upstream gradient of every
+// second derivative instead of the Laplacian's, and transposes the
+// forward's split second-order sums.
 #include <cuda_runtime.h>
 
 #include "hg_device.cuh"
@@ -67,7 +70,80 @@ __device__ __forceinline__ void blend3_t(float gg, const float (&gd)[3], float g
         }
 }
 
-template <int D, int FC, bool VEC>
+// Transposed 2D blend with the full Hessian: upstream (gg, gd[0..1],
+// gh = (xx, xy, yy)) -> qb[corner][alpha].
+__device__ __forceinline__ void blend2h_t(float gg, const float (&gd)[3], const float (&gh)[6], const Basis1& b0,
+                                          const Basis1& b1, float (&qb)[4][4]) {
+#pragma unroll
+    for (int v1 = 0; v1 < 2; ++v1)
+#pragma unroll
+        for (int a1 = 0; a1 < 2; ++a1) {
+            const float s = fmaf(gg, b1.w[v1][a1], fmaf(gd[1], b1.d1[v1][a1], gh[2] * b1.d2[v1][a1]));
+            const float s1 = fmaf(gd[0], b1.w[v1][a1], gh[1] * b1.d1[v1][a1]);
+            const float s2 = gh[0] * b1.w[v1][a1];
+#pragma unroll
+            for (int v0 = 0; v0 < 2; ++v0)
+#pragma unroll
+                for (int a0 = 0; a0 < 2; ++a0)
+                    qb[v0 + 2 * v1][a0 + 2 * a1] = fmaf(s, b0.w[v0][a0], fmaf(s1, b0.d1[v0][a0], s2 * b0.d2[v0][a0]));
+        }
+}
+
+// Transposed 3D blend with the full Hessian, gh = (xx, xy, xz, yy, yz, zz):
+// the adjoints of the forward's sums A, B, C, D00, D11, E01 per (v2, a2),
+// then of s, s1, s2 per (v1, a1).
+__device__ __forceinline__ void blend3h_t(float gg, const float (&gd)[3], const float (&gh)[6], const Basis1& b0,
+                                          const Basis1& b1, const Basis1& b2, float (&qb)[8][8]) {
+#pragma unroll
+    for (int v2 = 0; v2 < 2; ++v2)
+#pragma unroll
+        for (int a2 = 0; a2 < 2; ++a2) {
+            const float A = fmaf(gg, b2.w[v2][a2], fmaf(gd[2], b2.d1[v2][a2], gh[5] * b2.d2[v2][a2]));
+            const float B = fmaf(gd[0], b2.w[v2][a2], gh[2] * b2.d1[v2][a2]);
+            const float C = fmaf(gd[1], b2.w[v2][a2], gh[4] * b2.d1[v2][a2]);
+            const float D00 = gh[0] * b2.w[v2][a2];
+            const float D11 = gh[3] * b2.w[v2][a2];
+            const float E01 = gh[1] * b2.w[v2][a2];
+#pragma unroll
+            for (int v1 = 0; v1 < 2; ++v1)
+#pragma unroll
+                for (int a1 = 0; a1 < 2; ++a1) {
+                    const float s = fmaf(A, b1.w[v1][a1], fmaf(C, b1.d1[v1][a1], D11 * b1.d2[v1][a1]));
+                    const float s1 = fmaf(B, b1.w[v1][a1], E01 * b1.d1[v1][a1]);
+                    const float s2 = D00 * b1.w[v1][a1];
+#pragma unroll
+                    for (int v0 = 0; v0 < 2; ++v0)
+#pragma unroll
+                        for (int a0 = 0; a0 < 2; ++a0)
+                            qb[v0 + 2 * v1 + 4 * v2][a0 + 2 * a1 + 4 * a2] =
+                                fmaf(s, b0.w[v0][a0], fmaf(s1, b0.d1[v0][a0], s2 * b0.d2[v0][a0]));
+                }
+        }
+}
+
+// Upstream gradients of one (point, level, feature): gamma, grad, and the
+// Laplacian's (gl) or, under HESS, every Hessian entry's (gh[0..P-1]).
+template <int D, bool HESS>
+__device__ __forceinline__ void load_upstream(const BwdParams& p, int64_t n, int64_t lf, float& gg, float (&gd)[3],
+                                              float& gl, float (&gh)[6]) {
+    gg = p.g_gamma ? __ldg(p.g_gamma + n * p.c.sn + lf * p.c.sf) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+        gd[j] = (p.g_dgamma && j < D) ? __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf) : 0.f;
+    gl = 0.f;
+#pragma unroll
+    for (int k = 0; k < 6; ++k) gh[k] = 0.f;
+    if constexpr (HESS) {
+        if (p.g_hess) {
+#pragma unroll
+            for (int k = 0; k < D * (D + 1) / 2; ++k) gh[k] = __ldg(p.g_hess + n * p.c.hsn + k * p.c.hsq + lf * p.c.hsf);
+        }
+    } else {
+        gl = p.g_lap ? __ldg(p.g_lap + n * p.c.sn + lf * p.c.sf) : 0.f;
+    }
+}
+
+template <int D, int FC, bool VEC, bool HESS>
 __global__ void __launch_bounds__(kBlock) hermite_bwd_kernel(const __grid_constant__ BwdParams p) {
     constexpr int V = 1 << D;
     const int l = p.c.lvl[blockIdx.y];
@@ -102,14 +178,15 @@ __global__ void __launch_bounds__(kBlock) hermite_bwd_kernel(const __grid_consta
 #pragma unroll
         for (int f = 0; f < FC; ++f) {
             const int64_t lf = static_cast<int64_t>(l) * F + f0 + f;
-            const float gg = p.g_gamma ? __ldcs(p.g_gamma + n * p.c.sn + lf * p.c.sf) : 0.f;
-            const float gl = p.g_lap ? __ldcs(p.g_lap + n * p.c.sn + lf * p.c.sf) : 0.f;
-            float gd[3] = {0.f, 0.f, 0.f};
-            if (p.g_dgamma) {
-#pragma unroll
-                for (int j = 0; j < D; ++j) gd[j] = __ldcs(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf);
-            }
-            if constexpr (D == 2) {
+            float gg, gd[3], gl, gh[6];
+            load_upstream<D, HESS>(p, n, lf, gg, gd, gl, gh);
+            if constexpr (HESS) {
+                if constexpr (D == 2) {
+                    blend2h_t(gg, gd, gh, B[0], B[1], qb[f]);
+                } else {
+                    blend3h_t(gg, gd, gh, B[0], B[1], B[D - 1], qb[f]);
+                }
+            } else if constexpr (D == 2) {
                 blend2_t(gg, gd, gl, B[0], B[1], qb[f]);
             } else {
                 blend3_t(gg, gd, gl, B[0], B[1], B[D - 1], qb[f]);
@@ -216,6 +293,80 @@ __device__ __forceinline__ void unit_blend_t_f2(uint64_t gg, const uint64_t (&gd
     }
 }
 
+// unit_blend_t with the full Hessian (gh in the order of blend2h_t /
+// blend3h_t).
+template <int D>
+__device__ __forceinline__ void unit_blend_t_hess(float gg, const float (&gd)[3], const float (&gh)[6],
+                                                  const AxisW& W0, const AxisW& W1, const AxisW& W2,
+                                                  float (&qb)[1 << D]) {
+    if constexpr (D == 3) {
+#pragma unroll
+        for (int v2 = 0; v2 < 2; ++v2) {
+            const float A = fmaf(gg, W2.w[v2], fmaf(gd[2], W2.d1[v2], gh[5] * W2.d2[v2]));
+            const float B = fmaf(gd[0], W2.w[v2], gh[2] * W2.d1[v2]);
+            const float C = fmaf(gd[1], W2.w[v2], gh[4] * W2.d1[v2]);
+            const float D00 = gh[0] * W2.w[v2];
+            const float D11 = gh[3] * W2.w[v2];
+            const float E01 = gh[1] * W2.w[v2];
+#pragma unroll
+            for (int v1 = 0; v1 < 2; ++v1) {
+                const float s = fmaf(A, W1.w[v1], fmaf(C, W1.d1[v1], D11 * W1.d2[v1]));
+                const float s1 = fmaf(B, W1.w[v1], E01 * W1.d1[v1]);
+                const float s2 = D00 * W1.w[v1];
+#pragma unroll
+                for (int v0 = 0; v0 < 2; ++v0)
+                    qb[v0 + 2 * v1 + 4 * v2] = fmaf(s, W0.w[v0], fmaf(s1, W0.d1[v0], s2 * W0.d2[v0]));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int v1 = 0; v1 < 2; ++v1) {
+            const float s = fmaf(gg, W1.w[v1], fmaf(gd[1], W1.d1[v1], gh[2] * W1.d2[v1]));
+            const float s1 = fmaf(gd[0], W1.w[v1], gh[1] * W1.d1[v1]);
+            const float s2 = gh[0] * W1.w[v1];
+#pragma unroll
+            for (int v0 = 0; v0 < 2; ++v0) qb[v0 + 2 * v1] = fmaf(s, W0.w[v0], fmaf(s1, W0.d1[v0], s2 * W0.d2[v0]));
+        }
+    }
+}
+
+// The same for both features at once (F = 2), as unit_blend_t_f2.
+template <int D>
+__device__ __forceinline__ void unit_blend_t_hess_f2(uint64_t gg, const uint64_t (&gd)[3], const uint64_t (&gh)[6],
+                                                     const AxisW2& W0, const AxisW2& W1, const AxisW2& W2,
+                                                     uint64_t (&qb)[1 << D]) {
+    if constexpr (D == 3) {
+#pragma unroll
+        for (int v2 = 0; v2 < 2; ++v2) {
+            const uint64_t A = f2_fma(gg, W2.w[v2], f2_fma(gd[2], W2.d1[v2], f2_mul(gh[5], W2.d2[v2])));
+            const uint64_t B = f2_fma(gd[0], W2.w[v2], f2_mul(gh[2], W2.d1[v2]));
+            const uint64_t C = f2_fma(gd[1], W2.w[v2], f2_mul(gh[4], W2.d1[v2]));
+            const uint64_t D00 = f2_mul(gh[0], W2.w[v2]);
+            const uint64_t D11 = f2_mul(gh[3], W2.w[v2]);
+            const uint64_t E01 = f2_mul(gh[1], W2.w[v2]);
+#pragma unroll
+            for (int v1 = 0; v1 < 2; ++v1) {
+                const uint64_t s = f2_fma(A, W1.w[v1], f2_fma(C, W1.d1[v1], f2_mul(D11, W1.d2[v1])));
+                const uint64_t s1 = f2_fma(B, W1.w[v1], f2_mul(E01, W1.d1[v1]));
+                const uint64_t s2 = f2_mul(D00, W1.w[v1]);
+#pragma unroll
+                for (int v0 = 0; v0 < 2; ++v0)
+                    qb[v0 + 2 * v1 + 4 * v2] = f2_fma(s, W0.w[v0], f2_fma(s1, W0.d1[v0], f2_mul(s2, W0.d2[v0])));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int v1 = 0; v1 < 2; ++v1) {
+            const uint64_t s = f2_fma(gg, W1.w[v1], f2_fma(gd[1], W1.d1[v1], f2_mul(gh[2], W1.d2[v1])));
+            const uint64_t s1 = f2_fma(gd[0], W1.w[v1], f2_mul(gh[1], W1.d1[v1]));
+            const uint64_t s2 = f2_mul(gh[0], W1.w[v1]);
+#pragma unroll
+            for (int v0 = 0; v0 < 2; ++v0)
+                qb[v0 + 2 * v1] = f2_fma(s, W0.w[v0], f2_fma(s1, W0.d1[v0], f2_mul(s2, W0.d2[v0])));
+        }
+    }
+}
+
 // Lane-split backward for packed fp32 gradient rows of 32 or 64 bytes: G
 // lanes share one (point, level); lane g owns the 16-byte chunk g of every
 // corner row (S = 2^D/G slots x FC features = 4 floats), computes the
@@ -223,7 +374,10 @@ __device__ __forceinline__ void unit_blend_t_f2(uint64_t gg, const uint64_t (&gd
 // so one warp instruction reduces into whole rows.
 // Four 256-thread blocks per SM (64 registers): the run-aggregation branch,
 // rarely taken on random points, must not cost occupancy on the common path.
-template <int D, int FC, int G>
+// The full-Hessian variant (twice the upstream values) spills a few words to
+// local memory at this bound; on B300 that costs less than the occupancy it
+// keeps (3D, 2^21 points: 4.08 ms at four blocks, 4.42 at three, 5.98 at two).
+template <int D, int FC, int G, bool HESS>
 __global__ void __launch_bounds__(kBlock, 4) hermite_bwd_split_kernel(const __grid_constant__ BwdParams p) {
     constexpr int V = 1 << D, S = V / G;
     static_assert(S * FC == 4, "one 16-byte chunk per lane");
@@ -243,16 +397,9 @@ __global__ void __launch_bounds__(kBlock, 4) hermite_bwd_split_kernel(const __gr
         locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
         B[i] = hermite_basis(t[i], lv);
     }
-    float gg[FC], gl[FC], gd[FC][3];
+    float gg[FC], gl[FC], gd[FC][3], gh[FC][6];
 #pragma unroll
-    for (int f = 0; f < FC; ++f) {
-        const int64_t lf = static_cast<int64_t>(l) * F + f;
-        gg[f] = p.g_gamma ? __ldg(p.g_gamma + n * p.c.sn + lf * p.c.sf) : 0.f;
-        gl[f] = p.g_lap ? __ldg(p.g_lap + n * p.c.sn + lf * p.c.sf) : 0.f;
-#pragma unroll
-        for (int j = 0; j < 3; ++j)
-            gd[f][j] = (p.g_dgamma && j < D) ? __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf) : 0.f;
-    }
+    for (int f = 0; f < FC; ++f) load_upstream<D, HESS>(p, n, static_cast<int64_t>(l) * F + f, gg[f], gd[f], gl[f], gh[f]);
     float r[V][4];
 #pragma unroll
     for (int u = 0; u < S; ++u) {
@@ -263,15 +410,27 @@ __global__ void __launch_bounds__(kBlock, 4) hermite_bwd_split_kernel(const __gr
             const uint64_t gd2[3] = {f2_pack(gd[0][0], gd[1][0]), f2_pack(gd[0][1], gd[1][1]),
                                      f2_pack(gd[0][2], gd[1][2])};
             uint64_t qb[V];
-            unit_blend_t_f2<D>(f2_pack(gg[0], gg[1]), gd2, f2_pack(gl[0], gl[1]), axis_dup(W0), axis_dup(W1),
-                               axis_dup(W2), qb);
+            if constexpr (HESS) {
+                uint64_t gh2[6];
+#pragma unroll
+                for (int k = 0; k < 6; ++k) gh2[k] = f2_pack(gh[0][k], gh[1][k]);
+                unit_blend_t_hess_f2<D>(f2_pack(gg[0], gg[1]), gd2, gh2, axis_dup(W0), axis_dup(W1), axis_dup(W2),
+                                        qb);
+            } else {
+                unit_blend_t_f2<D>(f2_pack(gg[0], gg[1]), gd2, f2_pack(gl[0], gl[1]), axis_dup(W0), axis_dup(W1),
+                                   axis_dup(W2), qb);
+            }
 #pragma unroll
             for (int v = 0; v < V; ++v) f2_unpack(qb[v], r[v][u * FC], r[v][u * FC + 1]);
         } else {
 #pragma unroll
             for (int f = 0; f < FC; ++f) {
                 float qb[V];
-                unit_blend_t<D>(gg[f], gd[f], gl[f], W0, W1, W2, qb);
+                if constexpr (HESS) {
+                    unit_blend_t_hess<D>(gg[f], gd[f], gh[f], W0, W1, W2, qb);
+                } else {
+                    unit_blend_t<D>(gg[f], gd[f], gl[f], W0, W1, W2, qb);
+                }
 #pragma unroll
                 for (int v = 0; v < V; ++v) r[v][u * FC + f] = qb[v];
             }
@@ -302,7 +461,7 @@ constexpr int kPrivBlock = 512;
 // the coarsest levels -- a few hundred to a few thousand rows hit by millions
 // of points -- serialise on the same L2 addresses.  Each contribution is the
 // split kernel's (part g plays lane g).
-template <int D, int FC, int G>
+template <int D, int FC, int G, bool HESS>
 __global__ void __launch_bounds__(kPrivBlock) hermite_bwd_priv_kernel(const __grid_constant__ BwdParams p) {
     constexpr int V = 1 << D, S = V / G;
     static_assert(S * FC == 4, "one 16-byte part per row");
@@ -326,16 +485,10 @@ __global__ void __launch_bounds__(kPrivBlock) hermite_bwd_priv_kernel(const __gr
             locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
             B[i] = hermite_basis(t[i], lv);
         }
-        float gg[FC], gl[FC], gd[FC][3];
+        float gg[FC], gl[FC], gd[FC][3], gh[FC][6];
 #pragma unroll
-        for (int f = 0; f < FC; ++f) {
-            const int64_t lf = static_cast<int64_t>(l) * F + f;
-            gg[f] = p.g_gamma ? __ldg(p.g_gamma + n * p.c.sn + lf * p.c.sf) : 0.f;
-            gl[f] = p.g_lap ? __ldg(p.g_lap + n * p.c.sn + lf * p.c.sf) : 0.f;
-#pragma unroll
-            for (int j = 0; j < 3; ++j)
-                gd[f][j] = (p.g_dgamma && j < D) ? __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf) : 0.f;
-        }
+        for (int f = 0; f < FC; ++f)
+            load_upstream<D, HESS>(p, n, static_cast<int64_t>(l) * F + f, gg[f], gd[f], gl[f], gh[f]);
         float r[V][4];
 #pragma unroll
         for (int u = 0; u < S; ++u) {
@@ -345,7 +498,11 @@ __global__ void __launch_bounds__(kPrivBlock) hermite_bwd_priv_kernel(const __gr
 #pragma unroll
             for (int f = 0; f < FC; ++f) {
                 float qb[V];
-                unit_blend_t<D>(gg[f], gd[f], gl[f], W0, W1, W2, qb);
+                if constexpr (HESS) {
+                    unit_blend_t_hess<D>(gg[f], gd[f], gh[f], W0, W1, W2, qb);
+                } else {
+                    unit_blend_t<D>(gg[f], gd[f], gl[f], W0, W1, W2, qb);
+                }
 #pragma unroll
                 for (int v = 0; v < V; ++v) r[v][u * FC + f] = qb[v];
             }
@@ -372,57 +529,62 @@ __global__ void __launch_bounds__(kPrivBlock) hermite_bwd_priv_kernel(const __gr
     }
 }
 
-template <int D, int FC, int G>
+template <int D, int FC, int G, bool HESS>
 cudaError_t launch_priv(const BwdParams& p, cudaStream_t s) {
     if (p.priv.n == 0) return cudaSuccess;
     if (p.priv.smem_bytes > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(hermite_bwd_priv_kernel<D, FC, G>,
+        cudaError_t e = cudaFuncSetAttribute(hermite_bwd_priv_kernel<D, FC, G, HESS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, p.priv.smem_bytes);
         if (e != cudaSuccess) return e;
     }
     dim3 grid(static_cast<unsigned>((p.c.n + p.priv.chunk - 1) / p.priv.chunk), static_cast<unsigned>(p.priv.n), G);
-    hermite_bwd_priv_kernel<D, FC, G><<<grid, kPrivBlock, p.priv.smem_bytes, s>>>(p);
+    hermite_bwd_priv_kernel<D, FC, G, HESS><<<grid, kPrivBlock, p.priv.smem_bytes, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int D, int FC, int G>
+template <int D, int FC, int G, bool HESS>
 cudaError_t launch_split(const BwdParams& p, cudaStream_t s) {
-    cudaError_t e = launch_priv<D, FC, G>(p, s);
+    cudaError_t e = launch_priv<D, FC, G, HESS>(p, s);
     if (e != cudaSuccess || p.c.nlvl == 0) return e;
     dim3 grid(static_cast<unsigned>((p.c.n * G + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
-    hermite_bwd_split_kernel<D, FC, G><<<grid, kBlock, 0, s>>>(p);
+    hermite_bwd_split_kernel<D, FC, G, HESS><<<grid, kBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int D, int FC, bool VEC>
+template <int D, int FC, bool VEC, bool HESS>
 cudaError_t launch(const BwdParams& p, cudaStream_t s) {
     if (VEC && D == 2 && FC == 1) {  // 16-byte rows: one part per row
-        cudaError_t e = launch_priv<2, 1, 1>(p, s);
+        cudaError_t e = launch_priv<2, 1, 1, HESS>(p, s);
         if (e != cudaSuccess) return e;
     }
     if (p.c.nlvl == 0) return cudaSuccess;
     dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
-    hermite_bwd_kernel<D, FC, VEC><<<grid, kBlock, 0, s>>>(p);
+    hermite_bwd_kernel<D, FC, VEC, HESS><<<grid, kBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool HESS>
 cudaError_t pick(const BwdParams& p, int fc, bool vec, cudaStream_t s) {
-    if (fc == 2) return vec ? launch<D, 2, true>(p, s) : launch<D, 2, false>(p, s);
-    return vec ? launch<D, 1, true>(p, s) : launch<D, 1, false>(p, s);
+    if (fc == 2) return vec ? launch<D, 2, true, HESS>(p, s) : launch<D, 2, false, HESS>(p, s);
+    return vec ? launch<D, 1, true, HESS>(p, s) : launch<D, 1, false, HESS>(p, s);
+}
+
+template <bool HESS>
+cudaError_t dispatch(const BwdParams& p, int fc, bool vec, cudaStream_t s) {
+    if (vec && fc == p.c.F) {
+        // packed rows of 2^d * F floats: 32 bytes -> lane pairs, 64 bytes -> quads
+        if (p.c.d == 2 && p.c.F == 2) return launch_split<2, 2, 2, HESS>(p, s);
+        if (p.c.d == 3 && p.c.F == 1) return launch_split<3, 1, 2, HESS>(p, s);
+        if (p.c.d == 3 && p.c.F == 2) return launch_split<3, 2, 4, HESS>(p, s);
+    }
+    return p.c.d == 2 ? pick<2, HESS>(p, fc, vec, s) : pick<3, HESS>(p, fc, vec, s);
 }
 
 }  // namespace
 
-int launch_hermite_bwd(const BwdParams& p, int fc, bool vec, void* stream) {
+int launch_hermite_bwd(const BwdParams& p, int fc, bool vec, bool hess, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (vec && fc == p.c.F) {
-        // packed rows of 2^d * F floats: 32 bytes -> lane pairs, 64 bytes -> quads
-        if (p.c.d == 2 && p.c.F == 2) return launch_split<2, 2, 2>(p, s);
-        if (p.c.d == 3 && p.c.F == 1) return launch_split<3, 1, 2>(p, s);
-        if (p.c.d == 3 && p.c.F == 2) return launch_split<3, 2, 4>(p, s);
-    }
-    return p.c.d == 2 ? pick<2>(p, fc, vec, s) : pick<3>(p, fc, vec, s);
+    return hess ? dispatch<true>(p, fc, vec, s) : dispatch<false>(p, fc, vec, s);
 }
 
 }  // namespace hg

@@ -175,18 +175,25 @@ hg_status make_common(const hg_grid_desc* desc, int n_orders, int64_t n, hg::Com
         }
     }
     const int64_t LF = static_cast<int64_t>(desc->L) * desc->F;
+    const int P = desc->d * (desc->d + 1) / 2;  // Hessian entries (upper triangle)
     if (desc->layout == HG_POINT_MAJOR) {
         c.sn = LF;
         c.sf = 1;
         c.dsn = desc->d * LF;
         c.dsj = LF;
         c.dsf = 1;
+        c.hsn = P * LF;
+        c.hsq = LF;
+        c.hsf = 1;
     } else {
         c.sn = 1;
         c.sf = n;
         c.dsn = 1;
         c.dsj = LF * n;
         c.dsf = n;
+        c.hsn = 1;
+        c.hsq = LF * n;
+        c.hsf = n;
     }
     return HG_OK;
 }
@@ -304,6 +311,100 @@ hg_status launch_status(int err, const char* what) {
     return ok();
 }
 
+// Hermite forward, Laplacian or (hess) full-Hessian outputs in `second`.
+hg_status hermite_forward(const hg_grid_desc* desc, int64_t n, const float* coords, const hg_table* tables,
+                          float* gamma, float* dgamma, float* second, bool hess, hg_stream stream) {
+    hg_status st = check_desc(desc, desc ? desc->d + 1 : 0);
+    if (st != HG_OK) return st;
+    if ((st = check_n(n)) != HG_OK) return st;
+    if (!tables) return fail(HG_ERR_INVALID_ARG, "tables is NULL");
+    const int d = desc->d, F = desc->F, V = 1 << d;
+    const size_t es = dtype_size(desc->dtype);
+    const void* ptrs[4];
+    int64_t ls[4], rs[4];
+    for (int k = 0; k <= d; ++k) {
+        ptrs[k] = tables[k].ptr;
+        ls[k] = tables[k].level_stride;
+        rs[k] = tables[k].row_stride;
+        st = check_view("tables", k, ptrs[k], ls[k], rs[k], static_cast<int64_t>(binom(d, k)) * F,
+                        int64_t(1) << desc->log2_T[k], desc->L, es);
+        if (st != HG_OK) return st;
+    }
+    hg::FwdParams p;
+    if ((st = make_common(desc, d + 1, n, p.c)) != HG_OK) return st;
+    if (n == 0) return ok();
+    if (!coords || !gamma) return fail(HG_ERR_INVALID_ARG, "coords and gamma must not be NULL");
+    if (hess && !second) return fail(HG_ERR_INVALID_ARG, "hess must not be NULL");
+    if (!aligned(coords, 4) || !aligned(gamma, 4) || (dgamma && !aligned(dgamma, 4)) ||
+        (second && !aligned(second, 4)))
+        return fail(HG_ERR_INVALID_ARG, "coords and outputs must be 4-byte aligned");
+    for (int k = 0; k <= d; ++k) {
+        p.tab.ptr[k] = ptrs[k];
+        p.tab.ls[k] = ls[k];
+        p.tab.rs[k] = rs[k];
+    }
+    p.coords = coords;
+    p.gamma = gamma;
+    p.dgamma = dgamma;
+    p.lap = hess ? nullptr : second;
+    p.hess = hess ? second : nullptr;
+    const int fc = (F % 2 == 0) ? 2 : 1;
+    bool vec = fc == F && is_packed(desc, ptrs, ls, rs, es);
+    if (vec) {
+        const size_t row = static_cast<size_t>(V) * F * es;
+        const size_t al = row < 32 ? row : 32;  // 256-bit loads of 32-byte rows / half-rows
+        vec = aligned(ptrs[0], al) && (static_cast<size_t>(ls[0]) * es) % al == 0;
+    }
+    all_levels(p.c);
+    return launch_status(hg::launch_hermite_fwd(p, fc, vec, desc->dtype, hess, stream),
+                         hess ? "hermite forward (Hessian)" : "hermite forward");
+}
+
+// Hermite backward, upstream gradient of the Laplacian or (hess) of the
+// full Hessian in `g_second`.
+hg_status hermite_backward(const hg_grid_desc* desc, int64_t n, const float* coords, const float* g_gamma,
+                           const float* g_dgamma, const float* g_second, const hg_grad_table* grads, bool hess,
+                           hg_stream stream) {
+    hg_status st = check_desc(desc, desc ? desc->d + 1 : 0);
+    if (st != HG_OK) return st;
+    if ((st = check_n(n)) != HG_OK) return st;
+    if (!grads) return fail(HG_ERR_INVALID_ARG, "grads is NULL");
+    const int d = desc->d, F = desc->F, V = 1 << d;
+    const void* ptrs[4];
+    int64_t ls[4], rs[4];
+    for (int k = 0; k <= d; ++k) {
+        ptrs[k] = grads[k].ptr;
+        ls[k] = grads[k].level_stride;
+        rs[k] = grads[k].row_stride;
+        st = check_view("grads", k, ptrs[k], ls[k], rs[k], static_cast<int64_t>(binom(d, k)) * F,
+                        int64_t(1) << desc->log2_T[k], desc->L, 4);
+        if (st != HG_OK) return st;
+    }
+    hg::BwdParams p;
+    if ((st = make_common(desc, d + 1, n, p.c)) != HG_OK) return st;
+    if (n == 0 || (!g_gamma && !g_dgamma && !g_second)) return ok();
+    if (!coords) return fail(HG_ERR_INVALID_ARG, "coords must not be NULL");
+    if (!aligned(coords, 4) || (g_gamma && !aligned(g_gamma, 4)) || (g_dgamma && !aligned(g_dgamma, 4)) ||
+        (g_second && !aligned(g_second, 4)))
+        return fail(HG_ERR_INVALID_ARG, "coords and upstream gradients must be 4-byte aligned");
+    for (int k = 0; k <= d; ++k) {
+        p.grad.ptr[k] = const_cast<float*>(static_cast<const float*>(ptrs[k]));
+        p.grad.ls[k] = ls[k];
+        p.grad.rs[k] = rs[k];
+    }
+    p.coords = coords;
+    p.g_gamma = g_gamma;
+    p.g_dgamma = g_dgamma;
+    p.g_lap = hess ? nullptr : g_second;
+    p.g_hess = hess ? g_second : nullptr;
+    const int fc = (F % 2 == 0) ? 2 : 1;
+    bool vec = fc == F && is_packed(desc, ptrs, ls, rs, 4);
+    if (vec) vec = aligned(ptrs[0], 16) && (static_cast<size_t>(ls[0]) * 4) % 16 == 0 && (V * F) % 4 == 0;
+    plan_backward(p, vec, 16, vec ? V * F / 4 : 1, kHermitePrivLevelBytes);
+    return launch_status(hg::launch_hermite_bwd(p, fc, vec, hess, stream),
+                         hess ? "hermite backward (Hessian)" : "hermite backward");
+}
+
 }  // namespace
 
 extern "C" {
@@ -333,86 +434,23 @@ hg_status hg_level_resolutions(const hg_grid_desc* desc, int32_t* res_out) {
 
 hg_status hg_encode_fwd(const hg_grid_desc* desc, int64_t n, const float* coords, const hg_table* tables,
                         float* gamma, float* dgamma, float* lap, hg_stream stream) {
-    hg_status st = check_desc(desc, desc ? desc->d + 1 : 0);
-    if (st != HG_OK) return st;
-    if ((st = check_n(n)) != HG_OK) return st;
-    if (!tables) return fail(HG_ERR_INVALID_ARG, "tables is NULL");
-    const int d = desc->d, F = desc->F, V = 1 << d;
-    const size_t es = dtype_size(desc->dtype);
-    const void* ptrs[4];
-    int64_t ls[4], rs[4];
-    for (int k = 0; k <= d; ++k) {
-        ptrs[k] = tables[k].ptr;
-        ls[k] = tables[k].level_stride;
-        rs[k] = tables[k].row_stride;
-        st = check_view("tables", k, ptrs[k], ls[k], rs[k], static_cast<int64_t>(binom(d, k)) * F,
-                        int64_t(1) << desc->log2_T[k], desc->L, es);
-        if (st != HG_OK) return st;
-    }
-    hg::FwdParams p;
-    if ((st = make_common(desc, d + 1, n, p.c)) != HG_OK) return st;
-    if (n == 0) return ok();
-    if (!coords || !gamma) return fail(HG_ERR_INVALID_ARG, "coords and gamma must not be NULL");
-    if (!aligned(coords, 4) || !aligned(gamma, 4) || (dgamma && !aligned(dgamma, 4)) || (lap && !aligned(lap, 4)))
-        return fail(HG_ERR_INVALID_ARG, "coords and outputs must be 4-byte aligned");
-    for (int k = 0; k <= d; ++k) {
-        p.tab.ptr[k] = ptrs[k];
-        p.tab.ls[k] = ls[k];
-        p.tab.rs[k] = rs[k];
-    }
-    p.coords = coords;
-    p.gamma = gamma;
-    p.dgamma = dgamma;
-    p.lap = lap;
-    const int fc = (F % 2 == 0) ? 2 : 1;
-    bool vec = fc == F && is_packed(desc, ptrs, ls, rs, es);
-    if (vec) {
-        const size_t row = static_cast<size_t>(V) * F * es;
-        const size_t al = row < 32 ? row : 32;  // 256-bit loads of 32-byte rows / half-rows
-        vec = aligned(ptrs[0], al) && (static_cast<size_t>(ls[0]) * es) % al == 0;
-    }
-    all_levels(p.c);
-    return launch_status(hg::launch_hermite_fwd(p, fc, vec, desc->dtype, stream), "hermite forward");
+    return hermite_forward(desc, n, coords, tables, gamma, dgamma, lap, false, stream);
+}
+
+hg_status hg_encode_fwd_hessian(const hg_grid_desc* desc, int64_t n, const float* coords, const hg_table* tables,
+                                float* gamma, float* dgamma, float* hess, hg_stream stream) {
+    return hermite_forward(desc, n, coords, tables, gamma, dgamma, hess, true, stream);
 }
 
 hg_status hg_encode_bwd(const hg_grid_desc* desc, int64_t n, const float* coords, const float* g_gamma,
                         const float* g_dgamma, const float* g_lap, const hg_grad_table* grads, hg_stream stream) {
-    hg_status st = check_desc(desc, desc ? desc->d + 1 : 0);
-    if (st != HG_OK) return st;
-    if ((st = check_n(n)) != HG_OK) return st;
-    if (!grads) return fail(HG_ERR_INVALID_ARG, "grads is NULL");
-    const int d = desc->d, F = desc->F, V = 1 << d;
-    const void* ptrs[4];
-    int64_t ls[4], rs[4];
-    for (int k = 0; k <= d; ++k) {
-        ptrs[k] = grads[k].ptr;
-        ls[k] = grads[k].level_stride;
-        rs[k] = grads[k].row_stride;
-        st = check_view("grads", k, ptrs[k], ls[k], rs[k], static_cast<int64_t>(binom(d, k)) * F,
-                        int64_t(1) << desc->log2_T[k], desc->L, 4);
-        if (st != HG_OK) return st;
-    }
-    hg::BwdParams p;
-    if ((st = make_common(desc, d + 1, n, p.c)) != HG_OK) return st;
-    if (n == 0 || (!g_gamma && !g_dgamma && !g_lap)) return ok();
-    if (!coords) return fail(HG_ERR_INVALID_ARG, "coords must not be NULL");
-    if (!aligned(coords, 4) || (g_gamma && !aligned(g_gamma, 4)) || (g_dgamma && !aligned(g_dgamma, 4)) ||
-        (g_lap && !aligned(g_lap, 4)))
-        return fail(HG_ERR_INVALID_ARG, "coords and upstream gradients must be 4-byte aligned");
-    for (int k = 0; k <= d; ++k) {
-        p.grad.ptr[k] = const_cast<float*>(static_cast<const float*>(ptrs[k]));
-        p.grad.ls[k] = ls[k];
-        p.grad.rs[k] = rs[k];
-    }
-    p.coords = coords;
-    p.g_gamma = g_gamma;
-    p.g_dgamma = g_dgamma;
-    p.g_lap = g_lap;
-    const int fc = (F % 2 == 0) ? 2 : 1;
-    bool vec = fc == F && is_packed(desc, ptrs, ls, rs, 4);
-    if (vec) vec = aligned(ptrs[0], 16) && (static_cast<size_t>(ls[0]) * 4) % 16 == 0 && (V * F) % 4 == 0;
-    plan_backward(p, vec, 16, vec ? V * F / 4 : 1, kHermitePrivLevelBytes);
-    return launch_status(hg::launch_hermite_bwd(p, fc, vec, stream), "hermite backward");
+    return hermite_backward(desc, n, coords, g_gamma, g_dgamma, g_lap, grads, false, stream);
+}
+
+hg_status hg_encode_bwd_hessian(const hg_grid_desc* desc, int64_t n, const float* coords, const float* g_gamma,
+                                const float* g_dgamma, const float* g_hess, const hg_grad_table* grads,
+                                hg_stream stream) {
+    return hermite_backward(desc, n, coords, g_gamma, g_dgamma, g_hess, grads, true, stream);
 }
 
 hg_status hg_linear_fwd(const hg_grid_desc* desc, int64_t n, const float* coords, const hg_table* table,
@@ -439,6 +477,7 @@ hg_status hg_linear_fwd(const hg_grid_desc* desc, int64_t n, const float* coords
     p.gamma = gamma;
     p.dgamma = nullptr;
     p.lap = nullptr;
+    p.hess = nullptr;
     const int fc = (F % 2 == 0) ? 2 : 1;
     const bool vec = fc == 2 && aligned(table->ptr, 2 * es) && table->row_stride % 2 == 0 && table->level_stride % 2 == 0;
     all_levels(p.c);
@@ -469,6 +508,7 @@ hg_status hg_linear_bwd(const hg_grid_desc* desc, int64_t n, const float* coords
     p.g_gamma = g_gamma;
     p.g_dgamma = nullptr;
     p.g_lap = nullptr;
+    p.g_hess = nullptr;
     const int fc = (F % 2 == 0) ? 2 : 1;
     const bool vec = fc == 2 && aligned(grad->ptr, 8) && grad->row_stride % 2 == 0 && grad->level_stride % 2 == 0;
     plan_backward(p, true, static_cast<int64_t>(F) * 4, 1, kPrivMaxBytes);

@@ -28,7 +28,8 @@ struct Common {
     // output / upstream-gradient addressing, in elements:
     //   gamma, lap:  n*sn  + (l*F + f)*sf
     //   dgamma:      n*dsn + j*dsj + (l*F + f)*dsf
-    int64_t sn, sf, dsn, dsj, dsf;
+    //   hess:        n*hsn + q*hsq + (l*F + f)*hsf   (q: upper-triangle entry)
+    int64_t sn, sf, dsn, dsj, dsf, hsn, hsq, hsf;
     Level lv[HG_MAX_LEVELS];
     // levels this launch covers: blockIdx.y -> level lvl[blockIdx.y], nlvl of them
     int32_t nlvl;
@@ -62,6 +63,7 @@ struct FwdParams {
     float* gamma;
     float* dgamma;
     float* lap;
+    float* hess;      // full-Hessian forward only
 };
 
 struct BwdParams {
@@ -72,6 +74,7 @@ struct BwdParams {
     const float* g_gamma;
     const float* g_dgamma;
     const float* g_lap;
+    const float* g_hess;  // full-Hessian backward only
 };
 
 struct IdxParams {
@@ -82,8 +85,10 @@ struct IdxParams {
 
 // Launchers (one per kernel family); return the cudaError_t of the launch.
 // fc: features per pass (1 or 2); vec: whole-row vector access (packed layout).
-int launch_hermite_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream);
-int launch_hermite_bwd(const BwdParams& p, int fc, bool vec, void* stream);
+// hess: the full-Hessian variant (outputs / upstream gradients in hess / g_hess
+// instead of lap / g_lap).
+int launch_hermite_fwd(const FwdParams& p, int fc, bool vec, int dtype, bool hess, void* stream);
+int launch_hermite_bwd(const BwdParams& p, int fc, bool vec, bool hess, void* stream);
 int launch_linear_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream);
 int launch_linear_bwd(const BwdParams& p, int fc, bool vec, void* stream);
 int launch_indices(const IdxParams& p, void* stream);

@@ -134,6 +134,13 @@ def draw_upstream(rng: np.random.Generator, w: Workload, with_derivs: bool = Tru
     return gg, gd, gl
 
 
+def draw_upstream_hessian(rng: np.random.Generator, w: Workload) -> np.ndarray:
+    """N(0,1) upstream gradient of the full Hessian, point-major
+    [N][P][L][F] with P = d(d+1)/2 upper-triangle entries."""
+    P = w.d * (w.d + 1) // 2
+    return rng.standard_normal((w.n_points, P, w.L, w.F), dtype=np.float32)
+
+
 def make(w: Workload, seed: int | None = None, separate_orders: bool = False):
     """Draw a complete workload: dict with coords, table (interleaved) or
     order_tables (separate), and upstream gradients."""

@@ -33,7 +33,8 @@ def test_library_exports_every_declared_symbol(m):
     lib = m.hg.lib()
     names = _declared("hg.h") + _declared("hg_probe.h")
     assert {"hg_encode_fwd", "hg_encode_bwd", "hg_linear_fwd", "hg_linear_bwd", "hg_level_resolutions",
-            "hg_hash_indices", "hg_status_string", "hg_last_error", "hg_abi_version"} <= set(names)
+            "hg_hash_indices", "hg_status_string", "hg_last_error", "hg_abi_version", "hg_encode_fwd_hessian",
+            "hg_encode_bwd_hessian"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -142,6 +143,12 @@ def test_bad_arguments_are_rejected(m):
     # backward: misaligned upstream gradient, NULL coords
     assert hg.hg_encode_bwd(ok_desc(), 5, 16, 18, None, None, views, stream=0, check=False) == E
     assert hg.hg_encode_bwd(ok_desc(), 5, 0, 16, None, None, views, stream=0, check=False) == E
+    # full Hessian: NULL or misaligned hess, misaligned upstream g_hess
+    assert hg.hg_encode_fwd_hessian(ok_desc(), 5, 16, views, 32, None, None, stream=0, check=False) == E
+    assert hg.hg_encode_fwd_hessian(ok_desc(), 5, 16, views, 32, None, 34, stream=0, check=False) == E
+    assert hg.hg_encode_fwd_hessian(ok_desc(), 5, 16, views, 0, None, 64, stream=0, check=False) == E
+    assert hg.hg_encode_bwd_hessian(ok_desc(), 5, 16, None, None, 18, views, stream=0, check=False) == E
+    assert hg.hg_encode_bwd_hessian(ok_desc(), 5, 0, None, None, 16, views, stream=0, check=False) == E
     # d-linear and indices
     lv = hg.linear_view(_FakeTable((4, 256, 2), addr=1 << 20))
     assert hg.hg_linear_fwd(ok_desc(), 5, 0, lv, 32, stream=0, check=False) == E
@@ -160,4 +167,6 @@ def test_zero_points_touch_nothing(m):
     t = _FakeTable((3, 256, 4, 2), addr=1 << 20)
     assert hg.hg_encode_fwd(desc, 0, 0, hg.packed_views(t, 2), 0, stream=0, check=False) == hg.HG_OK
     assert hg.hg_encode_bwd(desc, 0, 0, 0, 0, 0, hg.packed_views(t, 2), stream=0, check=False) == hg.HG_OK
+    assert hg.hg_encode_fwd_hessian(desc, 0, 0, hg.packed_views(t, 2), 0, 0, 0, stream=0, check=False) == hg.HG_OK
+    assert hg.hg_encode_bwd_hessian(desc, 0, 0, 0, 0, 0, hg.packed_views(t, 2), stream=0, check=False) == hg.HG_OK
     assert hg.hg_last_error() == ""

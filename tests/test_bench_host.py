@@ -79,6 +79,11 @@ def test_algorithmic_bytes_and_patterns():
     assert bench.algorithmic_bytes(w2, (1 << 16) - 1) == ((1 << 20) * 16 * 4 * 8,) * 2
 
 
+def bench_workload(cfg):
+    from multiresolution_hash_grid_02_b300 import workloads as W
+    return W.WORKLOADS[cfg]
+
+
 SAMPLE_NCU_LOG = """==PROF== Connected to process 1 (/usr/bin/python3.12)
 ==PROF== Profiling "hermite_fwd_pair3_kernel": 0%....50%....100% - 1 pass
 {"metric": "ignored"}
@@ -109,7 +114,24 @@ def test_ncu_log_parser_and_traffic_staleness(tmp_path, monkeypatch):
     bench.record_traffic(str(log), "3d_hermite", "cmd")
     assert bench.recorded_traffic("3d_hermite", "hermite_bwd") == pytest.approx(2.05e9 + 287.08e6)
     assert bench.recorded_traffic("2d_hermite_pinn", "hermite_bwd") is None
+    # a second configuration is kept beside the first
+    bench.record_traffic(str(log), "3d_hermite+hessian", "cmd2")
+    assert bench.recorded_traffic("3d_hermite", "hermite_fwd") == pytest.approx(608.47e6 + 1.31e9)
+    assert bench.recorded_traffic("3d_hermite+hessian", "hermite_bwd") == pytest.approx(2.05e9 + 287.08e6)
     data = json.loads((tmp_path / "traffic.json").read_text())
     data["source_sha256"] = "0" * 64          # the kernels changed since the capture
     (tmp_path / "traffic.json").write_text(json.dumps(data))
     assert bench.recorded_traffic("3d_hermite", "hermite_bwd") is None
+    assert bench.traffic_key(bench_workload(4), None, True) == "3d_hermite+hessian"
+
+
+def test_reference_arm_hessian_line():
+    """The reference arm (the oracle) runs the full-Hessian step on the tiny
+    2D workload and labels its line accordingly."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "1",
+                          "--hessian", "--steps", "1", "--warmup", "0", "--cpu-sample", "2048"],
+                         env=dict(os.environ, RANK="0", WORLD_SIZE="1"), capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and "Hessian" in line["metric"]
+    assert line["config"]["second_order"] == "full Hessian" and line["value"] > 0

@@ -150,3 +150,43 @@ def test_fullsize_3d_hermite_fp16_coarse_to_fine(workload5, active):
     mask = (1 << active) - 1
     bwd = {4: (3,), 10: (9,), 16: (15,)}[active]
     _check_hermite(w, inp, mask, fwd_levels=(0, 3, 4, 9, 10, 15), bwd_levels=bwd, seed=50 + active)
+
+
+def test_fullsize_3d_hermite_hessian():
+    """The full-Hessian forward and backward on the 3D workload (2^21 points,
+    16 levels), packed table, feature-major outputs."""
+    m, hg, W, oracle = _mods()
+    w = W.WORKLOADS[4]
+    inp = W.make(w)
+    n, d, L, F = w.n_points, w.d, w.L, w.F
+    P = d * (d + 1) // 2
+    res = oracle.level_resolutions(L, w.n_min, w.n_max)
+    desc = m.GridDesc(d=d, L=L, F=F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T, layout=m.HG_FEATURE_MAJOR)
+    coords = torch.from_numpy(inp["coords"]).cuda()
+    table = torch.from_numpy(inp["table"]).cuda()
+    gamma = torch.empty((L, F, n), device="cuda")
+    dgamma = torch.empty((d, L, F, n), device="cuda")
+    hess = torch.empty((P, L, F, n), device="cuda")
+    hg.hg_encode_fwd_hessian(desc, n, coords, m.packed_views(table, d), gamma, dgamma, hess)
+    gh = W.draw_upstream_hessian(np.random.default_rng(61), w)
+    grad = torch.zeros(table.shape, dtype=torch.float32, device="cuda")
+    up = [torch.from_numpy(W.to_feature_major(a, ax)).cuda()
+          for a, ax in ((inp["g_gamma"], False), (inp["g_dgamma"], True), (gh, True))]
+    hg.hg_encode_bwd_hessian(desc, n, coords, up[0], up[1], up[2], m.packed_views(grad, d))
+    torch.cuda.synchronize()
+    del up, table
+    rng = np.random.default_rng(60)
+    rows = _sample_rows(rng, n)
+    ref = oracle.encode_fwd_hessian(d, F, res, w.log2_T, W.split_orders(inp["table"], d), inp["coords"][rows])
+    ri = torch.from_numpy(rows).cuda()
+    check_close("gamma", W.from_feature_major(host(gamma[:, :, ri]), False), ref["gamma"], ref["mgamma"])
+    check_close("dgamma", W.from_feature_major(host(dgamma[:, :, :, ri]), True), ref["dgamma"], ref["mdgamma"])
+    check_close("hess", W.from_feature_major(host(hess[:, :, :, ri]), True), ref["hess"], ref["mhess"])
+    levels = (0, 6, 7, 15)
+    grads, mags = oracle.encode_bwd_hessian(d, F, res, w.log2_T, inp["coords"], inp["g_gamma"], inp["g_dgamma"], gh,
+                                            levels=levels)
+    T = 1 << w.log2_T[0]
+    for l in levels:
+        got = W.split_orders(host(grad[l]).reshape(1, T, 1 << d, F), d)
+        for k in range(d + 1):
+            check_close(f"grad level {l} order {k}", got[k][0], grads[k][l], mags[k][l])
