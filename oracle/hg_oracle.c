@@ -35,14 +35,21 @@
  *    printed h^(0)(t), h^(1)(t).  Derivatives are the one-sided ones from inside
  *    the cell that contains x.
  *  - The hash is the XOR of g_i * pi_i (mod 2^32), pi = (1, 2654435761,
- *    805459861), then mod T.  A level whose (N+1)^d vertices fit in T is
- *    indexed one-to-one as sum_i g_i (N+1)^i.
+ *    805459861, 3674653429), then mod T.  The pages print no hash formula;
+ *    the first three primes are the spatial-hash primes of Instant-NGP, and
+ *    the fourth, for the 4D (space-time) grid, the next prime of the same
+ *    published list.  A level whose (N+1)^d vertices fit in T is indexed
+ *    one-to-one as sum_i g_i (N+1)^i.
  *  - x is clamped to [0,1] (NaN to 0); pos = fl32(x * N) (one fp32 multiply,
  *    rounded to nearest); c = min(floor(pos), N-1); t = pos - c.  Everything
  *    after that is fp64.
  *  - Tables are bucketed by derivative order k = |alpha| (d+1 tables); table k
  *    holds C(d,k) * F values per entry, alpha in lexicographic axis order
- *    (k=1: x,y,z; k=2: xy,xz,yz; k=3: xyz), then the feature index.
+ *    (k=1: x,y,z[,w]; k=2: xy,xz,[xw,]yz[,yw,zw]; k=3: xyz[,xyw,xzw,yzw];
+ *    k=4: xyzw), then the feature index.
+ *  - d = 2, 3 or 4.  The 4D (space-time) grid is the extension the
+ *    Hermite-NGP page names as the method's main storage cost (16
+ *    coefficients per vertex and feature); it follows the same equation.
  *  - "grad^2 gamma" is the Laplacian (trace of the Hessian), one value per
  *    (level, feature).
  *  - Inactive levels (bit l of the mask clear) output zero and receive no
@@ -62,9 +69,10 @@
 #include <omp.h>
 #endif
 
-#define OR_MAXD 3
+#define OR_MAXD 4
+#define OR_MAXP (OR_MAXD * (OR_MAXD + 1) / 2)   /* Hessian entries in OR_MAXD dimensions */
 
-static const uint32_t OR_PRIMES[OR_MAXD] = {1u, 2654435761u, 805459861u};
+static const uint32_t OR_PRIMES[OR_MAXD] = {1u, 2654435761u, 805459861u, 3674653429u};
 
 /* ------------------------------------------------------------------ */
 /* small combinatorics                                                  */
@@ -84,11 +92,12 @@ static int binom(int n, int k) {
 
 /* Position of the multi-index alpha (bit i set = derivative along axis i)
  * inside its order bucket |alpha|, counting the same-order multi-indices in
- * lexicographic axis order: k=1 -> x,y,z; k=2 -> xy,xz,yz; k=3 -> xyz.      */
+ * lexicographic axis order: in 3D k=1 -> x,y,z; k=2 -> xy,xz,yz; k=3 -> xyz;
+ * in 4D k=2 -> xy,xz,xw,yz,yw,zw and k=3 -> xyz,xyw,xzw,yzw.               */
 static int slot_in_bucket(int d, int alpha) {
     int k = popcount_small(alpha), slot = 0;
     /* enumerate same-order masks in lexicographic order of their axis lists */
-    int lists[8][OR_MAXD], nl = 0;
+    int lists[1 << OR_MAXD][OR_MAXD], nl = 0;
     for (int m = 0; m < (1 << d); ++m) {
         if (popcount_small(m) != k) continue;
         int p = 0;
@@ -185,7 +194,8 @@ typedef struct {
  * gamma[F], dgamma[d][F] (d/dx), lap[F], and the condition magnitudes.
  * Any output pointer may be NULL.                                           */
 /* Number of entries of the upper triangle of a d x d Hessian (i <= j, row-major:
- * 2D xx, xy, yy; 3D xx, xy, xz, yy, yz, zz) and the position of (i, j).   */
+ * 2D xx, xy, yy; 3D xx, xy, xz, yy, yz, zz; 4D xx, xy, xz, xw, yy, yz, yw,
+ * zz, zw, ww) and the position of (i, j).                                  */
 static int hess_entries(int d) { return d * (d + 1) / 2; }
 static int hess_pos(int d, int i, int j) {
     int p = 0;
@@ -400,7 +410,7 @@ int oracle_encode_bwd_level(int d, int L, int F, int l, const int32_t* res, cons
     const double dx = 1.0 / N;
     double scale[OR_MAXD + 1];
     for (int k = 0; k <= d; ++k) scale[k] = pow(dx, (double)k);   /* dx^{|alpha|} */
-    int slot_of[8], order_of[8];
+    int slot_of[1 << OR_MAXD], order_of[1 << OR_MAXD];
     for (int alpha = 0; alpha < (1 << d); ++alpha) {
         slot_of[alpha] = slot_in_bucket(d, alpha);
         order_of[alpha] = popcount_small(alpha);
@@ -563,7 +573,7 @@ int oracle_encode_fwd_hessian(int d, int L, int F, const int32_t* res, const int
     const int P = hess_entries(d);
 #pragma omp parallel for schedule(dynamic, 256)
     for (int64_t n = 0; n < n_pts; ++n) {
-        double g_[8], dg_[OR_MAXD * 8], h_[6 * 8], mg_[8], md_[OR_MAXD * 8], mh_[6 * 8];
+        double g_[8], dg_[OR_MAXD * 8], h_[OR_MAXP * 8], mg_[8], md_[OR_MAXD * 8], mh_[OR_MAXP * 8];
         for (int l = 0; l < L; ++l) {
             if ((level_mask >> l) & 1u) {
                 const double* tab_l[OR_MAXD + 1];
@@ -634,7 +644,7 @@ int oracle_encode_bwd_hessian_level(int d, int L, int F, int l, const int32_t* r
                 for (int i = 0; i < d; ++i) h[i] = &hb[i][v >> i & 1][alpha >> i & 1];
                 double H = 1.0;
                 for (int i = 0; i < d; ++i) H *= (*h[i])[0];
-                double dH[OR_MAXD], hij[6];
+                double dH[OR_MAXD], hij[OR_MAXP];
                 for (int j = 0; j < d; ++j) {
                     dH[j] = 1.0;
                     for (int i = 0; i < d; ++i) dH[j] *= (i == j) ? (*h[i])[1] : (*h[i])[0];

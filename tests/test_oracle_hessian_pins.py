@@ -34,7 +34,8 @@ def test_hessian_single_coefficient_closed_forms(oracle_mod):
         assert abs(out["gamma"][0, 0, 0] - case["gamma"]) < 1e-15
 
 
-@pytest.mark.parametrize("d,res,log2T", [(2, [4, 8, 20], [12, 12, 12]), (3, [4, 6, 10], [11, 11, 11, 11])])
+@pytest.mark.parametrize("d,res,log2T", [(2, [4, 8, 20], [12, 12, 12]), (3, [4, 6, 10], [11, 11, 11, 11]),
+                                          (4, [2, 3], [9, 9, 9, 9, 9])])
 def test_exact_tensor_cubic_hessian(oracle_mod, d, res, log2T):
     rng = np.random.default_rng(21)
     F = 2
@@ -59,7 +60,7 @@ def test_exact_tensor_cubic_hessian(oracle_mod, d, res, log2T):
     assert np.allclose(tr, lap, rtol=1e-12, atol=1e-12 * max(res) ** 2)
 
 
-@pytest.mark.parametrize("d", [2, 3])
+@pytest.mark.parametrize("d", [2, 3, 4])
 def test_hessian_by_finite_differences_of_the_gradient(oracle_mod, d):
     rng = np.random.default_rng(22)
     F, N, log2T = 2, 29, [7] * (d + 1)
@@ -80,7 +81,8 @@ def test_hessian_by_finite_differences_of_the_gradient(oracle_mod, d):
             assert np.allclose(fd, hess[q], rtol=1e-6, atol=1e-6 * N * N)
 
 
-@pytest.mark.parametrize("d,res,log2T", [(2, [4, 9, 30], [4, 5, 4]), (3, [3, 7, 11], [5, 6, 5, 4])])
+@pytest.mark.parametrize("d,res,log2T", [(2, [4, 9, 30], [4, 5, 4]), (3, [3, 7, 11], [5, 6, 5, 4]),
+                                          (4, [2, 5, 9], [6, 5, 7, 6, 4])])
 def test_hessian_backward_adjoint_identity(oracle_mod, d, res, log2T):
     rng = np.random.default_rng(23)
     F, n = 2, 200

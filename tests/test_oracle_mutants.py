@@ -25,7 +25,8 @@ MUTANTS = [
      "hermite_1d(a, t[i] - (double)vi, 1.0, hb[i][vi][a]);\n    for (int v = 0; v < (1 << d); ++v) {\n        int64_t g[OR_MAXD];\n        for (int i = 0; i < d; ++i) g[i] = c[i] + (v >> i & 1);     /* corner vertex */"),
     ("dense index axes transposed", "for (int i = 0; i < d; ++i) { idx += (uint64_t)g[i] * mul; mul *= side; }",
      "for (int i = 0; i < d; ++i) { idx += (uint64_t)g[d - 1 - i] * mul; mul *= side; }"),
-    ("wrong hash prime", "{1u, 2654435761u, 805459861u}", "{1u, 2654435769u, 805459861u}"),
+    ("wrong hash prime", "{1u, 2654435761u, 805459861u, 3674653429u}", "{1u, 2654435769u, 805459861u, 3674653429u}"),
+    ("wrong fourth hash prime", "805459861u, 3674653429u}", "805459861u, 3674653431u}"),
     ("hash adds instead of XOR", "h ^= (uint32_t)(((uint64_t)g[i] * OR_PRIMES[i]) & 0xffffffffu);",
      "h += (uint32_t)(((uint64_t)g[i] * OR_PRIMES[i]) & 0xffffffffu);"),
     ("colliding gradients overwrite", "gk[f] += w;", "gk[f] = w;"),
@@ -67,13 +68,28 @@ def source():
         return f.read()
 
 
-def test_unmodified_copy_passes(source, tmp_path):
-    ok, out = _pins_pass(_build(source, str(tmp_path), "control"))
+@pytest.fixture(scope="module")
+def outcomes(source, tmp_path_factory):
+    """Build the control and every mutant, and run their pin suites
+    concurrently (each in its own process): {name: (passed, tail of output)}."""
+    from concurrent.futures import ThreadPoolExecutor
+    d = str(tmp_path_factory.mktemp("mutants"))
+    jobs = {"control": source}
+    for i, (name, orig, bad) in enumerate(MUTANTS):
+        assert source.count(orig) == 1, f"mutation anchor for '{name}' not unique in hg_oracle.c"
+        jobs[name] = source.replace(orig, bad)
+    libs = {name: _build(text, d, f"m{i}") for i, (name, text) in enumerate(jobs.items())}
+    with ThreadPoolExecutor(max_workers=max(1, min(len(libs), os.cpu_count() or 2))) as ex:
+        res = dict(zip(libs, ex.map(_pins_pass, libs.values())))
+    return res
+
+
+def test_unmodified_copy_passes(outcomes):
+    ok, out = outcomes["control"]
     assert ok, out
 
 
 @pytest.mark.parametrize("name,orig,bad", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_planted_mistake_is_caught(source, tmp_path, name, orig, bad):
-    assert source.count(orig) == 1, f"mutation anchor for '{name}' not unique in hg_oracle.c"
-    ok, out = _pins_pass(_build(source.replace(orig, bad), str(tmp_path), "m"))
+def test_planted_mistake_is_caught(outcomes, name, orig, bad):
+    ok, out = outcomes[name]
     assert not ok, f"the pins did not catch: {name}"

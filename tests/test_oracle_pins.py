@@ -21,7 +21,7 @@ import numpy as np
 import pytest
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-PRIMES = (1, 2654435761, 805459861)   # the spatial-hash primes (one per axis)
+PRIMES = (1, 2654435761, 805459861, 3674653429)   # the spatial-hash primes (one per axis; the 4th for 4D)
 
 
 def _load_golden(name):
@@ -129,7 +129,8 @@ def _vertex_probe_points(d, N):
     return np.array(pts, np.float32), np.array(corners), verts
 
 
-@pytest.mark.parametrize("d,N,log2T", [(2, 3, 4), (2, 15, 8), (2, 31, 10), (3, 3, 6), (3, 7, 9), (3, 4, 7)])
+@pytest.mark.parametrize("d,N,log2T", [(2, 3, 4), (2, 15, 8), (2, 31, 10), (3, 3, 6), (3, 7, 9), (3, 4, 7),
+                                        (4, 3, 8), (4, 5, 11)])
 def test_dense_levels_are_a_bijection(oracle_mod, d, N, log2T):
     assert (N + 1) ** d <= (1 << log2T)
     pts, corners, verts = _vertex_probe_points(d, N)
@@ -142,7 +143,7 @@ def test_dense_levels_are_a_bijection(oracle_mod, d, N, log2T):
     assert by_vertex[tuple([0, 1] + [0] * (d - 2))] == N + 1
 
 
-@pytest.mark.parametrize("d,N,log2T", [(2, 40, 8), (3, 12, 9), (3, 40, 12), (2, 4, 4)])
+@pytest.mark.parametrize("d,N,log2T", [(2, 40, 8), (3, 12, 9), (3, 40, 12), (2, 4, 4), (4, 6, 9), (4, 9, 12)])
 def test_hashed_levels_xor_structure(oracle_mod, d, N, log2T):
     T = 1 << log2T
     assert (N + 1) ** d > T
@@ -264,7 +265,7 @@ def _fill_from_polys(oracle_mod, d, F, res, log2T, polys, degree_limit):
 
 
 @pytest.mark.parametrize("d,res,log2T", [(2, [4, 8, 16, 32], [12, 12, 12]), (2, [5, 20, 25], [10, 11, 12]),
-                                          (3, [4, 6, 10], [11, 11, 11, 11])])
+                                          (3, [4, 6, 10], [11, 11, 11, 11]), (4, [2, 3], [9, 9, 9, 9, 9])])
 def test_exact_tensor_cubic_reproduction(oracle_mod, d, res, log2T):
     """On one-to-one levels, coefficients sampled from a polynomial of degree
     <= 3 per axis reproduce it, its gradient and its Laplacian exactly."""
@@ -344,6 +345,11 @@ def test_slot_order_within_buckets(oracle_mod):
     assert [oracle_mod.slot_in_bucket(3, a) for a in (3, 5, 6)] == [0, 1, 2]
     assert oracle_mod.slot_in_bucket(3, 7) == 0
     assert [oracle_mod.slot_in_bucket(2, a) for a in (0, 1, 2, 3)] == [0, 0, 1, 0]
+    # 4D: k=1 x, y, z, w; k=2 xy, xz, xw, yz, yw, zw; k=3 xyz, xyw, xzw, yzw; k=4 xyzw
+    assert [oracle_mod.slot_in_bucket(4, a) for a in (1, 2, 4, 8)] == [0, 1, 2, 3]
+    assert [oracle_mod.slot_in_bucket(4, a) for a in (3, 5, 9, 6, 10, 12)] == [0, 1, 2, 3, 4, 5]
+    assert [oracle_mod.slot_in_bucket(4, a) for a in (7, 11, 13, 14)] == [0, 1, 2, 3]
+    assert oracle_mod.slot_in_bucket(4, 15) == 0
 
 
 # ---------------------------------------------------------------------------
@@ -354,7 +360,7 @@ def _level_tables(rng, d, F, log2T):
     return [rng.uniform(-1, 1, size=(1 << log2T[k], comb(d, k), F)) for k in range(d + 1)]
 
 
-@pytest.mark.parametrize("d", [2, 3])
+@pytest.mark.parametrize("d", [2, 3, 4])
 def test_c1_continuity_across_faces(oracle_mod, d):
     rng = np.random.default_rng(7)
     F, N, log2T = 2, 37, [6] * (d + 1)    # hashed, with collisions
@@ -373,7 +379,7 @@ def test_c1_continuity_across_faces(oracle_mod, d):
             assert np.allclose(dl, dr, rtol=0, atol=1e-11)
 
 
-@pytest.mark.parametrize("d", [2, 3])
+@pytest.mark.parametrize("d", [2, 3, 4])
 def test_gradient_and_laplacian_by_finite_differences(oracle_mod, d):
     rng = np.random.default_rng(8)
     F, N, log2T = 2, 23, [7] * (d + 1)
@@ -405,19 +411,21 @@ def test_gradient_and_laplacian_by_finite_differences(oracle_mod, d):
 # reduction to d-linear
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("d", [2, 3])
+@pytest.mark.parametrize("d", [2, 3, 4])
 def test_multilinear_reproduction_and_reduction(oracle_mod, d):
     """A multilinear p is reproduced by both the d-linear and the Hermite
     encodings (the latter with p's values and mixed partials stored)."""
     rng = np.random.default_rng(9)
     F, res = 2, [4, 8]
-    log2T = [12] * (d + 1)
+    lt = 13 if d == 4 else 12             # one-to-one levels: (N+1)^d <= T
+    assert all((N + 1) ** d <= (1 << lt) for N in res)
+    log2T = [lt] * (d + 1)
     polys = [[rng.uniform(-1, 1, size=(2,) * d) for _ in range(F)] for _ in res]
     tabs = _fill_from_polys(oracle_mod, d, F, res, log2T, polys, 1)
     lin_table = tabs[0][:, :, 0, :]
     xs = (rng.integers(0, 1 << 16, size=(50, d)) / float(1 << 16)).astype(np.float32)
     her = oracle_mod.encode_fwd(d, F, res, log2T, tabs, xs)
-    lin, _ = oracle_mod.linear_fwd(d, F, res, 12, lin_table, xs)
+    lin, _ = oracle_mod.linear_fwd(d, F, res, lt, lin_table, xs)
     for n in range(len(xs)):
         for l in range(len(res)):
             for f in range(F):
@@ -450,7 +458,8 @@ def _inner_tables(a, b):
     return sum(float((x * y).sum()) for x, y in zip(a, b))
 
 
-@pytest.mark.parametrize("d,res,log2T", [(2, [4, 9, 30], [4, 5, 4]), (3, [3, 7, 11], [5, 6, 5, 4])])
+@pytest.mark.parametrize("d,res,log2T", [(2, [4, 9, 30], [4, 5, 4]), (3, [3, 7, 11], [5, 6, 5, 4]),
+                                          (4, [2, 5, 9], [6, 5, 7, 6, 4])])
 def test_backward_adjoint_identity(oracle_mod, d, res, log2T):
     rng = np.random.default_rng(12)
     F, n = 2, 300
