@@ -353,18 +353,64 @@ def kernel_patterns(w):
     slots = (1 << w.d) if w.kind == "hermite" else 1
     trow = slots * w.F * es
     grow = slots * w.F * 4
-    # the lane-pair forward serves 3D F = 2 rows (64 B fp32, 32 B fp16); other rows: one thread per row
-    g = (trow, 2) if (w.kind == "hermite" and w.d == 3 and w.F == 2) else (32, 1)
-    r = {64: (64, 4), 32: (32, 2)}.get(grow, (16, 1))
+    # the lane-pair forward serves 3D F = 2 rows (64 B fp32, 32 B fp16), the lane-quad forward 4D F = 2
+    # rows (128 B fp32, 64 B fp16: 4 lanes of 32 B / 16 B); other rows: one thread per row
+    if w.kind == "hermite" and w.d == 3 and w.F == 2:
+        g = (trow, 2)
+    elif w.kind == "hermite" and w.d == 4 and w.F == 2:
+        g = (trow, 4)
+    else:
+        g = (32, 1)
+    r = {128: (128, 8), 64: (64, 4), 32: (32, 2)}.get(grow, (16, 1))
     return g, r
 
 
-def probe_peaks(torch, hg, gather_pat, red_pat, log2_bytes=25):
+def level_probe_sizes(w, res, mask) -> list[tuple[int, int]]:
+    """Per active level, log2 of the probe buffer sizes for the gather and
+    the RED: the bytes of the level's rows that the kernels touch -- all
+    (N_l+1)^d vertex rows of a one-to-one level, the whole table of T rows
+    of a hashed level -- in the table's dtype and in fp32 (gradients), each
+    at least 32 MiB (the smallest buffer the probes measure L2 with)."""
+    es = 2 if w.dtype == "f16" else 4
+    slots = (1 << w.d) if w.kind == "hermite" else 1
+    T = 1 << w.log2_T[0]
+    out = []
+    for l, N in enumerate(res):
+        if (mask >> l) & 1:
+            rows = min((N + 1) ** w.d, T)
+            vals = rows * slots * w.F
+            out.append((max(25, (vals * es - 1).bit_length()), max(25, (vals * 4 - 1).bit_length())))
+    return out
+
+
+def mixed_peaks(torch, hg, gather_pat, red_pat, sizes):
+    """Ceilings of the whole launch: every active level moves the same
+    algorithmic bytes, each at the rate the probe measures on a buffer of
+    that level's size, so the launch's ceiling is the harmonic mean of the
+    per-level rates.  Returns (gather GB/s, RED GB/s, description)."""
+    g_rate, r_rate = {}, {}
+    for gs, rs in sorted(set(sizes)):
+        if gs not in g_rate or rs not in r_rate:
+            g, r = probe_peaks(torch, hg, gather_pat, red_pat, (gs, rs))
+            g_rate.setdefault(gs, g)
+            r_rate.setdefault(rs, r)
+    g_peak = len(sizes) / sum(1.0 / g_rate[gs] for gs, _ in sizes)
+    r_peak = len(sizes) / sum(1.0 / r_rate[rs] for _, rs in sizes)
+    count = lambda k: {s: sum(1 for x in sizes if x[k] == s) for s in sorted({x[k] for x in sizes})}
+    desc = lambda k, rate: ", ".join(f"{(1 << s) >> 20} MiB x {c} level(s): {rate[s]:.0f} GB/s"
+                                     for s, c in count(k).items())
+    return g_peak, r_peak, (desc(0, g_rate), desc(1, r_rate))
+
+
+def probe_peaks(torch, hg, gather_pat, red_pat, log2_bytes=(25, 25)):
     """Measured ceilings for the kernels' own access patterns: random
-    whole-row gathers and random 16-byte vector REDs on a 2^log2_bytes buffer
-    (32 MiB: L2-resident; 1 GiB: HBM), rows split across lanes as the kernels
-    split them; best of 5 after one warm-up launch."""
-    buf = torch.zeros(1 << (log2_bytes - 2), dtype=torch.float32, device="cuda")
+    whole-row gathers and random 16-byte vector REDs on buffers of
+    2^log2_bytes[0] and 2^log2_bytes[1] bytes (32 MiB: L2-resident; 1 GiB:
+    HBM), rows split across lanes as the kernels split them; best of 5 after
+    one warm-up launch."""
+    if isinstance(log2_bytes, int):
+        log2_bytes = (log2_bytes, log2_bytes)
+    buf = torch.zeros(1 << (max(log2_bytes) - 2), dtype=torch.float32, device="cuda")
     n_threads = 148 * 2048 * 4
     sink = torch.empty(n_threads, device="cuda")
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -382,8 +428,8 @@ def probe_peaks(torch, hg, gather_pat, red_pat, log2_bytes=25):
 
     grow, glanes = gather_pat
     rrow, rlanes = red_pat
-    gl2 = log2_bytes - {64: 6, 32: 5}[grow]
-    rl2 = log2_bytes - {64: 6, 32: 5, 16: 4}[rrow]
+    gl2 = log2_bytes[0] - {128: 7, 64: 6, 32: 5}[grow]
+    rl2 = log2_bytes[1] - {128: 7, 64: 6, 32: 5, 16: 4}[rrow]
     per_g, per_r = 64, 64
     g = best(lambda i: hg.hg_probe_l2_gather(buf, gl2, grow, glanes, n_threads, per_g, i, sink),
              n_threads // glanes * per_g * grow)
@@ -511,7 +557,8 @@ def main():
             rec[2].record(stream)
 
     gather_pat, red_pat = kernel_patterns(w)
-    gather_peak, red_peak = probe_peaks(torch, hg, gather_pat, red_pat)
+    sizes = level_probe_sizes(w, hg.hg_level_resolutions(desc), mask)
+    gather_peak, red_peak, probe_desc = mixed_peaks(torch, hg, gather_pat, red_pat, sizes)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -554,11 +601,11 @@ def main():
     kernels = {
         "fwd": {"ms": t_fwd, "bound": "l2", "achieved": fwd_gbs, "peak": gather_peak, "unit": "GB/s",
                 "frac": fwd_gbs / gather_peak, "algorithmic_bytes": gather_bytes,
-                "probe": f"{gather_pat[0]}-byte rows, {gather_pat[1]} lane(s) per row",
+                "probe": f"{gather_pat[0]}-byte rows, {gather_pat[1]} lane(s) per row; {probe_desc[0]}",
                 "what": "compulsory coefficient bytes gathered / launch time vs the measured random-gather L2 peak"},
         "bwd": {"ms": t_bwd, "bound": "l2", "achieved": bwd_gbs, "peak": red_peak, "unit": "GB/s",
                 "frac": bwd_gbs / red_peak, "algorithmic_bytes": red_bytes,
-                "probe": f"{red_pat[0]}-byte rows, {red_pat[1]} lane(s) per row",
+                "probe": f"{red_pat[0]}-byte rows, {red_pat[1]} lane(s) per row; {probe_desc[1]}",
                 "what": "fp32 gradient RED payload bytes / launch time vs the measured random-RED L2 peak"},
     }
     dom = "bwd" if t_bwd >= t_fwd else "fwd"
@@ -568,7 +615,9 @@ def main():
     traffic = recorded_traffic(traffic_key(w, args.points, hessian), kname)
     roofline = {"bound": "l2", "kernel": dom, "achieved": k["achieved"], "peak": k["peak"], "unit": "GB/s",
                 "frac": k["frac"], "traffic": traffic,
-                "peak_source": "measured live by this run's L2 probes (hg_probe_l2_gather / hg_probe_l2_red)",
+                "peak_source": "measured live by this run's probes (hg_probe_l2_gather / hg_probe_l2_red), each "
+                               "level on a buffer the size of its touched table / gradient-table rows (at least "
+                               "32 MiB); harmonic mean over the active levels (equal work per level)",
                 "combined_frac": combined, "hbm_peak_gbs": hbm}
 
     e2e = None

@@ -40,17 +40,22 @@
  *     has N_l+1 vertices per axis.  pos = fl32(x * N_l) (one fp32 multiply,
  *     round to nearest), cell c = min(floor(pos), N_l - 1), local coordinate
  *     t = pos - c in [0,1].
+ *   - Dimension d = 2, 3 or 4.  The 4D (space-time) grid is the extension
+ *     [HNGP 局限与展望] names as the method's main storage cost: 16
+ *     coefficients per vertex and feature, same equation.
  *   - Vertex index in order table k (size T_k = 2^log2_T[k]): when the
  *     level's (N_l+1)^d vertices fit in T_k the index is one-to-one,
- *     g_0 + g_1 (N_l+1) [+ g_2 (N_l+1)^2]; otherwise it is the spatial hash
- *     (g_0 * 1 XOR g_1 * 2654435761 [XOR g_2 * 805459861]) mod 2^32 mod T_k.
- *     [INGP 流程与原理; NEWS]
+ *     sum_i g_i (N_l+1)^i; otherwise it is the spatial hash
+ *     (g_0 * 1 XOR g_1 * 2654435761 [XOR g_2 * 805459861 [XOR g_3 * 3674653429]])
+ *     mod 2^32 mod T_k.  [INGP 流程与原理; NEWS; the pages print no hash
+ *     formula: these are Instant-NGP's published primes, in order]
  *   - Corners of a cell are numbered v = sum_i v_i 2^i (bit i = axis i).
  *   - Multi-indices alpha in {0,1}^d (bit i = d/dx_i) are bucketed by order
  *     k = |alpha| into d+1 tables [HNGP 关键设计 1]; inside bucket k they are
- *     ordered lexicographically by axis list (k=1: x,y,z; k=2: xy,xz,yz;
- *     k=3: xyz), and each entry of table k holds C(d,k)*F values, alpha-major,
- *     feature-minor.
+ *     ordered lexicographically by axis list (3D: k=1 x,y,z; k=2 xy,xz,yz;
+ *     k=3 xyz; 4D: k=1 x,y,z,w; k=2 xy,xz,xw,yz,yw,zw; k=3 xyz,xyw,xzw,yzw;
+ *     k=4 xyzw), and each entry of table k holds C(d,k)*F values,
+ *     alpha-major, feature-minor.
  *   - Outputs and upstream gradients are float32 in one of two layouts
  *     (hg_layout):
  *       HG_POINT_MAJOR:   gamma, lap [n][L][F]; dgamma [n][d][L][F]
@@ -88,14 +93,14 @@ typedef enum { HG_POINT_MAJOR = 0, HG_FEATURE_MAJOR = 1 } hg_layout;
 
 /* Grid description (host memory, read during the call only). */
 typedef struct {
-    int32_t d;              /* spatial dimension: 2 or 3 */
+    int32_t d;              /* spatial dimension: 2, 3 or 4 */
     int32_t L;              /* number of levels: 1..32 */
     int32_t F;              /* features per level: 1, 2, 4 or 8 */
     int32_t n_min, n_max;   /* level schedule (see hg_level_resolutions);
                                ignored when res != NULL */
     const int32_t* res;     /* optional host array [L] of explicit resolutions,
                                each in 1..HG_MAX_RESOLUTION */
-    int32_t log2_T[4];      /* entries per level of order table k = 0..d
+    int32_t log2_T[5];      /* entries per level of order table k = 0..d
                                (0..HG_MAX_LOG2_T); the d-linear calls use
                                log2_T[0] only */
     uint32_t level_mask;    /* bit l set = level l active; bits >= L must be 0 */
@@ -123,7 +128,9 @@ typedef struct {
 
 /* Packed (interleaved) layout -- the fast path.  When all T_k are equal, one
  * buffer [L][T][2^d][F] holds every order with a vertex's 2^d slots ordered
- * (f, fx, fy, [fz], fxy, [fxz, fyz, fxyz]); table k is then the view
+ * by order, then as in the buckets: 2D (f, fx, fy, fxy); 3D (f, fx, fy, fz,
+ * fxy, fxz, fyz, fxyz); 4D (f, fx, fy, fz, fw, fxy, fxz, fxw, fyz, fyw, fzw,
+ * fxyz, fxyw, fxzw, fyzw, fxyzw); table k is then the view
  * ptr + off_k*F, row_stride 2^d*F, level_stride T*2^d*F, with
  * off_k = sum_{k'<k} C(d,k').  The library detects this layout (and 16-byte
  * alignment) and reads or scatters a vertex's whole row with vector accesses;
@@ -232,8 +239,9 @@ const char* hg_status_string(hg_status status);
 /* Reason for the most recent failing call on this thread ("" if none). */
 const char* hg_last_error(void);
 
-/* ABI version of this header (bumped on any incompatible change). */
-#define HG_ABI_VERSION 1
+/* ABI version of this header (bumped on any incompatible change; 2: log2_T
+ * has five entries, d may be 4). */
+#define HG_ABI_VERSION 2
 int32_t hg_abi_version(void);
 
 #ifdef __cplusplus

@@ -19,13 +19,14 @@ HG_OK, HG_ERR_INVALID_ARG, HG_ERR_UNSUPPORTED, HG_ERR_CUDA = 0, 1, 2, 3
 HG_F32, HG_F16 = 0, 1
 HG_POINT_MAJOR, HG_FEATURE_MAJOR = 0, 1
 HG_MAX_LEVELS = 32
+HG_ABI_VERSION = 2        # the include/hg.h layout this binding marshals
 
 c_i32, c_i64, c_u32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
 
 
 class hg_grid_desc(ctypes.Structure):
     _fields_ = [("d", c_i32), ("L", c_i32), ("F", c_i32), ("n_min", c_i32), ("n_max", c_i32),
-                ("res", ctypes.POINTER(c_i32)), ("log2_T", c_i32 * 4), ("level_mask", c_u32),
+                ("res", ctypes.POINTER(c_i32)), ("log2_T", c_i32 * 5), ("level_mask", c_u32),
                 ("dtype", c_i32), ("layout", c_i32)]
 
 
@@ -76,6 +77,9 @@ def lib() -> ctypes.CDLL:
     L.hg_last_error.restype = ctypes.c_char_p
     L.hg_abi_version.argtypes = []
     L.hg_abi_version.restype = c_i32
+    if L.hg_abi_version() != HG_ABI_VERSION:
+        raise ImportError(f"{_LIB_PATH} has ABI version {L.hg_abi_version()}, this binding marshals version "
+                          f"{HG_ABI_VERSION}; rebuild it with `python -m multiresolution_hash_grid_02_b300.build`")
     _lib = L
     return L
 
@@ -92,7 +96,7 @@ class GridDesc:
     F: int
     n_min: int = 16
     n_max: int = 512
-    log2_T: Sequence[int] = (19, 19, 19, 19)
+    log2_T: Sequence[int] = (19, 19, 19, 19, 19)
     level_mask: Optional[int] = None          # None = all levels active
     dtype: int = HG_F32
     layout: int = HG_FEATURE_MAJOR
@@ -102,8 +106,9 @@ class GridDesc:
     def as_c(self) -> hg_grid_desc:
         c = hg_grid_desc()
         c.d, c.L, c.F, c.n_min, c.n_max = self.d, self.L, self.F, self.n_min, self.n_max
-        lt = list(self.log2_T) + [0] * (4 - len(self.log2_T))
-        for k in range(4):
+        lt = list(self.log2_T)
+        lt += [lt[-1]] * (5 - len(lt))          # unlisted orders repeat the last size
+        for k in range(5):
             c.log2_T[k] = int(lt[k])
         mask = ((1 << self.L) - 1) if self.level_mask is None else self.level_mask
         c.level_mask = mask & 0xffffffff

@@ -451,6 +451,241 @@ __global__ void __launch_bounds__(kBlock, 2) hermite_fwd_pair3_kernel(const __gr
     }
 }
 
+// 4D (space-time) forward, any layout and F: one thread per (point, level),
+// one feature at a time.  The 4D blend is a sum over the four axis-3
+// slices (corner side v3, basis order a3): each slice is a 3D blend of the
+// 8 x 8 coefficients with v3 and alpha_3 fixed, and its outputs take the
+// axis-3 weight w, w' or w'' (the product rule of the tensor basis):
+//   gamma += G w,  d/dx_j += dG_j w (j < 3),  d/dx_3 += G w',
+//   lap += lap3 w + G w'',
+//   Hessian: the slice's (i, j < 3) entries times w, (j, 3) entries dG_j w',
+//   (3, 3) entry G w''.
+// Element loads: the 256 coefficients of a (point, level, feature) are read
+// one slice (64) at a time.
+template <typename TT, bool HESS>
+__global__ void __launch_bounds__(kBlock) hermite_fwd4_kernel(const __grid_constant__ FwdParams p) {
+    constexpr int D = 4, P = 10;
+    const int l = p.c.lvl[blockIdx.y];
+    const int64_t n = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    if (n >= p.c.n) return;
+    const int F = p.c.F;
+    const Level& lv = p.c.lv[l];
+    const bool active = (p.c.level_mask >> l) & 1u;
+
+    uint32_t c[D];
+    float t[D];
+    Basis1 B[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+        locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
+        B[i] = hermite_basis(t[i], lv);
+    }
+    for (int f = 0; f < F; ++f) {
+        float g = 0.f, dg[4] = {0.f, 0.f, 0.f, 0.f}, lap = 0.f, h[P];
+#pragma unroll
+        for (int k = 0; k < P; ++k) h[k] = 0.f;
+        if (active) {
+#pragma unroll 1
+            for (int v3 = 0; v3 < 2; ++v3) {
+                // indices of the slice's 8 corners in the five order tables
+                uint32_t idx[8][5];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const uint32_t gv[D] = {c[0] + (v & 1u), c[1] + ((v >> 1) & 1u), c[2] + ((v >> 2) & 1u),
+                                            c[3] + static_cast<uint32_t>(v3)};
+#pragma unroll
+                    for (int k = 0; k <= D; ++k) idx[v][k] = vertex_index<D>(gv, lv, (lv.dense >> k) & 1u, p.c.tmask[k]);
+                }
+#pragma unroll
+                for (int a3 = 0; a3 < 2; ++a3) {
+                    float q[8][8];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+#pragma unroll
+                        for (int a = 0; a < 8; ++a) {
+                            const int alpha = a + 8 * a3, k = alpha_order(alpha);
+                            const TT* e = static_cast<const TT*>(p.tab.ptr[k]) + l * p.tab.ls[k] +
+                                          static_cast<int64_t>(idx[v][k]) * p.tab.rs[k] + bucket_slot<D>(alpha) * F + f;
+                            q[v][a] = to_f32<TT>(*e);
+                        }
+                    const float w = B[3].w[v3][a3], w1 = B[3].d1[v3][a3], w2 = B[3].d2[v3][a3];
+                    float sg, sdg[3];
+                    if constexpr (HESS) {
+                        float sh[6];
+                        blend3h(q, B[0], B[1], B[2], sg, sdg, sh);
+                        h[0] = fmaf(sh[0], w, h[0]);
+                        h[1] = fmaf(sh[1], w, h[1]);
+                        h[2] = fmaf(sh[2], w, h[2]);
+                        h[3] = fmaf(sdg[0], w1, h[3]);
+                        h[4] = fmaf(sh[3], w, h[4]);
+                        h[5] = fmaf(sh[4], w, h[5]);
+                        h[6] = fmaf(sdg[1], w1, h[6]);
+                        h[7] = fmaf(sh[5], w, h[7]);
+                        h[8] = fmaf(sdg[2], w1, h[8]);
+                        h[9] = fmaf(sg, w2, h[9]);
+                    } else {
+                        float sl;
+                        blend3(q, B[0], B[1], B[2], sg, sdg, sl);
+                        lap = fmaf(sl, w, fmaf(sg, w2, lap));
+                    }
+                    g = fmaf(sg, w, g);
+#pragma unroll
+                    for (int j = 0; j < 3; ++j) dg[j] = fmaf(sdg[j], w, dg[j]);
+                    dg[3] = fmaf(sg, w1, dg[3]);
+                }
+            }
+        }
+        const int64_t lf = static_cast<int64_t>(l) * F + f;
+        __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, g);
+        if (p.dgamma) {
+#pragma unroll
+            for (int j = 0; j < D; ++j) __stcs(p.dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf, dg[j]);
+        }
+        if constexpr (HESS) {
+#pragma unroll
+            for (int k = 0; k < P; ++k) __stcs(p.hess + n * p.c.hsn + k * p.c.hsq + lf * p.c.hsf, h[k]);
+        } else if (p.lap) {
+            __stcs(p.lap + n * p.c.sn + lf * p.c.sf, lap);
+        }
+    }
+}
+
+// Reduce-scatter of NV per-lane partial sums over the 4 lanes of an item
+// (lanes 4i..4i+3 of the warp, all present in `mask`): lane (b1, b0) ends
+// with the sums of flat entries b1*NV/2 + b0*NV/4 + k, k < NV/4.  Index
+// choices are compile-time; the lane bits only select between two values.
+template <int NV>
+__device__ __forceinline__ void reduce_scatter4(unsigned mask, int lane, const float (&x)[NV], float (&y)[NV / 4]) {
+    static_assert(NV % 4 == 0, "pad to a multiple of 4");
+    constexpr int H = NV / 2, Q = NV / 4;
+    const bool b1 = lane & 2, b0 = lane & 1;
+    float z[H];
+#pragma unroll
+    for (int k = 0; k < H; ++k) {
+        const float mine = b1 ? x[k + H] : x[k], other = b1 ? x[k] : x[k + H];
+        z[k] = mine + __shfl_xor_sync(mask, other, 2);
+    }
+#pragma unroll
+    for (int k = 0; k < Q; ++k) {
+        const float mine = b0 ? z[k + Q] : z[k], other = b0 ? z[k] : z[k + Q];
+        y[k] = mine + __shfl_xor_sync(mask, other, 1);
+    }
+}
+
+// Store flat output entry j = 2 * o + f of a 4D F = 2 item: o = 0 gamma,
+// 1..4 d/dx_0..3, 5 the Laplacian (or 5..14 the Hessian entries).
+template <bool HESS>
+__device__ __forceinline__ void store4(const FwdParams& p, int64_t n, int l, int j, float v) {
+    const int o = j >> 1;
+    const int64_t lf = static_cast<int64_t>(l) * 2 + (j & 1);
+    if (o == 0) {
+        __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, v);
+    } else if (o <= 4) {
+        if (p.dgamma) __stcs(p.dgamma + n * p.c.dsn + (o - 1) * p.c.dsj + lf * p.c.dsf, v);
+    } else if (HESS) {
+        if (o < 15) __stcs(p.hess + n * p.c.hsn + (o - 5) * p.c.hsq + lf * p.c.hsf, v);
+    } else if (o == 5 && p.lap) {
+        __stcs(p.lap + n * p.c.sn + lf * p.c.sf, v);
+    }
+}
+
+// Lane-quad forward for packed 4D F = 2 rows (128 bytes fp32, 64 bytes
+// fp16).  Lane g of a quad reads the quarter g of every corner row (slots
+// 4g..4g+3, both features: one 256-bit or 128-bit load), so one warp load
+// covers whole rows.  The 16 corners are taken as two axis-3 halves: each
+// half is blended over axes 0-2 with the 3D unit blend (f32x2, both
+// features at once) and folded into the 4D outputs with the axis-3 weight of
+// the slot's order along axis 3 (w, w' or w'', as in hermite_fwd4_kernel).
+// A reduce-scatter over the quad leaves each lane a quarter of the outputs.
+// Two blocks per SM (128 registers, a few spilled words): 5.39 ms on the 4D
+// workload (2^20 points), against 6.53 ms at one block without spills.
+template <typename TT, bool HESS>
+__global__ void __launch_bounds__(kBlock, 2) hermite_fwd_quad4_kernel(const __grid_constant__ FwdParams p) {
+    constexpr int D = 4, G = 4, S = 4, NO = HESS ? 15 : 6, NV = (2 * NO + 3) / 4 * 4;
+    const int l = p.c.lvl[blockIdx.y];
+    const int64_t first = (static_cast<int64_t>(blockIdx.x) * kBlock + (threadIdx.x & ~31u)) / G;
+    const int64_t n = (static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x) / G;
+    const int lane = threadIdx.x % G;
+    if (n >= p.c.n) return;  // all four lanes share n
+    const unsigned mask = item_lanes<G>(first, p.c.n);
+    const Level& lv = p.c.lv[l];
+    float x[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) x[k] = 0.f;
+    if ((p.c.level_mask >> l) & 1u) {
+        uint32_t c[D];
+        float t[D];
+        Basis1 B[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) {
+            locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
+            B[i] = hermite_basis(t[i], lv);
+        }
+        const TT* base = static_cast<const TT*>(p.tab.ptr[0]) + l * p.tab.ls[0] + lane * (S * 2);
+        uint64_t o[NO];
+#pragma unroll
+        for (int k = 0; k < NO; ++k) o[k] = 0ull;
+#pragma unroll
+        for (int v3 = 0; v3 < 2; ++v3) {
+            uint64_t q[8][S];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint32_t g[D] = {c[0] + (v & 1u), c[1] + ((v >> 1) & 1u), c[2] + ((v >> 2) & 1u),
+                                       c[3] + static_cast<uint32_t>(v3)};
+                const uint32_t id = vertex_index<D>(g, lv, lv.dense & 1u, p.c.tmask[0]);
+                load_half_row<TT>(base + static_cast<int64_t>(id) * p.tab.rs[0], q[v]);
+            }
+#pragma unroll
+            for (int u = 0; u < S; ++u) {
+                const AxisW2 W0 = axis_dup(unit_axis<D, G>(B[0], lane, u, 0));
+                const AxisW2 W1 = axis_dup(unit_axis<D, G>(B[1], lane, u, 1));
+                const AxisW2 W2 = axis_dup(unit_axis<D, G>(B[2], lane, u, 2));
+                const AxisW W3 = unit_axis<D, G>(B[3], lane, u, 3);
+                const uint64_t w = f2_dup(W3.w[v3]), w1 = f2_dup(W3.d1[v3]), w2 = f2_dup(W3.d2[v3]);
+                uint64_t cv[8];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) cv[v] = q[v][u];
+                if constexpr (HESS) {
+                    uint64_t s3[10];
+#pragma unroll
+                    for (int k = 0; k < 10; ++k) s3[k] = 0ull;
+                    unit_blend3_f2_hess(cv, W0, W1, W2, s3);  // gamma, d0..d2, xx xy xz yy yz zz
+                    o[0] = f2_fma(s3[0], w, o[0]);
+#pragma unroll
+                    for (int j = 1; j < 4; ++j) o[j] = f2_fma(s3[j], w, o[j]);
+                    o[4] = f2_fma(s3[0], w1, o[4]);
+                    // 4D Hessian (o[5..14]): xx xy xz xw yy yz yw zz zw ww
+                    o[5] = f2_fma(s3[4], w, o[5]);
+                    o[6] = f2_fma(s3[5], w, o[6]);
+                    o[7] = f2_fma(s3[6], w, o[7]);
+                    o[8] = f2_fma(s3[1], w1, o[8]);
+                    o[9] = f2_fma(s3[7], w, o[9]);
+                    o[10] = f2_fma(s3[8], w, o[10]);
+                    o[11] = f2_fma(s3[2], w1, o[11]);
+                    o[12] = f2_fma(s3[9], w, o[12]);
+                    o[13] = f2_fma(s3[3], w1, o[13]);
+                    o[14] = f2_fma(s3[0], w2, o[14]);
+                } else {
+                    uint64_t s3[5] = {0ull, 0ull, 0ull, 0ull, 0ull};
+                    unit_blend3_f2(cv, W0, W1, W2, s3);       // gamma, d0..d2, lap over axes 0-2
+                    o[0] = f2_fma(s3[0], w, o[0]);
+#pragma unroll
+                    for (int j = 1; j < 4; ++j) o[j] = f2_fma(s3[j], w, o[j]);
+                    o[4] = f2_fma(s3[0], w1, o[4]);
+                    o[5] = f2_fma(s3[4], w, f2_fma(s3[0], w2, o[5]));
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NO; ++k) f2_unpack(o[k], x[2 * k], x[2 * k + 1]);
+    }
+    float y[NV / 4];
+    reduce_scatter4<NV>(mask, lane, x, y);
+    const int j0 = (lane >> 1) * (NV / 2) + (lane & 1) * (NV / 4);
+#pragma unroll
+    for (int k = 0; k < NV / 4; ++k) store4<HESS>(p, n, l, j0 + k, y[k]);
+}
+
 template <int D, int FC, typename TT, bool VEC, bool HESS>
 cudaError_t launch(const FwdParams& p, cudaStream_t s) {
     dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
@@ -475,8 +710,25 @@ cudaError_t launch_pair3(const FwdParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <typename TT, bool HESS>
+cudaError_t launch4(const FwdParams& p, cudaStream_t s) {
+    dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
+    hermite_fwd4_kernel<TT, HESS><<<grid, kBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename TT, bool HESS>
+cudaError_t launch_quad4(const FwdParams& p, cudaStream_t s) {
+    dim3 grid(static_cast<unsigned>((p.c.n * 4 + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
+    hermite_fwd_quad4_kernel<TT, HESS><<<grid, kBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <bool HESS>
 cudaError_t dispatch(const FwdParams& p, int fc, bool vec, int dtype, cudaStream_t s) {
+    if (p.c.d == 4 && vec && p.c.F == 2)
+        return dtype == HG_F16 ? launch_quad4<__half, HESS>(p, s) : launch_quad4<float, HESS>(p, s);
+    if (p.c.d == 4) return dtype == HG_F16 ? launch4<__half, HESS>(p, s) : launch4<float, HESS>(p, s);
     if (vec && p.c.d == 3 && p.c.F == 2)
         return dtype == HG_F16 ? launch_pair3<__half, HESS>(p, s) : launch_pair3<float, HESS>(p, s);
     if (p.c.d == 2)

@@ -115,7 +115,7 @@ size_t dtype_size(int dtype) { return dtype == HG_F16 ? 2 : 4; }
 
 hg_status check_desc(const hg_grid_desc* desc, int n_orders) {
     if (!desc) return fail(HG_ERR_INVALID_ARG, "desc is NULL");
-    if (desc->d != 2 && desc->d != 3) return fail(HG_ERR_INVALID_ARG, "d = %d; must be 2 or 3", desc->d);
+    if (desc->d < 2 || desc->d > 4) return fail(HG_ERR_INVALID_ARG, "d = %d; must be 2, 3 or 4", desc->d);
     if (desc->L < 1 || desc->L > HG_MAX_LEVELS)
         return fail(HG_ERR_INVALID_ARG, "L = %d; must be in 1..%d", desc->L, HG_MAX_LEVELS);
     if (desc->F != 1 && desc->F != 2 && desc->F != 4 && desc->F != 8)
@@ -149,13 +149,14 @@ hg_status make_common(const hg_grid_desc* desc, int n_orders, int64_t n, hg::Com
     int32_t res[HG_MAX_LEVELS];
     hg_status st = compute_resolutions(desc, res);
     if (st != HG_OK) return st;
-    for (int k = 0; k < 4; ++k) c.tmask[k] = k < n_orders ? (1u << desc->log2_T[k]) - 1u : 0u;
+    for (int k = 0; k < 5; ++k) c.tmask[k] = k < n_orders ? (1u << desc->log2_T[k]) - 1u : 0u;
     for (int l = 0; l < desc->L; ++l) {
         hg::Level& lv = c.lv[l];
         const uint32_t N = static_cast<uint32_t>(res[l]);
         lv.N = N;
         lv.side = N + 1;
         lv.side2 = (N + 1) * (N + 1);  // only used when the level is one-to-one (fits 2^30)
+        lv.side3 = static_cast<uint32_t>(static_cast<uint64_t>(N + 1) * (N + 1) * (N + 1));  // likewise (4D)
         lv.fN = static_cast<float>(N);
         lv.fN2 = static_cast<float>(static_cast<double>(N) * N);
         lv.dx = static_cast<float>(1.0 / N);
@@ -320,8 +321,8 @@ hg_status hermite_forward(const hg_grid_desc* desc, int64_t n, const float* coor
     if (!tables) return fail(HG_ERR_INVALID_ARG, "tables is NULL");
     const int d = desc->d, F = desc->F, V = 1 << d;
     const size_t es = dtype_size(desc->dtype);
-    const void* ptrs[4];
-    int64_t ls[4], rs[4];
+    const void* ptrs[5];
+    int64_t ls[5], rs[5];
     for (int k = 0; k <= d; ++k) {
         ptrs[k] = tables[k].ptr;
         ls[k] = tables[k].level_stride;
@@ -370,8 +371,8 @@ hg_status hermite_backward(const hg_grid_desc* desc, int64_t n, const float* coo
     if ((st = check_n(n)) != HG_OK) return st;
     if (!grads) return fail(HG_ERR_INVALID_ARG, "grads is NULL");
     const int d = desc->d, F = desc->F, V = 1 << d;
-    const void* ptrs[4];
-    int64_t ls[4], rs[4];
+    const void* ptrs[5];
+    int64_t ls[5], rs[5];
     for (int k = 0; k <= d; ++k) {
         ptrs[k] = grads[k].ptr;
         ls[k] = grads[k].level_stride;
@@ -400,7 +401,8 @@ hg_status hermite_backward(const hg_grid_desc* desc, int64_t n, const float* coo
     const int fc = (F % 2 == 0) ? 2 : 1;
     bool vec = fc == F && is_packed(desc, ptrs, ls, rs, 4);
     if (vec) vec = aligned(ptrs[0], 16) && (static_cast<size_t>(ls[0]) * 4) % 16 == 0 && (V * F) % 4 == 0;
-    plan_backward(p, vec, 16, vec ? V * F / 4 : 1, kHermitePrivLevelBytes);
+    // the 4D kernels scatter every level directly (no privatised variant)
+    plan_backward(p, vec && d != 4, 16, vec ? V * F / 4 : 1, kHermitePrivLevelBytes);
     return launch_status(hg::launch_hermite_bwd(p, fc, vec, hess, stream),
                          hess ? "hermite backward (Hessian)" : "hermite backward");
 }

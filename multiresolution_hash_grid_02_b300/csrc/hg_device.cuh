@@ -12,6 +12,7 @@ namespace hg {
 // Spatial-hash multipliers, one per axis (the first is 1).
 constexpr uint32_t kPrime1 = 2654435761u;
 constexpr uint32_t kPrime2 = 805459861u;
+constexpr uint32_t kPrime3 = 3674653429u;
 
 // Clamp x to [0,1] (fmaxf maps NaN to 0), pos = fl32(x * N), cell index
 // c = min(floor(pos), N-1) and local coordinate t = pos - c (exact in fp32).
@@ -30,11 +31,13 @@ __device__ __forceinline__ uint32_t vertex_index(const uint32_t (&g)[D], const L
                                                  uint32_t tmask) {
     if (dense) {
         uint32_t i = g[0] + g[1] * lv.side;
-        if (D == 3) i += g[D - 1] * lv.side2;
+        if constexpr (D >= 3) i += g[2] * lv.side2;
+        if constexpr (D == 4) i += g[3] * lv.side3;
         return i;
     }
     uint32_t h = g[0] ^ (g[1] * kPrime1);
-    if (D == 3) h ^= g[D - 1] * kPrime2;
+    if constexpr (D >= 3) h ^= g[2] * kPrime2;
+    if constexpr (D == 4) h ^= g[3] * kPrime3;
     return h & tmask;
 }
 
@@ -70,22 +73,40 @@ __device__ __forceinline__ Basis1 hermite_basis(float t, const Level& lv) {
     return b;
 }
 
+// 4D slot order (order-major, lexicographic axis lists inside an order):
+// f, fx, fy, fz, fw, fxy, fxz, fxw, fyz, fyw, fzw, fxyz, fxyw, fxzw, fyzw, fxyzw.
+// kSlotAlpha4[slot] = alpha mask; kAlphaSlot4[alpha] = slot; kOrderOff4[k] = first slot of order k.
+__host__ __device__ constexpr int slot_alpha4(int s) {
+    constexpr int t[16] = {0, 1, 2, 4, 8, 3, 5, 9, 6, 10, 12, 7, 11, 13, 14, 15};
+    return t[s];
+}
+__host__ __device__ constexpr int alpha_slot4(int a) {
+    constexpr int t[16] = {0, 1, 2, 5, 3, 6, 8, 11, 4, 7, 9, 12, 10, 13, 14, 15};
+    return t[a];
+}
+__host__ __device__ constexpr int order_off4(int k) {
+    constexpr int t[5] = {0, 1, 5, 11, 15};
+    return t[k];
+}
+
 // alpha (bit i = d/dx_i) -> position of its slot in the packed vertex row
 // (order-major, lexicographic inside an order): 2D f,fx,fy,fxy;
-// 3D f,fx,fy,fz,fxy,fxz,fyz,fxyz.
+// 3D f,fx,fy,fz,fxy,fxz,fyz,fxyz; 4D as above.
 template <int D>
 __device__ __forceinline__ constexpr int packed_slot(int alpha) {
     if (D == 2) return alpha;
+    if (D == 4) return alpha_slot4(alpha);
     // 3D: masks 0,1,2,4,3,5,6,7 occupy slots 0..7
     return alpha == 3 ? 4 : (alpha == 4 ? 3 : alpha);
 }
 
 // alpha -> its order k and its position inside bucket k.
 __device__ __forceinline__ constexpr int alpha_order(int alpha) {
-    return (alpha & 1) + ((alpha >> 1) & 1) + ((alpha >> 2) & 1);
+    return (alpha & 1) + ((alpha >> 1) & 1) + ((alpha >> 2) & 1) + ((alpha >> 3) & 1);
 }
 template <int D>
 __device__ __forceinline__ constexpr int bucket_slot(int alpha) {
+    if (D == 4) return alpha_slot4(alpha) - order_off4(alpha_order(alpha));
     // k=1: x,y,z -> 0,1,2; k=2: xy,xz,yz -> 0,1,2; k=0 and k=3 -> 0
     if (alpha_order(alpha) == 1) return alpha == 1 ? 0 : (alpha == 2 ? 1 : 2);
     if (alpha_order(alpha) == 2) return alpha == 3 ? 0 : (alpha == 5 ? 1 : 2);
@@ -167,7 +188,7 @@ namespace hg {
 // Multi-index alpha held by packed slot s (inverse of packed_slot).
 template <int D>
 __host__ __device__ constexpr int slot_alpha(int s) {
-    return D == 2 ? s : (s == 3 ? 4 : (s == 4 ? 3 : s));
+    return D == 2 ? s : (D == 4 ? slot_alpha4(s) : (s == 3 ? 4 : (s == 4 ? 3 : s)));
 }
 
 // Lane-split rows: G lanes share one (point, level); lane g owns the S = 2^D/G

@@ -17,14 +17,14 @@ struct Level {
     float fN;         // (float)N_l      -- d/dx = N d/dt
     float fN2;        // (float)N_l^2
     float dx;         // fp32(1/N_l)     -- the dx^|alpha| scaling
-    float pad;
+    uint32_t side3;   // (N_l + 1)^3 (only used when a 4D level is one-to-one)
 };
 
 struct Common {
     int32_t d, L, F;
     uint32_t level_mask;
     int64_t n;
-    uint32_t tmask[4];          // T_k - 1
+    uint32_t tmask[5];          // T_k - 1
     // output / upstream-gradient addressing, in elements:
     //   gamma, lap:  n*sn  + (l*F + f)*sf
     //   dgamma:      n*dsn + j*dsj + (l*F + f)*dsf
@@ -47,13 +47,13 @@ struct Priv {
 };
 
 struct Tables {
-    const void* ptr[4];         // order table k (for the vector path: ptr[0] is the packed row base)
-    int64_t ls[4], rs[4];       // level / row strides in elements
+    const void* ptr[5];         // order table k (for the vector path: ptr[0] is the packed row base)
+    int64_t ls[5], rs[5];       // level / row strides in elements
 };
 
 struct Grads {
-    float* ptr[4];
-    int64_t ls[4], rs[4];
+    float* ptr[5];
+    int64_t ls[5], rs[5];
 };
 
 struct FwdParams {

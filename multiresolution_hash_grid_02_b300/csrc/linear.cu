@@ -192,8 +192,8 @@ __global__ void __launch_bounds__(kBlock) indices_kernel(const __grid_constant__
     const int d = p.c.d;
     const Level& lv = p.c.lv[l];
     const int V = 1 << d;
-    uint32_t c[3];
-    float t[3];
+    uint32_t c[4];
+    float t[4];
     for (int i = 0; i < d; ++i) locate(p.coords[n * d + i], lv, c[i], t[i]);
     uint32_t* out = p.idx + (n * p.c.L + l) * static_cast<int64_t>((d + 1) * V);
     for (int k = 0; k <= d; ++k) {
@@ -202,9 +202,13 @@ __global__ void __launch_bounds__(kBlock) indices_kernel(const __grid_constant__
             if (d == 2) {
                 const uint32_t g[2] = {c[0] + (v & 1u), c[1] + ((v >> 1) & 1u)};
                 id = vertex_index<2>(g, lv, (lv.dense >> k) & 1u, p.c.tmask[k]);
-            } else {
+            } else if (d == 3) {
                 const uint32_t g[3] = {c[0] + (v & 1u), c[1] + ((v >> 1) & 1u), c[2] + ((v >> 2) & 1u)};
                 id = vertex_index<3>(g, lv, (lv.dense >> k) & 1u, p.c.tmask[k]);
+            } else {
+                const uint32_t g[4] = {c[0] + (v & 1u), c[1] + ((v >> 1) & 1u), c[2] + ((v >> 2) & 1u),
+                                       c[3] + ((v >> 3) & 1u)};
+                id = vertex_index<4>(g, lv, (lv.dense >> k) & 1u, p.c.tmask[k]);
             }
             out[k * V + v] = id;
         }
@@ -244,11 +248,13 @@ cudaError_t pick_bwd(const BwdParams& p, int fc, bool vec, cudaStream_t s) {
 int launch_linear_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p.c.d == 2) return dtype == HG_F16 ? pick_fwd<2, __half>(p, fc, vec, s) : pick_fwd<2, float>(p, fc, vec, s);
+    if (p.c.d == 4) return dtype == HG_F16 ? pick_fwd<4, __half>(p, fc, vec, s) : pick_fwd<4, float>(p, fc, vec, s);
     return dtype == HG_F16 ? pick_fwd<3, __half>(p, fc, vec, s) : pick_fwd<3, float>(p, fc, vec, s);
 }
 
 int launch_linear_bwd(const BwdParams& p, int fc, bool vec, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.c.d == 4) return pick_bwd<4>(p, fc, vec, s);
     return p.c.d == 2 ? pick_bwd<2>(p, fc, vec, s) : pick_bwd<3>(p, fc, vec, s);
 }
 

@@ -115,6 +115,7 @@ hg_status hg_probe_l2_gather(const void* buf, int32_t log2_rows, int32_t row_byt
     else if (row_bytes == 64 && lanes_per_row == 1) e = launch_gather<64, 1>(buf, mask, rows_per_group, seed, sink, n_threads, stream);
     else if (row_bytes == 64 && lanes_per_row == 2) e = launch_gather<64, 2>(buf, mask, rows_per_group, seed, sink, n_threads, stream);
     else if (row_bytes == 64 && lanes_per_row == 4) e = launch_gather<64, 4>(buf, mask, rows_per_group, seed, sink, n_threads, stream);
+    else if (row_bytes == 128 && lanes_per_row == 4) e = launch_gather<128, 4>(buf, mask, rows_per_group, seed, sink, n_threads, stream);
     else return HG_ERR_INVALID_ARG;
     return e == cudaSuccess ? HG_OK : HG_ERR_CUDA;
 }
@@ -122,7 +123,7 @@ hg_status hg_probe_l2_gather(const void* buf, int32_t log2_rows, int32_t row_byt
 hg_status hg_probe_l2_red(float* buf, int32_t log2_rows, int32_t row_bytes, int32_t lanes_per_row, int64_t n_threads,
                           int32_t rows_per_group, uint32_t seed, hg_stream stream) {
     if (!buf || !aligned(buf, 16) || log2_rows < 4 || log2_rows > 30 || rows_per_group < 1) return HG_ERR_INVALID_ARG;
-    if (lanes_per_row != 1 && lanes_per_row != 2 && lanes_per_row != 4) return HG_ERR_INVALID_ARG;
+    if (lanes_per_row != 1 && lanes_per_row != 2 && lanes_per_row != 4 && lanes_per_row != 8) return HG_ERR_INVALID_ARG;
     if (n_threads < lanes_per_row || n_threads % lanes_per_row || n_threads > int64_t(INT32_MAX)) return HG_ERR_INVALID_ARG;
     const uint32_t mask = (1u << log2_rows) - 1u;
     cudaError_t e;
@@ -132,6 +133,7 @@ hg_status hg_probe_l2_red(float* buf, int32_t log2_rows, int32_t row_bytes, int3
     else if (row_bytes == 64 && lanes_per_row == 1) e = launch_red<64, 1>(buf, mask, rows_per_group, seed, n_threads, stream);
     else if (row_bytes == 64 && lanes_per_row == 2) e = launch_red<64, 2>(buf, mask, rows_per_group, seed, n_threads, stream);
     else if (row_bytes == 64 && lanes_per_row == 4) e = launch_red<64, 4>(buf, mask, rows_per_group, seed, n_threads, stream);
+    else if (row_bytes == 128 && lanes_per_row == 8) e = launch_red<128, 8>(buf, mask, rows_per_group, seed, n_threads, stream);
     else return HG_ERR_INVALID_ARG;
     return e == cudaSuccess ? HG_OK : HG_ERR_CUDA;
 }

@@ -8,9 +8,12 @@ The five workloads follow the shapes the pages work with: a tiny 2D Hermite
 grid, the Instant-NGP 2D d-linear grid (L=16, F=2, T=2^19, the parameters the
 InstantNGP article fixes in its experiments section), a PINN-sized 2D Hermite
 grid with stratified collocation points (the stratified sampling of the
-DInf-Grid article, "可微的径向基函数插值"), and 3D Hermite grids, the largest
+DInf-Grid article, "可微的径向基函数插值"), 3D Hermite grids, the largest
 with fp16 coefficients and a coarse-to-fine active-level mask ("关键设计 3" of
-the Hermite-NGP notes).  No public dataset is involved.
+the Hermite-NGP notes), and a 4D space-time Hermite grid (the extension the
+Hermite-NGP notes name as the method's main storage cost; they give no 4D
+configuration, so it takes the 3D grid's parameters).  No public dataset is
+involved.
 
 Draw order for one workload (``numpy.random.default_rng(seed)``): coordinates,
 then the coefficient table(s), then the upstream gradients g_gamma, g_dgamma,
@@ -58,6 +61,9 @@ WORKLOADS = {
     4: Workload("3d_hermite", "hermite", 3, 1 << 21, 16, 2, 16, 512, (19, 19, 19, 19), "f32", 1e-2, seed=4),
     5: Workload("3d_hermite_large_fp16", "hermite", 3, 1 << 23, 16, 2, 16, 2048, (22, 22, 22, 22), "f16", 1e-2,
                 level_masks=((1 << 4) - 1, (1 << 10) - 1, (1 << 16) - 1), seed=5),
+    # space-time (x, y, z, t): workload 4's grid with a fourth axis, half the points
+    6: Workload("4d_hermite_spacetime", "hermite", 4, 1 << 20, 16, 2, 16, 512, (19, 19, 19, 19, 19), "f32", 1e-2,
+                seed=6),
 }
 
 

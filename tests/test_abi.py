@@ -97,11 +97,12 @@ class _FakeTable:
         return self._esize
 
 
-@pytest.mark.parametrize("field,value", [("d", 1), ("d", 4), ("L", 0), ("L", 33), ("F", 3), ("F", 16),
+@pytest.mark.parametrize("field,value", [("d", 1), ("d", 5), ("L", 0), ("L", 33), ("F", 3), ("F", 16),
                                          ("dtype", 2), ("layout", 7), ("n_min", 0), ("n_max", 1 << 23)])
 def test_bad_descriptor_is_rejected(m, field, value):
     desc = m.GridDesc(d=3, L=4, F=2, n_min=4, n_max=32, log2_T=(8, 8, 8, 8))
     setattr(desc, field, value)
+    assert m.hg.hg_abi_version() == m.hg.HG_ABI_VERSION
     t = _FakeTable((4, 256, 8, 2), addr=1 << 20)
     views = m.hg.packed_views(t, 3) if field != "d" else []
     st = m.hg.hg_encode_fwd(desc, 5, 16, views or m.hg.packed_views(t, 3), 1 << 21, None, None, stream=0,
@@ -158,6 +159,22 @@ def test_bad_arguments_are_rejected(m):
     lib = hg.lib()
     assert lib.hg_encode_fwd(None, 5, 16, None, 32, None, None, None) == E
     assert lib.hg_level_resolutions(None, None) == E
+
+
+def test_four_dimensional_descriptor_is_accepted(m):
+    """d = 4 (space-time) passes argument checking; n = 0 launches nothing."""
+    hg = m.hg
+    desc = m.GridDesc(d=4, L=3, F=2, n_min=4, n_max=16, log2_T=(8, 8, 8, 8, 8))
+    t = _FakeTable((3, 256, 16, 2), addr=1 << 20)
+    views = hg.packed_views(t, 4)
+    assert len(views) == 5
+    assert hg.hg_encode_fwd(desc, 0, 0, views, 0, stream=0, check=False) == hg.HG_OK
+    assert hg.hg_encode_bwd_hessian(desc, 0, 0, 0, 0, 0, views, stream=0, check=False) == hg.HG_OK
+    # the fifth table's size is checked too
+    desc.log2_T = (8, 8, 8, 8, 31)
+    assert hg.hg_encode_fwd(desc, 5, 16, views, 32, stream=0, check=False) == hg.HG_ERR_INVALID_ARG
+    # a level mask, schedule and index query in 4D pass checking as well
+    assert hg.hg_level_resolutions(m.GridDesc(d=4, L=3, F=2, n_min=4, n_max=16)) == [4, 8, 16]
 
 
 def test_zero_points_touch_nothing(m):

@@ -190,3 +190,12 @@ def test_fullsize_3d_hermite_hessian():
         got = W.split_orders(host(grad[l]).reshape(1, T, 1 << d, F), d)
         for k in range(d + 1):
             check_close(f"grad level {l} order {k}", got[k][0], grads[k][l], mags[k][l])
+
+
+def test_fullsize_4d_hermite_spacetime():
+    """The 4D space-time workload (2^20 points, 16 levels, 128-byte packed
+    rows): lane-quad forward and lane-octet backward, benchmark launch
+    configuration; dense levels 0-2 and hashed levels above."""
+    m, hg, W, oracle = _mods()
+    w = W.WORKLOADS[6]
+    _check_hermite(w, W.make(w), (1 << w.L) - 1, fwd_levels=range(w.L), bwd_levels=(0, 2, 3, 15), seed=70)

@@ -88,6 +88,15 @@ CASES = [
     ("2d_F1_stratified", 2, 4, 1, 4, 64, (10, 10, 10), "f32", 0, True, 10000, None),
     ("3d_F2_stratified", 3, 4, 2, 2, 40, (12, 12, 12, 12), "f32", 1, True, 13824, None),
     ("3d_F1_f16_stratified", 3, 3, 1, 2, 20, (10, 10, 10, 10), "f16", 1, True, 8000, None),
+    # 4D (space-time): 16 corners x 16 multi-indices, five order tables
+    ("4d_F2", 4, 3, 2, 2, 8, (12, 12, 12, 12, 12), "f32", 1, True, 1500, None),
+    ("4d_F2_point_major_hashed", 4, 3, 2, 4, 30, (10, 10, 10, 10, 10), "f32", 0, True, 900, None),
+    ("4d_F1_f16", 4, 3, 1, 2, 10, (10, 10, 10, 10, 10), "f16", 1, True, 700, None),
+    ("4d_F2_f16", 4, 2, 2, 3, 12, (11, 11, 11, 11, 11), "f16", 1, True, 600, None),
+    ("4d_orders_12_11_10_9_8", 4, 3, 2, 2, 9, (12, 11, 10, 9, 8), "f32", 1, False, 500, None),
+    ("4d_F4_mask_101", 4, 3, 4, 2, 12, (9, 9, 9, 9, 9), "f32", 0, True, 300, 0b101),
+    ("4d_one_point", 4, 2, 2, 2, 5, (10, 10, 10, 10, 10), "f32", 1, True, 1, None),
+    ("4d_F2_stratified", 4, 2, 2, 2, 6, (12, 12, 12, 12, 12), "f32", 1, True, 4096, None),
 ]
 
 
@@ -194,6 +203,9 @@ LIN_CASES = [
     ("2d_F1_coarse_many_points", 2, 3, 1, 4, 16, 10, "f32", 1, 30000, None),
     ("3d_F4_f16_coarse_many_points", 3, 3, 4, 2, 8, 9, "f16", 0, 30000, 0b101),
     ("2d_F2_stratified", 2, 6, 2, 4, 300, 12, "f32", 1, 16384, None),
+    ("4d_F2", 4, 4, 2, 2, 16, 12, "f32", 1, 2000, None),
+    ("4d_F1_f16_point_major", 4, 3, 1, 2, 9, 10, "f16", 0, 700, None),
+    ("4d_F2_coarse_many_points", 4, 2, 2, 2, 3, 12, "f32", 1, 20000, None),
 ]
 
 
@@ -236,6 +248,8 @@ INDEX_GEOMS = [
     ("2d_orders_14_14_10", 2, 16, 16, 1024, (14, 14, 10)),
     ("3d_orders_14_10_14_12", 3, 12, 4, 300, (14, 10, 14, 12)),
     ("2d_max_res", 2, 32, 2, 1 << 22, (30, 30, 30)),
+    ("4d_dense_and_hashed", 4, 8, 2, 200, (16, 15, 14, 13, 12)),
+    ("4d_max_res", 4, 16, 2, 1 << 22, (20, 20, 20, 20, 20)),
 ]
 
 
