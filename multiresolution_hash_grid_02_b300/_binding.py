@@ -300,3 +300,30 @@ def hg_probe_l2_red(buf, log2_rows: int, row_bytes: int, lanes_per_row: int, n_t
     L.hg_probe_l2_red.restype = ctypes.c_int
     _check(L.hg_probe_l2_red(_addr(buf), log2_rows, row_bytes, lanes_per_row, n_threads, rows_per_group,
                              seed & 0xffffffff, _stream(stream)), "hg_probe_l2_red")
+
+
+def hg_probe_replay_gather(desc: GridDesc, n: int, coords, table, level_stride_bytes: int, row_bytes: int,
+                           lanes_per_row: int, sink, stream=None, check: bool = True) -> int:
+    L = lib()
+    L.hg_probe_replay_gather.argtypes = [ctypes.POINTER(hg_grid_desc), c_i64, c_vp, c_vp, c_i64, c_i32, c_i32, c_vp,
+                                         c_vp]
+    L.hg_probe_replay_gather.restype = ctypes.c_int
+    c = desc.as_c()
+    st = L.hg_probe_replay_gather(ctypes.byref(c), int(n), _addr(coords), _addr(table), int(level_stride_bytes),
+                                  row_bytes, lanes_per_row, _addr(sink), _stream(stream) if n else 0)
+    if check:
+        _check(st, "hg_probe_replay_gather")
+    return st
+
+
+def hg_probe_replay_red(desc: GridDesc, n: int, coords, grad, level_stride_bytes: int, row_bytes: int,
+                        lanes_per_row: int, stream=None, check: bool = True) -> int:
+    L = lib()
+    L.hg_probe_replay_red.argtypes = [ctypes.POINTER(hg_grid_desc), c_i64, c_vp, c_vp, c_i64, c_i32, c_i32, c_vp]
+    L.hg_probe_replay_red.restype = ctypes.c_int
+    c = desc.as_c()
+    st = L.hg_probe_replay_red(ctypes.byref(c), int(n), _addr(coords), _addr(grad), int(level_stride_bytes),
+                               row_bytes, lanes_per_row, _stream(stream) if n else 0)
+    if check:
+        _check(st, "hg_probe_replay_red")
+    return st

@@ -10,6 +10,7 @@
 #include <cstdint>
 
 #include "hg_params.h"
+#include "../../include/hg_probe.h"
 
 namespace {
 
@@ -407,6 +408,38 @@ hg_status hermite_backward(const hg_grid_desc* desc, int64_t n, const float* coo
                          hess ? "hermite backward (Hessian)" : "hermite backward");
 }
 
+// Replay probe: shared checks, parameter block and launch.
+hg_status replay(const hg_grid_desc* desc, int64_t n, const float* coords, void* buf, int64_t level_bytes,
+                 int32_t row_bytes, int32_t lanes, float* sink, bool red, hg_stream stream) {
+    hg_status st = check_desc(desc, 1);
+    if (st != HG_OK) return st;
+    if ((st = check_n(n)) != HG_OK) return st;
+    if (lanes < 1 || row_bytes < 4 || row_bytes % lanes != 0)
+        return fail(HG_ERR_INVALID_ARG, "row_bytes %d, lanes_per_row %d: need a positive multiple", row_bytes, lanes);
+    const int ch = row_bytes / lanes;
+    if (!(ch == 4 || ch == 8 || ch == 16 || (ch == 32 && !red)))
+        return fail(HG_ERR_INVALID_ARG, "unsupported chunk of %d bytes", ch);
+    const int64_t T = int64_t(1) << desc->log2_T[0];
+    if (desc->L > 1 && level_bytes < T * row_bytes)
+        return fail(HG_ERR_INVALID_ARG, "level_stride_bytes %lld < T * row_bytes", (long long)level_bytes);
+    if (level_bytes < 0 || level_bytes % ch != 0 || row_bytes % ch != 0)
+        return fail(HG_ERR_INVALID_ARG, "strides must be non-negative multiples of the %d-byte chunk", ch);
+    hg::ReplayParams p;
+    if ((st = make_common(desc, 1, n, p.c)) != HG_OK) return st;
+    if (n == 0) return ok();
+    if (!coords || !buf || (!red && !sink)) return fail(HG_ERR_INVALID_ARG, "NULL coords, table or sink");
+    if (!aligned(coords, 4) || !aligned(buf, ch) || (sink && !aligned(sink, 4)))
+        return fail(HG_ERR_INVALID_ARG, "coords / sink must be 4-byte and the table chunk-aligned");
+    all_levels(p.c);
+    p.coords = coords;
+    p.base = static_cast<char*>(buf);
+    p.level_bytes = level_bytes;
+    p.row_bytes = row_bytes;
+    p.lanes = lanes;
+    p.sink = sink;
+    return launch_status(hg::launch_replay(p, red, stream), "replay probe");
+}
+
 }  // namespace
 
 extern "C" {
@@ -530,6 +563,18 @@ hg_status hg_hash_indices(const hg_grid_desc* desc, int64_t n, const float* coor
     p.idx = idx;
     all_levels(p.c);
     return launch_status(hg::launch_indices(p, stream), "vertex indices");
+}
+
+hg_status hg_probe_replay_gather(const hg_grid_desc* desc, int64_t n, const float* coords, const void* table,
+                                 int64_t level_stride_bytes, int32_t row_bytes, int32_t lanes_per_row, float* sink,
+                                 hg_stream stream) {
+    return replay(desc, n, coords, const_cast<void*>(table), level_stride_bytes, row_bytes, lanes_per_row, sink, false,
+                  stream);
+}
+
+hg_status hg_probe_replay_red(const hg_grid_desc* desc, int64_t n, const float* coords, float* grad,
+                              int64_t level_stride_bytes, int32_t row_bytes, int32_t lanes_per_row, hg_stream stream) {
+    return replay(desc, n, coords, grad, level_stride_bytes, row_bytes, lanes_per_row, nullptr, true, stream);
 }
 
 }  // extern "C"

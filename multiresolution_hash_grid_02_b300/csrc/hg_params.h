@@ -83,6 +83,17 @@ struct IdxParams {
     uint32_t* idx;
 };
 
+// Memory-only replay of an encoding launch's row stream (roofline probe).
+struct ReplayParams {
+    Common c;
+    const float* coords;
+    char* base;              // packed table (gather) or fp32 gradient table (RED), level 0 row 0
+    int64_t level_bytes;     // bytes between levels
+    int32_t row_bytes;       // bytes per vertex row
+    int32_t lanes;           // lanes sharing a row; each moves row_bytes / lanes bytes
+    float* sink;             // gather only: one float per thread
+};
+
 // Launchers (one per kernel family); return the cudaError_t of the launch.
 // fc: features per pass (1 or 2); vec: whole-row vector access (packed layout).
 // hess: the full-Hessian variant (outputs / upstream gradients in hess / g_hess
@@ -92,5 +103,7 @@ int launch_hermite_bwd(const BwdParams& p, int fc, bool vec, bool hess, void* st
 int launch_linear_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream);
 int launch_linear_bwd(const BwdParams& p, int fc, bool vec, void* stream);
 int launch_indices(const IdxParams& p, void* stream);
+// red: RED replay (adds 1.0 to every float of each chunk), else gather replay.
+int launch_replay(const ReplayParams& p, bool red, void* stream);
 
 }  // namespace hg

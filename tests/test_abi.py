@@ -177,6 +177,23 @@ def test_four_dimensional_descriptor_is_accepted(m):
     assert hg.hg_level_resolutions(m.GridDesc(d=4, L=3, F=2, n_min=4, n_max=16)) == [4, 8, 16]
 
 
+def test_replay_probe_arguments_are_checked(m):
+    """The replay probes reject unsupported chunks, short strides and NULL
+    pointers before any launch; n = 0 is a no-op."""
+    hg = m.hg
+    desc = m.GridDesc(d=3, L=4, F=2, n_min=4, n_max=32, log2_T=(8, 8, 8, 8))
+    E, buf = hg.HG_ERR_INVALID_ARG, 1 << 20
+    stride = 256 * 64
+    assert hg.hg_probe_replay_gather(desc, 5, 16, buf, stride, 64, 1, 32, stream=0, check=False) == E   # 64-B chunk
+    assert hg.hg_probe_replay_red(desc, 5, 16, buf, stride, 64, 2, stream=0, check=False) == E          # 32-B RED
+    assert hg.hg_probe_replay_red(desc, 5, 16, buf, stride, 64, 3, stream=0, check=False) == E          # 64 % 3
+    assert hg.hg_probe_replay_red(desc, 5, 16, buf, stride - 64, 64, 4, stream=0, check=False) == E     # overlap
+    assert hg.hg_probe_replay_red(desc, 5, 0, buf, stride, 64, 4, stream=0, check=False) == E           # NULL coords
+    assert hg.hg_probe_replay_gather(desc, 5, 16, buf, stride, 64, 2, 0, stream=0, check=False) == E    # NULL sink
+    assert hg.hg_probe_replay_red(desc, 5, 16, buf + 4, stride, 64, 4, stream=0, check=False) == E      # misaligned
+    assert hg.hg_probe_replay_red(desc, 0, 0, 0, stride, 64, 4, stream=0, check=False) == hg.HG_OK
+
+
 def test_zero_points_touch_nothing(m):
     """n = 0 with a valid descriptor succeeds without a launch (no GPU here)."""
     hg = m.hg

@@ -79,17 +79,10 @@ def test_algorithmic_bytes_and_patterns():
     # 4D: 2^20 points x 16 levels x 16 corners x (16 slots x 2 features x 4 bytes)
     assert bench.algorithmic_bytes(w6, (1 << 16) - 1) == ((1 << 20) * 16 * 16 * 128,) * 2
     assert bench.kernel_patterns(w6) == ((128, 4), (128, 8))
-    # probe buffers per active level: the touched rows of its table / fp32 gradient table, >= 32 MiB
-    import oracle
-    full = (1 << 16) - 1
-    assert set(bench.level_probe_sizes(w, oracle.level_resolutions(16, 16, 512), full)) == {(25, 25)}
-    s5 = bench.level_probe_sizes(w5, oracle.level_resolutions(16, 16, 2048), full)
-    assert s5[0] == (25, 25) and s5[-1] == (27, 28)          # 17^3 rows; 2^22 x 32 B fp16, x 64 B fp32
-    assert len(bench.level_probe_sizes(w5, oracle.level_resolutions(16, 16, 2048), 0b1111)) == 4
-    s6 = bench.level_probe_sizes(w6, oracle.level_resolutions(16, 16, 512), full)
-    assert s6[0] == (25, 25) and s6[-1] == (26, 26)          # 17^4 x 128 B = 10.7 MB; 2^19 x 128 B
     w2 = W.WORKLOADS[2]
     assert bench.algorithmic_bytes(w2, (1 << 16) - 1) == ((1 << 20) * 16 * 4 * 8,) * 2
+    assert bench.kernel_patterns(w2) == ((8, 1), (8, 1))          # d-linear: one float2 load / red.v2 per corner
+    assert bench.kernel_patterns(W.WORKLOADS[3]) == ((32, 1), (32, 2))
 
 
 def bench_workload(cfg):
