@@ -85,10 +85,16 @@ def _load():
                                               i64, P, P, P, P, P, P, P, ctypes.c_int]
     lib.oracle_encode_bwd_hessian_level.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                     P, P, i64, P, P, P, P, P, P]
+    f32 = ctypes.c_float
+    lib.oracle_linear_fd_fwd.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, ctypes.c_int, u32, P, i64,
+                                         P, f32, P, P, P, P, P, P, P, P, ctypes.c_int]
+    lib.oracle_linear_fd_bwd_level.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                                               ctypes.c_int, i64, P, f32, P, P, P, P, P, P]
     for name in ("oracle_eval_cell", "oracle_hash_indices", "oracle_encode_fwd",
                  "oracle_encode_bwd_level", "oracle_linear_fwd", "oracle_linear_bwd_level",
                  "oracle_slot_in_bucket", "oracle_hess_entries", "oracle_eval_cell_hessian",
-                 "oracle_encode_fwd_hessian", "oracle_encode_bwd_hessian_level"):
+                 "oracle_encode_fwd_hessian", "oracle_encode_bwd_hessian_level", "oracle_linear_fd_fwd",
+                 "oracle_linear_fd_bwd_level"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -351,6 +357,69 @@ def linear_bwd(d: int, F: int, res, log2T: int, coords: np.ndarray, g_gamma: np.
         grad[l] = g
         if with_mags:
             mag[l] = m
+    return (grad, mag) if with_mags else grad
+
+
+# ---------------------------------------------------------------------------
+# INGP-FD: d-linear encoding with central finite differences
+# ---------------------------------------------------------------------------
+
+def linear_fd_fwd(d: int, F: int, res, log2T: int, table: np.ndarray, coords: np.ndarray, eps: float,
+                  level_mask: int | None = None, nthreads: int | None = None, with_mags: bool = True):
+    """INGP-FD forward: point-major fp64 gamma [N][L][F] at x, central-difference
+    dgamma [N][d][L][F] and lap [N][L][F], and the stencil encodings
+    [N][2d][L][F] (j = 2i: x + eps e_i, j = 2i+1: x - eps e_i), from the
+    d-linear table [L][T][F]; eps is taken as float32 (the shift is one fp32 add)."""
+    lib = _load()
+    L = len(res)
+    if level_mask is None:
+        level_mask = (1 << L) - 1
+    tb = np.ascontiguousarray(table, np.float64)
+    if tb.shape != (L, 1 << int(log2T), F):
+        raise ValueError("linear table must be [L][T][F]")
+    coords = np.ascontiguousarray(coords, np.float32)
+    n = coords.shape[0]
+    r = np.asarray(res, np.int32)
+    out = {"gamma": np.zeros((n, L, F)), "dgamma": np.zeros((n, d, L, F)), "lap": np.zeros((n, L, F)),
+           "stencil": np.zeros((n, 2 * d, L, F))}
+    if with_mags:
+        out.update({"m" + k: np.zeros_like(v) for k, v in list(out.items())})
+    _check(lib.oracle_linear_fd_fwd(d, L, F, _ptr(r), int(log2T), level_mask & 0xffffffff, _ptr(tb), n, _ptr(coords),
+                                    float(np.float32(eps)), _ptr(out["gamma"]), _ptr(out["dgamma"]),
+                                    _ptr(out["lap"]), _ptr(out["stencil"]), _ptr(out.get("mgamma")),
+                                    _ptr(out.get("mdgamma")), _ptr(out.get("mlap")), _ptr(out.get("mstencil")),
+                                    nthreads or default_threads()), "linear_fd_fwd")
+    return out
+
+
+def linear_fd_bwd(d: int, F: int, res, log2T: int, coords: np.ndarray, eps: float, g_gamma=None, g_dgamma=None,
+                  g_lap=None, g_stencil=None, level_mask: int | None = None, levels=None, with_mags: bool = True,
+                  nthreads: int | None = None):
+    """Backward of :func:`linear_fd_fwd` (float32 point-major upstream; any may
+    be None): fp64 grad [L][T][F] and magnitude; levels outside ``levels`` /
+    the mask stay zero."""
+    from concurrent.futures import ThreadPoolExecutor
+    lib = _load()
+    L = len(res)
+    if level_mask is None:
+        level_mask = (1 << L) - 1
+    todo = [l for l in (range(L) if levels is None else levels) if (level_mask >> l) & 1]
+    coords = np.ascontiguousarray(coords, np.float32)
+    n = coords.shape[0]
+    r = np.asarray(res, np.int32)
+    f32 = lambda a: None if a is None else np.ascontiguousarray(a, np.float32)
+    gg, gd, gl, gs = f32(g_gamma), f32(g_dgamma), f32(g_lap), f32(g_stencil)
+    grad = np.zeros((L, 1 << int(log2T), F))
+    mag = np.zeros_like(grad) if with_mags else None
+
+    def one(l):
+        return lib.oracle_linear_fd_bwd_level(d, L, F, l, _ptr(r), int(log2T), n, _ptr(coords),
+                                              float(np.float32(eps)), _ptr(gg), _ptr(gd), _ptr(gl), _ptr(gs),
+                                              _ptr(grad[l]), _ptr(mag[l]) if with_mags else None)
+
+    with ThreadPoolExecutor(max_workers=max(1, min(len(todo) or 1, nthreads or default_threads()))) as ex:
+        for rc in ex.map(one, todo):
+            _check(rc, "linear_fd_bwd")
     return (grad, mag) if with_mags else grad
 
 

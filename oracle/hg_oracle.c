@@ -54,6 +54,9 @@
  *    (level, feature).
  *  - Inactive levels (bit l of the mask clear) output zero and receive no
  *    gradient.
+ *  - INGP-FD (the page's finite-difference baseline): stencil points
+ *    x +- eps e_i with the shifted coordinate computed as one fp32 add, and
+ *    the textbook central differences (see the INGP-FD section below).
  *
  * Each floating output is returned together with its condition magnitude:
  * the same sum with every factor replaced by its absolute value.  Tests use
@@ -678,6 +681,163 @@ int oracle_encode_bwd_hessian_level(int d, int L, int F, int l, const int32_t* r
                     }
                     grads[k][off + f] += w;
                     if (mags) mags[k][off + f] += m;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* INGP-FD: the d-linear encoding with central finite differences       */
+/* ------------------------------------------------------------------ */
+/* "Hermite-NGP: Gradient-Augmented Hash Encoding for Learning PDEs",
+ * sections 研究背景与动机 and 关键设计 2: the INGP-FD baseline takes the
+ * Laplacian by central differences from 2d+1 forward passes, at x and at
+ * x +- eps e_i.  Readings: the shifted coordinate is one fp32 add
+ * (x_i + eps, x_i - eps) and is then located like any coordinate (clamped
+ * to [0,1]); the differences are the textbook central ones,
+ *   d gamma / dx_i ~ (gamma(x + eps e_i) - gamma(x - eps e_i)) / (2 eps),
+ *   lap gamma      ~ sum_i (gamma(x + eps e_i) - 2 gamma(x) + gamma(x - eps e_i)) / eps^2.
+ * Stencil output j = 2i is x + eps e_i, j = 2i + 1 is x - eps e_i.          */
+
+/* d-linear encoding of one point at one level (table_l = [T][F]). */
+static void linear_point(int d, int F, int32_t N, int log2T, const double* table_l, const float* x,
+                         double* out, double* mag) {
+    int64_t c[OR_MAXD];
+    double t[OR_MAXD];
+    for (int i = 0; i < d; ++i) locate(x[i], N, &c[i], &t[i]);
+    for (int f = 0; f < F; ++f) out[f] = mag[f] = 0.0;
+    for (int v = 0; v < (1 << d); ++v) {
+        int64_t g[OR_MAXD];
+        double w = 1.0;
+        for (int i = 0; i < d; ++i) {
+            const int vi = v >> i & 1;
+            g[i] = c[i] + vi;
+            w *= vi ? t[i] : 1.0 - t[i];
+        }
+        const double* th = table_l + (size_t)vertex_index(d, g, N, log2T) * F;
+        for (int f = 0; f < F; ++f) {
+            out[f] += w * th[f];
+            mag[f] += fabs(w) * fabs(th[f]);
+        }
+    }
+}
+
+/* The coordinates of stencil point s of x: s = 0 is x, s = 1 + j is stencil
+ * output j (j = 2i: x + eps e_i; j = 2i + 1: x - eps e_i). */
+static void stencil_coords(int d, const float* x, float eps, int s, float* xs) {
+    for (int i = 0; i < d; ++i) xs[i] = x[i];
+    if (s > 0) {
+        const int j = s - 1, i = j / 2;
+        volatile float shifted = (j % 2 == 0) ? x[i] + eps : x[i] - eps;
+        xs[i] = shifted;
+    }
+}
+
+/* Forward: gamma[N][L][F] (at x), dgamma[N][d][L][F], lap[N][L][F] and the
+ * stencil encodings stencil[N][2d][L][F]; table [L][T][F].  Any output but
+ * gamma, and every magnitude array, may be NULL. */
+int oracle_linear_fd_fwd(int d, int L, int F, const int32_t* res, int log2T, uint32_t level_mask,
+                         const double* table, int64_t n_pts, const float* coords, float eps,
+                         double* gamma, double* dgamma, double* lap, double* stencil,
+                         double* mgamma, double* mdgamma, double* mlap, double* mstencil, int nthreads) {
+    if (d < 1 || d > OR_MAXD || L < 1 || F < 1 || F > 8 || !(eps > 0.0f)) return 1;
+    set_threads(nthreads);
+    const int S = 2 * d + 1;
+    const double e = (double)eps;
+#pragma omp parallel for schedule(dynamic, 256)
+    for (int64_t n = 0; n < n_pts; ++n) {
+        double gs[2 * OR_MAXD + 1][8], ms[2 * OR_MAXD + 1][8];
+        for (int l = 0; l < L; ++l) {
+            const int active = (level_mask >> l) & 1u;
+            for (int s = 0; s < S; ++s) {
+                if (active) {
+                    float xs[OR_MAXD];
+                    stencil_coords(d, coords + n * d, eps, s, xs);
+                    linear_point(d, F, res[l], log2T, table + (size_t)l * ((size_t)1 << log2T) * F, xs, gs[s], ms[s]);
+                } else {
+                    for (int f = 0; f < F; ++f) gs[s][f] = ms[s][f] = 0.0;
+                }
+            }
+            for (int f = 0; f < F; ++f) {
+                const size_t o = ((size_t)n * L + l) * F + f;
+                gamma[o] = gs[0][f];
+                if (mgamma) mgamma[o] = ms[0][f];
+                double lp = 0.0, ml = 0.0;
+                for (int i = 0; i < d; ++i) {
+                    const double gp = gs[1 + 2 * i][f], gm = gs[2 + 2 * i][f];
+                    const double mp = ms[1 + 2 * i][f], mm = ms[2 + 2 * i][f];
+                    const size_t od = (((size_t)n * d + i) * L + l) * F + f;
+                    if (dgamma) dgamma[od] = (gp - gm) / (2.0 * e);
+                    if (mdgamma) mdgamma[od] = (mp + mm) / (2.0 * e);
+                    lp += (gp - 2.0 * gs[0][f] + gm) / (e * e);
+                    ml += (mp + 2.0 * ms[0][f] + mm) / (e * e);
+                }
+                if (lap) lap[o] = lp;
+                if (mlap) mlap[o] = ml;
+                for (int j = 0; j < 2 * d; ++j) {
+                    const size_t os = (((size_t)n * 2 * d + j) * L + l) * F + f;
+                    if (stencil) stencil[os] = gs[1 + j][f];
+                    if (mstencil) mstencil[os] = ms[1 + j][f];
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Backward of oracle_linear_fd_fwd for ONE level l into grad[T][F] (this
+ * level only, caller-zeroed; mag may be NULL).  Upstream gradients are
+ * float32, point-major as the forward's outputs; any may be NULL.  Each
+ * stencil point s receives the upstream weight of its value in the outputs:
+ *   s = x:          g_gamma - (2d / eps^2) g_lap
+ *   s = x + eps e_i:  g_dgamma_i / (2 eps) + g_lap / eps^2 + g_stencil_2i
+ *   s = x - eps e_i: -g_dgamma_i / (2 eps) + g_lap / eps^2 + g_stencil_2i+1
+ * and scatters it with its d-linear corner weights.  Serial over points. */
+int oracle_linear_fd_bwd_level(int d, int L, int F, int l, const int32_t* res, int log2T, int64_t n_pts,
+                               const float* coords, float eps, const float* g_gamma, const float* g_dgamma,
+                               const float* g_lap, const float* g_stencil, double* grad, double* mag) {
+    if (d < 1 || d > OR_MAXD || l < 0 || l >= L || F < 1 || F > 8 || !(eps > 0.0f)) return 1;
+    const int S = 2 * d + 1;
+    const double e = (double)eps;
+    for (int64_t n = 0; n < n_pts; ++n) {
+        double u[2 * OR_MAXD + 1][8], mu[2 * OR_MAXD + 1][8];
+        for (int f = 0; f < F; ++f) {
+            const size_t o = ((size_t)n * L + l) * F + f;
+            const double gg = g_gamma ? (double)g_gamma[o] : 0.0;
+            const double gl = g_lap ? (double)g_lap[o] : 0.0;
+            u[0][f] = gg - 2.0 * d * gl / (e * e);
+            mu[0][f] = fabs(gg) + 2.0 * d * fabs(gl) / (e * e);
+            for (int i = 0; i < d; ++i) {
+                const double gd = g_dgamma ? (double)g_dgamma[(((size_t)n * d + i) * L + l) * F + f] : 0.0;
+                for (int sgn = 0; sgn < 2; ++sgn) {
+                    const int j = 2 * i + sgn;
+                    const double gs = g_stencil ? (double)g_stencil[(((size_t)n * 2 * d + j) * L + l) * F + f] : 0.0;
+                    const double dir = sgn ? -1.0 : 1.0;
+                    u[1 + j][f] = dir * gd / (2.0 * e) + gl / (e * e) + gs;
+                    mu[1 + j][f] = fabs(gd) / (2.0 * e) + fabs(gl) / (e * e) + fabs(gs);
+                }
+            }
+        }
+        for (int s = 0; s < S; ++s) {
+            float xs[OR_MAXD];
+            stencil_coords(d, coords + n * d, eps, s, xs);
+            int64_t c[OR_MAXD];
+            double t[OR_MAXD];
+            for (int i = 0; i < d; ++i) locate(xs[i], res[l], &c[i], &t[i]);
+            for (int v = 0; v < (1 << d); ++v) {
+                int64_t g[OR_MAXD];
+                double w = 1.0;
+                for (int i = 0; i < d; ++i) {
+                    const int vi = v >> i & 1;
+                    g[i] = c[i] + vi;
+                    w *= vi ? t[i] : 1.0 - t[i];
+                }
+                const size_t idx = vertex_index(d, g, res[l], log2T);
+                for (int f = 0; f < F; ++f) {
+                    grad[idx * F + f] += w * u[s][f];
+                    if (mag) mag[idx * F + f] += fabs(w) * mu[s][f];
                 }
             }
         }

@@ -38,6 +38,13 @@ MUTANTS = [
      "else hij *= (m == i || m == j) ? (*h[m])[1] : (*h[m])[0];",
      "else hij *= (m == i) ? (*h[m])[1] : (*h[m])[0];"),
     ("Hessian missing N^2", "hess[q * F + f] += th * scale[k] * N * N * hij;", "hess[q * F + f] += th * scale[k] * N * hij;"),
+    ("FD shift directions swapped", "(j % 2 == 0) ? x[i] + eps : x[i] - eps;", "(j % 2 == 0) ? x[i] - eps : x[i] + eps;"),
+    ("FD gradient over eps instead of 2 eps", "if (dgamma) dgamma[od] = (gp - gm) / (2.0 * e);",
+     "if (dgamma) dgamma[od] = (gp - gm) / e;"),
+    ("FD Laplacian drops the centre term", "lp += (gp - 2.0 * gs[0][f] + gm) / (e * e);", "lp += (gp + gm) / (e * e);"),
+    ("FD backward centre weight without d", "u[0][f] = gg - 2.0 * d * gl / (e * e);", "u[0][f] = gg - 2.0 * gl / (e * e);"),
+    ("FD backward stencil sign", "u[1 + j][f] = dir * gd / (2.0 * e) + gl / (e * e) + gs;",
+     "u[1 + j][f] = gd / (2.0 * e) + gl / (e * e) + gs;"),
     ("Hessian backward uses the pure derivative for mixed entries",
      "else x *= (m == i || m == j) ? (*h[m])[1] : (*h[m])[0];",
      "else x *= (m == i || m == j) ? (*h[m])[2] : (*h[m])[0];"),
@@ -57,7 +64,8 @@ def _build(src_text, out_dir, tag):
 def _pins_pass(lib_path):
     env = dict(os.environ, HG_ORACLE_LIB=lib_path)
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_hessian_pins.py"), "-x", "-q", "-p",
+                        os.path.join(ROOT, "tests", "test_oracle_hessian_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_fd_pins.py"), "-x", "-q", "-p",
                         "no:cacheprovider"], env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     return r.returncode == 0, r.stdout[-400:]
 
