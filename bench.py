@@ -36,6 +36,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "encoded points/s (Hermite fwd γ,∇γ,∇²γ + bwd) at 1 B300; % of L2/HBM gather roofline"
+METRIC_FD = ("encoded points/s (INGP-FD: d-linear encodes at x and the 2d stencil points x +- eps e_i, + bwd) "
+             "at 1 B300; % of L2 gather roofline")
 METRIC_HESSIAN = "encoded points/s (Hermite fwd γ,∇γ, full Hessian + bwd) at 1 B300; % of L2 gather roofline"
 L2_BYTES = 126 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -184,6 +186,8 @@ def describe(w, mask, layout, hessian=False):
         "l2_flush": "inputs larger than L2 (tables + upstream gradients + outputs exceed 126 MB per step)",
         "parallelism": "replicas",
         "second_order": ("full Hessian" if hessian else "Laplacian") if w.kind == "hermite" else None,
+        **({"fd_eps": w.eps, "fd_outputs": "gamma(x) and the 2d stencil encodings (the network inputs of INGP-FD)"}
+           if w.kind == "linear_fd" else {}),
     }
 
 
@@ -192,7 +196,9 @@ def algorithmic_bytes(w, mask):
 
     fwd: compulsory coefficient bytes gathered = N * L_active * 2^d corners *
          (2^d slots * F * elem) for Hermite, N * L_active * 2^d * F * elem for
-         d-linear.
+         d-linear.  INGP-FD counts the centre cell's rows only: a stencil
+         point that stays in the cell needs no other row, so the compulsory
+         set is at least those 2^d rows (crossing points add more).
     bwd: RED payload bytes = the same count of fp32 gradient values * 4 B.
     """
     La = bin(mask).count("1")
@@ -257,6 +263,10 @@ class ClockSampler:
 # the CPU oracle (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
+def metric_of(w, hessian=False) -> str:
+    return METRIC_HESSIAN if hessian else (METRIC_FD if w.kind == "linear_fd" else METRIC)
+
+
 def traffic_key(w, points=None, hessian=False):
     """Name under which the DRAM traffic of a bench configuration is recorded."""
     key = w.name if not points else f"{w.name}@{points}"
@@ -293,6 +303,12 @@ def oracle_step(oracle, w, res, tabs, inputs, lo, hi, mask, threads, hessian=Fal
         oracle.encode_fwd(w.d, w.F, res, w.log2_T, tabs, x, level_mask=mask, nthreads=threads, with_mags=False)
         oracle.encode_bwd(w.d, w.F, res, w.log2_T, x, inputs["g_gamma"][lo:hi], inputs["g_dgamma"][lo:hi],
                           inputs["g_lap"][lo:hi], level_mask=mask, with_mags=False, nthreads=threads)
+    elif w.kind == "linear_fd":
+        oracle.linear_fd_fwd(w.d, w.F, res, w.log2_T[0], tabs, x, w.eps, level_mask=mask, nthreads=threads,
+                             with_mags=False)
+        oracle.linear_fd_bwd(w.d, w.F, res, w.log2_T[0], x, w.eps, g_gamma=inputs["g_gamma"][lo:hi],
+                             g_stencil=inputs["g_stencil"][lo:hi], level_mask=mask, with_mags=False,
+                             nthreads=threads)
     else:
         oracle.linear_fwd(w.d, w.F, res, w.log2_T[0], tabs, x, level_mask=mask, nthreads=threads, with_mags=False)
         oracle.linear_bwd(w.d, w.F, res, w.log2_T[0], x, inputs["g_gamma"][lo:hi], level_mask=mask,
@@ -335,7 +351,7 @@ def run_reference(args):
             times.append(time.perf_counter() - t0)
     t = sum(times)
     value = per_step * len(times) / t
-    line = {"impl": "reference", "metric": METRIC_HESSIAN if hessian else METRIC, "value": value, "unit": "points/s", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric_of(w, hessian), "value": value, "unit": "points/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy)", "config": describe(w, mask, args.layout, hessian),
@@ -496,7 +512,7 @@ def main():
         add_hessian_upstream(w, inputs, rank)
     n, d, L, F = w.n_points, w.d, w.L, w.F
     P = d * (d + 1) // 2
-    desc = M.GridDesc(d=d, L=L, F=F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T * (d + 1) if w.kind == "linear"
+    desc = M.GridDesc(d=d, L=L, F=F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T * (d + 1) if w.kind != "hermite"
                       else w.log2_T, level_mask=mask, dtype=M.HG_F16 if w.dtype == "f16" else M.HG_F32, layout=layout)
 
     def dev(a):
@@ -513,6 +529,10 @@ def main():
     # second-order output and its upstream gradient: the Laplacian, or the full Hessian
     shape_s = ((P, L, F, n) if fm else (n, P, L, F)) if hessian else shape_g
     gl = (dev(conv(inputs["g_hess"], True)) if hessian else dev(conv(inputs["g_lap"], False))) if hermite else None
+    fd = w.kind == "linear_fd"
+    shape_st = (2 * d, L, F, n) if fm else (n, 2 * d, L, F)          # INGP-FD stencil encodings
+    gst = dev(conv(inputs["g_stencil"], True)) if fd else None
+    stencil = torch.empty(shape_st, device="cuda") if fd else None
     gamma = torch.empty(shape_g, device="cuda")
     dgamma = torch.empty(shape_d, device="cuda") if hermite else None
     lap = torch.empty(shape_s, device="cuda") if hermite else None
@@ -528,6 +548,8 @@ def main():
             hg.hg_encode_fwd_hessian(desc, n, coords, tviews, gamma, dgamma, lap, stream)
         elif hermite:
             hg.hg_encode_fwd(desc, n, coords, tviews, gamma, dgamma, lap, stream)
+        elif fd:
+            hg.hg_linear_fd_fwd(desc, n, coords, w.eps, tviews, gamma, None, None, stencil, stream)
         else:
             hg.hg_linear_fwd(desc, n, coords, tviews, gamma, stream)
 
@@ -536,6 +558,8 @@ def main():
             hg.hg_encode_bwd_hessian(desc, n, coords, gg, gd, gl, gviews, stream)
         elif hermite:
             hg.hg_encode_bwd(desc, n, coords, gg, gd, gl, gviews, stream)
+        elif fd:
+            hg.hg_linear_fd_bwd(desc, n, coords, w.eps, gg, None, None, gst, gviews, stream)
         else:
             hg.hg_linear_bwd(desc, n, coords, gg, gviews, stream)
 
@@ -617,8 +641,8 @@ def main():
     }
     dom = "bwd" if t_bwd >= t_fwd else "fwd"
     k = kernels[dom]
-    kname = {"fwd": "hermite_fwd" if w.kind == "hermite" else "linear_fwd",
-             "bwd": "hermite_bwd" if w.kind == "hermite" else "linear_bwd"}[dom]
+    prefix = {"hermite": "hermite", "linear": "linear", "linear_fd": "linear_fd"}[w.kind]
+    kname = {"fwd": prefix + "_fwd", "bwd": prefix + "_bwd"}[dom]
     traffic = recorded_traffic(traffic_key(w, args.points, hessian), kname)
     roofline = {"bound": "l2", "kernel": dom, "achieved": k["achieved"], "peak": k["peak"], "unit": "GB/s",
                 "frac": k["frac"], "traffic": traffic,
@@ -631,14 +655,14 @@ def main():
     e2e = None
     if not args.no_e2e and rank == 0:
         e2e = run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, shape_s, hermite,
-                      hessian, grad, stream)
+                      hessian, grad, stream, shape_st)
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(w, inputs, mask, args.cpu_sample, hessian)
 
     if rank == 0:
         line = {
-            "metric": METRIC_HESSIAN if hessian else METRIC, "value": value, "unit": "points/s", "n_gpus": world,
+            "metric": metric_of(w, hessian), "value": value, "unit": "points/s", "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -655,7 +679,7 @@ def main():
 
 
 def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, shape_s, hermite, hessian,
-            grad, stream, steps=8, warmup=2):
+            grad, stream, shape_st=None, steps=8, warmup=2):
     """The step through the C ABI with inputs starting in pinned host memory,
     pipelined over three streams as a streaming user would run it: the
     host-to-device copy of step i+1's coordinates and upstream gradients and
@@ -672,7 +696,10 @@ def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, sha
     if hermite:
         second = conv(inputs["g_hess"], True) if hessian else conv(inputs["g_lap"], False)
         h_in += [pinned(conv(inputs["g_dgamma"], True)), pinned(second)]
-    out_shapes = [shape_g] + ([shape_d, shape_s] if hermite else [])
+    fd = w.kind == "linear_fd"
+    if fd:
+        h_in += [pinned(conv(inputs["g_stencil"], True))]
+    out_shapes = [shape_g] + ([shape_d, shape_s] if hermite else []) + ([shape_st] if fd else [])
     d_in = [[torch.empty_like(t, device="cuda") for t in h_in] for _ in range(2)]
     d_out = [[torch.empty(sh, device="cuda") for sh in out_shapes] for _ in range(2)]
     h_out = [[torch.empty(sh).pin_memory() for sh in out_shapes] for _ in range(2)]
@@ -704,6 +731,9 @@ def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, sha
         elif hermite:
             hg.hg_encode_fwd(desc, n, c, tviews, d_out[b][0], d_out[b][1], d_out[b][2], s_comp)
             hg.hg_encode_bwd(desc, n, c, gg, d_in[b][2], d_in[b][3], gviews, s_comp)
+        elif fd:
+            hg.hg_linear_fd_fwd(desc, n, c, w.eps, tviews, d_out[b][0], None, None, d_out[b][1], s_comp)
+            hg.hg_linear_fd_bwd(desc, n, c, w.eps, gg, None, None, d_in[b][2], gviews, s_comp)
         else:
             hg.hg_linear_fwd(desc, n, c, tviews, d_out[b][0], s_comp)
             hg.hg_linear_bwd(desc, n, c, gg, gviews, s_comp)
@@ -727,8 +757,9 @@ def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, sha
     ms = a.elapsed_time(e) / steps
     return {"value": n / (ms * 1e-3), "unit": "points/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms, "steps": steps,
-            "note": "pinned host buffers; coordinates and upstream gradients in, gamma/grad gamma/"
-                    + ("Hessian" if hessian else "Laplacian") + " out, "
+            "note": "pinned host buffers; coordinates and upstream gradients in, "
+                    + ("gamma and the stencil encodings" if w.kind == "linear_fd" else
+                       "gamma/grad gamma/" + ("Hessian" if hessian else "Laplacian")) + " out, "
                     "every step; copies of neighbouring steps overlap the encode (3 streams, 2 buffer sets); "
                     "gradient tables stay on the device"}
 

@@ -227,6 +227,40 @@ hg_status hg_linear_fwd(const hg_grid_desc* desc, int64_t n, const float* coords
 hg_status hg_linear_bwd(const hg_grid_desc* desc, int64_t n, const float* coords,
                         const float* g_gamma, const hg_grad_table* grad, hg_stream stream);
 
+/* INGP-FD: the d-linear encoding with central finite differences -- the
+ * finite-difference baseline [HNGP 研究背景与动机, 关键设计 2] that takes the
+ * Laplacian from 2d+1 d-linear encodes.  For every point and active level,
+ * with the stencil points x + eps e_i and x - eps e_i (each shifted
+ * coordinate is one fp32 add, x_i + eps or x_i - eps, then clamped and
+ * located as in hg_linear_fwd):
+ *   gamma    = gamma(x)                                     [n][L][F] / [L][F][n]
+ *   dgamma_i = (gamma(x + eps e_i) - gamma(x - eps e_i)) / (2 eps)
+ *   lap      = sum_i (gamma(x + eps e_i) - 2 gamma(x) + gamma(x - eps e_i)) / eps^2
+ *   stencil_j = gamma at stencil point j (j = 2i: x + eps e_i; j = 2i + 1:
+ *              x - eps e_i): HG_POINT_MAJOR [n][2d][L][F], HG_FEATURE_MAJOR
+ *              [2d][L][F][n] -- the encodings INGP-FD feeds its network.
+ *   eps:     the step, positive and finite (1/eps^2 must not overflow fp32)
+ *   table:   as hg_linear_fwd (one table, log2_T[0])
+ *   gamma:   device float32 output (required when n > 0)
+ *   dgamma, lap, stencil: device float32 outputs or NULL (not computed)
+ * Arithmetic fp32 (the factors 1/(2 eps) and 1/eps^2 rounded once).
+ * Errors: as hg_linear_fwd; HG_ERR_INVALID_ARG for a bad eps. */
+hg_status hg_linear_fd_fwd(const hg_grid_desc* desc, int64_t n, const float* coords, float eps,
+                           const hg_table* table, float* gamma, float* dgamma, float* lap, float* stencil,
+                           hg_stream stream);
+
+/* Backward of hg_linear_fd_fwd: every stencil point scatters, with its
+ * d-linear corner weights, the upstream weight of its value in the outputs,
+ *   x:            g_gamma - (2d / eps^2) g_lap
+ *   x + eps e_i:  g_dgamma_i / (2 eps) + g_lap / eps^2 + g_stencil_2i
+ *   x - eps e_i: -g_dgamma_i / (2 eps) + g_lap / eps^2 + g_stencil_2i+1
+ * into the fp32 gradient table `grad` (accumulated, caller-zeroed).  Upstream
+ * gradients in the layouts of the forward's outputs; any may be NULL.
+ * Errors: as hg_linear_bwd; HG_ERR_INVALID_ARG for a bad eps. */
+hg_status hg_linear_fd_bwd(const hg_grid_desc* desc, int64_t n, const float* coords, float eps,
+                           const float* g_gamma, const float* g_dgamma, const float* g_lap,
+                           const float* g_stencil, const hg_grad_table* grad, hg_stream stream);
+
 /* Vertex indices, for checking the lookup bit for bit: idx is device uint32
  * [n][L][d+1][2^d], the index of corner v in order table k at level l, for
  * every level (level_mask does not apply).  Errors: as hg_encode_fwd. */

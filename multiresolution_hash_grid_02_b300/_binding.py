@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
         "hg_linear_fwd": [D, c_i64, c_vp, T, c_vp, c_vp],
         "hg_linear_bwd": [D, c_i64, c_vp, c_vp, G, c_vp],
         "hg_hash_indices": [D, c_i64, c_vp, c_vp, c_vp],
+        "hg_linear_fd_fwd": [D, c_i64, c_vp, ctypes.c_float, T, c_vp, c_vp, c_vp, c_vp, c_vp],
+        "hg_linear_fd_bwd": [D, c_i64, c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_vp, G, c_vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -269,6 +271,27 @@ def hg_linear_bwd(desc: GridDesc, n: int, coords, g_gamma, grad: TableView, stre
                              _stream(stream) if n else 0)
     if check:
         _check(st, "hg_linear_bwd")
+    return st
+
+
+def hg_linear_fd_fwd(desc: GridDesc, n: int, coords, eps: float, table: TableView, gamma, dgamma=None, lap=None,
+                     stencil=None, stream=None, check: bool = True) -> int:
+    c = desc.as_c()
+    st = lib().hg_linear_fd_fwd(ctypes.byref(c), int(n), _addr(coords), float(eps), _tables_c([table], hg_table),
+                                _addr(gamma), _addr(dgamma), _addr(lap), _addr(stencil), _stream(stream) if n else 0)
+    if check:
+        _check(st, "hg_linear_fd_fwd")
+    return st
+
+
+def hg_linear_fd_bwd(desc: GridDesc, n: int, coords, eps: float, g_gamma, g_dgamma, g_lap, g_stencil,
+                     grad: TableView, stream=None, check: bool = True) -> int:
+    c = desc.as_c()
+    st = lib().hg_linear_fd_bwd(ctypes.byref(c), int(n), _addr(coords), float(eps), _addr(g_gamma), _addr(g_dgamma),
+                                _addr(g_lap), _addr(g_stencil), _tables_c([grad], hg_grad_table),
+                                _stream(stream) if n else 0)
+    if check:
+        _check(st, "hg_linear_fd_bwd")
     return st
 
 

@@ -341,3 +341,16 @@ __device__ __forceinline__ unsigned item_lanes(int64_t first_item, int64_t n) {
 }
 
 }  // namespace hg
+
+namespace hg {
+
+// d-linear weight of corner v (bit i = high side along axis i) at local coordinates t.
+template <int D>
+__device__ __forceinline__ float corner_weight(const float (&t)[D], int v) {
+    float w = 1.f;
+#pragma unroll
+    for (int i = 0; i < D; ++i) w *= ((v >> i) & 1) ? t[i] : 1.f - t[i];
+    return w;
+}
+
+}  // namespace hg

@@ -29,7 +29,8 @@ struct Common {
     //   gamma, lap:  n*sn  + (l*F + f)*sf
     //   dgamma:      n*dsn + j*dsj + (l*F + f)*dsf
     //   hess:        n*hsn + q*hsq + (l*F + f)*hsf   (q: upper-triangle entry)
-    int64_t sn, sf, dsn, dsj, dsf, hsn, hsq, hsf;
+    //   stencil:     n*ssn + j*ssj + (l*F + f)*ssf   (j: finite-difference stencil point, 2d of them)
+    int64_t sn, sf, dsn, dsj, dsf, hsn, hsq, hsf, ssn, ssj, ssf;
     Level lv[HG_MAX_LEVELS];
     // levels this launch covers: blockIdx.y -> level lvl[blockIdx.y], nlvl of them
     int32_t nlvl;
@@ -64,6 +65,8 @@ struct FwdParams {
     float* dgamma;
     float* lap;
     float* hess;      // full-Hessian forward only
+    float* stencil;   // finite-difference forward only: the 2d stencil encodings
+    float eps, half_inv_eps, inv_eps2;  // finite-difference step, 1/(2 eps), 1/eps^2 (fp32)
 };
 
 struct BwdParams {
@@ -75,6 +78,8 @@ struct BwdParams {
     const float* g_dgamma;
     const float* g_lap;
     const float* g_hess;  // full-Hessian backward only
+    const float* g_stencil;               // finite-difference backward only
+    float eps, half_inv_eps, inv_eps2;    // as FwdParams
 };
 
 struct IdxParams {
@@ -102,6 +107,8 @@ int launch_hermite_fwd(const FwdParams& p, int fc, bool vec, int dtype, bool hes
 int launch_hermite_bwd(const BwdParams& p, int fc, bool vec, bool hess, void* stream);
 int launch_linear_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream);
 int launch_linear_bwd(const BwdParams& p, int fc, bool vec, void* stream);
+int launch_linear_fd_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream);
+int launch_linear_fd_bwd(const BwdParams& p, int fc, bool vec, void* stream);
 int launch_indices(const IdxParams& p, void* stream);
 // red: RED replay (adds 1.0 to every float of each chunk), else gather replay.
 int launch_replay(const ReplayParams& p, bool red, void* stream);

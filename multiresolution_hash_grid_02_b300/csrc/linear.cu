@@ -14,14 +14,6 @@ namespace {
 
 constexpr int kBlock = 256;
 
-template <int D>
-__device__ __forceinline__ float corner_weight(const float (&t)[D], int v) {
-    float w = 1.f;
-#pragma unroll
-    for (int i = 0; i < D; ++i) w *= ((v >> i) & 1) ? t[i] : 1.f - t[i];
-    return w;
-}
-
 // VEC: FC == 2 and the row's pair is 8-byte (f32) / 4-byte (f16) aligned.
 template <int D, int FC, typename TT, bool VEC>
 __global__ void __launch_bounds__(kBlock) linear_fwd_kernel(const __grid_constant__ FwdParams p) {

@@ -31,7 +31,7 @@ import numpy as np
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "hermite" or "linear"
+    kind: str                 # "hermite", "linear" or "linear_fd" (d-linear with central differences)
     d: int
     n_points: int
     L: int
@@ -44,6 +44,7 @@ class Workload:
     coords: str = "uniform"   # "uniform" or "stratified"
     level_masks: tuple = field(default=())  # extra active-level masks to exercise
     seed: int = 0
+    eps: float = 0.0          # finite-difference step (linear_fd)
 
     @property
     def V(self) -> int:
@@ -64,6 +65,9 @@ WORKLOADS = {
     # space-time (x, y, z, t): workload 4's grid with a fourth axis, half the points
     6: Workload("4d_hermite_spacetime", "hermite", 4, 1 << 20, 16, 2, 16, 512, (19, 19, 19, 19, 19), "f32", 1e-2,
                 seed=6),
+    # the pages' finite-difference baseline (INGP-FD) on workload 4's grid: 2d+1 = 7 d-linear encodes per point;
+    # eps = 2^-10, half the finest cell (the pages leave the step to hand tuning)
+    7: Workload("3d_linear_fd", "linear_fd", 3, 1 << 21, 16, 2, 16, 512, (19,), "f32", 1e-4, seed=7, eps=2.0 ** -10),
 }
 
 
@@ -87,7 +91,7 @@ def draw_packed_table(rng: np.random.Generator, w: Workload) -> np.ndarray:
 
     Hermite: [L][T][2^d][F], the 2^d slots of a vertex ordered by derivative
     order, then lexicographically (f, fx, fy, [fz], fxy, [fxz, fyz, fxyz]).
-    Linear: [L][T][F].  float32 or float16 (the float32 draw rounded).
+    Linear (and linear_fd): [L][T][F].  float32 or float16 (the float32 draw rounded).
     """
     T = 1 << w.log2_T[0]
     if w.kind == "hermite":
@@ -130,11 +134,15 @@ def draw_order_tables(rng: np.random.Generator, w: Workload) -> list[np.ndarray]
 
 def draw_upstream(rng: np.random.Generator, w: Workload, with_derivs: bool = True):
     """N(0,1) upstream gradients in the point-major logical layout:
-    g_gamma [N][L][F], g_dgamma [N][d][L][F], g_lap [N][L][F]."""
+    g_gamma [N][L][F], g_dgamma [N][d][L][F], g_lap [N][L][F] (Hermite);
+    for linear_fd the third is g_stencil [N][2d][L][F], the upstream of the
+    stencil encodings."""
     n, L, F, d = w.n_points, w.L, w.F, w.d
     gg = rng.standard_normal((n, L, F), dtype=np.float32)
     if not with_derivs or w.kind == "linear":
         return gg, None, None
+    if w.kind == "linear_fd":
+        return gg, None, rng.standard_normal((n, 2 * d, L, F), dtype=np.float32)
     gd = rng.standard_normal((n, d, L, F), dtype=np.float32)
     gl = rng.standard_normal((n, L, F), dtype=np.float32)
     return gg, gd, gl
@@ -156,7 +164,9 @@ def make(w: Workload, seed: int | None = None, separate_orders: bool = False):
         out["order_tables"] = draw_order_tables(rng, w)
     else:
         out["table"] = draw_packed_table(rng, w)
-    out["g_gamma"], out["g_dgamma"], out["g_lap"] = draw_upstream(rng, w)
+    gg, gd, third = draw_upstream(rng, w)
+    out["g_gamma"], out["g_dgamma"] = gg, gd
+    out["g_stencil" if w.kind == "linear_fd" else "g_lap"] = third
     return out
 
 

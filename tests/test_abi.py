@@ -194,6 +194,19 @@ def test_replay_probe_arguments_are_checked(m):
     assert hg.hg_probe_replay_red(desc, 0, 0, 0, stride, 64, 4, stream=0, check=False) == hg.HG_OK
 
 
+def test_finite_difference_step_is_checked(m):
+    hg = m.hg
+    desc = m.GridDesc(d=3, L=4, F=2, n_min=4, n_max=32, log2_T=(8,))
+    lv = hg.linear_view(_FakeTable((4, 256, 2), addr=1 << 20))
+    E = hg.HG_ERR_INVALID_ARG
+    for eps in (0.0, -1e-3, float("nan"), float("inf"), 1e-30):
+        assert hg.hg_linear_fd_fwd(desc, 5, 16, eps, lv, 32, stream=0, check=False) == E, eps
+        assert hg.hg_linear_fd_bwd(desc, 5, 16, eps, 32, None, None, None, lv, stream=0, check=False) == E, eps
+    assert hg.hg_linear_fd_fwd(desc, 5, 0, 1e-3, lv, 32, stream=0, check=False) == E          # NULL coords
+    assert hg.hg_linear_fd_fwd(desc, 0, 0, 1e-3, lv, 0, stream=0, check=False) == hg.HG_OK     # n = 0
+    assert hg.hg_linear_fd_bwd(desc, 0, 0, 1e-3, 0, 0, 0, 0, lv, stream=0, check=False) == hg.HG_OK
+
+
 def test_zero_points_touch_nothing(m):
     """n = 0 with a valid descriptor succeeds without a launch (no GPU here)."""
     hg = m.hg

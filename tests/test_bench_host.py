@@ -83,6 +83,10 @@ def test_algorithmic_bytes_and_patterns():
     assert bench.algorithmic_bytes(w2, (1 << 16) - 1) == ((1 << 20) * 16 * 4 * 8,) * 2
     assert bench.kernel_patterns(w2) == ((8, 1), (8, 1))          # d-linear: one float2 load / red.v2 per corner
     assert bench.kernel_patterns(W.WORKLOADS[3]) == ((32, 1), (32, 2))
+    w7 = W.WORKLOADS[7]                                          # INGP-FD: the centre cell's 8-byte rows
+    assert bench.algorithmic_bytes(w7, (1 << 16) - 1) == ((1 << 21) * 16 * 8 * 8,) * 2
+    assert bench.kernel_patterns(w7) == ((8, 1), (8, 1))
+    assert "INGP-FD" in bench.metric_of(w7) and bench.metric_of(w) != bench.metric_of(w7)
 
 
 def bench_workload(cfg):
@@ -129,6 +133,16 @@ def test_ncu_log_parser_and_traffic_staleness(tmp_path, monkeypatch):
     (tmp_path / "traffic.json").write_text(json.dumps(data))
     assert bench.recorded_traffic("3d_hermite", "hermite_bwd") is None
     assert bench.traffic_key(bench_workload(4), None, True) == "3d_hermite+hessian"
+
+
+def test_reference_arm_fd_line():
+    """The reference arm runs the INGP-FD workload's oracle step."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "7",
+                          "--steps", "1", "--warmup", "0", "--cpu-sample", "4096"],
+                         env=dict(os.environ, RANK="0", WORLD_SIZE="1"), capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert "INGP-FD" in line["metric"] and line["config"]["fd_eps"] == 2.0 ** -10 and line["value"] > 0
 
 
 def test_reference_arm_hessian_line():

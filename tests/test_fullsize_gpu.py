@@ -199,3 +199,38 @@ def test_fullsize_4d_hermite_spacetime():
     m, hg, W, oracle = _mods()
     w = W.WORKLOADS[6]
     _check_hermite(w, W.make(w), (1 << w.L) - 1, fwd_levels=range(w.L), bwd_levels=(0, 2, 3, 15), seed=70)
+
+
+def test_fullsize_3d_linear_fd():
+    """INGP-FD on workload 4's grid (2^21 points, 16 levels, T = 2^19): gamma
+    and the six stencil encodings forward, their upstream backward, as the
+    benchmark launches them; sampled points forward, whole levels backward
+    (levels 0-6 one-to-one and privatised or direct, 7-15 hashed)."""
+    m, hg, W, oracle = _mods()
+    w = W.WORKLOADS[7]
+    inp = W.make(w)
+    n, d, L, F = w.n_points, w.d, w.L, w.F
+    res = oracle.level_resolutions(L, w.n_min, w.n_max)
+    desc = m.GridDesc(d=d, L=L, F=F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T * (d + 1),
+                      layout=m.HG_FEATURE_MAJOR)
+    coords = torch.from_numpy(inp["coords"]).cuda()
+    table = torch.from_numpy(inp["table"]).cuda()
+    gamma = torch.empty((L, F, n), device="cuda")
+    stencil = torch.empty((2 * d, L, F, n), device="cuda")
+    hg.hg_linear_fd_fwd(desc, n, coords, w.eps, m.linear_view(table), gamma, None, None, stencil)
+    grad = torch.zeros_like(table)
+    hg.hg_linear_fd_bwd(desc, n, coords, w.eps, torch.from_numpy(W.to_feature_major(inp["g_gamma"], False)).cuda(),
+                        None, None, torch.from_numpy(W.to_feature_major(inp["g_stencil"], True)).cuda(),
+                        m.linear_view(grad))
+    torch.cuda.synchronize()
+    rows = _sample_rows(np.random.default_rng(80), n, 20000)
+    ref = oracle.linear_fd_fwd(d, F, res, w.log2_T[0], inp["table"], inp["coords"][rows], w.eps)
+    ri = torch.from_numpy(rows).cuda()
+    check_close("gamma", W.from_feature_major(host(gamma[:, :, ri]), False), ref["gamma"], ref["mgamma"])
+    check_close("stencil", W.from_feature_major(host(stencil[:, :, :, ri]), True), ref["stencil"], ref["mstencil"])
+    levels = (0, 6, 7, 15)
+    want, mag = oracle.linear_fd_bwd(d, F, res, w.log2_T[0], inp["coords"], w.eps, g_gamma=inp["g_gamma"],
+                                     g_stencil=inp["g_stencil"], levels=levels)
+    got = host(grad)
+    for l in levels:
+        check_close(f"grad level {l}", got[l], want[l], mag[l])
