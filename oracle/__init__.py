@@ -90,7 +90,11 @@ def _load():
                                          P, f32, P, P, P, P, P, P, P, P, ctypes.c_int]
     lib.oracle_linear_fd_bwd_level.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
                                                ctypes.c_int, i64, P, f32, P, P, P, P, P, P]
-    for name in ("oracle_eval_cell", "oracle_hash_indices", "oracle_encode_fwd",
+    lib.oracle_rbf_fwd.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, ctypes.c_int, u32, P, i64, P, f32,
+                                   ctypes.c_int, P, P, P, P, P, P, ctypes.c_int]
+    lib.oracle_rbf_bwd_level.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, ctypes.c_int,
+                                         i64, P, f32, ctypes.c_int, P, P, P, P, P]
+    for name in ("oracle_rbf_fwd", "oracle_rbf_bwd_level", "oracle_eval_cell", "oracle_hash_indices", "oracle_encode_fwd",
                  "oracle_encode_bwd_level", "oracle_linear_fwd", "oracle_linear_bwd_level",
                  "oracle_slot_in_bucket", "oracle_hess_entries", "oracle_eval_cell_hessian",
                  "oracle_encode_fwd_hessian", "oracle_encode_bwd_hessian_level", "oracle_linear_fd_fwd",
@@ -420,6 +424,65 @@ def linear_fd_bwd(d: int, F: int, res, log2T: int, coords: np.ndarray, eps: floa
     with ThreadPoolExecutor(max_workers=max(1, min(len(todo) or 1, nthreads or default_threads()))) as ex:
         for rc in ex.map(one, todo):
             _check(rc, "linear_fd_bwd")
+    return (grad, mag) if with_mags else grad
+
+
+# ---------------------------------------------------------------------------
+# Gaussian-RBF multi-resolution grid (DInf-Grid)
+# ---------------------------------------------------------------------------
+
+def rbf_fwd(d: int, F: int, res, log2T: int, table: np.ndarray, coords: np.ndarray, eps: float, rings: int,
+            level_mask: int | None = None, nthreads: int | None = None, with_mags: bool = True):
+    """Gaussian-RBF interpolation over the ring neighbourhood (distances in grid
+    units): point-major fp64 gamma [N][L][F], dgamma [N][d][L][F], lap [N][L][F]
+    (+ magnitudes) from the table [L][T][F]."""
+    lib = _load()
+    L = len(res)
+    if level_mask is None:
+        level_mask = (1 << L) - 1
+    tb = np.ascontiguousarray(table, np.float64)
+    if tb.shape != (L, 1 << int(log2T), F):
+        raise ValueError("RBF table must be [L][T][F]")
+    coords = np.ascontiguousarray(coords, np.float32)
+    n = coords.shape[0]
+    r = np.asarray(res, np.int32)
+    out = {"gamma": np.zeros((n, L, F)), "dgamma": np.zeros((n, d, L, F)), "lap": np.zeros((n, L, F))}
+    if with_mags:
+        out.update({"m" + k: np.zeros_like(v) for k, v in list(out.items())})
+    _check(lib.oracle_rbf_fwd(d, L, F, _ptr(r), int(log2T), level_mask & 0xffffffff, _ptr(tb), n, _ptr(coords),
+                              float(np.float32(eps)), int(rings), _ptr(out["gamma"]), _ptr(out["dgamma"]),
+                              _ptr(out["lap"]), _ptr(out.get("mgamma")), _ptr(out.get("mdgamma")),
+                              _ptr(out.get("mlap")), nthreads or default_threads()), "rbf_fwd")
+    return out
+
+
+def rbf_bwd(d: int, F: int, res, log2T: int, coords: np.ndarray, eps: float, rings: int, g_gamma=None,
+            g_dgamma=None, g_lap=None, level_mask: int | None = None, levels=None, with_mags: bool = True,
+            nthreads: int | None = None):
+    """Backward of :func:`rbf_fwd` (float32 point-major upstream, any may be
+    None): fp64 grad [L][T][F] and magnitude."""
+    from concurrent.futures import ThreadPoolExecutor
+    lib = _load()
+    L = len(res)
+    if level_mask is None:
+        level_mask = (1 << L) - 1
+    todo = [l for l in (range(L) if levels is None else levels) if (level_mask >> l) & 1]
+    coords = np.ascontiguousarray(coords, np.float32)
+    n = coords.shape[0]
+    r = np.asarray(res, np.int32)
+    f32 = lambda a: None if a is None else np.ascontiguousarray(a, np.float32)
+    gg, gd, gl = f32(g_gamma), f32(g_dgamma), f32(g_lap)
+    grad = np.zeros((L, 1 << int(log2T), F))
+    mag = np.zeros_like(grad) if with_mags else None
+
+    def one(l):
+        return lib.oracle_rbf_bwd_level(d, L, F, l, _ptr(r), int(log2T), n, _ptr(coords), float(np.float32(eps)),
+                                        int(rings), _ptr(gg), _ptr(gd), _ptr(gl), _ptr(grad[l]),
+                                        _ptr(mag[l]) if with_mags else None)
+
+    with ThreadPoolExecutor(max_workers=max(1, min(len(todo) or 1, nthreads or default_threads()))) as ex:
+        for rc in ex.map(one, todo):
+            _check(rc, "rbf_bwd")
     return (grad, mag) if with_mags else grad
 
 

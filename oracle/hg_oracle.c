@@ -7,7 +7,7 @@
  * suite, the smoke check and the benchmark's CPU-baseline leg may load this
  * file's shared library.  It shares no code with the CUDA library.
  *
- * Sources (page title, section):
+ * Sources (page title, section; the DInf-Grid page for the RBF grid):
  *  - "Hermite-NGP: Gradient-Augmented Hash Encoding for Learning PDEs",
  *    section "整体框架" (pipeline: per-level hash lookup of Hermite
  *    coefficients bucketed by derivative order, tensor-product Hermite
@@ -54,6 +54,8 @@
  *    (level, feature).
  *  - Inactive levels (bit l of the mask clear) output zero and receive no
  *    gradient.
+ *  - The Gaussian-RBF grid of the DInf-Grid page: distances in grid units,
+ *    ring-R box neighbourhoods clipped to the grid (see its section below).
  *  - INGP-FD (the page's finite-difference baseline): stencil points
  *    x +- eps e_i with the shifted coordinate computed as one fp32 add, and
  *    the textbook central differences (see the INGP-FD section below).
@@ -842,5 +844,190 @@ int oracle_linear_fd_bwd_level(int d, int L, int F, int l, const int32_t* res, i
             }
         }
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Gaussian-RBF multi-resolution grid (DInf-Grid)                        */
+/* ------------------------------------------------------------------ */
+/* "DInf-Grid：一种基于可微特征网格的神经微分方程求解器", sections 可微的径向基函数
+ * 插值 and 多分辨率特征网格: per grid (level), the feature at x is
+ *   f(x) = sum_{i in N(x)} w(x, x_i) F_i,
+ *   w(x, x_i) = phi(|x - x_i|) / sum_{j in N(x)} phi(|x - x_j|),
+ *   phi(r) = exp(-(eps r)^2),
+ * over a precomputed ring neighbourhood N(x) of the point's cell, and the
+ * levels' features are concatenated.  Readings: r is measured in the
+ * level's grid units (y = N_l x, vertex g at y = g), so eps = 1 with 3 rings
+ * covers the kernel's effective support; ring R holds the vertices g with
+ * c_i - R + 1 <= g_i <= c_i + R on every axis, clipped to the grid
+ * (0 <= g_i <= N_l); the cell c and y = c + t come from the same location
+ * as the hash grid (pos = fl32(x N_l)); vertices are indexed like the hash
+ * grid's (one-to-one when the level fits T, so the page's dense grids are
+ * that case).  Derivatives are exact: with S = sum_j phi_j,
+ *   d w_i / dy = (d phi_i - w_i dS) / S,
+ *   lap w_i    = (lap phi_i - 2 grad w_i . grad S - w_i lap S) / S,
+ *   d phi / dy_k = -2 eps^2 (y_k - g_k) phi,  lap phi = (4 eps^4 |y - g|^2 - 2 d eps^2) phi,
+ * and d/dx = N_l d/dy.                                                   */
+
+#define OR_MAX_RINGS 4
+
+/* Neighbourhood of one point at one level: vertex list, normalised weights
+ * w, their x-derivatives dw[k] and Laplacian lw, and the condition
+ * magnitudes of each (every term of the quotient rule in absolute value). */
+typedef struct {
+    int count;
+    int64_t g[(2 * OR_MAX_RINGS) * (2 * OR_MAX_RINGS) * (2 * OR_MAX_RINGS) * (2 * OR_MAX_RINGS)][OR_MAXD];
+    double w[4096], dw[4096][OR_MAXD], lw[4096];
+    double mw[4096], mdw[4096][OR_MAXD], mlw[4096];
+} rbf_nbhd;
+
+static void rbf_weights(int d, int32_t N, const float* x_in, double eps, int rings, rbf_nbhd* nb) {
+    int64_t c[OR_MAXD];
+    double t[OR_MAXD], y[OR_MAXD];
+    for (int i = 0; i < d; ++i) {
+        locate(x_in[i], N, &c[i], &t[i]);
+        y[i] = (double)c[i] + t[i];
+    }
+    const int side = 2 * rings;
+    int64_t total = 1;
+    for (int i = 0; i < d; ++i) total *= side;
+    const double e2 = eps * eps;
+    double phi[4096], dphi[4096][OR_MAXD], lphi[4096];
+    double S = 0.0, dS[OR_MAXD] = {0}, lS = 0.0, mdS[OR_MAXD] = {0}, mlS = 0.0;
+    nb->count = 0;
+    for (int64_t m = 0; m < total; ++m) {
+        int64_t g[OR_MAXD], rem = m;
+        int inside = 1;
+        for (int i = 0; i < d; ++i) {
+            g[i] = c[i] - rings + 1 + rem % side;
+            rem /= side;
+            if (g[i] < 0 || g[i] > N) inside = 0;
+        }
+        if (!inside) continue;
+        const int q = nb->count++;
+        double r2 = 0.0;
+        for (int i = 0; i < d; ++i) {
+            nb->g[q][i] = g[i];
+            r2 += (y[i] - (double)g[i]) * (y[i] - (double)g[i]);
+        }
+        phi[q] = exp(-e2 * r2);
+        for (int i = 0; i < d; ++i) dphi[q][i] = -2.0 * e2 * (y[i] - (double)g[i]) * phi[q];
+        lphi[q] = (4.0 * e2 * e2 * r2 - 2.0 * d * e2) * phi[q];
+        S += phi[q];
+        for (int i = 0; i < d; ++i) {
+            dS[i] += dphi[q][i];
+            mdS[i] += fabs(dphi[q][i]);
+        }
+        lS += lphi[q];
+        mlS += fabs(lphi[q]);
+    }
+    const double Nd = (double)N;
+    for (int q = 0; q < nb->count; ++q) {
+        const double w = phi[q] / S;
+        nb->w[q] = w;
+        nb->mw[q] = w;
+        double dot = 0.0, mdot = 0.0;
+        double dwy[OR_MAXD], mdwy[OR_MAXD];
+        for (int i = 0; i < d; ++i) {
+            dwy[i] = (dphi[q][i] - w * dS[i]) / S;
+            mdwy[i] = (fabs(dphi[q][i]) + w * mdS[i]) / S;
+            dot += dwy[i] * dS[i];
+            mdot += mdwy[i] * mdS[i];
+            nb->dw[q][i] = Nd * dwy[i];
+            nb->mdw[q][i] = Nd * mdwy[i];
+        }
+        nb->lw[q] = Nd * Nd * (lphi[q] - 2.0 * dot - w * lS) / S;
+        nb->mlw[q] = Nd * Nd * (fabs(lphi[q]) + 2.0 * mdot + w * mlS) / S;
+    }
+}
+
+static int rbf_args_ok(int d, int L, int F, float eps, int rings) {
+    return d >= 1 && d <= OR_MAXD && L >= 1 && F >= 1 && F <= 8 && eps > 0.0f && rings >= 1 &&
+           rings <= OR_MAX_RINGS;
+}
+
+/* Forward: gamma[N][L][F], dgamma[N][d][L][F], lap[N][L][F] and magnitudes
+ * (any but gamma may be NULL); table [L][T][F]. */
+int oracle_rbf_fwd(int d, int L, int F, const int32_t* res, int log2T, uint32_t level_mask, const double* table,
+                   int64_t n_pts, const float* coords, float eps, int rings, double* gamma, double* dgamma, double* lap,
+                   double* mgamma, double* mdgamma, double* mlap, int nthreads) {
+    if (!rbf_args_ok(d, L, F, eps, rings)) return 1;
+    set_threads(nthreads);
+#pragma omp parallel
+    {
+        rbf_nbhd* nb = (rbf_nbhd*)malloc(sizeof(rbf_nbhd));
+#pragma omp for schedule(dynamic, 64)
+        for (int64_t n = 0; n < n_pts; ++n) {
+            for (int l = 0; l < L; ++l) {
+                const int active = (level_mask >> l) & 1u;
+                if (active && nb) rbf_weights(d, res[l], coords + n * d, (double)eps, rings, nb);
+                for (int f = 0; f < F; ++f) {
+                    double g = 0, mg = 0, dg[OR_MAXD] = {0}, md[OR_MAXD] = {0}, lp = 0, ml = 0;
+                    if (active && nb) {
+                        for (int q = 0; q < nb->count; ++q) {
+                            const uint32_t idx = vertex_index(d, nb->g[q], res[l], log2T);
+                            const double th = table[((size_t)l * ((size_t)1 << log2T) + idx) * F + f];
+                            g += nb->w[q] * th;
+                            mg += nb->mw[q] * fabs(th);
+                            for (int i = 0; i < d; ++i) {
+                                dg[i] += nb->dw[q][i] * th;
+                                md[i] += nb->mdw[q][i] * fabs(th);
+                            }
+                            lp += nb->lw[q] * th;
+                            ml += nb->mlw[q] * fabs(th);
+                        }
+                    }
+                    const size_t o = ((size_t)n * L + l) * F + f;
+                    gamma[o] = g;
+                    if (mgamma) mgamma[o] = mg;
+                    if (lap) lap[o] = lp;
+                    if (mlap) mlap[o] = ml;
+                    for (int i = 0; i < d; ++i) {
+                        const size_t od = (((size_t)n * d + i) * L + l) * F + f;
+                        if (dgamma) dgamma[od] = dg[i];
+                        if (mdgamma) mdgamma[od] = md[i];
+                    }
+                }
+            }
+        }
+        free(nb);
+    }
+    return 0;
+}
+
+/* Backward for ONE level l into grad[T][F] (caller-zeroed; mag may be NULL):
+ * grad[idx(g)] += g_gamma w + sum_i g_dgamma_i dw_i + g_lap lw.  Serial. */
+int oracle_rbf_bwd_level(int d, int L, int F, int l, const int32_t* res, int log2T, int64_t n_pts,
+                         const float* coords, float eps, int rings, const float* g_gamma, const float* g_dgamma,
+                         const float* g_lap, double* grad, double* mag) {
+    if (!rbf_args_ok(d, L, F, eps, rings) || l < 0 || l >= L) return 1;
+    rbf_nbhd* nb = (rbf_nbhd*)malloc(sizeof(rbf_nbhd));
+    if (!nb) return 2;
+    for (int64_t n = 0; n < n_pts; ++n) {
+        rbf_weights(d, res[l], coords + n * d, (double)eps, rings, nb);
+        for (int q = 0; q < nb->count; ++q) {
+            const size_t idx = vertex_index(d, nb->g[q], res[l], log2T);
+            for (int f = 0; f < F; ++f) {
+                const size_t o = ((size_t)n * L + l) * F + f;
+                double w = 0.0, m = 0.0;
+                if (g_gamma) {
+                    w += (double)g_gamma[o] * nb->w[q];
+                    m += fabs((double)g_gamma[o]) * nb->mw[q];
+                }
+                for (int i = 0; i < d && g_dgamma; ++i) {
+                    const double u = (double)g_dgamma[(((size_t)n * d + i) * L + l) * F + f];
+                    w += u * nb->dw[q][i];
+                    m += fabs(u) * nb->mdw[q][i];
+                }
+                if (g_lap) {
+                    w += (double)g_lap[o] * nb->lw[q];
+                    m += fabs((double)g_lap[o]) * nb->mlw[q];
+                }
+                grad[idx * F + f] += w;
+                if (mag) mag[idx * F + f] += m;
+            }
+        }
+    }
+    free(nb);
     return 0;
 }

@@ -45,6 +45,13 @@ MUTANTS = [
     ("FD backward centre weight without d", "u[0][f] = gg - 2.0 * d * gl / (e * e);", "u[0][f] = gg - 2.0 * gl / (e * e);"),
     ("FD backward stencil sign", "u[1 + j][f] = dir * gd / (2.0 * e) + gl / (e * e) + gs;",
      "u[1 + j][f] = gd / (2.0 * e) + gl / (e * e) + gs;"),
+    ("RBF distance in x units", "y[i] = (double)c[i] + t[i];", "y[i] = ((double)c[i] + t[i]) / (double)N;"),
+    ("RBF ring box shifted by one", "g[i] = c[i] - rings + 1 + rem % side;", "g[i] = c[i] - rings + rem % side;"),
+    ("RBF weights not normalised", "const double w = phi[q] / S;", "const double w = phi[q];"),
+    ("RBF Laplacian drops the cross term", "nb->lw[q] = Nd * Nd * (lphi[q] - 2.0 * dot - w * lS) / S;",
+     "nb->lw[q] = Nd * Nd * (lphi[q] - w * lS) / S;"),
+    ("RBF kernel derivative sign", "dphi[q][i] = -2.0 * e2 * (y[i] - (double)g[i]) * phi[q];",
+     "dphi[q][i] = 2.0 * e2 * (y[i] - (double)g[i]) * phi[q];"),
     ("Hessian backward uses the pure derivative for mixed entries",
      "else x *= (m == i || m == j) ? (*h[m])[1] : (*h[m])[0];",
      "else x *= (m == i || m == j) ? (*h[m])[2] : (*h[m])[0];"),
@@ -65,7 +72,8 @@ def _pins_pass(lib_path):
     env = dict(os.environ, HG_ORACLE_LIB=lib_path)
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"),
                         os.path.join(ROOT, "tests", "test_oracle_hessian_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_fd_pins.py"), "-x", "-q", "-p",
+                        os.path.join(ROOT, "tests", "test_oracle_fd_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_rbf_pins.py"), "-x", "-q", "-p",
                         "no:cacheprovider"], env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     return r.returncode == 0, r.stdout[-400:]
 
