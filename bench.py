@@ -38,6 +38,8 @@ if ROOT not in sys.path:
 METRIC = "encoded points/s (Hermite fwd γ,∇γ,∇²γ + bwd) at 1 B300; % of L2/HBM gather roofline"
 METRIC_FD = ("encoded points/s (INGP-FD: d-linear encodes at x and the 2d stencil points x +- eps e_i, + bwd) "
              "at 1 B300; % of L2 gather roofline")
+METRIC_RBF = ("encoded points/s (Gaussian-RBF grid fwd gamma, grad, Laplacian + bwd) at 1 B300; "
+              "% of the measured ceiling")
 METRIC_HESSIAN = "encoded points/s (Hermite fwd γ,∇γ, full Hessian + bwd) at 1 B300; % of L2 gather roofline"
 L2_BYTES = 126 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -188,7 +190,25 @@ def describe(w, mask, layout, hessian=False):
         "second_order": ("full Hessian" if hessian else "Laplacian") if w.kind == "hermite" else None,
         **({"fd_eps": w.eps, "fd_outputs": "gamma(x) and the 2d stencil encodings (the network inputs of INGP-FD)"}
            if w.kind == "linear_fd" else {}),
+        **({"rbf_eps_grid_units": w.eps, "rbf_rings": w.rings, "taps_per_point_level": (2 * w.rings) ** w.d}
+           if w.kind == "rbf" else {}),
     }
+
+
+def rbf_flops(w, mask):
+    """Algorithmic FP32 flops of one RBF launch (forward or backward: the
+    transposed contraction has the same count): the separable contraction's
+    FMAs per (point, active level, feature) -- with K = 2 rings taps per
+    axis, K (3K + 5) in 2D and K (K (3K + 5) + 6) in 3D -- times 2."""
+    K = 2 * w.rings
+    per = K * (3 * K + 5) if w.d == 2 else K * (K * (3 * K + 5) + 6)
+    return 2 * per * w.F * w.n_points * bin(mask).count("1")
+
+
+def fp32_peak_tflops(torch, sm_mhz: float) -> float:
+    """FP32 FMA peak of the GPU: SMs x 128 lanes x 2 flops x SM clock."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
 def algorithmic_bytes(w, mask):
@@ -204,7 +224,8 @@ def algorithmic_bytes(w, mask):
     La = bin(mask).count("1")
     es = 2 if w.dtype == "f16" else 4
     slots = (1 << w.d) if w.kind == "hermite" else 1
-    per_pt_level_vals = (1 << w.d) * slots * w.F
+    taps = (2 * w.rings) ** w.d if w.kind == "rbf" else (1 << w.d)     # rbf: the ring box
+    per_pt_level_vals = taps * slots * w.F
     gather = w.n_points * La * per_pt_level_vals * es
     red = w.n_points * La * per_pt_level_vals * 4
     return gather, red
@@ -264,7 +285,9 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def metric_of(w, hessian=False) -> str:
-    return METRIC_HESSIAN if hessian else (METRIC_FD if w.kind == "linear_fd" else METRIC)
+    if hessian:
+        return METRIC_HESSIAN
+    return {"linear_fd": METRIC_FD, "rbf": METRIC_RBF}.get(w.kind, METRIC)
 
 
 def traffic_key(w, points=None, hessian=False):
@@ -303,6 +326,12 @@ def oracle_step(oracle, w, res, tabs, inputs, lo, hi, mask, threads, hessian=Fal
         oracle.encode_fwd(w.d, w.F, res, w.log2_T, tabs, x, level_mask=mask, nthreads=threads, with_mags=False)
         oracle.encode_bwd(w.d, w.F, res, w.log2_T, x, inputs["g_gamma"][lo:hi], inputs["g_dgamma"][lo:hi],
                           inputs["g_lap"][lo:hi], level_mask=mask, with_mags=False, nthreads=threads)
+    elif w.kind == "rbf":
+        oracle.rbf_fwd(w.d, w.F, res, w.log2_T[0], tabs, x, w.eps, w.rings, level_mask=mask, nthreads=threads,
+                       with_mags=False)
+        oracle.rbf_bwd(w.d, w.F, res, w.log2_T[0], x, w.eps, w.rings, g_gamma=inputs["g_gamma"][lo:hi],
+                       g_dgamma=inputs["g_dgamma"][lo:hi], g_lap=inputs["g_lap"][lo:hi], level_mask=mask,
+                       with_mags=False, nthreads=threads)
     elif w.kind == "linear_fd":
         oracle.linear_fd_fwd(w.d, w.F, res, w.log2_T[0], tabs, x, w.eps, level_mask=mask, nthreads=threads,
                              with_mags=False)
@@ -521,21 +550,23 @@ def main():
     coords = dev(inputs["coords"])
     table = dev(inputs["table"])
     hermite = w.kind == "hermite"
+    rbf = w.kind == "rbf"
     conv = (lambda a, ax: W.to_feature_major(a, ax)) if fm else (lambda a, ax: a)
     gg = dev(conv(inputs["g_gamma"], False))
-    gd = dev(conv(inputs["g_dgamma"], True)) if hermite else None
+    gd = dev(conv(inputs["g_dgamma"], True)) if (hermite or rbf) else None
     shape_g = (L, F, n) if fm else (n, L, F)
     shape_d = (d, L, F, n) if fm else (n, d, L, F)
     # second-order output and its upstream gradient: the Laplacian, or the full Hessian
     shape_s = ((P, L, F, n) if fm else (n, P, L, F)) if hessian else shape_g
-    gl = (dev(conv(inputs["g_hess"], True)) if hessian else dev(conv(inputs["g_lap"], False))) if hermite else None
+    gl = (dev(conv(inputs["g_hess"], True)) if hessian else dev(conv(inputs["g_lap"], False))) if (hermite or rbf) \
+        else None
     fd = w.kind == "linear_fd"
     shape_st = (2 * d, L, F, n) if fm else (n, 2 * d, L, F)          # INGP-FD stencil encodings
     gst = dev(conv(inputs["g_stencil"], True)) if fd else None
     stencil = torch.empty(shape_st, device="cuda") if fd else None
     gamma = torch.empty(shape_g, device="cuda")
-    dgamma = torch.empty(shape_d, device="cuda") if hermite else None
-    lap = torch.empty(shape_s, device="cuda") if hermite else None
+    dgamma = torch.empty(shape_d, device="cuda") if (hermite or rbf) else None
+    lap = torch.empty(shape_s, device="cuda") if (hermite or rbf) else None
     grad = torch.zeros(table.shape, dtype=torch.float32, device="cuda")
     if hermite:
         tviews, gviews = M.packed_views(table, d), M.packed_views(grad, d)
@@ -550,6 +581,8 @@ def main():
             hg.hg_encode_fwd(desc, n, coords, tviews, gamma, dgamma, lap, stream)
         elif fd:
             hg.hg_linear_fd_fwd(desc, n, coords, w.eps, tviews, gamma, None, None, stencil, stream)
+        elif rbf:
+            hg.hg_rbf_fwd(desc, n, coords, w.eps, w.rings, tviews, gamma, dgamma, lap, stream)
         else:
             hg.hg_linear_fwd(desc, n, coords, tviews, gamma, stream)
 
@@ -560,6 +593,8 @@ def main():
             hg.hg_encode_bwd(desc, n, coords, gg, gd, gl, gviews, stream)
         elif fd:
             hg.hg_linear_fd_bwd(desc, n, coords, w.eps, gg, None, None, gst, gviews, stream)
+        elif rbf:
+            hg.hg_rbf_bwd(desc, n, coords, w.eps, w.rings, gg, gd, gl, gviews, stream)
         else:
             hg.hg_linear_bwd(desc, n, coords, gg, gviews, stream)
 
@@ -579,8 +614,13 @@ def main():
 
     gather_pat, red_pat = kernel_patterns(w)
     gather_bytes, red_bytes = algorithmic_bytes(w, mask)
-    gather_peak, red_peak, t_replay_g, t_replay_r = replay_peaks(torch, hg, desc, n, coords, table, grad, gather_pat,
-                                                                 red_pat, gather_bytes, red_bytes, stream)
+    if rbf:   # the replay probes replay 2^d-corner streams, not the RBF's ring box
+        gather_peak = red_peak = 0.0
+        t_replay_g = t_replay_r = float("nan")
+    else:
+        gather_peak, red_peak, t_replay_g, t_replay_r = replay_peaks(torch, hg, desc, n, coords, table, grad,
+                                                                     gather_pat, red_pat, gather_bytes, red_bytes,
+                                                                     stream)
     uniform_g, uniform_r = probe_peaks(torch, hg, gather_pat, red_pat)
     # the ceiling is the larger of the two measured rates: the replay of the exact stream, and the
     # contention-free uniform-random rate of the same row pattern, which kernels that sum
@@ -639,18 +679,33 @@ def main():
                          f"{uniform_r:.0f} GB/s; peak = the larger",
                 "what": "fp32 gradient RED payload bytes / launch time vs the larger measured ceiling"},
     }
+    if rbf:
+        # the RBF grids are small and L1/L2-resident: the kernels are bound on chip (arithmetic latency,
+        # shared-memory atomics), so the roofline is FP32 arithmetic against the FMA peak at the sampled clock
+        flops = rbf_flops(w, mask)
+        fp32 = fp32_peak_tflops(torch, (clocks or {}).get("sm_mhz") or 2032.0)
+        for key, t in (("fwd", t_fwd), ("bwd", t_bwd)):
+            ach = flops / (t * 1e-3) / 1e12
+            kernels[key].update({"bound": "alu", "achieved": ach, "peak": fp32, "unit": "TFLOP/s",
+                                 "frac": ach / fp32, "algorithmic_flops": flops,
+                                 "probe": "FP32 FMA peak: SMs x 128 lanes x 2 flops x median sampled SM clock",
+                                 "what": "separable-contraction flops / launch time vs the FP32 FMA peak"})
+        combined = (2 * flops / (fp32 * 1e12)) / ((t_fwd + t_bwd) * 1e-3)
     dom = "bwd" if t_bwd >= t_fwd else "fwd"
     k = kernels[dom]
-    prefix = {"hermite": "hermite", "linear": "linear", "linear_fd": "linear_fd"}[w.kind]
+    prefix = {"hermite": "hermite", "linear": "linear", "linear_fd": "linear_fd", "rbf": "rbf"}[w.kind]
     kname = {"fwd": prefix + "_fwd", "bwd": prefix + "_bwd"}[dom]
     traffic = recorded_traffic(traffic_key(w, args.points, hessian), kname)
-    roofline = {"bound": "l2", "kernel": dom, "achieved": k["achieved"], "peak": k["peak"], "unit": "GB/s",
+    roofline = {"bound": k["bound"], "kernel": dom, "achieved": k["achieved"], "peak": k["peak"], "unit": k["unit"],
                 "frac": k["frac"], "traffic": traffic,
                 "peak_source": "measured live, the larger of: algorithmic bytes / time of hg_probe_replay_gather "
                                "or hg_probe_replay_red (the launch's own row addresses, lane split and vector "
                                "width, no arithmetic), and hg_probe_l2_gather / hg_probe_l2_red (uniform random "
                                "rows of the same size and split in an L2-resident 32 MiB buffer)",
                 "combined_frac": combined, "hbm_peak_gbs": hbm}
+    if rbf:
+        roofline["peak_source"] = ("FP32 FMA peak (SMs x 128 lanes x 2 flops x the median SM clock sampled during the "
+                                   "timed region); achieved = the separable contraction's flops / launch time")
 
     e2e = None
     if not args.no_e2e and rank == 0:
@@ -693,13 +748,14 @@ def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, sha
         return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
 
     h_in = [pinned(inputs["coords"]), pinned(conv(inputs["g_gamma"], False))]
-    if hermite:
+    rbf = w.kind == "rbf"
+    if hermite or rbf:
         second = conv(inputs["g_hess"], True) if hessian else conv(inputs["g_lap"], False)
         h_in += [pinned(conv(inputs["g_dgamma"], True)), pinned(second)]
     fd = w.kind == "linear_fd"
     if fd:
         h_in += [pinned(conv(inputs["g_stencil"], True))]
-    out_shapes = [shape_g] + ([shape_d, shape_s] if hermite else []) + ([shape_st] if fd else [])
+    out_shapes = [shape_g] + ([shape_d, shape_s] if (hermite or rbf) else []) + ([shape_st] if fd else [])
     d_in = [[torch.empty_like(t, device="cuda") for t in h_in] for _ in range(2)]
     d_out = [[torch.empty(sh, device="cuda") for sh in out_shapes] for _ in range(2)]
     h_out = [[torch.empty(sh).pin_memory() for sh in out_shapes] for _ in range(2)]
@@ -731,6 +787,9 @@ def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, sha
         elif hermite:
             hg.hg_encode_fwd(desc, n, c, tviews, d_out[b][0], d_out[b][1], d_out[b][2], s_comp)
             hg.hg_encode_bwd(desc, n, c, gg, d_in[b][2], d_in[b][3], gviews, s_comp)
+        elif rbf:
+            hg.hg_rbf_fwd(desc, n, c, w.eps, w.rings, tviews, d_out[b][0], d_out[b][1], d_out[b][2], s_comp)
+            hg.hg_rbf_bwd(desc, n, c, w.eps, w.rings, gg, d_in[b][2], d_in[b][3], gviews, s_comp)
         elif fd:
             hg.hg_linear_fd_fwd(desc, n, c, w.eps, tviews, d_out[b][0], None, None, d_out[b][1], s_comp)
             hg.hg_linear_fd_bwd(desc, n, c, w.eps, gg, None, None, d_in[b][2], gviews, s_comp)

@@ -261,6 +261,32 @@ hg_status hg_linear_fd_bwd(const hg_grid_desc* desc, int64_t n, const float* coo
                            const float* g_gamma, const float* g_dgamma, const float* g_lap,
                            const float* g_stencil, const hg_grad_table* grad, hg_stream stream);
 
+/* Gaussian-RBF multi-resolution grid (DInf-Grid) ["DInf-Grid：一种基于可微特征网格的
+ * 神经微分方程求解器", 可微的径向基函数插值, 多分辨率特征网格]: per point and active
+ * level, the features interpolated with normalised Gaussian weights over a
+ * ring neighbourhood of the point's cell,
+ *   gamma = sum_g w_g F_g,  w_g = phi(|y - g|) / sum_h phi(|y - h|),  phi(r) = exp(-(eps r)^2),
+ * with y = pos = fl32(x * N_l) the point in grid units (vertex g at y = g),
+ * the neighbourhood the box c_i - rings + 1 <= g_i <= c_i + rings clipped
+ * to the grid (0 <= g_i <= N_l), and dgamma, lap its exact gradient and
+ * Laplacian in x.  Vertices are indexed as in hg_linear_fwd (one-to-one
+ * when the level's (N_l+1)^d vertices fit T = 2^log2_T[0] -- the page's
+ * dense grids -- hashed otherwise); the table is [L][T][F] like the
+ * d-linear one.  Outputs as hg_encode_fwd (dgamma, lap may be NULL).
+ *   eps:   kernel width in grid units, positive and finite (the page: 1)
+ *   rings: 1..4 (the page: 3 for eps = 1)
+ * Arithmetic fp32.  Errors: as hg_linear_fwd; HG_ERR_INVALID_ARG for a bad
+ * eps or rings; HG_ERR_UNSUPPORTED for d = 4. */
+hg_status hg_rbf_fwd(const hg_grid_desc* desc, int64_t n, const float* coords, float eps, int32_t rings,
+                     const hg_table* table, float* gamma, float* dgamma, float* lap, hg_stream stream);
+
+/* Backward of hg_rbf_fwd: grad[l][idx(g)][f] += g_gamma w_g + sum_j g_dgamma_j
+ * dw_g/dx_j + g_lap lap w_g for every tap g, into the fp32 table `grad`
+ * (accumulated, caller-zeroed).  Errors: as hg_rbf_fwd. */
+hg_status hg_rbf_bwd(const hg_grid_desc* desc, int64_t n, const float* coords, float eps, int32_t rings,
+                     const float* g_gamma, const float* g_dgamma, const float* g_lap, const hg_grad_table* grad,
+                     hg_stream stream);
+
 /* Vertex indices, for checking the lookup bit for bit: idx is device uint32
  * [n][L][d+1][2^d], the index of corner v in order table k at level l, for
  * every level (level_mask does not apply).  Errors: as hg_encode_fwd. */

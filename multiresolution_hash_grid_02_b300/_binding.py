@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         "hg_hash_indices": [D, c_i64, c_vp, c_vp, c_vp],
         "hg_linear_fd_fwd": [D, c_i64, c_vp, ctypes.c_float, T, c_vp, c_vp, c_vp, c_vp, c_vp],
         "hg_linear_fd_bwd": [D, c_i64, c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_vp, G, c_vp],
+        "hg_rbf_fwd": [D, c_i64, c_vp, ctypes.c_float, c_i32, T, c_vp, c_vp, c_vp, c_vp],
+        "hg_rbf_bwd": [D, c_i64, c_vp, ctypes.c_float, c_i32, c_vp, c_vp, c_vp, G, c_vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -292,6 +294,26 @@ def hg_linear_fd_bwd(desc: GridDesc, n: int, coords, eps: float, g_gamma, g_dgam
                                 _stream(stream) if n else 0)
     if check:
         _check(st, "hg_linear_fd_bwd")
+    return st
+
+
+def hg_rbf_fwd(desc: GridDesc, n: int, coords, eps: float, rings: int, table: TableView, gamma, dgamma=None,
+               lap=None, stream=None, check: bool = True) -> int:
+    c = desc.as_c()
+    st = lib().hg_rbf_fwd(ctypes.byref(c), int(n), _addr(coords), float(eps), int(rings), _tables_c([table], hg_table),
+                          _addr(gamma), _addr(dgamma), _addr(lap), _stream(stream) if n else 0)
+    if check:
+        _check(st, "hg_rbf_fwd")
+    return st
+
+
+def hg_rbf_bwd(desc: GridDesc, n: int, coords, eps: float, rings: int, g_gamma, g_dgamma, g_lap, grad: TableView,
+               stream=None, check: bool = True) -> int:
+    c = desc.as_c()
+    st = lib().hg_rbf_bwd(ctypes.byref(c), int(n), _addr(coords), float(eps), int(rings), _addr(g_gamma),
+                          _addr(g_dgamma), _addr(g_lap), _tables_c([grad], hg_grad_table), _stream(stream) if n else 0)
+    if check:
+        _check(st, "hg_rbf_bwd")
     return st
 
 

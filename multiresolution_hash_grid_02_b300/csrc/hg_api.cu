@@ -646,6 +646,84 @@ hg_status hg_linear_fd_bwd(const hg_grid_desc* desc, int64_t n, const float* coo
     return launch_status(hg::launch_linear_fd_bwd(p, fc, vec, stream), "finite-difference backward");
 }
 
+// Gaussian-RBF grid: shared argument checks (the d-linear table's, plus d, eps and rings).
+hg_status rbf_check(const hg_grid_desc* desc, int64_t n, float eps, int32_t rings) {
+    hg_status st = check_desc(desc, 1);
+    if (st != HG_OK) return st;
+    if ((st = check_n(n)) != HG_OK) return st;
+    if (desc->d > 3) return fail(HG_ERR_UNSUPPORTED, "the Gaussian-RBF grid is built for d = 2 and 3, not %d", desc->d);
+    if (!(eps > 0.0f) || !(eps < INFINITY)) return fail(HG_ERR_INVALID_ARG, "eps = %g; must be positive and finite", eps);
+    if (rings < 1 || rings > 4) return fail(HG_ERR_INVALID_ARG, "rings = %d; must be in 1..4", rings);
+    return HG_OK;
+}
+
+hg_status hg_rbf_fwd(const hg_grid_desc* desc, int64_t n, const float* coords, float eps, int32_t rings,
+                     const hg_table* table, float* gamma, float* dgamma, float* lap, hg_stream stream) {
+    hg_status st = rbf_check(desc, n, eps, rings);
+    if (st != HG_OK) return st;
+    if (!table) return fail(HG_ERR_INVALID_ARG, "table is NULL");
+    const int F = desc->F;
+    const size_t es = dtype_size(desc->dtype);
+    st = check_view("table", 0, table->ptr, table->level_stride, table->row_stride, F, int64_t(1) << desc->log2_T[0],
+                    desc->L, es);
+    if (st != HG_OK) return st;
+    hg::FwdParams p;
+    if ((st = make_common(desc, 1, n, p.c)) != HG_OK) return st;
+    if (n == 0) return ok();
+    if (!coords || !gamma) return fail(HG_ERR_INVALID_ARG, "coords and gamma must not be NULL");
+    if (!aligned(coords, 4) || !aligned(gamma, 4) || (dgamma && !aligned(dgamma, 4)) || (lap && !aligned(lap, 4)))
+        return fail(HG_ERR_INVALID_ARG, "coords and outputs must be 4-byte aligned");
+    memset(&p.tab, 0, sizeof(p.tab));
+    p.tab.ptr[0] = table->ptr;
+    p.tab.ls[0] = table->level_stride;
+    p.tab.rs[0] = table->row_stride;
+    p.coords = coords;
+    p.gamma = gamma;
+    p.dgamma = dgamma;
+    p.lap = lap;
+    p.hess = nullptr;
+    p.stencil = nullptr;
+    p.eps = eps;
+    all_levels(p.c);
+    return launch_status(hg::launch_rbf_fwd(p, (F % 2 == 0) ? 2 : 1, rings, desc->dtype, stream), "RBF forward");
+}
+
+hg_status hg_rbf_bwd(const hg_grid_desc* desc, int64_t n, const float* coords, float eps, int32_t rings,
+                     const float* g_gamma, const float* g_dgamma, const float* g_lap, const hg_grad_table* grad,
+                     hg_stream stream) {
+    hg_status st = rbf_check(desc, n, eps, rings);
+    if (st != HG_OK) return st;
+    if (!grad) return fail(HG_ERR_INVALID_ARG, "grad is NULL");
+    const int F = desc->F;
+    st = check_view("grad", 0, grad->ptr, grad->level_stride, grad->row_stride, F, int64_t(1) << desc->log2_T[0],
+                    desc->L, 4);
+    if (st != HG_OK) return st;
+    hg::BwdParams p;
+    if ((st = make_common(desc, 1, n, p.c)) != HG_OK) return st;
+    if (n == 0 || (!g_gamma && !g_dgamma && !g_lap)) return ok();
+    if (!coords) return fail(HG_ERR_INVALID_ARG, "coords must not be NULL");
+    if (!aligned(coords, 4) || (g_gamma && !aligned(g_gamma, 4)) || (g_dgamma && !aligned(g_dgamma, 4)) ||
+        (g_lap && !aligned(g_lap, 4)))
+        return fail(HG_ERR_INVALID_ARG, "coords and upstream gradients must be 4-byte aligned");
+    memset(&p.grad, 0, sizeof(p.grad));
+    p.grad.ptr[0] = grad->ptr;
+    p.grad.ls[0] = grad->level_stride;
+    p.grad.rs[0] = grad->row_stride;
+    p.coords = coords;
+    p.g_gamma = g_gamma;
+    p.g_dgamma = g_dgamma;
+    p.g_lap = g_lap;
+    p.g_hess = nullptr;
+    p.g_stencil = nullptr;
+    p.eps = eps;
+    const int fc = (F % 2 == 0) ? 2 : 1;
+    const bool vec = fc == 2 && aligned(grad->ptr, 8) && grad->row_stride % 2 == 0 && grad->level_stride % 2 == 0;
+    all_levels(p.c);  // every level takes the tiled kernel (a CTA's tile covers its points' taps)
+    const bool any = p.c.level_mask != 0;
+    if (!any) return ok();
+    return launch_status(hg::launch_rbf_bwd(p, fc, vec, rings, stream), "RBF backward");
+}
+
 hg_status hg_hash_indices(const hg_grid_desc* desc, int64_t n, const float* coords, uint32_t* idx, hg_stream stream) {
     hg_status st = check_desc(desc, desc ? desc->d + 1 : 0);
     if (st != HG_OK) return st;

@@ -108,6 +108,9 @@ int launch_hermite_bwd(const BwdParams& p, int fc, bool vec, bool hess, void* st
 int launch_linear_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream);
 int launch_linear_bwd(const BwdParams& p, int fc, bool vec, void* stream);
 int launch_linear_fd_fwd(const FwdParams& p, int fc, bool vec, int dtype, void* stream);
+// Gaussian-RBF grid: eps (FwdParams/BwdParams.eps) is the kernel width in grid units, rings 1..4.
+int launch_rbf_fwd(const FwdParams& p, int fc, int rings, int dtype, void* stream);
+int launch_rbf_bwd(const BwdParams& p, int fc, bool vec, int rings, void* stream);
 int launch_linear_fd_bwd(const BwdParams& p, int fc, bool vec, void* stream);
 int launch_indices(const IdxParams& p, void* stream);
 // red: RED replay (adds 1.0 to every float of each chunk), else gather replay.

@@ -31,7 +31,7 @@ import numpy as np
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "hermite", "linear" or "linear_fd" (d-linear with central differences)
+    kind: str                 # "hermite", "linear", "linear_fd" (d-linear with central differences) or "rbf"
     d: int
     n_points: int
     L: int
@@ -44,7 +44,8 @@ class Workload:
     coords: str = "uniform"   # "uniform" or "stratified"
     level_masks: tuple = field(default=())  # extra active-level masks to exercise
     seed: int = 0
-    eps: float = 0.0          # finite-difference step (linear_fd)
+    eps: float = 0.0          # finite-difference step (linear_fd); Gaussian width in grid units (rbf)
+    rings: int = 0            # rbf: ring neighbourhood
 
     @property
     def V(self) -> int:
@@ -68,6 +69,12 @@ WORKLOADS = {
     # the pages' finite-difference baseline (INGP-FD) on workload 4's grid: 2d+1 = 7 d-linear encodes per point;
     # eps = 2^-10, half the finest cell (the pages leave the step to hand tuning)
     7: Workload("3d_linear_fd", "linear_fd", 3, 1 << 21, 16, 2, 16, 512, (19,), "f32", 1e-4, seed=7, eps=2.0 ** -10),
+    # DInf-Grid's Gaussian-RBF grids with the page's settings: eps = 1 with 3 rings, 4 dense levels, the
+    # finest 512 in 2D and 56 in 3D; stratified collocation points (its structured sampling)
+    8: Workload("2d_dinf_rbf", "rbf", 2, 1 << 20, 4, 2, 64, 512, (19,), "f32", 1e-2, coords="stratified", seed=8,
+                eps=1.0, rings=3),
+    9: Workload("3d_dinf_rbf", "rbf", 3, 1 << 21, 4, 2, 7, 56, (18,), "f32", 1e-2, coords="stratified", seed=9,
+                eps=1.0, rings=3),
 }
 
 
@@ -91,7 +98,7 @@ def draw_packed_table(rng: np.random.Generator, w: Workload) -> np.ndarray:
 
     Hermite: [L][T][2^d][F], the 2^d slots of a vertex ordered by derivative
     order, then lexicographically (f, fx, fy, [fz], fxy, [fxz, fyz, fxyz]).
-    Linear (and linear_fd): [L][T][F].  float32 or float16 (the float32 draw rounded).
+    Linear, linear_fd and rbf: [L][T][F].  float32 or float16 (the float32 draw rounded).
     """
     T = 1 << w.log2_T[0]
     if w.kind == "hermite":
@@ -141,6 +148,7 @@ def draw_upstream(rng: np.random.Generator, w: Workload, with_derivs: bool = Tru
     gg = rng.standard_normal((n, L, F), dtype=np.float32)
     if not with_derivs or w.kind == "linear":
         return gg, None, None
+    # hermite and rbf: gradient and Laplacian upstream
     if w.kind == "linear_fd":
         return gg, None, rng.standard_normal((n, 2 * d, L, F), dtype=np.float32)
     gd = rng.standard_normal((n, d, L, F), dtype=np.float32)

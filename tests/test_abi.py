@@ -207,6 +207,19 @@ def test_finite_difference_step_is_checked(m):
     assert hg.hg_linear_fd_bwd(desc, 0, 0, 1e-3, 0, 0, 0, 0, lv, stream=0, check=False) == hg.HG_OK
 
 
+def test_rbf_arguments_are_checked(m):
+    hg = m.hg
+    desc = m.GridDesc(d=3, L=4, F=2, n_min=4, n_max=32, log2_T=(8,))
+    lv = hg.linear_view(_FakeTable((4, 256, 2), addr=1 << 20))
+    E = hg.HG_ERR_INVALID_ARG
+    for eps, rings in ((0.0, 3), (-1.0, 3), (float("nan"), 3), (1.0, 0), (1.0, 5)):
+        assert hg.hg_rbf_fwd(desc, 5, 16, eps, rings, lv, 32, stream=0, check=False) == E, (eps, rings)
+        assert hg.hg_rbf_bwd(desc, 5, 16, eps, rings, 32, None, None, lv, stream=0, check=False) == E, (eps, rings)
+    d4 = m.GridDesc(d=4, L=4, F=2, n_min=4, n_max=32, log2_T=(8,))
+    assert hg.hg_rbf_fwd(d4, 5, 16, 1.0, 3, lv, 32, stream=0, check=False) == hg.HG_ERR_UNSUPPORTED
+    assert hg.hg_rbf_fwd(desc, 0, 0, 1.0, 3, lv, 0, stream=0, check=False) == hg.HG_OK
+
+
 def test_zero_points_touch_nothing(m):
     """n = 0 with a valid descriptor succeeds without a launch (no GPU here)."""
     hg = m.hg

@@ -87,6 +87,12 @@ def test_algorithmic_bytes_and_patterns():
     assert bench.algorithmic_bytes(w7, (1 << 16) - 1) == ((1 << 21) * 16 * 8 * 8,) * 2
     assert bench.kernel_patterns(w7) == ((8, 1), (8, 1))
     assert "INGP-FD" in bench.metric_of(w7) and bench.metric_of(w) != bench.metric_of(w7)
+    # RBF: the ring box of taps; the separable contraction's flops (3D, 6 taps/axis: 6 (6 * 23 + 6) FMAs)
+    w9 = W.WORKLOADS[9]
+    assert bench.algorithmic_bytes(w9, 0b1111) == ((1 << 21) * 4 * 216 * 2 * 4,) * 2
+    assert bench.rbf_flops(w9, 0b1111) == 2 * 864 * 2 * (1 << 21) * 4
+    assert bench.rbf_flops(W.WORKLOADS[8], 0b1111) == 2 * 6 * 23 * 2 * (1 << 20) * 4
+    assert "RBF" in bench.metric_of(w9)
 
 
 def bench_workload(cfg):

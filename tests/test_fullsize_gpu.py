@@ -234,3 +234,40 @@ def test_fullsize_3d_linear_fd():
     got = host(grad)
     for l in levels:
         check_close(f"grad level {l}", got[l], want[l], mag[l])
+
+
+@pytest.mark.parametrize("cfg,levels", [(8, (0, 3)), (9, (0, 3))])
+def test_fullsize_dinf_rbf(cfg, levels):
+    """The DInf-Grid Gaussian-RBF workloads (2D: 2^20 stratified points, 4
+    dense levels up to 512; 3D: 2^21 points, up to 56; eps = 1, 3 rings) as
+    the benchmark launches them: sampled points forward, whole levels
+    backward (the coarsest privatised, the finest direct)."""
+    m, hg, W, oracle = _mods()
+    w = W.WORKLOADS[cfg]
+    inp = W.make(w)
+    n, d, L, F = w.n_points, w.d, w.L, w.F
+    res = oracle.level_resolutions(L, w.n_min, w.n_max)
+    desc = m.GridDesc(d=d, L=L, F=F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T * (d + 1),
+                      layout=m.HG_FEATURE_MAJOR)
+    coords = torch.from_numpy(inp["coords"]).cuda()
+    table = torch.from_numpy(inp["table"]).cuda()
+    gamma = torch.empty((L, F, n), device="cuda")
+    dgamma = torch.empty((d, L, F, n), device="cuda")
+    lap = torch.empty((L, F, n), device="cuda")
+    hg.hg_rbf_fwd(desc, n, coords, w.eps, w.rings, m.linear_view(table), gamma, dgamma, lap)
+    grad = torch.zeros_like(table)
+    up = [torch.from_numpy(W.to_feature_major(inp[k], k == "g_dgamma")).cuda() for k in ("g_gamma", "g_dgamma", "g_lap")]
+    hg.hg_rbf_bwd(desc, n, coords, w.eps, w.rings, up[0], up[1], up[2], m.linear_view(grad))
+    torch.cuda.synchronize()
+    del up
+    rows = _sample_rows(np.random.default_rng(90 + cfg), n, 5000)
+    ref = oracle.rbf_fwd(d, F, res, w.log2_T[0], inp["table"], inp["coords"][rows], w.eps, w.rings)
+    ri = torch.from_numpy(rows).cuda()
+    check_close("gamma", W.from_feature_major(host(gamma[:, :, ri]), False), ref["gamma"], ref["mgamma"])
+    check_close("dgamma", W.from_feature_major(host(dgamma[:, :, :, ri]), True), ref["dgamma"], ref["mdgamma"])
+    check_close("lap", W.from_feature_major(host(lap[:, :, ri]), False), ref["lap"], ref["mlap"])
+    want, mag = oracle.rbf_bwd(d, F, res, w.log2_T[0], inp["coords"], w.eps, w.rings, g_gamma=inp["g_gamma"],
+                               g_dgamma=inp["g_dgamma"], g_lap=inp["g_lap"], levels=levels)
+    got = host(grad)
+    for l in levels:
+        check_close(f"grad level {l}", got[l], want[l], mag[l])
