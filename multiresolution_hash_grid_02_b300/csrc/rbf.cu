@@ -29,13 +29,20 @@ namespace {
 
 constexpr int kBlock = 256;
 
-// The 2R taps of one axis: vertex g = first + k, its normalised 1D weight
-// and that weight's first and second x-derivatives; `valid` bit k = inside.
+// The 2R taps of one axis: vertex g = first + k (bit k of `valid` set when
+// it lies inside the grid) and its normalised 1D weight w[k].  The weight's
+// derivatives need no more per-tap state: with e_k = exp(-eps^2 r_k^2),
+// r_k = y - g_k, the quotient rule gives dw_k/dy = -2 eps^2 w_k delta_k and
+// d2w_k/dy2 = 4 eps^4 w_k (delta_k^2 - var), where delta_k = r_k - mu and
+// mu, var are the weighted mean and variance of the offsets r_k.  So an
+// axis holds 2R weights plus tau = delta_0 (delta_k = tau - k) and var,
+// which keeps three axes of a point in registers.
 template <int K>
 struct RbfAxis {
     int32_t first;
     uint32_t valid;
-    float w[K], d1[K], d2[K];
+    float tau, var;
+    float w[K];
 };
 
 template <int K>
@@ -43,32 +50,49 @@ __device__ __forceinline__ RbfAxis<K> rbf_axis(uint32_t c, float t, const Level&
     RbfAxis<K> a;
     a.first = static_cast<int32_t>(c) - K / 2 + 1;
     a.valid = 0u;
-    float e[K], e1[K], e2[K], s = 0.f, s1 = 0.f, s2 = 0.f;
+    float e[K], s = 0.f;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const int32_t g = a.first + k;
         const bool in = g >= 0 && g <= static_cast<int32_t>(lv.N);
         a.valid |= static_cast<uint32_t>(in) << k;
         const float r = t - static_cast<float>(k - K / 2 + 1);        // y - g, in grid units
-        const float ek = in ? expf(-eps2 * r * r) : 0.f;
-        e[k] = ek;
-        e1[k] = -2.f * eps2 * r * ek;
-        e2[k] = fmaf(4.f * eps2 * eps2, r * r, -2.f * eps2) * ek;
+        e[k] = in ? expf(-eps2 * r * r) : 0.f;
         s += e[k];
-        s1 += e1[k];
-        s2 += e2[k];
     }
     const float inv = 1.f / s;
+    float mu = 0.f;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-        const float w = e[k] * inv;
-        const float w1 = (e1[k] - w * s1) * inv;
-        const float w2 = (e2[k] - 2.f * w1 * s1 - w * s2) * inv;
-        a.w[k] = w;
-        a.d1[k] = w1 * lv.fN;
-        a.d2[k] = w2 * lv.fN2;
+        a.w[k] = e[k] * inv;
+        mu = fmaf(a.w[k], t - static_cast<float>(k - K / 2 + 1), mu);
     }
+    a.tau = (t - mu) + static_cast<float>(K / 2 - 1);
+    float var = 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const float dl = a.tau - static_cast<float>(k);
+        var = fmaf(a.w[k] * dl, dl, var);
+    }
+    a.var = var;
     return a;
+}
+
+// w[k] for a k only known at run time, by selects: indexing the array
+// itself would move the point's axes to local memory.
+template <int K>
+__device__ __forceinline__ float rbf_weight(const RbfAxis<K>& a, int k) {
+    float w = a.w[0];
+#pragma unroll
+    for (int j = 1; j < K; ++j) w = k == j ? a.w[j] : w;
+    return w;
+}
+
+// delta_k and q_k = delta_k^2 - var of tap k of an axis.
+template <int K>
+__device__ __forceinline__ void rbf_moments(const RbfAxis<K>& a, int k, float& dl, float& q) {
+    dl = a.tau - static_cast<float>(k);
+    q = fmaf(dl, dl, -a.var);
 }
 
 template <int D, int K>
@@ -99,30 +123,35 @@ __device__ __forceinline__ int64_t rbf_row(const Level& lv, uint32_t tmask, int3
     return vertex_index<D>(g, lv, lv.dense & 1u, tmask);
 }
 
-// Axis-0 contraction of one row of taps (fixed g1, g2): s, s1, s2 per feature.
+// Axis-0 contraction of one row of taps (fixed g1, g2) per feature:
+// s = sum w theta, sd = sum w delta theta, sq = sum w q theta.
 template <int D, int K, int FC, typename TT>
 __device__ __forceinline__ void rbf_line(const TT* base, int64_t rs, int f0, const Level& lv, uint32_t tmask,
                                          const RbfAxis<K>& a0, int32_t g1, int32_t g2, float (&s)[FC],
-                                         float (&s1)[FC], float (&s2)[FC]) {
+                                         float (&sd)[FC], float (&sq)[FC]) {
 #pragma unroll
-    for (int f = 0; f < FC; ++f) s[f] = s1[f] = s2[f] = 0.f;
+    for (int f = 0; f < FC; ++f) s[f] = sd[f] = sq[f] = 0.f;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         if ((a0.valid >> k) & 1u) {
-            float v[FC];
+            float v[FC], dl, q;
             load_fc<FC, TT>(base + rbf_row<D>(lv, tmask, a0.first + k, g1, g2) * rs + f0, v);
+            rbf_moments(a0, k, dl, q);
+            const float wd = a0.w[k] * dl, wq = a0.w[k] * q;
 #pragma unroll
             for (int f = 0; f < FC; ++f) {
                 s[f] = fmaf(a0.w[k], v[f], s[f]);
-                s1[f] = fmaf(a0.d1[k], v[f], s1[f]);
-                s2[f] = fmaf(a0.d2[k], v[f], s2[f]);
+                sd[f] = fmaf(wd, v[f], sd[f]);
+                sq[f] = fmaf(wq, v[f], sq[f]);
             }
         }
     }
 }
 
+// Six blocks per SM (at most 40 registers): latency-bound, so occupancy pays -- 3D workload 3.82 ms at
+// two blocks (95 registers), 2.81 ms at four, 2.62 ms at six.
 template <int D, int R, int FC, typename TT>
-__global__ void __launch_bounds__(kBlock) rbf_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kBlock, 6) rbf_fwd_kernel(const __grid_constant__ FwdParams p) {
     constexpr int K = 2 * R;
     const int l = p.c.lvl[blockIdx.y];
     const int64_t n = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
@@ -132,6 +161,7 @@ __global__ void __launch_bounds__(kBlock) rbf_fwd_kernel(const __grid_constant__
     const bool active = (p.c.level_mask >> l) & 1u;
     RbfAxis<K> A[D];
     rbf_axes<D, K>(p.coords, n, lv, p.eps * p.eps, A);
+    const float v = 2.f * p.eps * p.eps * lv.fN, v2 = v * v;  // d/dx = N d/dy on the weights' derivatives
     const TT* base = static_cast<const TT*>(p.tab.ptr[0]) + l * p.tab.ls[0];
     const int64_t rs = p.tab.rs[0];
     const uint32_t tm = p.c.tmask[0];
@@ -139,19 +169,23 @@ __global__ void __launch_bounds__(kBlock) rbf_fwd_kernel(const __grid_constant__
         float g[FC], dg[3][FC], lp[FC];
 #pragma unroll
         for (int f = 0; f < FC; ++f) g[f] = dg[0][f] = dg[1][f] = dg[2][f] = lp[f] = 0.f;
+        // sums in offset units: dg_i = sum W delta_i theta, lp = sum W (q_0 + q_1 [+ q_2]) theta with the
+        // tap weight W = w_0 w_1 [w_2]; the gradient and Laplacian are -v dg and v^2 lp
         if (active) {
             if constexpr (D == 2) {
 #pragma unroll
                 for (int k1 = 0; k1 < K; ++k1) {
                     if (!((A[1].valid >> k1) & 1u)) continue;
-                    float s[FC], s1[FC], s2[FC];
-                    rbf_line<2, K, FC, TT>(base, rs, f0, lv, tm, A[0], A[1].first + k1, 0, s, s1, s2);
+                    float s[FC], sd[FC], sq[FC], dl1, q1;
+                    rbf_line<2, K, FC, TT>(base, rs, f0, lv, tm, A[0], A[1].first + k1, 0, s, sd, sq);
+                    rbf_moments(A[1], k1, dl1, q1);
+                    const float w1 = A[1].w[k1], wd1 = w1 * dl1;
 #pragma unroll
                     for (int f = 0; f < FC; ++f) {
-                        g[f] = fmaf(s[f], A[1].w[k1], g[f]);
-                        dg[0][f] = fmaf(s1[f], A[1].w[k1], dg[0][f]);
-                        dg[1][f] = fmaf(s[f], A[1].d1[k1], dg[1][f]);
-                        lp[f] = fmaf(s2[f], A[1].w[k1], fmaf(s[f], A[1].d2[k1], lp[f]));
+                        g[f] = fmaf(w1, s[f], g[f]);
+                        dg[0][f] = fmaf(w1, sd[f], dg[0][f]);
+                        dg[1][f] = fmaf(wd1, s[f], dg[1][f]);
+                        lp[f] = fmaf(w1, fmaf(q1, s[f], sq[f]), lp[f]);
                     }
                 }
             } else {
@@ -164,28 +198,38 @@ __global__ void __launch_bounds__(kBlock) rbf_fwd_kernel(const __grid_constant__
 #pragma unroll
                     for (int k1 = 0; k1 < K; ++k1) {
                         if (!((A[1].valid >> k1) & 1u)) continue;
-                        float s[FC], s1[FC], s2[FC];
-                        rbf_line<3, K, FC, TT>(base, rs, f0, lv, tm, A[0], A[1].first + k1, A[2].first + k2, s, s1,
-                                               s2);
+                        float s[FC], sd[FC], sq[FC], dl1, q1;
+                        rbf_line<3, K, FC, TT>(base, rs, f0, lv, tm, A[0], A[1].first + k1, A[2].first + k2, s, sd,
+                                               sq);
+                        rbf_moments(A[1], k1, dl1, q1);
+                        const float w1 = A[1].w[k1], wd1 = w1 * dl1;
 #pragma unroll
                         for (int f = 0; f < FC; ++f) {
-                            a[f] = fmaf(s[f], A[1].w[k1], a[f]);
-                            b[f] = fmaf(s1[f], A[1].w[k1], b[f]);
-                            cc[f] = fmaf(s[f], A[1].d1[k1], cc[f]);
-                            dl[f] = fmaf(s2[f], A[1].w[k1], fmaf(s[f], A[1].d2[k1], dl[f]));
+                            a[f] = fmaf(w1, s[f], a[f]);
+                            b[f] = fmaf(w1, sd[f], b[f]);
+                            cc[f] = fmaf(wd1, s[f], cc[f]);
+                            dl[f] = fmaf(w1, fmaf(q1, s[f], sq[f]), dl[f]);
                         }
                     }
-                    const float w2 = A[2].w[k2], d12 = A[2].d1[k2], d22 = A[2].d2[k2];
+                    float dl2, q2;
+                    rbf_moments(A[2], k2, dl2, q2);
+                    const float w2 = rbf_weight(A[2], k2), wd2 = w2 * dl2;
 #pragma unroll
                     for (int f = 0; f < FC; ++f) {
-                        g[f] = fmaf(a[f], w2, g[f]);
-                        dg[0][f] = fmaf(b[f], w2, dg[0][f]);
-                        dg[1][f] = fmaf(cc[f], w2, dg[1][f]);
-                        dg[2][f] = fmaf(a[f], d12, dg[2][f]);
-                        lp[f] = fmaf(dl[f], w2, fmaf(a[f], d22, lp[f]));
+                        g[f] = fmaf(w2, a[f], g[f]);
+                        dg[0][f] = fmaf(w2, b[f], dg[0][f]);
+                        dg[1][f] = fmaf(w2, cc[f], dg[1][f]);
+                        dg[2][f] = fmaf(wd2, a[f], dg[2][f]);
+                        lp[f] = fmaf(w2, fmaf(q2, a[f], dl[f]), lp[f]);
                     }
                 }
             }
+        }
+#pragma unroll
+        for (int f = 0; f < FC; ++f) {
+            lp[f] *= v2;
+#pragma unroll
+            for (int j = 0; j < 3; ++j) dg[j][f] *= -v;
         }
 #pragma unroll
         for (int f = 0; f < FC; ++f) {
@@ -203,70 +247,66 @@ __global__ void __launch_bounds__(kBlock) rbf_fwd_kernel(const __grid_constant__
 // Transposed contraction of one (point, level, feature chunk): the
 // coefficient gradient of every tap inside the grid, handed to
 // add(g0, g1, g2, values) with the tap's vertex coordinates (g2 = 0 in 2D).
+// With the moment form of the weights' derivatives the gradient of tap
+// (k0, k1[, k2]) is W (g_gamma - v sum_i g_dgamma_i delta_i + v^2 g_lap
+// sum_i q_i), W = w_0 w_1 [w_2], folded in axis by axis from the outside.
 template <int D, int R, int FC, typename Add>
 __device__ __forceinline__ void rbf_point_bwd(const BwdParams& p, int64_t n, int l, int f0, const RbfAxis<2 * R> (&A)[D],
                                               const Level& lv, Add&& add) {
     constexpr int K = 2 * R;
     const int F = p.c.F;
-    float gg[FC], gd[3][FC], gl[FC];
+    const float v = 2.f * p.eps * p.eps * lv.fN;
+    float a0[FC], bd[3][FC], cl[FC];  // g_gamma, -v g_dgamma_i, v^2 g_lap
 #pragma unroll
     for (int f = 0; f < FC; ++f) {
         const int64_t lf = static_cast<int64_t>(l) * F + f0 + f;
-        gg[f] = p.g_gamma ? __ldg(p.g_gamma + n * p.c.sn + lf * p.c.sf) : 0.f;
-        gl[f] = p.g_lap ? __ldg(p.g_lap + n * p.c.sn + lf * p.c.sf) : 0.f;
+        a0[f] = p.g_gamma ? __ldg(p.g_gamma + n * p.c.sn + lf * p.c.sf) : 0.f;
+        cl[f] = p.g_lap ? v * v * __ldg(p.g_lap + n * p.c.sn + lf * p.c.sf) : 0.f;
 #pragma unroll
         for (int j = 0; j < 3; ++j)
-            gd[j][f] = (p.g_dgamma && j < D) ? __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf) : 0.f;
+            bd[j][f] = (p.g_dgamma && j < D) ? -v * __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf) : 0.f;
     }
-    // per (g1[, g2]): the adjoints s, s1, s2 of the axis-0 line sums, then each tap's gradient
-    auto line = [&](int32_t g1, int32_t g2, const float (&s)[FC], const float (&s1)[FC], const float (&s2)[FC]) {
+    // one row of taps along axis 0: weight beta w_0 and factor alpha + bd_0 delta_0 + cl q_0
+    auto line = [&](int32_t g1, int32_t g2, float beta, const float (&alpha)[FC]) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             if ((A[0].valid >> k) & 1u) {
-                float v[FC];
+                float dl, q, val[FC];
+                rbf_moments(A[0], k, dl, q);
+                const float bw = beta * A[0].w[k];
 #pragma unroll
-                for (int f = 0; f < FC; ++f) v[f] = fmaf(s[f], A[0].w[k], fmaf(s1[f], A[0].d1[k], s2[f] * A[0].d2[k]));
-                add(A[0].first + k, g1, g2, v);
+                for (int f = 0; f < FC; ++f) val[f] = bw * fmaf(cl[f], q, fmaf(bd[0][f], dl, alpha[f]));
+                add(A[0].first + k, g1, g2, val);
             }
         }
     };
     if constexpr (D == 2) {
-#pragma unroll
+#pragma unroll 1
         for (int k1 = 0; k1 < K; ++k1) {
             if (!((A[1].valid >> k1) & 1u)) continue;
-            float s[FC], s1[FC], s2[FC];
+            float dl1, q1, al[FC];
+            rbf_moments(A[1], k1, dl1, q1);
 #pragma unroll
-            for (int f = 0; f < FC; ++f) {
-                s[f] = fmaf(gg[f], A[1].w[k1], fmaf(gd[1][f], A[1].d1[k1], gl[f] * A[1].d2[k1]));
-                s1[f] = gd[0][f] * A[1].w[k1];
-                s2[f] = gl[f] * A[1].w[k1];
-            }
-            line(A[1].first + k1, 0, s, s1, s2);
+            for (int f = 0; f < FC; ++f) al[f] = fmaf(cl[f], q1, fmaf(bd[1][f], dl1, a0[f]));
+            line(A[1].first + k1, 0, rbf_weight(A[1], k1), al);
         }
     } else {
 #pragma unroll 1
         for (int k2 = 0; k2 < K; ++k2) {
             if (!((A[2].valid >> k2) & 1u)) continue;
-            const float w2 = A[2].w[k2], d12 = A[2].d1[k2], d22 = A[2].d2[k2];
-            float a[FC], b[FC], cc[FC], dl[FC];
+            float dl2, q2, al2[FC];
+            rbf_moments(A[2], k2, dl2, q2);
+            const float w2 = rbf_weight(A[2], k2);
 #pragma unroll
-            for (int f = 0; f < FC; ++f) {
-                a[f] = fmaf(gg[f], w2, fmaf(gd[2][f], d12, gl[f] * d22));
-                b[f] = gd[0][f] * w2;
-                cc[f] = gd[1][f] * w2;
-                dl[f] = gl[f] * w2;
-            }
+            for (int f = 0; f < FC; ++f) al2[f] = fmaf(cl[f], q2, fmaf(bd[2][f], dl2, a0[f]));
 #pragma unroll
             for (int k1 = 0; k1 < K; ++k1) {
                 if (!((A[1].valid >> k1) & 1u)) continue;
-                float s[FC], s1[FC], s2[FC];
+                float dl1, q1, al[FC];
+                rbf_moments(A[1], k1, dl1, q1);
 #pragma unroll
-                for (int f = 0; f < FC; ++f) {
-                    s[f] = fmaf(a[f], A[1].w[k1], fmaf(cc[f], A[1].d1[k1], dl[f] * A[1].d2[k1]));
-                    s1[f] = b[f] * A[1].w[k1];
-                    s2[f] = dl[f] * A[1].w[k1];
-                }
-                line(A[1].first + k1, A[2].first + k2, s, s1, s2);
+                for (int f = 0; f < FC; ++f) al[f] = fmaf(cl[f], q1, fmaf(bd[1][f], dl1, al2[f]));
+                line(A[1].first + k1, A[2].first + k2, w2 * A[1].w[k1], al);
             }
         }
     }
@@ -274,18 +314,23 @@ __device__ __forceinline__ void rbf_point_bwd(const BwdParams& p, int64_t n, int
 
 constexpr int kTileBlock = 256;  // 8 warps: the lane interleave below relies on it
 static_assert(kTileBlock == 8 * 32, "eight warps of 32 lanes");
-constexpr int kTileFloats = 24 * 1024;  // 96 KB of dynamic shared memory: two CTAs per SM
+// Tile capacity (floats, 48 KB of shared memory) and CTAs per SM.
+constexpr int kTileFloats = 12 * 1024;
+constexpr int kTileCtas = 4;
 
 // Tiled backward for coherent points (the page's structured sampling): a CTA
 // takes kTileBlock consecutive points of one level, finds the bounding box
 // of their tap neighbourhoods (a block reduction of their cells), and when
-// the box's rows fit kTileFloats it accumulates every contribution in a
+// the box's rows fit the tile it accumulates every contribution in a
 // shared-memory tile of that box and then adds each touched row into the
 // table once -- consecutive stratified points share most of their taps, so
 // this replaces tens of REDs on the same rows by one.  A CTA whose box does
 // not fit (scattered points on a fine level) scatters directly.
+// The shared-memory adds are latency-bound, so occupancy pays: 3D workload 13.3 ms at two blocks per SM
+// (96 KB tiles, 110 registers), 7.4 ms at four (48 KB, 64 registers); five (40 KB) spill at 48
+// registers and take 7.7 ms, three 8.2 ms.
 template <int D, int R, int FC, bool VEC>
-__global__ void __launch_bounds__(kTileBlock) rbf_bwd_tile_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kTileBlock, kTileCtas) rbf_bwd_tile_kernel(const __grid_constant__ BwdParams p) {
     extern __shared__ float tile[];
     __shared__ int32_t box_lo[3], box_hi[3];
     const int l = p.c.lvl[blockIdx.y];
