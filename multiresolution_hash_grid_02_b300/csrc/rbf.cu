@@ -245,11 +245,14 @@ __global__ void __launch_bounds__(kBlock, 6) rbf_fwd_kernel(const __grid_constan
 }
 
 // Transposed contraction of one (point, level, feature chunk): the
-// coefficient gradient of every tap inside the grid, handed to
-// add(g0, g1, g2, values) with the tap's vertex coordinates (g2 = 0 in 2D).
-// With the moment form of the weights' derivatives the gradient of tap
-// (k0, k1[, k2]) is W (g_gamma - v sum_i g_dgamma_i delta_i + v^2 g_lap
-// sum_i q_i), W = w_0 w_1 [w_2], folded in axis by axis from the outside.
+// coefficient gradient of every tap of the ring box, handed to
+// add(g0, g1, g2, in, values) with the tap's vertex coordinates (g2 = 0 in
+// 2D) and whether it lies inside the grid (taps outside weigh 0 and must not
+// be written).  The loops are the same for every lane of a warp, so add()
+// may use warp shuffles.  With the moment form of the weights' derivatives
+// the gradient of tap (k0, k1[, k2]) is W (g_gamma - v sum_i g_dgamma_i
+// delta_i + v^2 g_lap sum_i q_i), W = w_0 w_1 [w_2], folded in axis by axis
+// from the outside.
 template <int D, int R, int FC, typename Add>
 __device__ __forceinline__ void rbf_point_bwd(const BwdParams& p, int64_t n, int l, int f0, const RbfAxis<2 * R> (&A)[D],
                                               const Level& lv, Add&& add) {
@@ -267,47 +270,82 @@ __device__ __forceinline__ void rbf_point_bwd(const BwdParams& p, int64_t n, int
             bd[j][f] = (p.g_dgamma && j < D) ? -v * __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf) : 0.f;
     }
     // one row of taps along axis 0: weight beta w_0 and factor alpha + bd_0 delta_0 + cl q_0
-    auto line = [&](int32_t g1, int32_t g2, float beta, const float (&alpha)[FC]) {
+    auto line = [&](int32_t g1, int32_t g2, bool row_in, float beta, const float (&alpha)[FC]) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-            if ((A[0].valid >> k) & 1u) {
-                float dl, q, val[FC];
-                rbf_moments(A[0], k, dl, q);
-                const float bw = beta * A[0].w[k];
+            float dl, q, val[FC];
+            rbf_moments(A[0], k, dl, q);
+            const float bw = beta * A[0].w[k];
 #pragma unroll
-                for (int f = 0; f < FC; ++f) val[f] = bw * fmaf(cl[f], q, fmaf(bd[0][f], dl, alpha[f]));
-                add(A[0].first + k, g1, g2, val);
-            }
+            for (int f = 0; f < FC; ++f) val[f] = bw * fmaf(cl[f], q, fmaf(bd[0][f], dl, alpha[f]));
+            add(A[0].first + k, g1, g2, row_in && ((A[0].valid >> k) & 1u), val);
         }
     };
     if constexpr (D == 2) {
 #pragma unroll 1
         for (int k1 = 0; k1 < K; ++k1) {
-            if (!((A[1].valid >> k1) & 1u)) continue;
             float dl1, q1, al[FC];
             rbf_moments(A[1], k1, dl1, q1);
 #pragma unroll
             for (int f = 0; f < FC; ++f) al[f] = fmaf(cl[f], q1, fmaf(bd[1][f], dl1, a0[f]));
-            line(A[1].first + k1, 0, rbf_weight(A[1], k1), al);
+            line(A[1].first + k1, 0, (A[1].valid >> k1) & 1u, rbf_weight(A[1], k1), al);
         }
     } else {
 #pragma unroll 1
         for (int k2 = 0; k2 < K; ++k2) {
-            if (!((A[2].valid >> k2) & 1u)) continue;
             float dl2, q2, al2[FC];
             rbf_moments(A[2], k2, dl2, q2);
             const float w2 = rbf_weight(A[2], k2);
+            const bool in2 = (A[2].valid >> k2) & 1u;
 #pragma unroll
             for (int f = 0; f < FC; ++f) al2[f] = fmaf(cl[f], q2, fmaf(bd[2][f], dl2, a0[f]));
 #pragma unroll
             for (int k1 = 0; k1 < K; ++k1) {
-                if (!((A[1].valid >> k1) & 1u)) continue;
                 float dl1, q1, al[FC];
                 rbf_moments(A[1], k1, dl1, q1);
 #pragma unroll
                 for (int f = 0; f < FC; ++f) al[f] = fmaf(cl[f], q1, fmaf(bd[1][f], dl1, al2[f]));
-                line(A[1].first + k1, A[2].first + k2, w2 * A[1].w[k1], al);
+                line(A[1].first + k1, A[2].first + k2, in2 && ((A[1].valid >> k1) & 1u), w2 * A[1].w[k1], al);
             }
+        }
+    }
+}
+
+// Runs of consecutive lanes whose points lie in the same cell (so have the
+// same taps): their contributions are summed in the warp and added by the
+// run's first lane.  `key` differs between lanes in different cells.
+struct LaneRuns {
+    uint32_t end;  // one past the last lane of this lane's run
+    int span;      // the warp's longest run
+    bool lead;     // first lane of its run
+};
+
+template <int D, int K>
+__device__ __forceinline__ LaneRuns lane_runs(const RbfAxis<K> (&A)[D], bool unique) {
+    const uint32_t lane = threadIdx.x & 31u;
+    int32_t key[3] = {A[0].first, A[1].first, D == 3 ? A[D - 1].first : 0};
+    if (unique) key[2] = INT32_MIN + static_cast<int32_t>(lane);  // no tap's coordinate: a run of its own
+    bool same = lane > 0;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) same = (__shfl_up_sync(0xffffffffu, key[i], 1) == key[i]) && same;
+    LaneRuns r;
+    r.lead = !same;
+    const uint32_t starts = __ballot_sync(0xffffffffu, r.lead);
+    const uint32_t above = lane == 31u ? 0u : starts & (0xffffffffu << (lane + 1u));
+    r.end = above ? static_cast<uint32_t>(__ffs(above) - 1) : 32u;
+    r.span = static_cast<int>(__reduce_max_sync(0xffffffffu, r.lead ? r.end - lane : 0u));
+    return r;
+}
+
+// Sum of v over the lane's run, complete in the run's first lane.
+template <int FC>
+__device__ __forceinline__ void run_sum(const LaneRuns& r, float (&v)[FC]) {
+    const uint32_t lane = threadIdx.x & 31u;
+    for (int o = 1; o < r.span; o <<= 1) {
+#pragma unroll
+        for (int f = 0; f < FC; ++f) {
+            const float t = __shfl_down_sync(0xffffffffu, v[f], o);
+            if (lane + o < r.end) v[f] += t;
         }
     }
 }
@@ -328,22 +366,24 @@ constexpr int kTileCtas = 4;
 // not fit (scattered points on a fine level) scatters directly.
 // The shared-memory adds are latency-bound, so occupancy pays: 3D workload 13.3 ms at two blocks per SM
 // (96 KB tiles, 110 registers), 7.4 ms at four (48 KB, 64 registers); five (40 KB) spill at 48
-// registers and take 7.7 ms, three 8.2 ms.
+// registers and take 7.7 ms, three 8.2 ms.  Summing the runs of same-cell lanes in the warp before the
+// adds: 7.4 -> 6.9 ms (2D 0.67 -> 0.50 ms; interleaving the points over the lanes instead, so that the
+// lanes of one add sit in different cells, gives 7.0 and 0.62 ms).
 template <int D, int R, int FC, bool VEC>
 __global__ void __launch_bounds__(kTileBlock, kTileCtas) rbf_bwd_tile_kernel(const __grid_constant__ BwdParams p) {
     extern __shared__ float tile[];
     __shared__ int32_t box_lo[3], box_hi[3];
     const int l = p.c.lvl[blockIdx.y];
     if (!((p.c.level_mask >> l) & 1u)) return;
-    // the CTA's points, interleaved over the lanes: lane j of warp w takes point w + 8 j, so the lanes of
-    // one instruction sit in different cells and their shared-memory adds rarely collide (measured: 2D
-    // workload 1.70 -> 0.82 ms, 3D 22.5 -> 13.3 ms against consecutive points per warp)
-    const int64_t n = static_cast<int64_t>(blockIdx.x) * kTileBlock + (threadIdx.x >> 5) + 8 * (threadIdx.x & 31);
+    // consecutive points per warp: lanes in one cell form runs whose contributions are summed in the warp
+    // first, so one lane per run adds them (a lane past the end works on the last point and adds nothing)
+    const int64_t n = static_cast<int64_t>(blockIdx.x) * kTileBlock + threadIdx.x;
     const bool have = n < p.c.n;
+    const int64_t nc = have ? n : p.c.n - 1;
     const Level& lv = p.c.lv[l];
     const int F = p.c.F;
     RbfAxis<2 * R> A[D];
-    if (have) rbf_axes<D, 2 * R>(p.coords, n, lv, p.eps * p.eps, A);
+    rbf_axes<D, 2 * R>(p.coords, nc, lv, p.eps * p.eps, A);
     // bounding box of the CTA's taps, clipped to the grid
     if (threadIdx.x < 3) {
         box_lo[threadIdx.x] = INT32_MAX;
@@ -358,6 +398,8 @@ __global__ void __launch_bounds__(kTileBlock, kTileCtas) rbf_bwd_tile_kernel(con
         }
     }
     __syncthreads();
+    if (!have) A[0].valid = 0u;
+    const LaneRuns run = lane_runs<D>(A, !have);
     int32_t lo[3] = {0, 0, 0}, ext[3] = {1, 1, 1};
     int64_t vol = 1;
 #pragma unroll
@@ -369,9 +411,11 @@ __global__ void __launch_bounds__(kTileBlock, kTileCtas) rbf_bwd_tile_kernel(con
     float* base = p.grad.ptr[0] + l * p.grad.ls[0];
     const uint32_t tm = p.c.tmask[0];
     if (vol * F > kTileFloats) {  // the same branch for the whole CTA: scatter directly
-        if (!have) return;
         for (int f0 = 0; f0 < F; f0 += FC) {
-            rbf_point_bwd<D, R, FC>(p, n, l, f0, A, lv, [&](int32_t g0, int32_t g1, int32_t g2, const float (&v)[FC]) {
+            rbf_point_bwd<D, R, FC>(p, nc, l, f0, A, lv,
+                                    [&](int32_t g0, int32_t g1, int32_t g2, bool in, float (&v)[FC]) {
+                run_sum<FC>(run, v);
+                if (!(run.lead && in)) return;
                 float* e = base + rbf_row<D>(lv, tm, g0, g1, g2) * p.grad.rs[0] + f0;
                 if constexpr (VEC) {
                     red_add_v2(e, v[0], v[FC - 1]);
@@ -386,15 +430,15 @@ __global__ void __launch_bounds__(kTileBlock, kTileCtas) rbf_bwd_tile_kernel(con
     const int32_t vals = static_cast<int32_t>(vol) * F;
     for (int32_t i = threadIdx.x; i < vals; i += kTileBlock) tile[i] = 0.f;
     __syncthreads();
-    if (have) {
-        for (int f0 = 0; f0 < F; f0 += FC) {
-            rbf_point_bwd<D, R, FC>(p, n, l, f0, A, lv, [&](int32_t g0, int32_t g1, int32_t g2, const float (&v)[FC]) {
-                const int32_t r = (g0 - lo[0]) + ext[0] * ((g1 - lo[1]) + ext[1] * (D == 3 ? g2 - lo[2] : 0));
-                float* a = tile + r * F + f0;
+    for (int f0 = 0; f0 < F; f0 += FC) {
+        rbf_point_bwd<D, R, FC>(p, nc, l, f0, A, lv, [&](int32_t g0, int32_t g1, int32_t g2, bool in, float (&v)[FC]) {
+            run_sum<FC>(run, v);
+            if (!(run.lead && in)) return;
+            const int32_t r = (g0 - lo[0]) + ext[0] * ((g1 - lo[1]) + ext[1] * (D == 3 ? g2 - lo[2] : 0));
+            float* a = tile + r * F + f0;
 #pragma unroll
-                for (int f = 0; f < FC; ++f) atomicAdd(a + f, v[f]);
-            });
-        }
+            for (int f = 0; f < FC; ++f) atomicAdd(a + f, v[f]);
+        });
     }
     __syncthreads();
     for (int32_t r = threadIdx.x; r < static_cast<int32_t>(vol); r += kTileBlock) {
