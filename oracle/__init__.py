@@ -572,3 +572,16 @@ def encode_bwd_hessian(d: int, F: int, res, log2T, coords: np.ndarray, g_gamma=N
         for rc in ex.map(one, todo):
             _check(rc, "encode_bwd_hessian")
     return grads, mags
+
+
+# The SIREN consumer (numpy fp64).  HG_SIREN_ORACLE names a copy of siren.py with a
+# planted mistake (tests/test_oracle_siren_mutants.py), as HG_ORACLE_LIB does for the C part.
+if os.environ.get("HG_SIREN_ORACLE"):
+    import importlib.util as _ilu
+
+    _spec = _ilu.spec_from_file_location("oracle_siren_variant", os.environ["HG_SIREN_ORACLE"])
+    _siren = _ilu.module_from_spec(_spec)
+    _spec.loader.exec_module(_siren)
+    siren_fwd, siren_bwd = _siren.siren_fwd, _siren.siren_bwd
+else:
+    from .siren import siren_bwd, siren_fwd  # noqa: E402,F401
