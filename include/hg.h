@@ -287,6 +287,49 @@ hg_status hg_rbf_bwd(const hg_grid_desc* desc, int64_t n, const float* coords, f
                      const float* g_gamma, const float* g_dgamma, const float* g_lap, const hg_grad_table* grad,
                      hg_stream stream);
 
+/* SIREN chain-rule consumer of the encoding ["Hermite-NGP: Gradient-Augmented
+ * Hash Encoding for Learning PDEs", 整体框架 (grad u = du/dgamma grad gamma,
+ * lap u = d2u/dgamma2 (grad gamma)^2 + du/dgamma lap gamma) and 关键设计 2
+ * (SIREN, sigma = sin(omega .), one-layer Laplacian)]:
+ *   z = W1 gamma + b1,  a = sin(omega z),  y_i = W1 dgamma/dx_i,  s = W1 lap gamma,
+ *   u = W2 a + b2,  du/dx_i = W2 (omega cos(omega z) * y_i),
+ *   lap u = W2 (omega cos(omega z) * s - omega^2 a * sum_i y_i^2).
+ * The inputs are the encoding's outputs in its feature-major layout with the
+ * levels' features concatenated (K = L F): gamma [K][n], dgamma [d][K][n],
+ * lap [K][n]. */
+typedef struct {
+    int32_t d;      /* spatial dimensions of the derivatives, 1..4 */
+    int32_t K;      /* inputs per point (L F), a multiple of 8 up to 64 */
+    int32_t H;      /* hidden width: 16, 32, 64 or 128 */
+    int32_t O;      /* outputs, 1..4 */
+    float omega;    /* frequency of the sine layer (omega_0 = 30 on the page), finite */
+} hg_siren_desc;
+
+/* Forward.  Device pointers, fp32, all 4-byte aligned: gamma [K][n];
+ * dgamma [d][K][n] (needed for du or lapu, else may be NULL); lap [K][n]
+ * (needed for lapu); W1 [H][K], b1 [H], W2 [O][H] row-major, b2 [O] (NULL =
+ * zero).  Outputs (written; each may be NULL): u [O][n], du [d][O][n],
+ * lapu [O][n].  Arithmetic fp32.  Errors: HG_ERR_INVALID_ARG for NULL
+ * required pointers, a bad desc or n outside 0..2^31-1; HG_ERR_UNSUPPORTED
+ * when a CTA's tile does not fit in shared memory; HG_ERR_CUDA on a launch
+ * failure. */
+hg_status hg_siren_fwd(const hg_siren_desc* desc, int64_t n, const float* gamma, const float* dgamma,
+                       const float* lap, const float* W1, const float* b1, const float* W2, const float* b2,
+                       float* u, float* du, float* lapu, hg_stream stream);
+
+/* Backward: the vector-Jacobian product of hg_siren_fwd with upstream
+ * gradients g_u [O][n], g_du [d][O][n], g_lapu [O][n] (NULL = zero).
+ * Inputs gamma, dgamma, lap, W1, b1, W2 as for the forward (all required).
+ * Input gradients (written; NULL = not wanted): g_gamma [K][n], g_dgamma
+ * [d][K][n], g_lap [K][n] -- the upstream gradients of the encoding's
+ * backward.  Weight gradients (ACCUMULATED with +=, caller-zeroed; NULL =
+ * not wanted): gW1 [H][K], gb1 [H], gW2 [O][H], gb2 [O].  Errors: as
+ * hg_siren_fwd. */
+hg_status hg_siren_bwd(const hg_siren_desc* desc, int64_t n, const float* gamma, const float* dgamma,
+                       const float* lap, const float* W1, const float* b1, const float* W2, const float* g_u,
+                       const float* g_du, const float* g_lapu, float* g_gamma, float* g_dgamma, float* g_lap,
+                       float* gW1, float* gb1, float* gW2, float* gb2, hg_stream stream);
+
 /* Vertex indices, for checking the lookup bit for bit: idx is device uint32
  * [n][L][d+1][2^d], the index of corner v in order table k at level l, for
  * every level (level_mask does not apply).  Errors: as hg_encode_fwd. */
@@ -300,8 +343,8 @@ const char* hg_status_string(hg_status status);
 const char* hg_last_error(void);
 
 /* ABI version of this header (bumped on any incompatible change; 2: log2_T
- * has five entries, d may be 4). */
-#define HG_ABI_VERSION 2
+ * has five entries, d may be 4; 3: the SIREN consumer). */
+#define HG_ABI_VERSION 3
 int32_t hg_abi_version(void);
 
 #ifdef __cplusplus

@@ -8,5 +8,5 @@ package does not load the CUDA library; the first call does, and raises if it
 is missing.
 """
 from . import _binding as hg  # noqa: F401
-from ._binding import (GridDesc, TableView, HGError, packed_views, order_views, linear_view,  # noqa: F401
+from ._binding import (GridDesc, SirenDesc, TableView, HGError, packed_views, order_views, linear_view,  # noqa: F401
                        HG_F32, HG_F16, HG_POINT_MAJOR, HG_FEATURE_MAJOR)

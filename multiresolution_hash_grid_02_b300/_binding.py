@@ -19,7 +19,7 @@ HG_OK, HG_ERR_INVALID_ARG, HG_ERR_UNSUPPORTED, HG_ERR_CUDA = 0, 1, 2, 3
 HG_F32, HG_F16 = 0, 1
 HG_POINT_MAJOR, HG_FEATURE_MAJOR = 0, 1
 HG_MAX_LEVELS = 32
-HG_ABI_VERSION = 2        # the include/hg.h layout this binding marshals
+HG_ABI_VERSION = 3        # the include/hg.h layout this binding marshals
 
 c_i32, c_i64, c_u32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
 
@@ -28,6 +28,10 @@ class hg_grid_desc(ctypes.Structure):
     _fields_ = [("d", c_i32), ("L", c_i32), ("F", c_i32), ("n_min", c_i32), ("n_max", c_i32),
                 ("res", ctypes.POINTER(c_i32)), ("log2_T", c_i32 * 5), ("level_mask", c_u32),
                 ("dtype", c_i32), ("layout", c_i32)]
+
+
+class hg_siren_desc(ctypes.Structure):
+    _fields_ = [("d", c_i32), ("K", c_i32), ("H", c_i32), ("O", c_i32), ("omega", ctypes.c_float)]
 
 
 class hg_table(ctypes.Structure):
@@ -57,6 +61,7 @@ def lib() -> ctypes.CDLL:
                           "`python -m multiresolution_hash_grid_02_b300.build`")
     L = ctypes.CDLL(_LIB_PATH)
     D, T, G = ctypes.POINTER(hg_grid_desc), ctypes.POINTER(hg_table), ctypes.POINTER(hg_grad_table)
+    S = ctypes.POINTER(hg_siren_desc)
     sig = {
         "hg_level_resolutions": [D, ctypes.POINTER(c_i32)],
         "hg_encode_fwd": [D, c_i64, c_vp, T, c_vp, c_vp, c_vp, c_vp],
@@ -70,6 +75,8 @@ def lib() -> ctypes.CDLL:
         "hg_linear_fd_bwd": [D, c_i64, c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_vp, G, c_vp],
         "hg_rbf_fwd": [D, c_i64, c_vp, ctypes.c_float, c_i32, T, c_vp, c_vp, c_vp, c_vp],
         "hg_rbf_bwd": [D, c_i64, c_vp, ctypes.c_float, c_i32, c_vp, c_vp, c_vp, G, c_vp],
+        "hg_siren_fwd": [S] + [c_i64] + [c_vp] * 11,
+        "hg_siren_bwd": [S] + [c_i64] + [c_vp] * 17,
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -314,6 +321,43 @@ def hg_rbf_bwd(desc: GridDesc, n: int, coords, eps: float, rings: int, g_gamma, 
                           _addr(g_dgamma), _addr(g_lap), _tables_c([grad], hg_grad_table), _stream(stream) if n else 0)
     if check:
         _check(st, "hg_rbf_bwd")
+    return st
+
+
+@dataclass
+class SirenDesc:
+    """The SIREN consumer's shape: d spatial dimensions, K = L F inputs, H
+    hidden units, O outputs and the sine frequency omega (hg_siren_desc)."""
+    d: int
+    K: int
+    H: int
+    O: int = 1
+    omega: float = 30.0
+
+    def as_c(self) -> hg_siren_desc:
+        return hg_siren_desc(self.d, self.K, self.H, self.O, self.omega)
+
+
+def hg_siren_fwd(desc: SirenDesc, n: int, gamma, dgamma, lap, W1, b1, W2, b2, u, du=None, lapu=None, stream=None,
+                 check: bool = True) -> int:
+    c = desc.as_c()
+    st = lib().hg_siren_fwd(ctypes.byref(c), int(n), *[_addr(a) for a in (gamma, dgamma, lap, W1, b1, W2, b2, u, du,
+                                                                           lapu)], _stream(stream) if n else 0)
+    if check:
+        _check(st, "hg_siren_fwd")
+    return st
+
+
+def hg_siren_bwd(desc: SirenDesc, n: int, gamma, dgamma, lap, W1, b1, W2, g_u, g_du, g_lapu, g_gamma=None,
+                 g_dgamma=None, g_lap=None, gW1=None, gb1=None, gW2=None, gb2=None, stream=None,
+                 check: bool = True) -> int:
+    c = desc.as_c()
+    st = lib().hg_siren_bwd(ctypes.byref(c), int(n), *[_addr(a) for a in (gamma, dgamma, lap, W1, b1, W2, g_u, g_du,
+                                                                           g_lapu, g_gamma, g_dgamma, g_lap, gW1,
+                                                                           gb1, gW2, gb2)],
+                            _stream(stream) if n else 0)
+    if check:
+        _check(st, "hg_siren_bwd")
     return st
 
 

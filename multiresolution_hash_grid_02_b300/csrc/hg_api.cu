@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -458,6 +459,52 @@ hg_status fd_step(float eps, float& half_inv, float& inv2) {
     return HG_OK;
 }
 
+
+// SIREN consumer: argument checks and the tile plan (threads per point, points per tile,
+// weight-gradient splits), then one wave of persistent CTAs.
+hg_status siren_plan(const hg_siren_desc* desc, int64_t n, hg::SirenParams& p) {
+    if (!desc) return fail(HG_ERR_INVALID_ARG, "desc is NULL");
+    hg_status st = check_n(n);
+    if (st != HG_OK) return st;
+    if (desc->d < 1 || desc->d > 4) return fail(HG_ERR_INVALID_ARG, "d = %d; must be in 1..4", desc->d);
+    if (desc->K < 8 || desc->K > 64 || desc->K % 8 != 0)
+        return fail(HG_ERR_INVALID_ARG, "K = %d; must be a multiple of 8 in 8..64", desc->K);
+    if (desc->H != 16 && desc->H != 32 && desc->H != 64 && desc->H != 128)
+        return fail(HG_ERR_INVALID_ARG, "H = %d; must be 16, 32, 64 or 128", desc->H);
+    if (desc->O < 1 || desc->O > 4) return fail(HG_ERR_INVALID_ARG, "O = %d; must be in 1..4", desc->O);
+    if (!(fabsf(desc->omega) < INFINITY)) return fail(HG_ERR_INVALID_ARG, "omega must be finite");
+    memset(&p, 0, sizeof(p));
+    p.d = desc->d;
+    p.K = desc->K;
+    p.H = desc->H;
+    p.O = desc->O;
+    p.tp = desc->H / 16;
+    p.pts = 256 / p.tp;
+    const int nb = (desc->H / 4) * (desc->K / 4);
+    p.groups = nb >= 256 ? 1 : 256 / nb;
+    p.n = n;
+    p.omega = desc->omega;
+    return HG_OK;
+}
+
+// One wave of persistent CTAs for a planned launch (n > 0).
+hg_status siren_grid(const hg::SirenParams& p, bool bwd, int& ctas) {
+    const int64_t n = p.n;
+    const size_t bytes = hg::siren_smem_bytes(p, bwd);
+    int dev = 0, sms = 0, smem_max = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return fail(HG_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+    if (bytes > static_cast<size_t>(smem_max))
+        return fail(HG_ERR_UNSUPPORTED, "a SIREN tile needs %zu bytes of shared memory (at most %d)", bytes, smem_max);
+    e = static_cast<cudaError_t>(hg::siren_ctas_per_sm(p, bwd, &per_sm));
+    if (e != cudaSuccess || per_sm < 1) return fail(HG_ERR_CUDA, "SIREN occupancy query failed");
+    const int64_t tiles = (n + p.pts - 1) / p.pts;
+    ctas = static_cast<int>(std::min<int64_t>(tiles, static_cast<int64_t>(sms) * per_sm));
+    return HG_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -749,6 +796,73 @@ hg_status hg_probe_replay_gather(const hg_grid_desc* desc, int64_t n, const floa
 hg_status hg_probe_replay_red(const hg_grid_desc* desc, int64_t n, const float* coords, float* grad,
                               int64_t level_stride_bytes, int32_t row_bytes, int32_t lanes_per_row, hg_stream stream) {
     return replay(desc, n, coords, grad, level_stride_bytes, row_bytes, lanes_per_row, nullptr, true, stream);
+}
+
+
+hg_status hg_siren_fwd(const hg_siren_desc* desc, int64_t n, const float* gamma, const float* dgamma,
+                       const float* lap, const float* W1, const float* b1, const float* W2, const float* b2,
+                       float* u, float* du, float* lapu, hg_stream stream) {
+    hg::SirenParams p;
+    int ctas = 0;
+    hg_status st = siren_plan(desc, n, p);
+    if (st != HG_OK) return st;
+    if (!gamma || !W1 || !b1 || !W2) return fail(HG_ERR_INVALID_ARG, "gamma, W1, b1 and W2 must not be NULL");
+    if ((du || lapu) && !dgamma) return fail(HG_ERR_INVALID_ARG, "du and lapu need dgamma");
+    if (lapu && !lap) return fail(HG_ERR_INVALID_ARG, "lapu needs lap");
+    const void* ptrs[] = {gamma, dgamma, lap, W1, b1, W2, b2, u, du, lapu};
+    for (const void* q : ptrs)
+        if (q && !aligned(q, 4)) return fail(HG_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
+    if (n == 0 || (!u && !du && !lapu)) return ok();
+    p.in[0] = gamma;
+    for (int i = 0; i < p.d; ++i) p.in[1 + i] = dgamma ? dgamma + static_cast<int64_t>(i) * p.K * n : nullptr;
+    p.in[p.d + 1] = lap;
+    p.W1 = W1;
+    p.b1 = b1;
+    p.W2 = W2;
+    p.b2 = b2;
+    p.u = u;
+    p.du = du;
+    p.lapu = lapu;
+    if ((st = siren_grid(p, false, ctas)) != HG_OK) return st;
+    return launch_status(hg::launch_siren_fwd(p, ctas, stream), "SIREN forward");
+}
+
+hg_status hg_siren_bwd(const hg_siren_desc* desc, int64_t n, const float* gamma, const float* dgamma,
+                       const float* lap, const float* W1, const float* b1, const float* W2, const float* g_u,
+                       const float* g_du, const float* g_lapu, float* g_gamma, float* g_dgamma, float* g_lap,
+                       float* gW1, float* gb1, float* gW2, float* gb2, hg_stream stream) {
+    hg::SirenParams p;
+    int ctas = 0;
+    hg_status st = siren_plan(desc, n, p);
+    if (st != HG_OK) return st;
+    if (!gamma || !dgamma || !lap || !W1 || !b1 || !W2)
+        return fail(HG_ERR_INVALID_ARG, "gamma, dgamma, lap, W1, b1 and W2 must not be NULL");
+    const void* ptrs[] = {gamma, dgamma, lap, W1, b1, W2, g_u, g_du, g_lapu, g_gamma, g_dgamma, g_lap,
+                          gW1, gb1, gW2, gb2};
+    for (const void* q : ptrs)
+        if (q && !aligned(q, 4)) return fail(HG_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
+    if (n == 0 || (!g_gamma && !g_dgamma && !g_lap && !gW1 && !gb1 && !gW2 && !gb2)) return ok();
+    const int64_t row = static_cast<int64_t>(p.K) * n;
+    p.in[0] = gamma;
+    p.g_in[0] = g_gamma;
+    for (int i = 0; i < p.d; ++i) {
+        p.in[1 + i] = dgamma + i * row;
+        p.g_in[1 + i] = g_dgamma ? g_dgamma + i * row : nullptr;
+    }
+    p.in[p.d + 1] = lap;
+    p.g_in[p.d + 1] = g_lap;
+    p.W1 = W1;
+    p.b1 = b1;
+    p.W2 = W2;
+    p.g_u = g_u;
+    p.g_du = g_du;
+    p.g_lapu = g_lapu;
+    p.gW1 = gW1;
+    p.gb1 = gb1;
+    p.gW2 = gW2;
+    p.gb2 = gb2;
+    if ((st = siren_grid(p, true, ctas)) != HG_OK) return st;
+    return launch_status(hg::launch_siren_bwd(p, ctas, stream), "SIREN backward");
 }
 
 }  // extern "C"

@@ -116,4 +116,29 @@ int launch_indices(const IdxParams& p, void* stream);
 // red: RED replay (adds 1.0 to every float of each chunk), else gather replay.
 int launch_replay(const ReplayParams& p, bool red, void* stream);
 
+// SIREN chain-rule consumer of the encoding.  Rows r of a point: 0 = gamma,
+// 1..d = d gamma / d x_i, d + 1 = lap gamma (each feature-major, [K][n]).
+struct SirenParams {
+    int32_t d, K, H, O;
+    int32_t tp;          // threads per point (H / 16; each owns 16 hidden units)
+    int32_t pts;         // points per tile (256 / tp)
+    int32_t groups;      // splits of the first-layer weight-gradient reduction over a tile
+    int64_t n;
+    float omega;
+    const float* in[6];  // rows; NULL = zero
+    const float *W1, *b1, *W2, *b2;
+    // forward outputs ([O][n], [d][O][n], [O][n]; NULL = not wanted)
+    float *u, *du, *lapu;
+    // backward: upstream gradients (NULL = zero), input gradients (NULL = not wanted),
+    // weight gradients (accumulated; NULL = not wanted)
+    const float *g_u, *g_du, *g_lapu;
+    float* g_in[6];
+    float *gW1, *gb1, *gW2, *gb2;
+};
+// Dynamic shared memory of one CTA, and the launch (persistent CTAs, at most `ctas`).
+size_t siren_smem_bytes(const SirenParams& p, bool bwd);
+int launch_siren_fwd(const SirenParams& p, int ctas, void* stream);
+int launch_siren_bwd(const SirenParams& p, int ctas, void* stream);
+int siren_ctas_per_sm(const SirenParams& p, bool bwd, int* ctas);
+
 }  // namespace hg

@@ -1,0 +1,479 @@
+// SIREN chain-rule consumer of the multiresolution encoding: forward and backward.
+//
+// "Hermite-NGP: Gradient-Augmented Hash Encoding for Learning PDEs", 整体框架
+// and 关键设计 2: the encoding's outputs gamma, grad gamma and lap gamma feed a
+// SIREN, u = W2 sin(omega z) + b2 with z = W1 gamma + b1, and the chain rule
+// with sigma'' = -omega^2 sigma gives, in one pass,
+//   d u / d x_i = W2 [omega cos(omega z) * y_i],          y_i = W1 d gamma / d x_i,
+//   lap u       = W2 [omega cos(omega z) * s - omega^2 sin(omega z) * sum_i y_i^2],  s = W1 lap gamma.
+// The backward is the vector-Jacobian product to the encoder outputs (what
+// the encoding's backward takes) and to the weights.
+//
+// Design: FP32 FMA on the CUDA cores.  The first layer contracts the d + 2
+// input rows of a point (K = L F features each) with W1: small K, and with
+// omega = 30 magnifying the rounding of z thirtyfold, too precision-sensitive
+// for tf32 or bf16 tensor cores.  A CTA of 256 threads takes a tile of `pts`
+// points staged in shared memory; tp = H / 16 threads share a point, each
+// owning 16 hidden units, so every weight read from shared memory feeds d + 2
+// FMAs.  CTAs are persistent (one wave): the weights are staged once per CTA
+// and the weight gradients are added to global memory once per CTA.
+#include <cuda_runtime.h>
+
+#include "hg_params.h"
+
+namespace hg {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnits = 16;  // hidden units per thread
+constexpr int kMaxO = 4;
+
+// Shared-memory layout of a CTA, in floats; every region starts on 16 bytes.
+struct SirenSmem {
+    int w1t, b1, w2, b2, x, w1, g, gw1, gw2, gb1, gb2, total;
+};
+
+__host__ __device__ inline int take(int& at, int n) {
+    const int here = at;
+    at += (n + 3) & ~3;
+    return here;
+}
+
+__host__ __device__ inline SirenSmem siren_layout(const SirenParams& p, bool bwd) {
+    const int R = p.d + 2;
+    SirenSmem m;
+    int at = 0;
+    m.w1t = take(at, p.K * p.H);             // W1 transposed, [K][H]: the forward contraction
+    m.b1 = take(at, p.H);
+    m.w2 = take(at, p.O * p.H);
+    m.b2 = take(at, p.O);
+    m.x = take(at, R * p.pts * (p.K + 4));   // inputs [R][pts][K + 4] (padding: no bank conflicts)
+    if (bwd) {
+        m.w1 = take(at, p.H * p.K);          // W1 as given, [H][K]: the input gradients
+        m.g = take(at, R * p.pts * (p.H + 4));  // pre-activation gradients [R][pts][H + 4]
+        m.gw1 = take(at, p.groups * p.H * p.K);
+        m.gw2 = take(at, p.O * p.H);
+        m.gb1 = take(at, p.H);
+        m.gb2 = take(at, p.O);
+    } else {
+        m.w1 = m.g = m.gw1 = m.gw2 = m.gb1 = m.gb2 = -1;
+    }
+    m.total = at;
+    return m;
+}
+
+// Weights into shared memory (W1 transposed for the forward contraction).
+__device__ void stage_weights(const SirenParams& p, const SirenSmem& L, float* sm, bool bwd) {
+    for (int i = threadIdx.x; i < p.H * p.K; i += kThreads) {
+        const float w = __ldg(p.W1 + i);
+        sm[L.w1t + (i % p.K) * p.H + i / p.K] = w;
+        if (bwd) sm[L.w1 + i] = w;
+    }
+    for (int i = threadIdx.x; i < p.H; i += kThreads) sm[L.b1 + i] = __ldg(p.b1 + i);
+    for (int i = threadIdx.x; i < p.O * p.H; i += kThreads) sm[L.w2 + i] = __ldg(p.W2 + i);
+    for (int i = threadIdx.x; i < p.O; i += kThreads) sm[L.b2 + i] = p.b2 ? __ldg(p.b2 + i) : 0.f;
+}
+
+// The tile's input rows, [R][pts][K + 4]; points past n and NULL rows are zero.
+__device__ void load_tile(const SirenParams& p, float* X, int64_t n0, int R) {
+    const int P = p.pts, K = p.K;
+    const int total = R * K * P;
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+        const int pp = i % P, k = (i / P) % K, r = i / (P * K);
+        const int64_t n = n0 + pp;
+        const float* src = p.in[r];
+        X[(r * P + pp) * (K + 4) + k] = (src && n < p.n) ? __ldg(src + k * p.n + n) : 0.f;
+    }
+}
+
+__device__ __forceinline__ float lane4(const float4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// First layer for the thread's point (row pl of the tile) and units j0 .. j0 + 15:
+// acc[r][jj] = sum_k W1[j0 + jj][k] X[r][pl][k], k ascending.
+template <int R>
+__device__ __forceinline__ void first_layer(const float* W1T, const float* X, int K, int H, int P, int pl, int j0,
+                                            float (&acc)[R][kUnits]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int jj = 0; jj < kUnits; ++jj) acc[r][jj] = 0.f;
+    const int ld = K + 4;
+    const float* xp = X + pl * ld;
+    for (int k = 0; k < K; k += 4) {
+        float4 xr[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) xr[r] = *reinterpret_cast<const float4*>(xp + r * P * ld + k);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float4* wv = reinterpret_cast<const float4*>(W1T + (k + kk) * H + j0);
+            float w[kUnits];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const float4 q = wv[v];
+                w[4 * v] = q.x;
+                w[4 * v + 1] = q.y;
+                w[4 * v + 2] = q.z;
+                w[4 * v + 3] = q.w;
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float xv = lane4(xr[r], kk);
+#pragma unroll
+                for (int jj = 0; jj < kUnits; ++jj) acc[r][jj] = fmaf(w[jj], xv, acc[r][jj]);
+            }
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2) siren_fwd_kernel(const __grid_constant__ SirenParams p) {
+    constexpr int R = D + 2;
+    extern __shared__ float4 smem4[];
+    float* sm = reinterpret_cast<float*>(smem4);
+    const SirenSmem L = siren_layout(p, false);
+    stage_weights(p, L, sm, false);
+    const float* W1T = sm + L.w1t;
+    const float* b1 = sm + L.b1;
+    const float* W2 = sm + L.w2;
+    const float* b2 = sm + L.b2;
+    float* X = sm + L.x;
+    const int tp = p.tp, P = p.pts, H = p.H, O = p.O;
+    const int pl = threadIdx.x / tp, q = threadIdx.x % tp, j0 = kUnits * q;
+    const float om = p.omega, om2 = om * om;
+    const int64_t tiles = (p.n + P - 1) / P;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        __syncthreads();  // weights staged; the previous tile's inputs read
+        const int64_t n0 = t * P;
+        load_tile(p, X, n0, R);
+        __syncthreads();
+        float acc[R][kUnits];
+        first_layer<R>(W1T, X, p.K, H, P, pl, j0, acc);
+        float pu[kMaxO], pdu[D][kMaxO], plap[kMaxO];
+#pragma unroll
+        for (int o = 0; o < kMaxO; ++o) {
+            pu[o] = plap[o] = 0.f;
+#pragma unroll
+            for (int i = 0; i < D; ++i) pdu[i][o] = 0.f;
+        }
+#pragma unroll
+        for (int jj = 0; jj < kUnits; ++jj) {
+            const int j = j0 + jj;
+            float a, c;
+            sincosf(om * (acc[0][jj] + b1[j]), &a, &c);
+            float y2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < D; ++i) y2 = fmaf(acc[1 + i][jj], acc[1 + i][jj], y2);
+            const float oc = om * c;
+            const float tl = fmaf(oc, acc[R - 1][jj], -om2 * a * y2);  // omega c s - omega^2 a sum y^2
+#pragma unroll
+            for (int o = 0; o < kMaxO; ++o) {
+                if (o < O) {
+                    const float w2 = W2[o * H + j];
+                    pu[o] = fmaf(w2, a, pu[o]);
+#pragma unroll
+                    for (int i = 0; i < D; ++i) pdu[i][o] = fmaf(w2, oc * acc[1 + i][jj], pdu[i][o]);
+                    plap[o] = fmaf(w2, tl, plap[o]);
+                }
+            }
+        }
+        // sum over the tp threads of the point (consecutive lanes)
+        for (int m = 1; m < tp; m <<= 1) {
+#pragma unroll
+            for (int o = 0; o < kMaxO; ++o) {
+                pu[o] += __shfl_xor_sync(0xffffffffu, pu[o], m);
+                plap[o] += __shfl_xor_sync(0xffffffffu, plap[o], m);
+#pragma unroll
+                for (int i = 0; i < D; ++i) pdu[i][o] += __shfl_xor_sync(0xffffffffu, pdu[i][o], m);
+            }
+        }
+        const int64_t n = n0 + pl;
+        if (q == 0 && n < p.n) {
+#pragma unroll
+            for (int o = 0; o < kMaxO; ++o) {
+                if (o < O) {
+                    if (p.u) __stcs(p.u + o * p.n + n, pu[o] + b2[o]);
+                    if (p.du) {
+#pragma unroll
+                        for (int i = 0; i < D; ++i) __stcs(p.du + (static_cast<int64_t>(i) * O + o) * p.n + n, pdu[i][o]);
+                    }
+                    if (p.lapu) __stcs(p.lapu + o * p.n + n, plap[o]);
+                }
+            }
+        }
+    }
+}
+
+// Backward.  Per tile: (1) recompute the first layer, form the pre-activation
+// gradients g_z = d/dz, g_y_i = d/dy_i, g_s = d/ds of the thread's 16 units
+// into shared memory ([R][pts][H + 4]; rows z, y_1 .. y_d, s), and sum the
+// output-layer and bias gradients over the warp's points; (2) input gradients
+// g_in[r][k] = sum_j W1[j][k] G[r][j] per point; (3) first-layer weight
+// gradient gW1[j][k] += sum_{r, point} G[r][j] X[r][k], each 4 x 4 block of it
+// owned by one thread of each of `groups` splits of the tile's rows.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_constant__ SirenParams p) {
+    constexpr int R = D + 2;
+    extern __shared__ float4 smem4[];
+    float* sm = reinterpret_cast<float*>(smem4);
+    const SirenSmem L = siren_layout(p, true);
+    stage_weights(p, L, sm, true);
+    for (int i = threadIdx.x; i < p.groups * p.H * p.K; i += kThreads) sm[L.gw1 + i] = 0.f;
+    for (int i = threadIdx.x; i < p.O * p.H; i += kThreads) sm[L.gw2 + i] = 0.f;
+    for (int i = threadIdx.x; i < p.H; i += kThreads) sm[L.gb1 + i] = 0.f;
+    for (int i = threadIdx.x; i < p.O; i += kThreads) sm[L.gb2 + i] = 0.f;
+    const float* W1T = sm + L.w1t;
+    const float* W1 = sm + L.w1;
+    const float* b1 = sm + L.b1;
+    const float* W2 = sm + L.w2;
+    float* X = sm + L.x;
+    float* G = sm + L.g;
+    float* gW1s = sm + L.gw1;
+    float* gW2s = sm + L.gw2;
+    float* gb1s = sm + L.gb1;
+    float* gb2s = sm + L.gb2;
+    const int tp = p.tp, P = p.pts, H = p.H, K = p.K, O = p.O;
+    const int pl = threadIdx.x / tp, q = threadIdx.x % tp, j0 = kUnits * q;
+    const int lane = threadIdx.x & 31;
+    const float om = p.omega, om2 = om * om;
+    const int gld = H + 4, xld = K + 4;
+    bool want_in = false;
+#pragma unroll
+    for (int r = 0; r < R; ++r) want_in = want_in || p.g_in[r];
+    // first-layer weight-gradient ownership: 4 x 4 blocks; `groups` threads share a block, each
+    // summing a contiguous share of the tile's R * pts rows
+    const int nb = (H / 4) * (K / 4);
+    const int grp = nb >= kThreads ? 0 : threadIdx.x / nb;
+    const int rows = R * P, share = (rows + p.groups - 1) / p.groups;
+    const int m0 = grp * share, m1 = min(rows, m0 + share);
+    const int64_t tiles = (p.n + P - 1) / P;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        __syncthreads();  // weights staged; the previous tile's X and G read
+        const int64_t n0 = t * P;
+        load_tile(p, X, n0, R);
+        const int64_t n = n0 + pl;
+        const bool have = n < p.n;
+        float gu[kMaxO], gdu[D][kMaxO], glu[kMaxO];
+#pragma unroll
+        for (int o = 0; o < kMaxO; ++o) {
+            const bool ok = have && o < O;
+            gu[o] = (ok && p.g_u) ? __ldg(p.g_u + o * p.n + n) : 0.f;
+            glu[o] = (ok && p.g_lapu) ? __ldg(p.g_lapu + o * p.n + n) : 0.f;
+#pragma unroll
+            for (int i = 0; i < D; ++i)
+                gdu[i][o] = (ok && p.g_du) ? __ldg(p.g_du + (static_cast<int64_t>(i) * O + o) * p.n + n) : 0.f;
+        }
+        __syncthreads();
+        // (1) pre-activation gradients
+        {
+            float acc[R][kUnits];
+            first_layer<R>(W1T, X, K, H, P, pl, j0, acc);
+            float* Gp = G + pl * gld;
+#pragma unroll
+            for (int jj = 0; jj < kUnits; ++jj) {
+                const int j = j0 + jj;
+                float a, c;
+                sincosf(om * (acc[0][jj] + b1[j]), &a, &c);
+                const float oc = om * c, oa = om * a;
+                float y2 = 0.f;
+#pragma unroll
+                for (int i = 0; i < D; ++i) y2 = fmaf(acc[1 + i][jj], acc[1 + i][jj], y2);
+                const float s = acc[R - 1][jj];
+                // adjoints of a, omega c y_i and the Laplacian's bracket through W2
+                float U = 0.f, Pl = 0.f, Dv[D];
+#pragma unroll
+                for (int i = 0; i < D; ++i) Dv[i] = 0.f;
+#pragma unroll
+                for (int o = 0; o < kMaxO; ++o) {
+                    if (o < O) {
+                        const float w2 = W2[o * H + j];
+                        U = fmaf(w2, gu[o], U);
+                        Pl = fmaf(w2, glu[o], Pl);
+#pragma unroll
+                        for (int i = 0; i < D; ++i) Dv[i] = fmaf(w2, gdu[i][o], Dv[i]);
+                    }
+                }
+                const float ga = fmaf(-om2 * Pl, y2, U);  // d/da
+                float gc = Pl * s;                         // d/dc, over omega
+#pragma unroll
+                for (int i = 0; i < D; ++i) gc = fmaf(Dv[i], acc[1 + i][jj], gc);
+                gc *= om;
+                Gp[j] = fmaf(oc, ga, -oa * gc);  // d/dz: a = sin(omega z), c = cos(omega z)
+#pragma unroll
+                for (int i = 0; i < D; ++i)
+                    Gp[(1 + i) * P * gld + j] = fmaf(oc, Dv[i], -2.f * om2 * a * Pl * acc[1 + i][jj]);
+                Gp[(R - 1) * P * gld + j] = oc * Pl;
+                // output-layer and bias gradients of unit j, summed over the warp's points
+                if (p.gb1) {
+                    float v = Gp[j];
+                    for (int m = tp; m < 32; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+                    if (lane < tp) atomicAdd(gb1s + j, v);
+                }
+                if (p.gW2) {
+                    const float tl = fmaf(oc, s, -om2 * a * y2);
+#pragma unroll
+                    for (int o = 0; o < kMaxO; ++o) {
+                        if (o < O) {
+                            float v = fmaf(glu[o], tl, gu[o] * a);
+#pragma unroll
+                            for (int i = 0; i < D; ++i) v = fmaf(gdu[i][o], oc * acc[1 + i][jj], v);
+                            for (int m = tp; m < 32; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+                            if (lane < tp) atomicAdd(gW2s + o * H + j, v);
+                        }
+                    }
+                }
+            }
+            if (p.gb2) {
+#pragma unroll
+                for (int o = 0; o < kMaxO; ++o) {
+                    if (o < O) {
+                        float v = q == 0 ? gu[o] : 0.f;
+                        for (int m = 1; m < 32; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+                        if (lane == 0) atomicAdd(gb2s + o, v);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        // (2) input gradients of the thread's point, 8 features at a time
+        if (want_in) {
+            for (int kc = 8 * q; kc < K; kc += 8 * tp) {
+                float acc2[R][8];
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) acc2[r][kk] = 0.f;
+                for (int j = 0; j < H; j += 4) {
+                    float4 g4[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) g4[r] = *reinterpret_cast<const float4*>(G + (r * P + pl) * gld + j);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const float4* wv = reinterpret_cast<const float4*>(W1 + (j + jj) * K + kc);
+                        const float4 wa = wv[0], wb = wv[1];
+                        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const float gv = lane4(g4[r], jj);
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) acc2[r][kk] = fmaf(gv, w[kk], acc2[r][kk]);
+                        }
+                    }
+                }
+                if (have) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        if (p.g_in[r]) {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) __stcs(p.g_in[r] + (kc + kk) * p.n + n, acc2[r][kk]);
+                        }
+                    }
+                }
+            }
+        }
+        // (3) first-layer weight gradient
+        if (p.gW1 && grp < p.groups) {
+            for (int b = nb >= kThreads ? threadIdx.x : threadIdx.x % nb; b < nb; b += kThreads) {
+                const int j = 4 * (b / (K / 4)), k = 4 * (b % (K / 4));
+                float acc3[4][4] = {};
+                for (int m = m0; m < m1; ++m) {
+                    const float4 g4 = *reinterpret_cast<const float4*>(G + m * gld + j);
+                    const float4 x4 = *reinterpret_cast<const float4*>(X + m * xld + k);
+#pragma unroll
+                    for (int aa = 0; aa < 4; ++aa) {
+                        const float gv = lane4(g4, aa);
+                        acc3[aa][0] = fmaf(gv, x4.x, acc3[aa][0]);
+                        acc3[aa][1] = fmaf(gv, x4.y, acc3[aa][1]);
+                        acc3[aa][2] = fmaf(gv, x4.z, acc3[aa][2]);
+                        acc3[aa][3] = fmaf(gv, x4.w, acc3[aa][3]);
+                    }
+                }
+                float* dst = gW1s + (grp * H + j) * K + k;
+#pragma unroll
+                for (int aa = 0; aa < 4; ++aa)
+#pragma unroll
+                    for (int bb = 0; bb < 4; ++bb) dst[aa * K + bb] += acc3[aa][bb];
+                if (nb < kThreads) break;  // one block per thread of a group
+            }
+        }
+    }
+    __syncthreads();
+    // the CTA's weight gradients, added once
+    if (p.gW1) {
+        for (int e = threadIdx.x; e < H * K; e += kThreads) {
+            float v = 0.f;
+            for (int g = 0; g < p.groups; ++g) v += gW1s[g * H * K + e];
+            atomicAdd(p.gW1 + e, v);
+        }
+    }
+    if (p.gW2)
+        for (int e = threadIdx.x; e < O * H; e += kThreads) atomicAdd(p.gW2 + e, gW2s[e]);
+    if (p.gb1)
+        for (int e = threadIdx.x; e < H; e += kThreads) atomicAdd(p.gb1 + e, gb1s[e]);
+    if (p.gb2)
+        for (int e = threadIdx.x; e < O; e += kThreads) atomicAdd(p.gb2 + e, gb2s[e]);
+}
+
+template <int D>
+cudaError_t set_smem(bool bwd, size_t bytes) {
+    return bwd ? cudaFuncSetAttribute(siren_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(bytes))
+               : cudaFuncSetAttribute(siren_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(bytes));
+}
+
+template <int D>
+cudaError_t occupancy(bool bwd, size_t bytes, int* blocks) {
+    cudaError_t e = set_smem<D>(bwd, bytes);
+    if (e != cudaSuccess) return e;
+    return bwd ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, siren_bwd_kernel<D>, kThreads, bytes)
+               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, siren_fwd_kernel<D>, kThreads, bytes);
+}
+
+template <int D>
+cudaError_t launch(const SirenParams& p, bool bwd, int ctas, cudaStream_t s) {
+    const size_t bytes = siren_smem_bytes(p, bwd);
+    cudaError_t e = set_smem<D>(bwd, bytes);
+    if (e != cudaSuccess) return e;
+    if (bwd)
+        siren_bwd_kernel<D><<<ctas, kThreads, bytes, s>>>(p);
+    else
+        siren_fwd_kernel<D><<<ctas, kThreads, bytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t dispatch(const SirenParams& p, bool bwd, int ctas, cudaStream_t s) {
+    switch (p.d) {
+        case 1: return launch<1>(p, bwd, ctas, s);
+        case 2: return launch<2>(p, bwd, ctas, s);
+        case 3: return launch<3>(p, bwd, ctas, s);
+        default: return launch<4>(p, bwd, ctas, s);
+    }
+}
+
+}  // namespace
+
+size_t siren_smem_bytes(const SirenParams& p, bool bwd) {
+    return static_cast<size_t>(siren_layout(p, bwd).total) * sizeof(float);
+}
+
+int siren_ctas_per_sm(const SirenParams& p, bool bwd, int* ctas) {
+    const size_t bytes = siren_smem_bytes(p, bwd);
+    switch (p.d) {
+        case 1: return occupancy<1>(bwd, bytes, ctas);
+        case 2: return occupancy<2>(bwd, bytes, ctas);
+        case 3: return occupancy<3>(bwd, bytes, ctas);
+        default: return occupancy<4>(bwd, bytes, ctas);
+    }
+}
+
+int launch_siren_fwd(const SirenParams& p, int ctas, void* stream) {
+    return dispatch(p, false, ctas, static_cast<cudaStream_t>(stream));
+}
+
+int launch_siren_bwd(const SirenParams& p, int ctas, void* stream) {
+    return dispatch(p, true, ctas, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace hg

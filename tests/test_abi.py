@@ -230,3 +230,28 @@ def test_zero_points_touch_nothing(m):
     assert hg.hg_encode_fwd_hessian(desc, 0, 0, hg.packed_views(t, 2), 0, 0, 0, stream=0, check=False) == hg.HG_OK
     assert hg.hg_encode_bwd_hessian(desc, 0, 0, 0, 0, 0, hg.packed_views(t, 2), stream=0, check=False) == hg.HG_OK
     assert hg.hg_last_error() == ""
+
+
+def test_siren_arguments_are_checked(m):
+    """Descriptor and pointer checks of the SIREN consumer, before any launch."""
+    hg = m.hg
+    E, A = hg.HG_ERR_INVALID_ARG, 1 << 20
+    good = m.SirenDesc(d=3, K=32, H=64, O=1, omega=30.0)
+    bad = [m.SirenDesc(d=0, K=32, H=64), m.SirenDesc(d=5, K=32, H=64), m.SirenDesc(d=3, K=12, H=64),
+           m.SirenDesc(d=3, K=72, H=64), m.SirenDesc(d=3, K=32, H=48), m.SirenDesc(d=3, K=32, H=256),
+           m.SirenDesc(d=3, K=32, H=64, O=0), m.SirenDesc(d=3, K=32, H=64, O=5),
+           m.SirenDesc(d=3, K=32, H=64, omega=float("inf"))]
+    for desc in bad:
+        assert hg.hg_siren_fwd(desc, 5, A, A, A, A, A, A, A, A, stream=0, check=False) == E, desc
+        assert hg.hg_siren_bwd(desc, 5, A, A, A, A, A, A, A, None, None, A, stream=0, check=False) == E, desc
+    # required pointers, and what the requested outputs need
+    assert hg.hg_siren_fwd(good, 5, 0, A, A, A, A, A, A, A, stream=0, check=False) == E            # gamma
+    assert hg.hg_siren_fwd(good, 5, A, 0, A, A, A, A, A, A, du=A, stream=0, check=False) == E      # du needs dgamma
+    assert hg.hg_siren_fwd(good, 5, A, A, 0, A, A, A, A, A, lapu=A, stream=0, check=False) == E    # lapu needs lap
+    assert hg.hg_siren_fwd(good, 5, A + 2, A, A, A, A, A, A, A, stream=0, check=False) == E        # alignment
+    assert hg.hg_siren_bwd(good, 5, A, 0, A, A, A, A, A, None, None, A, stream=0, check=False) == E  # dgamma
+    assert hg.hg_siren_fwd(good, -1, A, A, A, A, A, A, A, A, stream=0, check=False) == E
+    # n = 0, or nothing requested: no launch
+    assert hg.hg_siren_fwd(good, 0, 0, 0, 0, 0, 0, 0, 0, 0, stream=0, check=False) == E             # still NULL
+    assert hg.hg_siren_fwd(good, 0, A, A, A, A, A, A, A, A, stream=0, check=False) == hg.HG_OK
+    assert hg.hg_siren_bwd(good, 5, A, A, A, A, A, A, A, A, A, stream=0, check=False) == hg.HG_OK
