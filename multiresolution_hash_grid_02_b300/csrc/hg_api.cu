@@ -479,6 +479,7 @@ hg_status siren_plan(const hg_siren_desc* desc, int64_t n, hg::SirenParams& p) {
     p.H = desc->H;
     p.O = desc->O;
     p.tp = desc->H / 16;
+    p.nbuf = 1;
     p.pts = 256 / p.tp;
     const int nb = (desc->H / 4) * (desc->K / 4);
     p.groups = nb >= 256 ? 1 : 256 / nb;
@@ -487,15 +488,18 @@ hg_status siren_plan(const hg_siren_desc* desc, int64_t n, hg::SirenParams& p) {
     return HG_OK;
 }
 
-// One wave of persistent CTAs for a planned launch (n > 0).
-hg_status siren_grid(const hg::SirenParams& p, bool bwd, int& ctas) {
+// One wave of persistent CTAs for a planned launch (n > 0), and the number of input buffers.
+hg_status siren_grid(hg::SirenParams& p, bool bwd, int& ctas) {
     const int64_t n = p.n;
-    const size_t bytes = hg::siren_smem_bytes(p, bwd);
     int dev = 0, sms = 0, smem_max = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return fail(HG_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+    // two input buffers (the next tile's copy overlapping this one's compute) when they fit
+    p.nbuf = 2;
+    if (hg::siren_smem_bytes(p, bwd) > static_cast<size_t>(smem_max)) p.nbuf = 1;
+    const size_t bytes = hg::siren_smem_bytes(p, bwd);
     if (bytes > static_cast<size_t>(smem_max))
         return fail(HG_ERR_UNSUPPORTED, "a SIREN tile needs %zu bytes of shared memory (at most %d)", bytes, smem_max);
     e = static_cast<cudaError_t>(hg::siren_ctas_per_sm(p, bwd, &per_sm));

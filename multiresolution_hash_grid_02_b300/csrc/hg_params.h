@@ -123,6 +123,7 @@ struct SirenParams {
     int32_t tp;          // threads per point (H / 16; each owns 16 hidden units)
     int32_t pts;         // points per tile (256 / tp)
     int32_t groups;      // splits of the first-layer weight-gradient reduction over a tile
+    int32_t nbuf;        // input tile buffers: 2 = the next tile loads while this one computes
     int64_t n;
     float omega;
     const float* in[6];  // rows; NULL = zero

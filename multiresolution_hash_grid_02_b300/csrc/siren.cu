@@ -47,7 +47,7 @@ __host__ __device__ inline SirenSmem siren_layout(const SirenParams& p, bool bwd
     m.b1 = take(at, p.H);
     m.w2 = take(at, p.O * p.H);
     m.b2 = take(at, p.O);
-    m.x = take(at, R * p.pts * (p.K + 4));   // inputs [R][pts][K + 4] (padding: no bank conflicts)
+    m.x = take(at, p.nbuf * R * p.pts * (p.K + 4));  // inputs [nbuf][R][pts][K + 4] (padding: no bank conflicts)
     if (bwd) {
         m.w1 = take(at, p.H * p.K);          // W1 as given, [H][K]: the input gradients
         m.g = take(at, R * p.pts * (p.H + 4));  // pre-activation gradients [R][pts][H + 4]
@@ -74,27 +74,50 @@ __device__ void stage_weights(const SirenParams& p, const SirenSmem& L, float* s
     for (int i = threadIdx.x; i < p.O; i += kThreads) sm[L.b2 + i] = p.b2 ? __ldg(p.b2 + i) : 0.f;
 }
 
-// The tile's input rows, [R][pts][K + 4]; points past n and NULL rows are zero.
-__device__ void load_tile(const SirenParams& p, float* X, int64_t n0, int R) {
-    const int P = p.pts, K = p.K;
-    const int total = R * K * P;
+__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid) {
+    const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(d), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// Issue the asynchronous copy of a tile's input rows into X, [R][pts][K + 4];
+// points past n and NULL rows are zero-filled.  A thread takes four
+// consecutive features of one point (lanes: consecutive points, so the reads
+// are coalesced).
+__device__ void issue_tile(const SirenParams& p, float* X, int64_t n0, int R) {
+    const int P = p.pts, K4 = p.K / 4;
+    const int total = R * K4 * P;
     for (int i = threadIdx.x; i < total; i += kThreads) {
-        const int pp = i % P, k = (i / P) % K, r = i / (P * K);
+        const int pp = i & (P - 1), rk = i / P;  // P is a power of two
+        const int k = 4 * (rk % K4), r = rk / K4;
         const int64_t n = n0 + pp;
         const float* src = p.in[r];
-        X[(r * P + pp) * (K + 4) + k] = (src && n < p.n) ? __ldg(src + k * p.n + n) : 0.f;
+        const bool ok = src && n < p.n;
+        const float* e = ok ? src + k * p.n + n : p.W1;  // nothing is read when !ok (zero fill)
+        float* d = X + (r * P + pp) * (p.K + 4) + k;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cp_async4(d + c, ok ? e + c * p.n : e, ok);
     }
 }
+
+// Hidden unit of a thread's slot jj: thread q of a point owns j = 4 q + 4 tp t + e
+// (jj = 4 t + e), so the four weight vectors a thread loads for one feature lie
+// in different banks from those of the point's other threads.
+__device__ __forceinline__ int unit_of(int q, int tp, int jj) { return 4 * q + 4 * tp * (jj >> 2) + (jj & 3); }
 
 __device__ __forceinline__ float lane4(const float4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// First layer for the thread's point (row pl of the tile) and units j0 .. j0 + 15:
-// acc[r][jj] = sum_k W1[j0 + jj][k] X[r][pl][k], k ascending.
+// First layer for the thread's point (row pl of the tile) and its units:
+// acc[r][jj] = sum_k W1[unit_of(q, tp, jj)][k] X[r][pl][k], k ascending.
 template <int R>
-__device__ __forceinline__ void first_layer(const float* W1T, const float* X, int K, int H, int P, int pl, int j0,
-                                            float (&acc)[R][kUnits]) {
+__device__ __forceinline__ void first_layer(const float* W1T, const float* X, int K, int H, int P, int pl, int q,
+                                            int tp, float (&acc)[R][kUnits]) {
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -107,15 +130,15 @@ __device__ __forceinline__ void first_layer(const float* W1T, const float* X, in
         for (int r = 0; r < R; ++r) xr[r] = *reinterpret_cast<const float4*>(xp + r * P * ld + k);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const float4* wv = reinterpret_cast<const float4*>(W1T + (k + kk) * H + j0);
+            const float* wrow = W1T + (k + kk) * H + 4 * q;
             float w[kUnits];
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-                const float4 q = wv[v];
-                w[4 * v] = q.x;
-                w[4 * v + 1] = q.y;
-                w[4 * v + 2] = q.z;
-                w[4 * v + 3] = q.w;
+                const float4 wq = *reinterpret_cast<const float4*>(wrow + 4 * tp * v);
+                w[4 * v] = wq.x;
+                w[4 * v + 1] = wq.y;
+                w[4 * v + 2] = wq.z;
+                w[4 * v + 3] = wq.w;
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -138,18 +161,28 @@ __global__ void __launch_bounds__(kThreads, 2) siren_fwd_kernel(const __grid_con
     const float* b1 = sm + L.b1;
     const float* W2 = sm + L.w2;
     const float* b2 = sm + L.b2;
-    float* X = sm + L.x;
     const int tp = p.tp, P = p.pts, H = p.H, O = p.O;
-    const int pl = threadIdx.x / tp, q = threadIdx.x % tp, j0 = kUnits * q;
+    float* Xb[2] = {sm + L.x, sm + L.x + (p.nbuf - 1) * R * P * (p.K + 4)};
+    const int pl = threadIdx.x / tp, q = threadIdx.x % tp;
     const float om = p.omega, om2 = om * om;
     const int64_t tiles = (p.n + P - 1) / P;
+    int cur = 0;
+    if (static_cast<int64_t>(blockIdx.x) < tiles) issue_tile(p, Xb[0], static_cast<int64_t>(blockIdx.x) * P, R);
+    cp_async_commit();
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-        __syncthreads();  // weights staged; the previous tile's inputs read
+        const int64_t tn = t + gridDim.x;
+        if (p.nbuf == 2) {  // the next tile's copy flies while this one computes
+            if (tn < tiles) issue_tile(p, Xb[cur ^ 1], tn * P, R);
+            cp_async_commit();
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();  // this tile (and the weights) visible to every thread
+        const float* X = Xb[cur];
         const int64_t n0 = t * P;
-        load_tile(p, X, n0, R);
-        __syncthreads();
         float acc[R][kUnits];
-        first_layer<R>(W1T, X, p.K, H, P, pl, j0, acc);
+        first_layer<R>(W1T, X, p.K, H, P, pl, q, tp, acc);
         float pu[kMaxO], pdu[D][kMaxO], plap[kMaxO];
 #pragma unroll
         for (int o = 0; o < kMaxO; ++o) {
@@ -159,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 2) siren_fwd_kernel(const __grid_con
         }
 #pragma unroll
         for (int jj = 0; jj < kUnits; ++jj) {
-            const int j = j0 + jj;
+            const int j = unit_of(q, tp, jj);
             float a, c;
             sincosf(om * (acc[0][jj] + b1[j]), &a, &c);
             float y2 = 0.f;
@@ -202,7 +235,14 @@ __global__ void __launch_bounds__(kThreads, 2) siren_fwd_kernel(const __grid_con
                 }
             }
         }
+        __syncthreads();  // this tile's buffer read by every thread
+        if (p.nbuf == 1 && tn < tiles) {
+            issue_tile(p, Xb[0], tn * P, R);
+            cp_async_commit();
+        }
+        cur ^= p.nbuf - 1;
     }
+    cp_async_wait<0>();
 }
 
 // Backward.  Per tile: (1) recompute the first layer, form the pre-activation
@@ -227,14 +267,14 @@ __global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_con
     const float* W1 = sm + L.w1;
     const float* b1 = sm + L.b1;
     const float* W2 = sm + L.w2;
-    float* X = sm + L.x;
     float* G = sm + L.g;
     float* gW1s = sm + L.gw1;
     float* gW2s = sm + L.gw2;
     float* gb1s = sm + L.gb1;
     float* gb2s = sm + L.gb2;
     const int tp = p.tp, P = p.pts, H = p.H, K = p.K, O = p.O;
-    const int pl = threadIdx.x / tp, q = threadIdx.x % tp, j0 = kUnits * q;
+    float* Xb[2] = {sm + L.x, sm + L.x + (p.nbuf - 1) * R * P * (K + 4)};
+    const int pl = threadIdx.x / tp, q = threadIdx.x % tp;
     const int lane = threadIdx.x & 31;
     const float om = p.omega, om2 = om * om;
     const int gld = H + 4, xld = K + 4;
@@ -248,10 +288,17 @@ __global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_con
     const int rows = R * P, share = (rows + p.groups - 1) / p.groups;
     const int m0 = grp * share, m1 = min(rows, m0 + share);
     const int64_t tiles = (p.n + P - 1) / P;
+    int cur = 0;
+    if (static_cast<int64_t>(blockIdx.x) < tiles) issue_tile(p, Xb[0], static_cast<int64_t>(blockIdx.x) * P, R);
+    cp_async_commit();
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-        __syncthreads();  // weights staged; the previous tile's X and G read
+        const int64_t tn = t + gridDim.x;
+        if (p.nbuf == 2) {  // the next tile's copy flies while this one computes
+            if (tn < tiles) issue_tile(p, Xb[cur ^ 1], tn * P, R);
+            cp_async_commit();
+        }
+        const float* X = Xb[cur];
         const int64_t n0 = t * P;
-        load_tile(p, X, n0, R);
         const int64_t n = n0 + pl;
         const bool have = n < p.n;
         float gu[kMaxO], gdu[D][kMaxO], glu[kMaxO];
@@ -264,15 +311,19 @@ __global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_con
             for (int i = 0; i < D; ++i)
                 gdu[i][o] = (ok && p.g_du) ? __ldg(p.g_du + (static_cast<int64_t>(i) * O + o) * p.n + n) : 0.f;
         }
-        __syncthreads();
+        if (p.nbuf == 2)
+            cp_async_wait<1>();
+        else
+            cp_async_wait<0>();
+        __syncthreads();  // this tile (and the weights) visible to every thread
         // (1) pre-activation gradients
         {
             float acc[R][kUnits];
-            first_layer<R>(W1T, X, K, H, P, pl, j0, acc);
+            first_layer<R>(W1T, X, K, H, P, pl, q, tp, acc);
             float* Gp = G + pl * gld;
 #pragma unroll
             for (int jj = 0; jj < kUnits; ++jj) {
-                const int j = j0 + jj;
+                const int j = unit_of(q, tp, jj);
                 float a, c;
                 sincosf(om * (acc[0][jj] + b1[j]), &a, &c);
                 const float oc = om * c, oa = om * a;
@@ -397,7 +448,14 @@ __global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_con
                 if (nb < kThreads) break;  // one block per thread of a group
             }
         }
+        __syncthreads();  // this tile's X and G read by every thread
+        if (p.nbuf == 1 && tn < tiles) {
+            issue_tile(p, Xb[0], tn * P, R);
+            cp_async_commit();
+        }
+        cur ^= p.nbuf - 1;
     }
+    cp_async_wait<0>();
     __syncthreads();
     // the CTA's weight gradients, added once
     if (p.gW1) {
