@@ -13,6 +13,11 @@ Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 a bounded sample of the same workload instead (the oracle is a deliberately
 slow fp64 program; the ratio against it is context, not a target).
 
+``--siren`` times the encoder with its consumer instead: Hermite forward,
+the SIREN chain rule (u, grad u, lap u from gamma, grad gamma, lap gamma),
+the SIREN's backward from N(0,1) gradients of u, grad u and lap u, and the
+Hermite backward of the SIREN's input gradients.
+
 Multi-GPU (torchrun): every rank runs its own replica on its own shard of
 points (the forward and backward of different points are independent); the
 timed region is bracketed by barriers and the slowest rank's time is used.
@@ -41,6 +46,8 @@ METRIC_FD = ("encoded points/s (INGP-FD: d-linear encodes at x and the 2d stenci
 METRIC_RBF = ("encoded points/s (Gaussian-RBF grid fwd gamma, grad, Laplacian + bwd) at 1 B300; "
               "% of the measured ceiling")
 METRIC_HESSIAN = "encoded points/s (Hermite fwd γ,∇γ, full Hessian + bwd) at 1 B300; % of L2 gather roofline"
+METRIC_SIREN = ("points/s of encoder + SIREN (Hermite fwd γ,∇γ,∇²γ; SIREN u,∇u,∇²u; SIREN bwd; Hermite bwd) "
+                "at 1 B300; % of the dominant kernel's roofline")
 L2_BYTES = 126 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
@@ -61,6 +68,9 @@ def parse_args():
     p.add_argument("--hessian", action="store_true",
                    help="Hermite workloads: the full-Hessian entry points (every d2/dx_i dx_j) instead of the "
                         "Laplacian ones")
+    p.add_argument("--siren", action="store_true",
+                   help="Hermite workloads: time the encoder with its SIREN chain-rule consumer (forward and "
+                        "backward of both)")
     p.add_argument("--probe-patterns", action="store_true",
                    help="print the L2 random-row gather / RED rates for 1, 2 and 4 lanes per row "
                         "(32- and 64-byte rows) as one JSON line, then exit")
@@ -172,7 +182,7 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
 # workload description and algorithmic byte counts
 # ---------------------------------------------------------------------------
 
-def describe(w, mask, layout, hessian=False):
+def describe(w, mask, layout, hessian=False, siren=False):
     res_note = f"N_min={w.n_min}, N_max={w.n_max}"
     lt = w.log2_T[0]
     return {
@@ -192,6 +202,8 @@ def describe(w, mask, layout, hessian=False):
            if w.kind == "linear_fd" else {}),
         **({"rbf_eps_grid_units": w.eps, "rbf_rings": w.rings, "taps_per_point_level": (2 * w.rings) ** w.d}
            if w.kind == "rbf" else {}),
+        **({"consumer": "SIREN u = W2 sin(omega (W1 gamma + b1)) + b2 with the chain rule for grad u and lap u",
+            "siren_K": w.L * w.F, "siren_H": 64, "siren_O": 1, "siren_omega": 30.0} if siren else {}),
     }
 
 
@@ -203,6 +215,15 @@ def rbf_flops(w, mask):
     K = 2 * w.rings
     per = K * (3 * K + 5) if w.d == 2 else K * (K * (3 * K + 5) + 6)
     return 2 * per * w.F * w.n_points * bin(mask).count("1")
+
+
+def siren_flops(n, d, K, H):
+    """Algorithmic flops of the SIREN forward: its first layer contracts the
+    d + 2 input rows of every point (gamma, d gamma/dx_i, lap gamma; K
+    features) with W1 [H][K].  The backward's three contractions (the
+    recomputed first layer, the input gradients and the W1 gradient) are
+    three times that."""
+    return 2 * n * (d + 2) * K * H
 
 
 def fp32_peak_tflops(torch, sm_mhz: float) -> float:
@@ -284,7 +305,9 @@ class ClockSampler:
 # the CPU oracle (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def metric_of(w, hessian=False) -> str:
+def metric_of(w, hessian=False, siren=False) -> str:
+    if siren:
+        return METRIC_SIREN
     if hessian:
         return METRIC_HESSIAN
     return {"linear_fd": METRIC_FD, "rbf": METRIC_RBF}.get(w.kind, METRIC)
@@ -344,17 +367,47 @@ def oracle_step(oracle, w, res, tabs, inputs, lo, hi, mask, threads, hessian=Fal
                           with_mags=False, nthreads=threads)
 
 
-def cpu_baseline(w, inputs, mask, sample, hessian=False):
+def siren_inputs(w, rank=0):
+    """Seeded SIREN weights and upstream gradients for a Hermite workload."""
+    from multiresolution_hash_grid_02_b300 import workloads as W
+    rng = np.random.default_rng(w.seed + 2000 + rank)
+    return W.siren_weights(rng, w.L * w.F), W.siren_upstream(rng, w.n_points, w.d)
+
+
+def oracle_siren_step(oracle, w, res, tabs, inputs, sw, sup, lo, hi, mask, threads):
+    """Oracle encoder + SIREN step on points [lo, hi): Hermite forward, SIREN
+    forward and backward, Hermite backward of the SIREN's input gradients."""
+    x = inputs["coords"][lo:hi]
+    m, d, K = hi - lo, w.d, w.L * w.F
+    enc = oracle.encode_fwd(w.d, w.F, res, w.log2_T, tabs, x, level_mask=mask, nthreads=threads, with_mags=False)
+    feats = {"gamma": enc["gamma"].reshape(m, K), "dgamma": enc["dgamma"].reshape(m, d, K),
+             "lap": enc["lap"].reshape(m, K)}
+    from multiresolution_hash_grid_02_b300 import workloads as W
+    oracle.siren_fwd(omega=W.SIREN_OMEGA, with_mags=False, **feats, **sw)
+    g = oracle.siren_bwd(omega=W.SIREN_OMEGA, with_mags=False, **feats, **sw,
+                         **{k: v[lo:hi] for k, v in sup.items()})
+    oracle.encode_bwd(w.d, w.F, res, w.log2_T, x, g["g_gamma"].reshape(m, w.L, w.F),
+                      g["g_dgamma"].reshape(m, d, w.L, w.F), g["g_lap"].reshape(m, w.L, w.F), level_mask=mask,
+                      with_mags=False, nthreads=threads)
+
+
+def cpu_baseline(w, inputs, mask, sample, hessian=False, siren=None):
     oracle, res, tabs = oracle_setup(w, inputs)
     threads = len(os.sched_getaffinity(0))
     sample = min(sample, w.n_points)
-    oracle_step(oracle, w, res, tabs, inputs, 0, min(256, sample), mask, threads, hessian)  # warm the code path
+
+    def run(lo, hi):
+        if siren:
+            oracle_siren_step(oracle, w, res, tabs, inputs, siren[0], siren[1], lo, hi, mask, threads)
+        else:
+            oracle_step(oracle, w, res, tabs, inputs, lo, hi, mask, threads, hessian)
+    run(0, min(256, sample))  # warm the code path
     t0 = time.perf_counter()
-    oracle_step(oracle, w, res, tabs, inputs, 0, sample, mask, threads, hessian)
+    run(0, sample)
     dt = time.perf_counter() - t0
     return {"value": sample / dt, "unit": "points/s", "cores": threads, "kind": "oracle",
             "sample": f"first {sample} of the {w.n_points} points, all {bin(mask).count('1')} active levels, "
-                      f"fwd + bwd, fp64, {dt:.1f} s"}
+                      f"fwd + bwd{' of encoder and SIREN' if siren else ''}, fp64, {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -366,26 +419,32 @@ def run_reference(args):
     mask = args.level_mask if args.level_mask is not None else (1 << w.L) - 1
     inputs = W.make(w)
     hessian = args.hessian and w.kind == "hermite"
+    siren = siren_inputs(w) if (args.siren and w.kind == "hermite") else None
     if hessian:
         add_hessian_upstream(w, inputs)
     oracle, res, tabs = oracle_setup(w, inputs)
     threads = len(os.sched_getaffinity(0))
-    per_step = min(max(256, args.cpu_sample // 8), w.n_points)
+    per_step = min(max(256, args.cpu_sample // (32 if siren else 8)), w.n_points)
     times = []
     for i in range(args.warmup + args.steps):
         lo = (i * per_step) % max(1, w.n_points - per_step)
         t0 = time.perf_counter()
-        oracle_step(oracle, w, res, tabs, inputs, lo, lo + per_step, mask, threads, hessian)
+        if siren:
+            oracle_siren_step(oracle, w, res, tabs, inputs, siren[0], siren[1], lo, lo + per_step, mask, threads)
+        else:
+            oracle_step(oracle, w, res, tabs, inputs, lo, lo + per_step, mask, threads, hessian)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     t = sum(times)
     value = per_step * len(times) / t
-    line = {"impl": "reference", "metric": metric_of(w, hessian), "value": value, "unit": "points/s", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric_of(w, hessian, siren is not None), "value": value, "unit": "points/s",
+            "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded numpy)", "config": describe(w, mask, args.layout, hessian),
+            "data": "synthetic (seeded numpy)", "config": describe(w, mask, args.layout, hessian, siren is not None),
             "cpu_baseline": {"value": value, "unit": "points/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{per_step} points per step (of {w.n_points}), fwd + bwd, all active levels"},
+                             "sample": f"{per_step} points per step (of {w.n_points}), fwd + bwd"
+                                       f"{' of encoder and SIREN' if siren else ''}, all active levels"},
             "e2e": {"value": value, "unit": "points/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -516,6 +575,9 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.siren:
+        run_siren(args)
         return
     import torch
     import torch.distributed as dist
@@ -821,6 +883,220 @@ def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, sha
                        "gamma/grad gamma/" + ("Hessian" if hessian else "Laplacian")) + " out, "
                     "every step; copies of neighbouring steps overlap the encode (3 streams, 2 buffer sets); "
                     "gradient tables stay on the device"}
+
+
+def run_siren(args):
+    """The encoder + SIREN step (native arm): Hermite forward into the
+    feature-major gamma, grad gamma and Laplacian; the SIREN forward (u, grad
+    u, lap u); the SIREN backward from N(0,1) upstream gradients of those
+    (input gradients and weight gradients); the Hermite backward of the input
+    gradients.  Four launches of this library per step."""
+    import torch
+    import torch.distributed as dist
+    from multiresolution_hash_grid_02_b300 import hg, workloads as W
+    import multiresolution_hash_grid_02_b300 as M
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = W.WORKLOADS[args.config]
+    if w.kind != "hermite":
+        raise SystemExit("--siren needs a Hermite workload (it consumes gamma, grad gamma and lap gamma)")
+    if args.points:
+        w = w.scaled(args.points)
+    mask = args.level_mask if args.level_mask is not None else (1 << w.L) - 1
+    inputs = W.make(w, seed=w.seed + rank)
+    sw, sup = siren_inputs(w, rank)
+    n, d, L, F = w.n_points, w.d, w.L, w.F
+    K, H, O = L * F, W.SIREN_H, W.SIREN_O
+    desc = M.GridDesc(d=d, L=L, F=F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T, level_mask=mask,
+                      dtype=M.HG_F16 if w.dtype == "f16" else M.HG_F32, layout=M.HG_FEATURE_MAJOR)
+    sdesc = M.SirenDesc(d=d, K=K, H=H, O=O, omega=W.SIREN_OMEGA)
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    def fmaj(a):  # point-major [n][...] -> feature-major [...][n]
+        return np.ascontiguousarray(np.moveaxis(a, 0, -1))
+
+    coords, table = dev(inputs["coords"]), dev(inputs["table"])
+    grad = torch.zeros(table.shape, dtype=torch.float32, device="cuda")
+    tviews, gviews = M.packed_views(table, d), M.packed_views(grad, d)
+    W1, b1, W2, b2 = (dev(sw[k]) for k in ("W1", "b1", "W2", "b2"))
+    g_u, g_du, g_lapu = (dev(fmaj(sup[k])) for k in ("g_u", "g_du", "g_lapu"))
+    gamma, dgamma, lap = (torch.empty(sh, device="cuda") for sh in ((L, F, n), (d, L, F, n), (L, F, n)))
+    u, du, lapu = (torch.empty(sh, device="cuda") for sh in ((O, n), (d, O, n), (O, n)))
+    gg, gd, gl = (torch.empty(sh, device="cuda") for sh in ((L, F, n), (d, L, F, n), (L, F, n)))
+    gW1, gb1, gW2, gb2 = (torch.zeros(sh, device="cuda") for sh in ((H, K), (H,), (O, H), (O,)))
+    stream = torch.cuda.current_stream()
+
+    def step(rec=None):
+        grad.zero_()
+        for t in (gW1, gb1, gW2, gb2):
+            t.zero_()
+        if rec:
+            rec[0].record(stream)
+        hg.hg_encode_fwd(desc, n, coords, tviews, gamma, dgamma, lap, stream)
+        if rec:
+            rec[1].record(stream)
+        hg.hg_siren_fwd(sdesc, n, gamma, dgamma, lap, W1, b1, W2, b2, u, du, lapu, stream)
+        if rec:
+            rec[2].record(stream)
+        hg.hg_siren_bwd(sdesc, n, gamma, dgamma, lap, W1, b1, W2, g_u, g_du, g_lapu, gg, gd, gl, gW1, gb1, gW2,
+                        gb2, stream)
+        if rec:
+            rec[3].record(stream)
+        hg.hg_encode_bwd(desc, n, coords, gg, gd, gl, gviews, stream)
+        if rec:
+            rec[4].record(stream)
+
+    gather_pat, red_pat = kernel_patterns(w)
+    gather_bytes, red_bytes = algorithmic_bytes(w, mask)
+    replay_g, replay_r, t_replay_g, t_replay_r = replay_peaks(torch, hg, desc, n, coords, table, grad, gather_pat,
+                                                              red_pat, gather_bytes, red_bytes, stream)
+    uniform_g, uniform_r = probe_peaks(torch, hg, gather_pat, red_pat)
+    gather_peak, red_peak = max(replay_g, uniform_g), max(replay_r, uniform_r)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, "cuda")
+    names = ("encode_fwd", "siren_fwd", "siren_bwd", "encode_bwd")
+    ms = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev) for i, nm in enumerate(names)}
+    fp32 = fp32_peak_tflops(torch, (clocks or {}).get("sm_mhz") or 2032.0)
+    fl = siren_flops(n, d, K, H)
+    kernels = {
+        "encode_fwd": {"ms": ms["encode_fwd"], "bound": "l2", "peak": gather_peak, "unit": "GB/s",
+                       "achieved": gather_bytes / (ms["encode_fwd"] * 1e-3) / 1e9, "algorithmic_bytes": gather_bytes},
+        "siren_fwd": {"ms": ms["siren_fwd"], "bound": "alu", "peak": fp32, "unit": "TFLOP/s",
+                      "achieved": fl / (ms["siren_fwd"] * 1e-3) / 1e12, "algorithmic_flops": fl},
+        "siren_bwd": {"ms": ms["siren_bwd"], "bound": "alu", "peak": fp32, "unit": "TFLOP/s",
+                      "achieved": 3 * fl / (ms["siren_bwd"] * 1e-3) / 1e12, "algorithmic_flops": 3 * fl},
+        "encode_bwd": {"ms": ms["encode_bwd"], "bound": "l2", "peak": red_peak, "unit": "GB/s",
+                       "achieved": red_bytes / (ms["encode_bwd"] * 1e-3) / 1e9, "algorithmic_bytes": red_bytes},
+    }
+    for k in kernels.values():
+        k["frac"] = k["achieved"] / k["peak"]
+    dom = max(kernels, key=lambda nm: kernels[nm]["ms"])
+    k = kernels[dom]
+    roofline = {"bound": k["bound"], "kernel": dom, "achieved": k["achieved"], "peak": k["peak"], "unit": k["unit"],
+                "frac": k["frac"], "traffic": recorded_traffic(traffic_key(w, args.points) + "+siren", dom),
+                "peak_source": ("FP32 FMA peak (SMs x 128 lanes x 2 flops x the median SM clock sampled during the "
+                                "timed region); achieved = the SIREN contractions' flops / launch time")
+                if k["bound"] == "alu" else
+                ("measured live, the larger of the replay of the launch's own row stream and the uniform-random "
+                 "L2 rate of the same row pattern")}
+    e2e = None
+    if not args.no_e2e and rank == 0:
+        e2e = run_e2e_siren(torch, hg, w, desc, sdesc, inputs, sup, tviews, gviews, grad, (W1, b1, W2, b2),
+                            (gW1, gb1, gW2, gb2), stream)
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        cpu = cpu_baseline(w, inputs, mask, min(args.cpu_sample, 1 << 17), siren=(sw, sup))
+    if rank == 0:
+        line = {
+            "metric": METRIC_SIREN, "value": n * world * args.steps / (elapsed_ms * 1e-3), "unit": "points/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded numpy: uniform coords and coefficients, SIREN initialisation, N(0,1) "
+                    "upstream gradients of u, grad u, lap u)",
+            "config": describe(w, mask, "feature", siren=True),
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 4 * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e_siren(torch, hg, w, desc, sdesc, inputs, sup, tviews, gviews, grad, weights, wgrads, stream, steps=8,
+                  warmup=2):
+    """The encoder + SIREN step through the C ABI from pinned host memory:
+    every step copies in the coordinates and the upstream gradients of u,
+    grad u and lap u, and copies out u, grad u and lap u; copies of
+    neighbouring steps overlap the kernels (three streams, two buffer sets),
+    as in the encoder's end-to-end leg."""
+    n, d, L, F, O = w.n_points, w.d, w.L, w.F, sdesc.O
+
+    def pinned(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+    h_in = [pinned(inputs["coords"])] + [pinned(np.moveaxis(sup[k], 0, -1)) for k in ("g_u", "g_du", "g_lapu")]
+    out_shapes = [(O, n), (d, O, n), (O, n)]
+    d_in = [[torch.empty_like(t, device="cuda") for t in h_in] for _ in range(2)]
+    d_out = [[torch.empty(sh, device="cuda") for sh in out_shapes] for _ in range(2)]
+    h_out = [[torch.empty(sh).pin_memory() for sh in out_shapes] for _ in range(2)]
+    enc = [torch.empty(sh, device="cuda") for sh in ((L, F, n), (d, L, F, n), (L, F, n))]
+    genc = [torch.empty(sh, device="cuda") for sh in ((L, F, n), (d, L, F, n), (L, F, n))]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    s_in, s_out, s_comp = torch.cuda.Stream(), torch.cuda.Stream(), stream
+    ev_in, ev_comp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+    started = [False, False]
+    W1, b1, W2, b2 = weights
+
+    def step(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if started[b]:
+                s_in.wait_event(ev_comp[b])
+            for dd, h in zip(d_in[b], h_in):
+                dd.copy_(h, non_blocking=True)
+            ev_in[b].record(s_in)
+        s_comp.wait_event(ev_in[b])
+        if started[b]:
+            s_comp.wait_event(ev_out[b])
+        grad.zero_()
+        for t in wgrads:
+            t.zero_()
+        c, gu, gdu, glu = d_in[b]
+        hg.hg_encode_fwd(desc, n, c, tviews, enc[0], enc[1], enc[2], s_comp)
+        hg.hg_siren_fwd(sdesc, n, enc[0], enc[1], enc[2], W1, b1, W2, b2, d_out[b][0], d_out[b][1], d_out[b][2],
+                        s_comp)
+        hg.hg_siren_bwd(sdesc, n, enc[0], enc[1], enc[2], W1, b1, W2, gu, gdu, glu, genc[0], genc[1], genc[2],
+                        *wgrads, s_comp)
+        hg.hg_encode_bwd(desc, n, c, genc[0], genc[1], genc[2], gviews, s_comp)
+        ev_comp[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[b])
+            for h, dd in zip(h_out[b], d_out[b]):
+                h.copy_(dd, non_blocking=True)
+            ev_out[b].record(s_out)
+        started[b] = True
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_in)
+    for i in range(warmup, warmup + steps):
+        step(i)
+    e.record(s_out)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(e) / steps
+    return {"value": n / (ms * 1e-3), "unit": "points/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": steps,
+            "note": "pinned host buffers; coordinates and the upstream gradients of u, grad u, lap u in, u, grad u, "
+                    "lap u out, every step; copies of neighbouring steps overlap the kernels (3 streams, 2 buffer "
+                    "sets); the encoder outputs, gradient table and weight gradients stay on the device"}
 
 
 if __name__ == "__main__":

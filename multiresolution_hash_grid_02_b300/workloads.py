@@ -190,3 +190,31 @@ def from_feature_major(a: np.ndarray, has_axis: bool) -> np.ndarray:
     if has_axis:
         return np.ascontiguousarray(np.transpose(a, (3, 0, 1, 2)))
     return np.ascontiguousarray(np.transpose(a, (2, 0, 1)))
+
+
+# ---------------------------------------------------------------------------
+# the SIREN consumer of the encoding (Hermite-NGP, 关键设计 2)
+# ---------------------------------------------------------------------------
+
+SIREN_H = 64        # hidden width: the page does not fix it
+SIREN_O = 1         # a scalar field u
+SIREN_OMEGA = 30.0  # omega_0 of the page's training setup ("损失函数 / 训练策略")
+
+
+def siren_weights(rng: np.random.Generator, K: int, H: int = SIREN_H, O: int = SIREN_O,
+                  omega: float = SIREN_OMEGA) -> dict:
+    """SIREN initialisation (first layer U(-1/K, 1/K); bias U(-1/sqrt K, 1/sqrt K);
+    output layer U(-sqrt(6/H)/omega, sqrt(6/H)/omega); zero output bias), float32."""
+    f32 = np.float32
+    return {"W1": rng.uniform(-1 / K, 1 / K, (H, K)).astype(f32),
+            "b1": (rng.uniform(-1, 1, H) / np.sqrt(K)).astype(f32),
+            "W2": (rng.uniform(-1, 1, (O, H)) * np.sqrt(6 / H) / omega).astype(f32),
+            "b2": np.zeros(O, f32)}
+
+
+def siren_upstream(rng: np.random.Generator, n: int, d: int, O: int = SIREN_O) -> dict:
+    """N(0,1) gradients of a loss with respect to u [n][O], grad u [n][d][O]
+    and lap u [n][O] (point-major), float32."""
+    return {"g_u": rng.standard_normal((n, O), dtype=np.float32),
+            "g_du": rng.standard_normal((n, d, O), dtype=np.float32),
+            "g_lapu": rng.standard_normal((n, O), dtype=np.float32)}

@@ -161,3 +161,21 @@ def test_reference_arm_hessian_line():
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and "Hessian" in line["metric"]
     assert line["config"]["second_order"] == "full Hessian" and line["value"] > 0
+
+
+def test_reference_arm_siren_line():
+    """The reference arm runs the encoder + SIREN oracle step (workload 1: K = L F = 8)."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "1",
+                          "--siren", "--steps", "1", "--warmup", "0", "--cpu-sample", "8192"],
+                         env=dict(os.environ, RANK="0", WORLD_SIZE="1"), capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and "SIREN" in line["metric"] and line["value"] > 0
+    assert line["config"]["siren_K"] == 8 and line["config"]["siren_omega"] == 30.0
+
+
+def test_siren_flops():
+    """The SIREN forward's algorithmic flops: its first layer, 2 (d + 2) K H per point."""
+    import bench
+    assert bench.siren_flops(1, 3, 32, 64) == 2 * 5 * 32 * 64
+    assert bench.siren_flops(1 << 21, 2, 32, 64) == (1 << 21) * 2 * 4 * 32 * 64
