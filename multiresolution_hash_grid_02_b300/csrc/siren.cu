@@ -19,6 +19,7 @@
 // and the weight gradients are added to global memory once per CTA.
 #include <cuda_runtime.h>
 
+#include "hg_device.cuh"
 #include "hg_params.h"
 
 namespace hg {
@@ -114,14 +115,17 @@ __device__ __forceinline__ float lane4(const float4& v, int i) {
 }
 
 // First layer for the thread's point (row pl of the tile) and its units:
-// acc[r][jj] = sum_k W1[unit_of(q, tp, jj)][k] X[r][pl][k], k ascending.
+// acc[r][jj] = sum_k W1[unit_of(q, tp, jj)][k] X[r][pl][k], k ascending.  The
+// contraction runs on f32x2 pairs of units (two round-to-nearest FMAs per
+// instruction, the same sums), which halves the issued FMA instructions.
 template <int R>
 __device__ __forceinline__ void first_layer(const float* W1T, const float* X, int K, int H, int P, int pl, int q,
                                             int tp, float (&acc)[R][kUnits]) {
+    uint64_t a2[R][kUnits / 2];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int jj = 0; jj < kUnits; ++jj) acc[r][jj] = 0.f;
+        for (int e = 0; e < kUnits / 2; ++e) a2[r][e] = 0;
     const int ld = K + 4;
     const float* xp = X + pl * ld;
     for (int k = 0; k < K; k += 4) {
@@ -131,23 +135,25 @@ __device__ __forceinline__ void first_layer(const float* W1T, const float* X, in
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const float* wrow = W1T + (k + kk) * H + 4 * q;
-            float w[kUnits];
+            uint64_t w[kUnits / 2];
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
                 const float4 wq = *reinterpret_cast<const float4*>(wrow + 4 * tp * v);
-                w[4 * v] = wq.x;
-                w[4 * v + 1] = wq.y;
-                w[4 * v + 2] = wq.z;
-                w[4 * v + 3] = wq.w;
+                w[2 * v] = f2_pack(wq.x, wq.y);
+                w[2 * v + 1] = f2_pack(wq.z, wq.w);
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float xv = lane4(xr[r], kk);
+                const uint64_t xv = f2_dup(lane4(xr[r], kk));
 #pragma unroll
-                for (int jj = 0; jj < kUnits; ++jj) acc[r][jj] = fmaf(w[jj], xv, acc[r][jj]);
+                for (int e = 0; e < kUnits / 2; ++e) a2[r][e] = f2_fma(w[e], xv, a2[r][e]);
             }
         }
     }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int e = 0; e < kUnits / 2; ++e) f2_unpack(a2[r][e], acc[r][2 * e], acc[r][2 * e + 1]);
 }
 
 template <int D>
@@ -390,11 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_con
         // (2) input gradients of the thread's point, 8 features at a time
         if (want_in) {
             for (int kc = 8 * q; kc < K; kc += 8 * tp) {
-                float acc2[R][8];
+                uint64_t a2[R][4];  // f32x2 pairs of features
 #pragma unroll
                 for (int r = 0; r < R; ++r)
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) acc2[r][kk] = 0.f;
+                    for (int e = 0; e < 4; ++e) a2[r][e] = 0;
                 for (int j = 0; j < H; j += 4) {
                     float4 g4[R];
 #pragma unroll
@@ -403,15 +409,21 @@ __global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_con
                     for (int jj = 0; jj < 4; ++jj) {
                         const float4* wv = reinterpret_cast<const float4*>(W1 + (j + jj) * K + kc);
                         const float4 wa = wv[0], wb = wv[1];
-                        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                        const uint64_t w[4] = {f2_pack(wa.x, wa.y), f2_pack(wa.z, wa.w), f2_pack(wb.x, wb.y),
+                                               f2_pack(wb.z, wb.w)};
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
-                            const float gv = lane4(g4[r], jj);
+                            const uint64_t gv = f2_dup(lane4(g4[r], jj));
 #pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) acc2[r][kk] = fmaf(gv, w[kk], acc2[r][kk]);
+                            for (int e = 0; e < 4; ++e) a2[r][e] = f2_fma(gv, w[e], a2[r][e]);
                         }
                     }
                 }
+                float acc2[R][8];
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) f2_unpack(a2[r][e], acc2[r][2 * e], acc2[r][2 * e + 1]);
                 if (have) {
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
@@ -427,18 +439,23 @@ __global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_con
         if (p.gW1 && grp < p.groups) {
             for (int b = nb >= kThreads ? threadIdx.x : threadIdx.x % nb; b < nb; b += kThreads) {
                 const int j = 4 * (b / (K / 4)), k = 4 * (b % (K / 4));
-                float acc3[4][4] = {};
+                uint64_t a3[4][2] = {};  // f32x2 pairs over k
                 for (int m = m0; m < m1; ++m) {
                     const float4 g4 = *reinterpret_cast<const float4*>(G + m * gld + j);
                     const float4 x4 = *reinterpret_cast<const float4*>(X + m * xld + k);
+                    const uint64_t x01 = f2_pack(x4.x, x4.y), x23 = f2_pack(x4.z, x4.w);
 #pragma unroll
                     for (int aa = 0; aa < 4; ++aa) {
-                        const float gv = lane4(g4, aa);
-                        acc3[aa][0] = fmaf(gv, x4.x, acc3[aa][0]);
-                        acc3[aa][1] = fmaf(gv, x4.y, acc3[aa][1]);
-                        acc3[aa][2] = fmaf(gv, x4.z, acc3[aa][2]);
-                        acc3[aa][3] = fmaf(gv, x4.w, acc3[aa][3]);
+                        const uint64_t gv = f2_dup(lane4(g4, aa));
+                        a3[aa][0] = f2_fma(gv, x01, a3[aa][0]);
+                        a3[aa][1] = f2_fma(gv, x23, a3[aa][1]);
                     }
+                }
+                float acc3[4][4];
+#pragma unroll
+                for (int aa = 0; aa < 4; ++aa) {
+                    f2_unpack(a3[aa][0], acc3[aa][0], acc3[aa][1]);
+                    f2_unpack(a3[aa][1], acc3[aa][2], acc3[aa][3]);
                 }
                 float* dst = gW1s + (grp * H + j) * K + k;
 #pragma unroll
