@@ -15,6 +15,8 @@
 // axis pair instead of adding them into one Laplacian term.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "hg_device.cuh"
 
 namespace hg {
@@ -451,6 +453,163 @@ __global__ void __launch_bounds__(kBlock, 2) hermite_fwd_pair3_kernel(const __gr
     }
 }
 
+// Asynchronous 16-byte copies global -> shared (L2 only), and their groups.
+__device__ __forceinline__ void async_copy16(void* dst, const void* src) {
+    const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+constexpr int kPipeBlock = 128;  // threads of a pipelined CTA: 64 points per batch
+
+// The lane-pair forward of hermite_fwd_pair3_kernel, pipelined: persistent
+// CTAs walk the batches of one level; each lane copies its eight half-rows
+// of the next batch into a private shared-memory slot with cp.async while it
+// blends the current batch, so gathers overlap arithmetic without holding
+// registers.  Slots are [stage][corner][16-byte chunk][thread], so a warp's
+// copies and reads cover consecutive 16-byte words (no bank conflicts); a
+// lane reads only what it copied, so its own wait suffices.  Lanes past the
+// last point copy the last point's rows and store nothing.  The blend is
+// hermite_fwd_pair3_kernel's, so the outputs are bit-identical.
+// Used for fp16 tables, whose half-row is one 16-byte copy: 3D fp16 workload
+// (2^23 points, 10 active levels) 6.55 -> 5.63 ms, full Hessian 7.11 -> 6.95
+// ms.  An fp32 half-row (32 bytes) takes two 16-byte copies, i.e. twice the
+// L2 requests of one 256-bit load, and the kernel is bound by them: the 3D
+// fp32 workload ran 2.26 -> 4.26 ms, so fp32 stays on the unpipelined kernel.
+template <typename TT, bool HESS>
+__global__ void __launch_bounds__(kPipeBlock) hermite_fwd_pipe3_kernel(const __grid_constant__ FwdParams p) {
+    constexpr int D = 3, V = 8, G = 2, S = 4, NO = HESS ? 10 : 5;
+    constexpr int CH = S * 2 * static_cast<int>(sizeof(TT)) / 16;  // 16-byte chunks per half-row
+    constexpr int PB = kPipeBlock / 2;                                 // points per batch
+    extern __shared__ uint4 slots[];                                   // [2][V][CH][kPipeBlock]
+    const int l = p.c.lvl[blockIdx.y];
+    const int lane = threadIdx.x & 1;
+    const int F = p.c.F;
+    const Level& lv = p.c.lv[l];
+    const int64_t lf = static_cast<int64_t>(l) * F + lane;
+    const int64_t batches = (p.c.n + PB - 1) / PB;
+    if (!((p.c.level_mask >> l) & 1u)) {
+        for (int64_t b = blockIdx.x; b < batches; b += gridDim.x) {
+            const int64_t n = b * PB + (threadIdx.x >> 1);
+            if (n >= p.c.n) continue;
+            __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, 0.f);
+            if (p.dgamma) {
+#pragma unroll
+                for (int j = 0; j < D; ++j) __stcs(p.dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf, 0.f);
+            }
+            if constexpr (HESS) {
+#pragma unroll
+                for (int k = 0; k < 6; ++k) __stcs(p.hess + n * p.c.hsn + k * p.c.hsq + lf * p.c.hsf, 0.f);
+            } else if (p.lap) {
+                __stcs(p.lap + n * p.c.sn + lf * p.c.sf, 0.f);
+            }
+        }
+        return;
+    }
+    const TT* base = static_cast<const TT*>(p.tab.ptr[0]) + l * p.tab.ls[0] + lane * (S * 2);
+    auto point_of = [&](int64_t b) {
+        const int64_t n = b * PB + (threadIdx.x >> 1);
+        return n < p.c.n ? n : p.c.n - 1;
+    };
+    auto issue = [&](int64_t b, int st) {
+        const int64_t n = point_of(b);
+        uint32_t c[D];
+        float t[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const uint32_t g[D] = {c[0] + (v & 1u), c[1] + ((v >> 1) & 1u), c[2] + ((v >> 2) & 1u)};
+            const uint32_t id = vertex_index<D>(g, lv, lv.dense & 1u, p.c.tmask[0]);
+            const TT* e = base + static_cast<int64_t>(id) * p.tab.rs[0];
+#pragma unroll
+            for (int ch = 0; ch < CH; ++ch)
+                async_copy16(&slots[((st * V + v) * CH + ch) * kPipeBlock + threadIdx.x], e + ch * (16 / sizeof(TT)));
+        }
+    };
+    int64_t b = blockIdx.x;
+    if (b < batches) issue(b, 0);
+    async_commit();
+    int st = 0;
+    for (; b < batches; b += gridDim.x) {
+        if (b + gridDim.x < batches) issue(b + gridDim.x, st ^ 1);
+        async_commit();
+        async_wait<1>();  // this lane's copies of batch b have landed
+        const int64_t n = b * PB + (threadIdx.x >> 1);
+        uint32_t c[D];
+        float t[D];
+        Basis1 B[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) {
+            locate(__ldg(p.coords + point_of(b) * D + i), lv, c[i], t[i]);
+            B[i] = hermite_basis(t[i], lv);
+        }
+        uint64_t q[V][S];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            if constexpr (sizeof(TT) == 4) {
+#pragma unroll
+                for (int ch = 0; ch < CH; ++ch) {
+                    const uint4 r = slots[((st * V + v) * CH + ch) * kPipeBlock + threadIdx.x];
+                    q[v][2 * ch] = f2_pack(__uint_as_float(r.x), __uint_as_float(r.y));
+                    q[v][2 * ch + 1] = f2_pack(__uint_as_float(r.z), __uint_as_float(r.w));
+                }
+            } else {
+                const uint4 r = slots[(st * V + v) * kPipeBlock + threadIdx.x];
+                const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+                    q[v][i] = f2_pack(f.x, f.y);
+                }
+            }
+        }
+        uint64_t o[NO];
+#pragma unroll
+        for (int k = 0; k < NO; ++k) o[k] = 0ull;  // (+0.0f, +0.0f)
+#pragma unroll
+        for (int u = 0; u < S; ++u) {
+            const AxisW2 W0 = axis_dup(unit_axis<D, G>(B[0], lane, u, 0));
+            const AxisW2 W1 = axis_dup(unit_axis<D, G>(B[1], lane, u, 1));
+            const AxisW2 W2 = axis_dup(unit_axis<D, G>(B[2], lane, u, 2));
+            uint64_t cv[V];
+#pragma unroll
+            for (int v = 0; v < V; ++v) cv[v] = q[v][u];
+            if constexpr (HESS) {
+                unit_blend3_f2_hess(cv, W0, W1, W2, o);
+            } else {
+                unit_blend3_f2(cv, W0, W1, W2, o);
+            }
+        }
+        float r[NO];
+#pragma unroll
+        for (int k = 0; k < NO; ++k) {
+            float x, y;
+            f2_unpack(o[k], x, y);
+            const float mine = lane ? y : x;
+            const float other = lane ? x : y;
+            r[k] = mine + __shfl_xor_sync(0xffffffffu, other, 1);
+        }
+        if (n < p.c.n) {
+            __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, r[0]);
+            if (p.dgamma) {
+#pragma unroll
+                for (int j = 0; j < D; ++j) __stcs(p.dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf, r[1 + j]);
+            }
+            if constexpr (HESS) {
+#pragma unroll
+                for (int k = 0; k < 6; ++k) __stcs(p.hess + n * p.c.hsn + k * p.c.hsq + lf * p.c.hsf, r[4 + k]);
+            } else if (p.lap) {
+                __stcs(p.lap + n * p.c.sn + lf * p.c.sf, r[4]);
+            }
+        }
+        st ^= 1;
+    }
+    async_wait<0>();
+}
+
 // 4D (space-time) forward, any layout and F: one thread per (point, level),
 // one feature at a time.  The 4D blend is a sum over the four axis-3
 // slices (corner side v3, basis order a3): each slice is a 3D blend of the
@@ -710,6 +869,32 @@ cudaError_t launch_pair3(const FwdParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// One wave of persistent pipelined CTAs per level (level-major dispatch: the
+// first wave walks level 0's batches while the next level's CTAs wait).
+template <typename TT, bool HESS>
+cudaError_t launch_pipe3(const FwdParams& p, cudaStream_t s) {
+    constexpr int kSmem = 2 * 8 * (4 * 2 * static_cast<int>(sizeof(TT)) / 16) * kPipeBlock * 16;
+    static int per_sm = 0, sms = 0;  // per instantiation; the device does not change within a process
+    if (per_sm == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(hermite_fwd_pipe3_kernel<TT, HESS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmem);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hermite_fwd_pipe3_kernel<TT, HESS>, kPipeBlock,
+                                                              kSmem);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) per_sm = 1;
+    }
+    const int64_t batches = (p.c.n + kPipeBlock / 2 - 1) / (kPipeBlock / 2);
+    const int64_t ctas = std::min<int64_t>(batches, static_cast<int64_t>(sms) * per_sm);
+    dim3 grid(static_cast<unsigned>(ctas), static_cast<unsigned>(p.c.nlvl));
+    hermite_fwd_pipe3_kernel<TT, HESS><<<grid, kPipeBlock, kSmem, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <typename TT, bool HESS>
 cudaError_t launch4(const FwdParams& p, cudaStream_t s) {
     dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
@@ -730,7 +915,7 @@ cudaError_t dispatch(const FwdParams& p, int fc, bool vec, int dtype, cudaStream
         return dtype == HG_F16 ? launch_quad4<__half, HESS>(p, s) : launch_quad4<float, HESS>(p, s);
     if (p.c.d == 4) return dtype == HG_F16 ? launch4<__half, HESS>(p, s) : launch4<float, HESS>(p, s);
     if (vec && p.c.d == 3 && p.c.F == 2)
-        return dtype == HG_F16 ? launch_pair3<__half, HESS>(p, s) : launch_pair3<float, HESS>(p, s);
+        return dtype == HG_F16 ? launch_pipe3<__half, HESS>(p, s) : launch_pair3<float, HESS>(p, s);
     if (p.c.d == 2)
         return dtype == HG_F16 ? pick_fc<2, __half, HESS>(p, fc, vec, s) : pick_fc<2, float, HESS>(p, fc, vec, s);
     return dtype == HG_F16 ? pick_fc<3, __half, HESS>(p, fc, vec, s) : pick_fc<3, float, HESS>(p, fc, vec, s);
