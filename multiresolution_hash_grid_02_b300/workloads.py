@@ -41,7 +41,7 @@ class Workload:
     log2_T: tuple             # per order table k = 0..d (hermite) or (T,) (linear)
     dtype: str                # "f32" or "f16" table storage
     coef_range: float         # tables ~ U[-r, r)
-    coords: str = "uniform"   # "uniform" or "stratified"
+    coords: str = "uniform"   # "uniform", "stratified" or "stratified_shuffled"
     level_masks: tuple = field(default=())  # extra active-level masks to exercise
     seed: int = 0
     eps: float = 0.0          # finite-difference step (linear_fd); Gaussian width in grid units (rbf)
@@ -75,11 +75,25 @@ WORKLOADS = {
                 eps=1.0, rings=3),
     9: Workload("3d_dinf_rbf", "rbf", 3, 1 << 21, 4, 2, 7, 56, (18,), "f32", 1e-2, coords="stratified", seed=9,
                 eps=1.0, rings=3),
+    # workload 3 with its collocation points in a seeded random order, as a training loop that shuffles its
+    # mini-batches would present them (the DInf-Grid page fixes the strata, not their order); the tables and
+    # upstream gradients are workload 3's draws
+    10: Workload("2d_hermite_pinn_shuffled", "hermite", 2, 1 << 20, 16, 2, 16, 1024, (19, 19, 19), "f32", 1e-2,
+                 coords="stratified_shuffled", seed=3),
 }
+
+SHUFFLE_SEED_OFFSET = 3000   # the permutation of the shuffled order comes from default_rng(seed + 3000)
 
 
 def draw_coords(rng: np.random.Generator, w: Workload) -> np.ndarray:
-    """float32 [N][d] in [0,1]^d."""
+    """float32 [N][d] in [0,1]^d.  "stratified_shuffled": the stratified
+    points (the same draws from ``rng``) permuted by a second generator,
+    ``default_rng(seed + SHUFFLE_SEED_OFFSET)``, so every other draw of the
+    workload is unchanged."""
+    if w.coords == "stratified_shuffled":
+        x = draw_coords(rng, replace(w, coords="stratified"))
+        perm = np.random.default_rng(w.seed + SHUFFLE_SEED_OFFSET).permutation(w.n_points)
+        return np.ascontiguousarray(x[perm])
     if w.coords == "stratified":
         side = int(round(w.n_points ** (1.0 / w.d)))
         if side ** w.d != w.n_points:

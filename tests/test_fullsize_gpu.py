@@ -1,14 +1,19 @@
-"""Full-size GPU parity: workloads 2-5 at their published sizes, run exactly
-as the benchmark launches them (packed table, feature-major outputs, every
-level or the coarse-to-fine active-level masks), checked against the oracle.
+"""Full-size GPU parity: the workloads at their published sizes, run exactly as
+the benchmark launches them (packed table, feature-major outputs, every level
+or the coarse-to-fine active-level masks), checked against the oracle on
+every point and every level.
 
-The forward is compared on sampled points (the oracle computes them one by
-one) for a set of levels; the backward is compared on whole gradient-table
-levels, which the oracle accumulates over every point.  To keep host memory
-bounded, the oracle receives only the checked levels, as a smaller grid with
-explicit resolutions.  Tolerance as in the small cases (1e-5 of the oracle's
-condition magnitude); fp16 coefficients widen exactly, so the same bound
-applies to workload 5.
+Forward: every output of every point at every level is compared.  The oracle
+is called one level at a time on chunks of points (a one-level grid with
+that level's explicit resolution and tables, widened to fp64 level by
+level), which keeps host memory bounded and the oracle's table accesses
+cache-local; its arithmetic is the same as a call over all levels.
+Backward: every active level's whole gradient table is compared; the oracle
+accumulates each level over all points (levels in parallel threads).  Inactive levels must be exactly zero.
+
+Tolerance as in the small cases (1e-5 of the oracle's condition magnitude);
+fp16 coefficients widen exactly, so the same bound applies to the fp16
+workload.
 """
 from math import comb
 
@@ -20,6 +25,8 @@ from _harness import check_close, host
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 torch = pytest.importorskip("torch")
+
+CHUNK = 1 << 20   # points per oracle forward call
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,73 +42,142 @@ def _mods():
     return m, hg, W, oracle
 
 
-def _sample_rows(rng, n, k=3000):
-    idx = rng.choice(n, size=min(k, n), replace=False)
-    return np.sort(np.concatenate([idx, [0, n - 1]]))
+# ---------------------------------------------------------------------------
+# helpers: level slices of feature-major device outputs, per-level oracle calls
+# ---------------------------------------------------------------------------
+
+def _fm_level(t, l, has_axis):
+    """Level l of a feature-major device output as host point-major:
+    [L][F][n] -> [n][F]; [A][L][F][n] -> [n][A][F]."""
+    if has_axis:
+        return np.transpose(host(t[:, l]), (2, 0, 1))
+    return host(t[l]).T
 
 
-def _run_hermite(w, inp, mask):
-    """GPU forward + backward in the benchmark's launch configuration."""
+def _ref_level(a):
+    """The single level of a one-level oracle output ([m][1][F] or [m][A][1][F])."""
+    return a[:, 0] if a.ndim == 3 else a[:, :, 0]
+
+
+def _level_orders(packed, d, l):
+    """fp64 order tables [1][T][C(d,k)][F] of level l of an interleaved table."""
+    _, _, W, _ = _mods()
+    row = np.asarray(packed[l:l + 1], np.float64)
+    return [np.ascontiguousarray(o) for o in W.split_orders(row, d)]
+
+
+def _check_fwd_all_points(tag, n, levels, runs, oracle_level, keys):
+    """Compare every point of every level.
+
+    runs: [(label, mask, {key: (device tensor, has_axis)})] -- several GPU runs
+    (e.g. the coarse-to-fine masks) against one oracle pass.
+    oracle_level(l, lo, hi): one-level oracle outputs for points lo..hi.
+    Inactive levels of a run must be exactly zero."""
+    for l in levels:
+        got = []
+        for label, mask, outs in runs:
+            if (mask >> l) & 1:
+                got.append((label, {k: _fm_level(t, l, ax) for k, (t, ax) in outs.items()}))
+            else:
+                for k, (t, ax) in outs.items():
+                    sl = t[:, l] if ax else t[l]
+                    assert float(sl.abs().max()) == 0.0, f"{tag}{label}: inactive level {l} {k} not zero"
+        if not got:
+            continue
+        for lo in range(0, n, CHUNK):
+            hi = min(n, lo + CHUNK)
+            ref = oracle_level(l, lo, hi)
+            for label, outs in got:
+                for k in keys:
+                    check_close(f"{tag}{label} {k} level {l} points {lo}..{hi}", outs[k][lo:hi],
+                                _ref_level(ref[k]), _ref_level(ref["m" + k]))
+
+
+def _hermite_oracle_level(w, inp, res, hessian=False):
     m, hg, W, oracle = _mods()
-    n, d, L, F = w.n_points, w.d, w.L, w.F
-    desc = m.GridDesc(d=d, L=L, F=F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T, level_mask=mask,
+    cache = {}
+
+    def call(l, lo, hi):
+        if cache.get("l") != l:
+            cache.clear()
+            cache["l"], cache["tabs"] = l, _level_orders(inp["table"], w.d, l)
+        f = oracle.encode_fwd_hessian if hessian else oracle.encode_fwd
+        return f(w.d, w.F, [res[l]], w.log2_T, cache["tabs"], inp["coords"][lo:hi])
+    return call
+
+
+def _hermite_desc(w, mask):
+    m, hg, W, oracle = _mods()
+    return m.GridDesc(d=w.d, L=w.L, F=w.F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T, level_mask=mask,
                       dtype=m.HG_F16 if w.dtype == "f16" else m.HG_F32, layout=m.HG_FEATURE_MAJOR)
-    coords = torch.from_numpy(inp["coords"]).cuda()
-    table = torch.from_numpy(inp["table"]).cuda()
-    gamma = torch.empty((L, F, n), device="cuda")
-    dgamma = torch.empty((d, L, F, n), device="cuda")
-    lap = torch.empty((L, F, n), device="cuda")
-    hg.hg_encode_fwd(desc, n, coords, m.packed_views(table, d), gamma, dgamma, lap)
-    grad = torch.zeros(table.shape, dtype=torch.float32, device="cuda")
-    gg = torch.from_numpy(W.to_feature_major(inp["g_gamma"], False)).cuda()
-    gd = torch.from_numpy(W.to_feature_major(inp["g_dgamma"], True)).cuda()
-    gl = torch.from_numpy(W.to_feature_major(inp["g_lap"], False)).cuda()
-    hg.hg_encode_bwd(desc, n, coords, gg, gd, gl, m.packed_views(grad, d))
-    torch.cuda.synchronize()
-    del gg, gd, gl, table
-    return gamma, dgamma, lap, grad
 
 
-def _check_hermite(w, inp, mask, fwd_levels, bwd_levels, seed):
+def _run_hermite(w, dev_in, mask):
+    """GPU forward + backward in the benchmark's launch configuration; the
+    device inputs (coords, table, feature-major upstream) stay with the caller."""
     m, hg, W, oracle = _mods()
-    rng = np.random.default_rng(seed)
     n, d, L, F = w.n_points, w.d, w.L, w.F
-    res = oracle.level_resolutions(L, w.n_min, w.n_max)
-    gamma, dgamma, lap, grad = _run_hermite(w, inp, mask)
-    T = 1 << w.log2_T[0]
-    # forward on sampled points, selected levels (a reduced grid for the oracle)
-    rows = _sample_rows(rng, n)
-    lv = list(fwd_levels)
-    sub_res = [res[l] for l in lv]
-    sub_tabs = [np.ascontiguousarray(o[lv], np.float64) for o in W.split_orders(inp["table"], d)]
-    sub_mask = sum(1 << i for i, l in enumerate(lv) if (mask >> l) & 1)
-    ref = oracle.encode_fwd(d, F, sub_res, w.log2_T, sub_tabs, inp["coords"][rows], level_mask=sub_mask)
-    del sub_tabs
-    ri = torch.from_numpy(rows).cuda()
-    for i, l in enumerate(lv):
-        g = host(gamma[l][:, ri]).T            # [rows][F]
-        check_close(f"gamma level {l}", g, ref["gamma"][:, i], ref["mgamma"][:, i])
-        lp = host(lap[l][:, ri]).T
-        check_close(f"lap level {l}", lp, ref["lap"][:, i], ref["mlap"][:, i])
-        for j in range(d):
-            dg = host(dgamma[j, l][:, ri]).T
-            check_close(f"dgamma{j} level {l}", dg, ref["dgamma"][:, j, i], ref["mdgamma"][:, j, i])
-    # backward on whole levels
-    want = oracle.encode_bwd_levels(d, F, res, w.log2_T, inp["coords"], inp["g_gamma"], inp["g_dgamma"],
-                                    inp["g_lap"], levels=[l for l in bwd_levels if (mask >> l) & 1])
-    for l, (gk, mk) in want.items():
-        got = W.split_orders(host(grad[l]).reshape(1, T, 1 << d, F), d)
-        for k in range(d + 1):
-            check_close(f"grad level {l} order {k}", got[k][0], gk[k], mk[k])
-    # inactive levels: zero outputs, zero gradients
-    for l in range(L):
-        if not (mask >> l) & 1:
-            assert float(gamma[l].abs().max()) == 0.0 and float(lap[l].abs().max()) == 0.0
-            assert float(dgamma[:, l].abs().max()) == 0.0
-            assert float(grad[l].abs().max()) == 0.0
+    desc = _hermite_desc(w, mask)
+    gamma = torch.full((L, F, n), float("nan"), device="cuda")
+    dgamma = torch.full((d, L, F, n), float("nan"), device="cuda")
+    lap = torch.full((L, F, n), float("nan"), device="cuda")
+    hg.hg_encode_fwd(desc, n, dev_in["coords"], m.packed_views(dev_in["table"], d), gamma, dgamma, lap)
+    grad = torch.zeros(dev_in["table"].shape, dtype=torch.float32, device="cuda")
+    hg.hg_encode_bwd(desc, n, dev_in["coords"], dev_in["gg"], dev_in["gd"], dev_in["gl"], m.packed_views(grad, d))
+    torch.cuda.synchronize()
+    return {"gamma": (gamma, False), "dgamma": (dgamma, True), "lap": (lap, False)}, grad
+
+
+def _hermite_device_inputs(w, inp):
+    m, hg, W, oracle = _mods()
+    return {"coords": torch.from_numpy(inp["coords"]).cuda(), "table": torch.from_numpy(inp["table"]).cuda(),
+            "gg": torch.from_numpy(W.to_feature_major(inp["g_gamma"], False)).cuda(),
+            "gd": torch.from_numpy(W.to_feature_major(inp["g_dgamma"], True)).cuda(),
+            "gl": torch.from_numpy(W.to_feature_major(inp["g_lap"], False)).cuda()}
+
+
+def _check_hermite_bwd_all_levels(tag, w, inp, res, grads_by_run, group, bwd=None):
+    """Every active level of every run's packed gradient table against the
+    oracle's level gradient (computed once per level, `group` levels at a time).
+    grads_by_run: [(label, mask, device grad [L][T][2^d][F])]."""
+    m, hg, W, oracle = _mods()
+    d, F, T = w.d, w.F, 1 << w.log2_T[0]
+    todo = [l for l in range(w.L) if any((mask >> l) & 1 for _, mask, _ in grads_by_run)]
+    for label, mask, grad in grads_by_run:
+        for l in range(w.L):
+            if not (mask >> l) & 1:
+                assert float(grad[l].abs().max()) == 0.0, f"{tag}{label}: inactive level {l} has gradients"
+    for i in range(0, len(todo), group):
+        levels = todo[i:i + group]
+        if bwd is None:
+            want = oracle.encode_bwd_levels(d, F, res, w.log2_T, inp["coords"], inp["g_gamma"], inp["g_dgamma"],
+                                            inp["g_lap"], levels=levels)
+        else:
+            want = bwd(levels)
+        for l in levels:
+            gk, mk = want[l]
+            for label, mask, grad in grads_by_run:
+                if not (mask >> l) & 1:
+                    continue
+                got = W.split_orders(host(grad[l]).reshape(1, T, 1 << d, F), d)
+                for k in range(d + 1):
+                    check_close(f"{tag}{label} grad level {l} order {k}", got[k][0], gk[k], mk[k])
+        del want
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def workload4():
+    m, hg, W, oracle = _mods()
+    return W.WORKLOADS[4], W.make(W.WORKLOADS[4])
 
 
 def test_fullsize_2d_linear_ingp():
+    """The d-linear Instant-NGP workload (2^20 points, 16 levels, T = 2^19):
+    every point forward, the whole gradient table backward."""
     m, hg, W, oracle = _mods()
     w = W.WORKLOADS[2]
     inp = W.make(w)
@@ -110,63 +186,96 @@ def test_fullsize_2d_linear_ingp():
     desc = m.GridDesc(d=d, L=L, F=F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T * 3, layout=m.HG_FEATURE_MAJOR)
     coords = torch.from_numpy(inp["coords"]).cuda()
     table = torch.from_numpy(inp["table"]).cuda()
-    gamma = torch.empty((L, F, n), device="cuda")
+    gamma = torch.full((L, F, n), float("nan"), device="cuda")
     hg.hg_linear_fwd(desc, n, coords, m.linear_view(table), gamma)
     grad = torch.zeros_like(table)
     hg.hg_linear_bwd(desc, n, coords, torch.from_numpy(W.to_feature_major(inp["g_gamma"], False)).cuda(),
                      m.linear_view(grad))
     torch.cuda.synchronize()
-    rng = np.random.default_rng(20)
-    rows = _sample_rows(rng, n, 20000)
-    want, mag = oracle.linear_fwd(d, F, res, w.log2_T[0], inp["table"], inp["coords"][rows])
-    got = W.from_feature_major(host(gamma[:, :, torch.from_numpy(rows).cuda()]), False)
-    check_close("linear gamma", got, want, mag)
+
+    def level(l, lo, hi):
+        g, mg = oracle.linear_fwd(d, F, [res[l]], w.log2_T[0], np.asarray(inp["table"][l:l + 1], np.float64),
+                                  inp["coords"][lo:hi])
+        return {"gamma": g, "mgamma": mg}
+
+    _check_fwd_all_points("", n, range(L), [("", (1 << L) - 1, {"gamma": (gamma, False)})], level, ("gamma",))
     gw, gm = oracle.linear_bwd(d, F, res, w.log2_T[0], inp["coords"], inp["g_gamma"])
     check_close("linear grad", host(grad), gw, gm)
 
 
-def test_fullsize_2d_hermite_pinn():
+@pytest.mark.parametrize("cfg", [3, 10], ids=["stratum_order", "shuffled"])
+def test_fullsize_2d_hermite_pinn(cfg):
+    """The PINN-sized 2D Hermite workload (2^20 stratified points, 16
+    levels, 14 one-to-one), in stratum order (consecutive points share cells:
+    the backward sums their runs in the warp) and shuffled (no runs): every
+    point and level forward, every level backward."""
     m, hg, W, oracle = _mods()
-    w = W.WORKLOADS[3]
-    _check_hermite(w, W.make(w), (1 << w.L) - 1, fwd_levels=range(w.L), bwd_levels=range(w.L), seed=30)
-
-
-def test_fullsize_3d_hermite():
-    m, hg, W, oracle = _mods()
-    w = W.WORKLOADS[4]
-    # levels 0-6 are one-to-one, 7-15 hashed (T = 2^19)
-    _check_hermite(w, W.make(w), (1 << w.L) - 1, fwd_levels=range(w.L), bwd_levels=(0, 6, 7, 15), seed=40)
-
-
-@pytest.fixture(scope="module")
-def workload5():
-    m, hg, W, oracle = _mods()
-    return W.WORKLOADS[5], W.make(W.WORKLOADS[5])
-
-
-@pytest.mark.parametrize("active", [4, 10, 16])
-def test_fullsize_3d_hermite_fp16_coarse_to_fine(workload5, active):
-    w, inp = workload5
-    mask = (1 << active) - 1
-    bwd = {4: (3,), 10: (9,), 16: (15,)}[active]
-    _check_hermite(w, inp, mask, fwd_levels=(0, 3, 4, 9, 10, 15), bwd_levels=bwd, seed=50 + active)
-
-
-def test_fullsize_3d_hermite_hessian():
-    """The full-Hessian forward and backward on the 3D workload (2^21 points,
-    16 levels), packed table, feature-major outputs."""
-    m, hg, W, oracle = _mods()
-    w = W.WORKLOADS[4]
+    w = W.WORKLOADS[cfg]
     inp = W.make(w)
+    res = oracle.level_resolutions(w.L, w.n_min, w.n_max)
+    full = (1 << w.L) - 1
+    outs, grad = _run_hermite(w, _hermite_device_inputs(w, inp), full)
+    _check_fwd_all_points("", w.n_points, range(w.L), [("", full, outs)], _hermite_oracle_level(w, inp, res),
+                          ("gamma", "dgamma", "lap"))
+    _check_hermite_bwd_all_levels("", w, inp, res, [("", full, grad)], group=16)
+
+
+def test_fullsize_3d_hermite(workload4):
+    """The 3D Hermite workload of the headline (2^21 points, 16 levels,
+    levels 0-6 one-to-one, 7-15 hashed): every point and level forward,
+    every level backward."""
+    w, inp = workload4
+    m, hg, W, oracle = _mods()
+    res = oracle.level_resolutions(w.L, w.n_min, w.n_max)
+    full = (1 << w.L) - 1
+    dev_in = _hermite_device_inputs(w, inp)
+    outs, grad = _run_hermite(w, dev_in, full)
+    del dev_in
+    _check_fwd_all_points("", w.n_points, range(w.L), [("", full, outs)], _hermite_oracle_level(w, inp, res),
+                          ("gamma", "dgamma", "lap"))
+    del outs
+    _check_hermite_bwd_all_levels("", w, inp, res, [("", full, grad)], group=16)
+
+
+def test_fullsize_3d_hermite_fp16_coarse_to_fine():
+    """The large fp16 workload (2^23 points, 16 levels, T = 2^22) at the three
+    coarse-to-fine masks L_active = 4, 10, 16: every point and active level
+    forward and every active level backward of each run, against one oracle
+    pass; inactive levels exactly zero."""
+    m, hg, W, oracle = _mods()
+    w = W.WORKLOADS[5]
+    inp = W.make(w)
+    res = oracle.level_resolutions(w.L, w.n_min, w.n_max)
+    dev_in = _hermite_device_inputs(w, inp)
+    runs, grads = [], []
+    for active in (4, 10, 16):
+        mask = (1 << active) - 1
+        outs, grad = _run_hermite(w, dev_in, mask)
+        runs.append((f" L_active={active}", mask, outs))
+        grads.append((f" L_active={active}", mask, grad))
+    del dev_in
+    _check_fwd_all_points("", w.n_points, range(w.L), runs, _hermite_oracle_level(w, inp, res),
+                          ("gamma", "dgamma", "lap"))
+    del runs
+    # 1 GB of oracle gradient and magnitude per level, all levels in parallel threads
+    _check_hermite_bwd_all_levels("", w, inp, res, grads, group=16)
+
+
+def test_fullsize_3d_hermite_hessian(workload4):
+    """The full-Hessian forward and backward on the 3D workload (2^21 points,
+    16 levels), packed table, feature-major outputs: every point and level
+    forward, every level backward."""
+    w, inp = workload4
+    m, hg, W, oracle = _mods()
     n, d, L, F = w.n_points, w.d, w.L, w.F
     P = d * (d + 1) // 2
     res = oracle.level_resolutions(L, w.n_min, w.n_max)
-    desc = m.GridDesc(d=d, L=L, F=F, n_min=w.n_min, n_max=w.n_max, log2_T=w.log2_T, layout=m.HG_FEATURE_MAJOR)
+    desc = _hermite_desc(w, (1 << L) - 1)
     coords = torch.from_numpy(inp["coords"]).cuda()
     table = torch.from_numpy(inp["table"]).cuda()
-    gamma = torch.empty((L, F, n), device="cuda")
-    dgamma = torch.empty((d, L, F, n), device="cuda")
-    hess = torch.empty((P, L, F, n), device="cuda")
+    gamma = torch.full((L, F, n), float("nan"), device="cuda")
+    dgamma = torch.full((d, L, F, n), float("nan"), device="cuda")
+    hess = torch.full((P, L, F, n), float("nan"), device="cuda")
     hg.hg_encode_fwd_hessian(desc, n, coords, m.packed_views(table, d), gamma, dgamma, hess)
     gh = W.draw_upstream_hessian(np.random.default_rng(61), w)
     grad = torch.zeros(table.shape, dtype=torch.float32, device="cuda")
@@ -175,37 +284,43 @@ def test_fullsize_3d_hermite_hessian():
     hg.hg_encode_bwd_hessian(desc, n, coords, up[0], up[1], up[2], m.packed_views(grad, d))
     torch.cuda.synchronize()
     del up, table
-    rng = np.random.default_rng(60)
-    rows = _sample_rows(rng, n)
-    ref = oracle.encode_fwd_hessian(d, F, res, w.log2_T, W.split_orders(inp["table"], d), inp["coords"][rows])
-    ri = torch.from_numpy(rows).cuda()
-    check_close("gamma", W.from_feature_major(host(gamma[:, :, ri]), False), ref["gamma"], ref["mgamma"])
-    check_close("dgamma", W.from_feature_major(host(dgamma[:, :, :, ri]), True), ref["dgamma"], ref["mdgamma"])
-    check_close("hess", W.from_feature_major(host(hess[:, :, :, ri]), True), ref["hess"], ref["mhess"])
-    levels = (0, 6, 7, 15)
-    grads, mags = oracle.encode_bwd_hessian(d, F, res, w.log2_T, inp["coords"], inp["g_gamma"], inp["g_dgamma"], gh,
-                                            levels=levels)
-    T = 1 << w.log2_T[0]
-    for l in levels:
-        got = W.split_orders(host(grad[l]).reshape(1, T, 1 << d, F), d)
-        for k in range(d + 1):
-            check_close(f"grad level {l} order {k}", got[k][0], grads[k][l], mags[k][l])
+    outs = {"gamma": (gamma, False), "dgamma": (dgamma, True), "hess": (hess, True)}
+    _check_fwd_all_points("", n, range(L), [("", (1 << L) - 1, outs)], _hermite_oracle_level(w, inp, res, True),
+                          ("gamma", "dgamma", "hess"))
+    del outs, gamma, dgamma, hess
+
+    def bwd(levels):
+        grads, mags = oracle.encode_bwd_hessian(d, F, res, w.log2_T, inp["coords"], inp["g_gamma"], inp["g_dgamma"],
+                                                gh, levels=levels)
+        return {l: ([g[l] for g in grads], [mm[l] for mm in mags]) for l in levels}
+
+    _check_hermite_bwd_all_levels("hessian", w, inp, res, [("", (1 << L) - 1, grad)], group=16, bwd=bwd)
 
 
 def test_fullsize_4d_hermite_spacetime():
     """The 4D space-time workload (2^20 points, 16 levels, 128-byte packed
     rows): lane-quad forward and lane-octet backward, benchmark launch
-    configuration; dense levels 0-2 and hashed levels above."""
+    configuration; dense levels 0-2 and hashed levels above; every point and
+    level forward, every level backward."""
     m, hg, W, oracle = _mods()
     w = W.WORKLOADS[6]
-    _check_hermite(w, W.make(w), (1 << w.L) - 1, fwd_levels=range(w.L), bwd_levels=(0, 2, 3, 15), seed=70)
+    inp = W.make(w)
+    res = oracle.level_resolutions(w.L, w.n_min, w.n_max)
+    full = (1 << w.L) - 1
+    dev_in = _hermite_device_inputs(w, inp)
+    outs, grad = _run_hermite(w, dev_in, full)
+    del dev_in
+    _check_fwd_all_points("", w.n_points, range(w.L), [("", full, outs)], _hermite_oracle_level(w, inp, res),
+                          ("gamma", "dgamma", "lap"))
+    del outs
+    _check_hermite_bwd_all_levels("", w, inp, res, [("", full, grad)], group=16)
 
 
 def test_fullsize_3d_linear_fd():
-    """INGP-FD on workload 4's grid (2^21 points, 16 levels, T = 2^19): gamma
-    and the six stencil encodings forward, their upstream backward, as the
-    benchmark launches them; sampled points forward, whole levels backward
-    (levels 0-6 one-to-one and privatised or direct, 7-15 hashed)."""
+    """INGP-FD on the 3D grid (2^21 points, 16 levels, T = 2^19): gamma and
+    the six stencil encodings forward, their upstream backward, as the
+    benchmark launches them; every point and level forward, every level
+    backward (levels 0-6 one-to-one and privatised or direct, 7-15 hashed)."""
     m, hg, W, oracle = _mods()
     w = W.WORKLOADS[7]
     inp = W.make(w)
@@ -215,32 +330,33 @@ def test_fullsize_3d_linear_fd():
                       layout=m.HG_FEATURE_MAJOR)
     coords = torch.from_numpy(inp["coords"]).cuda()
     table = torch.from_numpy(inp["table"]).cuda()
-    gamma = torch.empty((L, F, n), device="cuda")
-    stencil = torch.empty((2 * d, L, F, n), device="cuda")
+    gamma = torch.full((L, F, n), float("nan"), device="cuda")
+    stencil = torch.full((2 * d, L, F, n), float("nan"), device="cuda")
     hg.hg_linear_fd_fwd(desc, n, coords, w.eps, m.linear_view(table), gamma, None, None, stencil)
     grad = torch.zeros_like(table)
     hg.hg_linear_fd_bwd(desc, n, coords, w.eps, torch.from_numpy(W.to_feature_major(inp["g_gamma"], False)).cuda(),
                         None, None, torch.from_numpy(W.to_feature_major(inp["g_stencil"], True)).cuda(),
                         m.linear_view(grad))
     torch.cuda.synchronize()
-    rows = _sample_rows(np.random.default_rng(80), n, 20000)
-    ref = oracle.linear_fd_fwd(d, F, res, w.log2_T[0], inp["table"], inp["coords"][rows], w.eps)
-    ri = torch.from_numpy(rows).cuda()
-    check_close("gamma", W.from_feature_major(host(gamma[:, :, ri]), False), ref["gamma"], ref["mgamma"])
-    check_close("stencil", W.from_feature_major(host(stencil[:, :, :, ri]), True), ref["stencil"], ref["mstencil"])
-    levels = (0, 6, 7, 15)
+
+    def level(l, lo, hi):
+        return oracle.linear_fd_fwd(d, F, [res[l]], w.log2_T[0], np.asarray(inp["table"][l:l + 1], np.float64),
+                                    inp["coords"][lo:hi], w.eps)
+
+    _check_fwd_all_points("", n, range(L), [("", (1 << L) - 1, {"gamma": (gamma, False), "stencil": (stencil, True)})],
+                          level, ("gamma", "stencil"))
     want, mag = oracle.linear_fd_bwd(d, F, res, w.log2_T[0], inp["coords"], w.eps, g_gamma=inp["g_gamma"],
-                                     g_stencil=inp["g_stencil"], levels=levels)
+                                     g_stencil=inp["g_stencil"])
     got = host(grad)
-    for l in levels:
+    for l in range(L):
         check_close(f"grad level {l}", got[l], want[l], mag[l])
 
 
-@pytest.mark.parametrize("cfg,levels", [(8, (0, 3)), (9, (0, 3))])
-def test_fullsize_dinf_rbf(cfg, levels):
+@pytest.mark.parametrize("cfg", [8, 9])
+def test_fullsize_dinf_rbf(cfg):
     """The DInf-Grid Gaussian-RBF workloads (2D: 2^20 stratified points, 4
     dense levels up to 512; 3D: 2^21 points, up to 56; eps = 1, 3 rings) as
-    the benchmark launches them: sampled points forward, whole levels
+    the benchmark launches them: every point and level forward, every level
     backward (the coarsest privatised, the finest direct)."""
     m, hg, W, oracle = _mods()
     w = W.WORKLOADS[cfg]
@@ -251,39 +367,40 @@ def test_fullsize_dinf_rbf(cfg, levels):
                       layout=m.HG_FEATURE_MAJOR)
     coords = torch.from_numpy(inp["coords"]).cuda()
     table = torch.from_numpy(inp["table"]).cuda()
-    gamma = torch.empty((L, F, n), device="cuda")
-    dgamma = torch.empty((d, L, F, n), device="cuda")
-    lap = torch.empty((L, F, n), device="cuda")
+    gamma = torch.full((L, F, n), float("nan"), device="cuda")
+    dgamma = torch.full((d, L, F, n), float("nan"), device="cuda")
+    lap = torch.full((L, F, n), float("nan"), device="cuda")
     hg.hg_rbf_fwd(desc, n, coords, w.eps, w.rings, m.linear_view(table), gamma, dgamma, lap)
     grad = torch.zeros_like(table)
     up = [torch.from_numpy(W.to_feature_major(inp[k], k == "g_dgamma")).cuda() for k in ("g_gamma", "g_dgamma", "g_lap")]
     hg.hg_rbf_bwd(desc, n, coords, w.eps, w.rings, up[0], up[1], up[2], m.linear_view(grad))
     torch.cuda.synchronize()
     del up
-    rows = _sample_rows(np.random.default_rng(90 + cfg), n, 5000)
-    ref = oracle.rbf_fwd(d, F, res, w.log2_T[0], inp["table"], inp["coords"][rows], w.eps, w.rings)
-    ri = torch.from_numpy(rows).cuda()
-    check_close("gamma", W.from_feature_major(host(gamma[:, :, ri]), False), ref["gamma"], ref["mgamma"])
-    check_close("dgamma", W.from_feature_major(host(dgamma[:, :, :, ri]), True), ref["dgamma"], ref["mdgamma"])
-    check_close("lap", W.from_feature_major(host(lap[:, :, ri]), False), ref["lap"], ref["mlap"])
+
+    def level(l, lo, hi):
+        return oracle.rbf_fwd(d, F, [res[l]], w.log2_T[0], np.asarray(inp["table"][l:l + 1], np.float64),
+                              inp["coords"][lo:hi], w.eps, w.rings)
+
+    outs = {"gamma": (gamma, False), "dgamma": (dgamma, True), "lap": (lap, False)}
+    _check_fwd_all_points("", n, range(L), [("", (1 << L) - 1, outs)], level, ("gamma", "dgamma", "lap"))
     want, mag = oracle.rbf_bwd(d, F, res, w.log2_T[0], inp["coords"], w.eps, w.rings, g_gamma=inp["g_gamma"],
-                               g_dgamma=inp["g_dgamma"], g_lap=inp["g_lap"], levels=levels)
+                               g_dgamma=inp["g_dgamma"], g_lap=inp["g_lap"])
     got = host(grad)
-    for l in levels:
+    for l in range(L):
         check_close(f"grad level {l}", got[l], want[l], mag[l])
 
 
 def test_fullsize_siren_consumer():
     """The SIREN consumer in the benchmark's launch configuration: 2^21
     points, d = 3, K = L F = 32, H = 64, O = 1, omega = 30, inputs in the
-    encoder's feature-major layout.  Per-point outputs (u, grad u, lap u and
-    the input gradients) on sampled points, to 1e-5 of the oracle's magnitude;
-    the weight gradients whole, against the oracle summed over chunks of
-    points.  Those are sums over 2^21 points: a CTA accumulates its ~221 tiles
-    in shared memory (about 8 adds per tile for the output-layer and bias
-    gradients) and adds once to global memory, up to ~1900 fp32 roundings in
-    a row, whose worst-case bound is ~1.1e-4 of the magnitude -- the test
-    takes 2e-4 (the errors seen are far smaller)."""
+    encoder's feature-major layout.  Every point's outputs (u, grad u, lap u
+    and the input gradients) to 1e-5 of the oracle's magnitude; the weight
+    gradients whole, against the oracle summed over chunks of points.  Those
+    are sums over 2^21 points: a CTA accumulates its ~221 tiles in shared
+    memory (about 8 adds per tile for the output-layer and bias gradients) and
+    adds once to global memory, up to ~1900 fp32 roundings in a row, whose
+    worst-case bound is ~1.1e-4 of the magnitude -- the test takes 2e-4 (the
+    errors seen are far smaller)."""
     m, hg, W, oracle = _mods()
     n, d, L, F = 1 << 21, 3, 16, 2
     K, H, O = L * F, W.SIREN_H, W.SIREN_O
@@ -301,28 +418,29 @@ def test_fullsize_siren_consumer():
     fin = [fm(feats[k]) for k in ("gamma", "dgamma", "lap")]
     wts = [torch.from_numpy(sw[k]).cuda() for k in ("W1", "b1", "W2", "b2")]
     ups = [fm(sup[k]) for k in ("g_u", "g_du", "g_lapu")]
-    u, du, lu = (torch.empty(sh, device="cuda") for sh in ((O, n), (d, O, n), (O, n)))
+    u, du, lu = (torch.full(sh, float("nan"), device="cuda") for sh in ((O, n), (d, O, n), (O, n)))
     hg.hg_siren_fwd(desc, n, *fin, *wts, u, du, lu)
-    gin = [torch.empty_like(t) for t in fin]
+    gin = [torch.full_like(t, float("nan")) for t in fin]
     wg = [torch.zeros(sh, device="cuda") for sh in ((H, K), (H,), (O, H), (O,))]
     hg.hg_siren_bwd(desc, n, *fin, *wts[:3], *ups, *gin, *wg)
     torch.cuda.synchronize()
     del fin, ups
-    idx = _sample_rows(rng, n, 4096)
-    sub = {k: v[idx] for k, v in feats.items()}
-    ref = oracle.siren_fwd(omega=W.SIREN_OMEGA, **sub, **sw)
-    for name, t in (("u", u), ("du", du), ("lapu", lu)):
-        check_close(name, np.moveaxis(host(t), -1, 0)[idx], ref[name], ref["m" + name])
-    ref = oracle.siren_bwd(omega=W.SIREN_OMEGA, **sub, **sw, **{k: v[idx] for k, v in sup.items()})
-    for name, t in (("g_gamma", gin[0]), ("g_dgamma", gin[1]), ("g_lap", gin[2])):
-        check_close(name, np.moveaxis(host(t), -1, 0)[idx], ref[name], ref["m" + name])
+    outs = {name: np.moveaxis(host(t), -1, 0) for name, t in (("u", u), ("du", du), ("lapu", lu))}
+    gins = {name: np.moveaxis(host(t), -1, 0) for name, t in (("g_gamma", gin[0]), ("g_dgamma", gin[1]),
+                                                              ("g_lap", gin[2]))}
     keys = ("gW1", "gb1", "gW2", "gb2")
     tot = {k: 0.0 for k in keys}
     mag = {k: 0.0 for k in keys}
     step = 1 << 17
     for lo in range(0, n, step):
-        r = oracle.siren_bwd(omega=W.SIREN_OMEGA, **{k: v[lo:lo + step] for k, v in feats.items()}, **sw,
-                             **{k: v[lo:lo + step] for k, v in sup.items()})
+        hi = lo + step
+        sub = {k: v[lo:hi] for k, v in feats.items()}
+        ref = oracle.siren_fwd(omega=W.SIREN_OMEGA, **sub, **sw)
+        for name in ("u", "du", "lapu"):
+            check_close(f"{name} points {lo}..{hi}", outs[name][lo:hi], ref[name], ref["m" + name])
+        r = oracle.siren_bwd(omega=W.SIREN_OMEGA, **sub, **sw, **{k: v[lo:hi] for k, v in sup.items()})
+        for name in ("g_gamma", "g_dgamma", "g_lap"):
+            check_close(f"{name} points {lo}..{hi}", gins[name][lo:hi], r[name], r["m" + name])
         for k in keys:
             tot[k] = tot[k] + r[k]
             mag[k] = mag[k] + r["m" + k]

@@ -283,3 +283,40 @@ def test_zero_points_is_a_no_op():
     hg.hg_linear_bwd(desc, 0, None, None, m.linear_view(lin))
     torch.cuda.synchronize()
     assert float(t.abs().sum()) == 0.0 and float(lin.abs().sum()) == 0.0
+
+
+@pytest.mark.parametrize("mask", [None, 0b1011], ids=["all_levels", "mask_1011"])
+def test_fp16_pipelined_forward_steady_state(mask):
+    """The fp16 3D F = 2 packed forward is a persistent kernel: a CTA of 128
+    threads walks 64-point batches, copying batch b + gridDim.x into the
+    other shared-memory stage while it blends batch b.  Its grid holds at
+    most (SMs x CTAs per SM) CTAs, and CTAs per SM are at most the SM's
+    thread limit / 128.  With 2^19 points every CTA walks at least three
+    batches, so the prefetch and the stage toggle run; every output
+    (Laplacian and full-Hessian forwards) is compared with the oracle."""
+    m, W, oracle = _mods()
+    from multiresolution_hash_grid_02_b300 import hg
+    from test_hessian_gpu import gpu_hessian_fwd
+    n, d, L, F, nmin, nmax, log2T = 1 << 19, 3, 4, 2, 4, 64, 12
+    props = torch.cuda.get_device_properties(0)
+    max_ctas = props.multi_processor_count * (props.max_threads_per_multi_processor // 128)
+    assert (n + 63) // 64 >= 3 * max_ctas
+    rng = np.random.default_rng(1902)
+    res = oracle.level_resolutions(L, nmin, nmax)
+    coords = _coords(rng, n, d, res)
+    table = (rng.random((L, 1 << log2T, 1 << d, F), dtype=np.float32) * 2 - 1).astype(np.float16)
+    orders = W.split_orders(table, d)
+    t_dev = dev(table)
+    views = m.packed_views(t_dev, d)
+    desc = m.GridDesc(d=d, L=L, F=F, n_min=nmin, n_max=nmax, log2_T=(log2T,) * 4, level_mask=mask,
+                      dtype=m.HG_F16, layout=m.HG_FEATURE_MAJOR)
+    ref = oracle.encode_fwd(d, F, res, (log2T,) * 4, orders, coords, level_mask=mask)
+    g, dg, lp = gpu_hermite_fwd(desc, coords, views)
+    check_close("gamma", g, ref["gamma"], ref["mgamma"])
+    check_close("dgamma", dg, ref["dgamma"], ref["mdgamma"])
+    check_close("lap", lp, ref["lap"], ref["mlap"])
+    ref = oracle.encode_fwd_hessian(d, F, res, (log2T,) * 4, orders, coords, level_mask=mask)
+    g, dg, h = gpu_hessian_fwd(desc, coords, views)
+    check_close("hessian gamma", g, ref["gamma"], ref["mgamma"])
+    check_close("hessian dgamma", dg, ref["dgamma"], ref["mdgamma"])
+    check_close("hess", h, ref["hess"], ref["mhess"])
