@@ -35,8 +35,13 @@ def _f64(*arrays):
     return [None if a is None else np.asarray(a, np.float64) for a in arrays]
 
 
-def siren_fwd(gamma, dgamma, lap, W1, b1, W2, b2, omega, with_mags=True):
-    """u, grad u and lap u of the SIREN at the encoder outputs ("关键设计 2")."""
+def siren_fwd(gamma, dgamma, lap, W1, b1, W2, b2, omega, with_mags=True, mgamma=None, mdgamma=None, mlap=None):
+    """u, grad u and lap u of the SIREN at the encoder outputs ("关键设计 2").
+
+    The magnitudes treat the inputs as exact unless their own condition
+    magnitudes are given (mgamma, mdgamma, mlap: same shapes, e.g. the
+    encoder oracle's), in which case those replace |gamma|, |dgamma|, |lap|
+    and the returned magnitudes are those of the composed evaluation."""
     gamma, dgamma, lap, W1, b1, W2, b2 = _f64(gamma, dgamma, lap, W1, b1, W2, b2)
     z = gamma @ W1.T + b1                      # [n][H]
     a = np.sin(omega * z)
@@ -49,9 +54,12 @@ def siren_fwd(gamma, dgamma, lap, W1, b1, W2, b2, omega, with_mags=True):
     out = {"u": u, "du": du, "lapu": lapu}
     if with_mags:
         A = np.abs
-        mz = A(gamma) @ A(W1).T + A(b1)
-        my = A(dgamma) @ A(W1).T
-        ms = A(lap) @ A(W1).T
+        mg = A(gamma) if mgamma is None else np.asarray(mgamma, np.float64)
+        mdg = A(dgamma) if mdgamma is None else np.asarray(mdgamma, np.float64)
+        ml = A(lap) if mlap is None else np.asarray(mlap, np.float64)
+        mz = mg @ A(W1).T + A(b1)
+        my = mdg @ A(W1).T
+        ms = ml @ A(W1).T
         ma = A(a) + omega * mz
         mc = A(c) + omega * mz
         y2 = (y ** 2).sum(axis=1)

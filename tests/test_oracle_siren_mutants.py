@@ -27,6 +27,9 @@ MUTANTS = [
     ("backward: first-layer gradient pairs gamma with lap", "\"gW1\": g_z.T @ gamma", "\"gW1\": g_z.T @ lap"),
     ("backward: output bias from the Laplacian upstream", "\"gb2\": gu.sum(axis=0)", "\"gb2\": glu.sum(axis=0)"),
     ("backward: lap-gamma gradient without the cosine", "g_s = omega * c * P", "g_s = omega * P"),
+    ("forward magnitudes ignore the input magnitudes", "mz = mg @ A(W1).T + A(b1)", "mz = A(gamma) @ A(W1).T + A(b1)"),
+    ("forward magnitudes ignore the gradient-input magnitudes", "my = mdg @ A(W1).T\n        ms = ml",
+     "my = A(dgamma) @ A(W1).T\n        ms = ml"),
 ]
 
 

@@ -141,3 +141,45 @@ def test_siren_magnitudes_bound_values(oracle_mod):
     b = oracle_mod.siren_bwd(omega=OMEGA, **inp, **up)
     for k in ("g_gamma", "g_dgamma", "g_lap", "gW1", "gb1", "gW2", "gb2"):
         assert np.all(np.abs(b[k]) <= b["m" + k] * (1 + 1e-12)), k
+
+
+def test_siren_input_magnitudes_bound_input_perturbations(oracle_mod):
+    """Given condition magnitudes of its inputs (the encoder's), the forward's
+    magnitudes bound, to first order, the change of u, grad u and lap u when
+    every input moves by up to eta times its magnitude.  The worst move is
+    along the sign of each output's gradient (from the backward with a unit
+    upstream); the input magnitudes are taken ten times the inputs' size, so
+    a magnitude that ignored them is exceeded (one hidden unit, so the bound
+    is nearly reached).  With |inputs| as magnitudes
+    the defaults come back."""
+    rng = np.random.default_rng(77)
+    # few hidden units: the magnitude's sum of absolute values over units is
+    # then close to the largest reachable change (no cancellation to hide in)
+    n, d, K, H = 256, 2, 16, 1
+    W1, b1, W2, b2 = _net(rng, K, H, 1)
+    g = rng.uniform(-0.5, 0.5, (n, K))
+    dg = rng.normal(0, 3, (n, d, K))
+    lg = rng.normal(0, 30, (n, K))
+    mags = [np.abs(a) + 10 * np.abs(a).mean() * rng.uniform(0.5, 1.0, a.shape) for a in (g, dg, lg)]
+    base = oracle_mod.siren_fwd(g, dg, lg, W1, b1, W2, b2, OMEGA, mgamma=mags[0], mdgamma=mags[1], mlap=mags[2])
+    eta = 1e-9
+    one, zero = np.ones((n, 1)), np.zeros((n, 1))
+    ups = {"u": (one, None, None), "lapu": (None, None, one)}
+    for i in range(d):
+        e = np.zeros((n, d, 1))
+        e[:, i] = 1.0
+        ups[f"du{i}"] = (None, e, None)
+    for key, (gu, gdu, glu) in ups.items():
+        grad = oracle_mod.siren_bwd(g, dg, lg, W1, b1, W2, b2, OMEGA, gu, gdu, glu, with_mags=False)
+        moved = [a + eta * m * np.sign(grad[k]) for a, m, k in zip((g, dg, lg), mags, ("g_gamma", "g_dgamma", "g_lap"))]
+        out = oracle_mod.siren_fwd(*moved, W1, b1, W2, b2, OMEGA, with_mags=False)
+        name = key[:2] if key.startswith("du") else key
+        sel = (slice(None), int(key[2]), 0) if key.startswith("du") else (slice(None), 0)
+        ratio = np.abs(out[name] - base[name])[sel] / (eta * base["m" + name][sel])
+        assert ratio.max() <= 1.0 + 1e-3, f"{key}: a move within the input magnitudes exceeds the output magnitude"
+        assert ratio.max() > 0.05, f"{key}: the magnitude is far above any reachable change ({ratio.max()})"
+    plain = oracle_mod.siren_fwd(g, dg, lg, W1, b1, W2, b2, OMEGA)
+    same = oracle_mod.siren_fwd(g, dg, lg, W1, b1, W2, b2, OMEGA, mgamma=np.abs(g), mdgamma=np.abs(dg),
+                                mlap=np.abs(lg))
+    for k in ("mu", "mdu", "mlapu"):
+        assert np.array_equal(plain[k], same[k])
