@@ -58,10 +58,14 @@ def parse_args():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
-    p.add_argument("--config", type=int, default=4, help="workload 1..5 (default 4: 3D Hermite, 2^21 points)")
+    p.add_argument("--config", type=int, default=4,
+                   help="workload 1..10 (default 4: 3D Hermite, 2^21 points; 10: workload 3 in shuffled order)")
     p.add_argument("--level-mask", type=lambda s: int(s, 0), default=None)
     p.add_argument("--layout", choices=["feature", "point"], default="feature")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-all-configs", action="store_true",
+                   help="skip the other workloads reported beside the headline (workloads 1, 2, 3, 3 shuffled, "
+                        "5 at L_active 4/10/16)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=1 << 20, help="points in the oracle's timed sample")
     p.add_argument("--points", type=int, default=None, help="override the workload's point count (profiling)")
@@ -78,6 +82,8 @@ def parse_args():
                    help="parse an ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum log of the benchmark "
                         "command and record per-launch DRAM traffic (with the kernel-source hash) in "
                         "profiles/dram_traffic.json, then exit")
+    p.add_argument("--record-traffic-kernel", choices=["fwd", "bwd"], default="fwd",
+                   help="which kernel the --record-traffic capture covered (one kernel per capture)")
     return p.parse_args()
 
 
@@ -140,7 +146,13 @@ def record_traffic(log_path: str, workload: str, command: str):
         data = {}
     if data.get("source_sha256") != sha or "entries" not in data:
         data = {"source_sha256": sha, "entries": {}}
-    data["entries"][workload] = {"command": command, "kernels": parse_ncu_dram_log(log_path)}
+    # one capture per kernel (forward, backward): each adds its kernels to the configuration's entry
+    entry = data["entries"].setdefault(workload, {"commands": [], "kernels": {}})
+    entry.pop("command", None)
+    entry.setdefault("commands", [])
+    if command not in entry["commands"]:
+        entry["commands"].append(command)
+    entry.setdefault("kernels", {}).update(parse_ncu_dram_log(log_path))
     os.makedirs(os.path.dirname(TRAFFIC_FILE), exist_ok=True)
     with open(TRAFFIC_FILE, "w") as f:
         json.dump(data, f, indent=1)
@@ -566,12 +578,13 @@ def main():
     if args.record_traffic:
         from multiresolution_hash_grid_02_b300 import workloads as W
         w = W.WORKLOADS[args.config]
+        kern = "hermite_bwd" if args.record_traffic_kernel == "bwd" else "hermite_fwd"
         extra = (f" --config {args.config}" if args.config != 4 else "") + (" --hessian" if args.hessian else "") + \
             (f" --points {args.points}" if args.points else "")
         record_traffic(args.record_traffic, traffic_key(w, args.points, args.hessian),
                        "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
-                       "--clock-control none -k regex:hermite -s 2 -c 2 python bench.py --steps 2 --warmup 1 "
-                       "--no-e2e --no-cpu-baseline" + extra)
+                       f"--clock-control none -k regex:{kern} -s 1 -c 1 python bench.py --steps 2 --warmup 1 "
+                       "--no-e2e --no-cpu-baseline --no-all-configs" + extra)
         return
     if args.impl == "reference":
         run_reference(args)
@@ -581,8 +594,6 @@ def main():
         return
     import torch
     import torch.distributed as dist
-    from multiresolution_hash_grid_02_b300 import hg, workloads as W
-    import multiresolution_hash_grid_02_b300 as M
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -590,15 +601,79 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from multiresolution_hash_grid_02_b300 import workloads as W
 
     w = W.WORKLOADS[args.config]
     if args.points:
         w = w.scaled(args.points)
     mask = args.level_mask if args.level_mask is not None else (1 << w.L) - 1
+    hessian = args.hessian and w.kind == "hermite"
+    line = measure_native(args, w, mask, hessian, world, rank, local, with_e2e=not args.no_e2e and rank == 0,
+                          cpu_sample=None if (args.no_cpu_baseline or rank != 0 or world > 1) else args.cpu_sample)
+    # the other workloads of the metric, each timed the same way (same steps and warm-up), reported inside
+    # the headline line so that one run records them all; the headline's own keys keep their meaning
+    if (rank == 0 and world == 1 and not args.no_all_configs and args.config == 4 and not hessian
+            and args.points is None and args.level_mask is None):
+        line["all_configs"] = all_configs(args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# the workloads reported beside the headline (workload number, active levels or None = all)
+OTHER_CONFIGS = ((1, None), (2, None), (3, None), (10, None), (5, 4), (5, 10), (5, 16))
+
+
+def all_configs(args):
+    """One compact record per other workload of the metric (the tiny 2D
+    Hermite grid, the d-linear Instant-NGP grid, the PINN grid in stratum and
+    in shuffled order, the large fp16 grid at L_active = 4, 10, 16): the
+    device-timed step with its roofline and the oracle's CPU rate on a small
+    sample.  A failure is recorded, not raised, so the headline still prints."""
+    import torch
+    from multiresolution_hash_grid_02_b300 import workloads as W
+    out = []
+    cache = {}
+    for cfg, active in OTHER_CONFIGS:
+        w = W.WORKLOADS[cfg]
+        mask = (1 << w.L) - 1 if active is None else (1 << active) - 1
+        try:
+            if cache.get("cfg") != cfg:
+                cache.clear()
+                cache["cfg"], cache["inputs"] = cfg, W.make(w)
+            ln = measure_native(args, w, mask, False, 1, 0, int(os.environ.get("LOCAL_RANK", "0")), with_e2e=False,
+                                cpu_sample=None if args.no_cpu_baseline else min(w.n_points, 1 << 15),
+                                inputs=cache["inputs"])
+            out.append({"workload": w.name, "config_index": cfg, "active_levels": bin(mask).count("1"),
+                        "value": ln["value"], "unit": ln["unit"], "ms_per_step": ln["ms_per_step"],
+                        "ms_per_step_median": ln["ms_per_step_median"], "fwd_ms": ln["kernels"]["fwd"]["ms"],
+                        "bwd_ms": ln["kernels"]["bwd"]["ms"], "fwd_frac": ln["kernels"]["fwd"]["frac"],
+                        "bwd_frac": ln["kernels"]["bwd"]["frac"], "fwd_probe": ln["kernels"]["fwd"]["probe"],
+                        "bwd_probe": ln["kernels"]["bwd"]["probe"],
+                        "roofline": {k: ln["roofline"][k] for k in ("bound", "kernel", "achieved", "peak", "unit",
+                                                                    "frac", "combined_frac", "traffic")},
+                        "cpu_baseline": ln["cpu_baseline"], "clocks": ln["clocks"], "config": ln["config"]})
+        except Exception as e:  # noqa: BLE001 -- recorded in the line
+            out.append({"workload": w.name, "config_index": cfg, "active_levels": bin(mask).count("1"),
+                        "error": f"{type(e).__name__}: {e}"})
+        torch.cuda.empty_cache()
+    return out
+
+
+def measure_native(args, w, mask, hessian, world, rank, local, with_e2e, cpu_sample, inputs=None):
+    """Time args.steps steps of one workload (after args.warmup untimed ones)
+    and return the JSON record: whole-run throughput, per-kernel medians and
+    rooflines, optional end-to-end leg and CPU baseline."""
+    import torch
+    import torch.distributed as dist
+    from multiresolution_hash_grid_02_b300 import hg, workloads as W
+    import multiresolution_hash_grid_02_b300 as M
+
     layout = M.HG_FEATURE_MAJOR if args.layout == "feature" else M.HG_POINT_MAJOR
     fm = layout == M.HG_FEATURE_MAJOR
-    inputs = W.make(w, seed=w.seed + rank)
-    hessian = args.hessian and w.kind == "hermite"
+    if inputs is None:
+        inputs = W.make(w, seed=w.seed + rank)
     if hessian:
         add_hessian_upstream(w, inputs, rank)
     n, d, L, F = w.n_points, w.d, w.L, w.F
@@ -661,18 +736,21 @@ def main():
             hg.hg_linear_bwd(desc, n, coords, gg, gviews, stream)
 
     launches_per_step = 2
-    ev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # per step: before the zeroing, before the forward, between, after the backward
+    ev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
     def step(rec=None):
-        grad.zero_()
         if rec:
             rec[0].record(stream)
-        fwd()
+        grad.zero_()
         if rec:
             rec[1].record(stream)
-        bwd()
+        fwd()
         if rec:
             rec[2].record(stream)
+        bwd()
+        if rec:
+            rec[3].record(stream)
 
     gather_pat, red_pat = kernel_patterns(w)
     gather_bytes, red_bytes = algorithmic_bytes(w, mask)
@@ -710,10 +788,10 @@ def main():
         dist.barrier()
     clocks = sampler.stop()
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, "cuda")
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev_f]
-    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev_f]
-    t_fwd = statistics.mean(fwd_ms)
-    t_bwd = statistics.mean(bwd_ms)
+    # per-launch durations: the median over the timed steps of each launch's events
+    t_fwd = statistics.median(e[1].elapsed_time(e[2]) for e in ev_f)
+    t_bwd = statistics.median(e[2].elapsed_time(e[3]) for e in ev_f)
+    t_step_med = statistics.median(e[0].elapsed_time(e[3]) for e in ev_f)
 
     total_points = n * world * args.steps
     value = total_points / (elapsed_ms * 1e-3)
@@ -733,14 +811,17 @@ def main():
                 "probe": f"{gather_pat[0]}-byte rows, {gather_pat[1]} lane(s) per row; replay of this launch's "
                          f"row stream {t_replay_g:.3f} ms = {replay_g:.0f} GB/s, uniform random rows in 32 MiB "
                          f"{uniform_g:.0f} GB/s; peak = the larger",
-                "what": "compulsory coefficient bytes gathered / launch time vs the larger measured ceiling"},
+                "what": "compulsory coefficient bytes gathered / median launch time vs the larger measured ceiling"},
         "bwd": {"ms": t_bwd, "bound": "l2", "achieved": bwd_gbs, "peak": red_peak, "unit": "GB/s",
                 "frac": bwd_gbs / red_peak, "algorithmic_bytes": red_bytes,
                 "probe": f"{red_pat[0]}-byte rows, {red_pat[1]} lane(s) per row; replay of this launch's "
                          f"row stream {t_replay_r:.3f} ms = {replay_r:.0f} GB/s, uniform random rows in 32 MiB "
                          f"{uniform_r:.0f} GB/s; peak = the larger",
-                "what": "fp32 gradient RED payload bytes / launch time vs the larger measured ceiling"},
+                "what": "fp32 gradient RED payload bytes / median launch time vs the larger measured ceiling"},
     }
+    if hbm:
+        for key, ach in (("fwd", fwd_gbs), ("bwd", bwd_gbs)):
+            kernels[key]["frac_of_hbm_peak"] = ach / hbm
     if rbf:
         # the RBF grids are small and L1/L2-resident: the kernels are bound on chip (arithmetic latency,
         # shared-memory atomics), so the roofline is FP32 arithmetic against the FMA peak at the sampled clock
@@ -748,10 +829,11 @@ def main():
         fp32 = fp32_peak_tflops(torch, (clocks or {}).get("sm_mhz") or 2032.0)
         for key, t in (("fwd", t_fwd), ("bwd", t_bwd)):
             ach = flops / (t * 1e-3) / 1e12
+            kernels[key].pop("frac_of_hbm_peak", None)
             kernels[key].update({"bound": "alu", "achieved": ach, "peak": fp32, "unit": "TFLOP/s",
                                  "frac": ach / fp32, "algorithmic_flops": flops,
                                  "probe": "FP32 FMA peak: SMs x 128 lanes x 2 flops x median sampled SM clock",
-                                 "what": "separable-contraction flops / launch time vs the FP32 FMA peak"})
+                                 "what": "separable-contraction flops / median launch time vs the FP32 FMA peak"})
         combined = (2 * flops / (fp32 * 1e12)) / ((t_fwd + t_bwd) * 1e-3)
     dom = "bwd" if t_bwd >= t_fwd else "fwd"
     k = kernels[dom]
@@ -764,35 +846,33 @@ def main():
                                "or hg_probe_replay_red (the launch's own row addresses, lane split and vector "
                                "width, no arithmetic), and hg_probe_l2_gather / hg_probe_l2_red (uniform random "
                                "rows of the same size and split in an L2-resident 32 MiB buffer)",
-                "combined_frac": combined, "hbm_peak_gbs": hbm}
+                "combined_frac": combined, "hbm_peak_gbs": hbm,
+                "frac_of_hbm_peak": k.get("frac_of_hbm_peak")}
     if rbf:
         roofline["peak_source"] = ("FP32 FMA peak (SMs x 128 lanes x 2 flops x the median SM clock sampled during the "
                                    "timed region); achieved = the separable contraction's flops / launch time")
 
     e2e = None
-    if not args.no_e2e and rank == 0:
+    if with_e2e:
         e2e = run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, shape_s, hermite,
-                      hessian, grad, stream, shape_st)
+                      hessian, grad, stream, shape_st, steps=args.steps, warmup=max(2, args.warmup))
     cpu = None
-    if not args.no_cpu_baseline and rank == 0 and world == 1:
-        cpu = cpu_baseline(w, inputs, mask, args.cpu_sample, hessian)
+    if cpu_sample:
+        cpu = cpu_baseline(w, inputs, mask, cpu_sample, hessian)
 
-    if rank == 0:
-        line = {
-            "metric": metric_of(w, hessian), "value": value, "unit": "points/s", "n_gpus": world,
-            "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded numpy: uniform coords, uniform coefficients, N(0,1) upstream gradients)",
-            "config": describe(w, mask, args.layout, hessian),
-            "roofline": roofline, "kernels": kernels,
-            "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks,
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    return {
+        "metric": metric_of(w, hessian), "value": value, "unit": "points/s", "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "ms_per_step_median": t_step_med,
+        "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy: uniform coords, uniform coefficients, N(0,1) upstream gradients)",
+        "config": describe(w, mask, args.layout, hessian),
+        "roofline": roofline, "kernels": kernels,
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
 
 
 def run_e2e(torch, hg, M, W, w, desc, inputs, tviews, gviews, conv, shape_g, shape_d, shape_s, hermite, hessian,
@@ -980,7 +1060,7 @@ def run_siren(args):
     clocks = sampler.stop()
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, "cuda")
     names = ("encode_fwd", "siren_fwd", "siren_bwd", "encode_bwd")
-    ms = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev) for i, nm in enumerate(names)}
+    ms = {nm: statistics.median(e[i].elapsed_time(e[i + 1]) for e in ev) for i, nm in enumerate(names)}
     fp32 = fp32_peak_tflops(torch, (clocks or {}).get("sm_mhz") or 2032.0)
     fl = siren_flops(n, d, K, H)
     kernels = {
@@ -1007,7 +1087,7 @@ def run_siren(args):
     e2e = None
     if not args.no_e2e and rank == 0:
         e2e = run_e2e_siren(torch, hg, w, desc, sdesc, inputs, sup, tviews, gviews, grad, (W1, b1, W2, b2),
-                            (gW1, gb1, gW2, gb2), stream)
+                            (gW1, gb1, gW2, gb2), stream, steps=args.steps, warmup=max(2, args.warmup))
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(w, inputs, mask, min(args.cpu_sample, 1 << 17), siren=(sw, sup))

@@ -1,0 +1,79 @@
+// Hermite-NGP blends of one (point, level) on one thread.
+//
+// "Hermite-NGP: Gradient-Augmented Hash Encoding for Learning PDEs",
+// 关键设计 1 (tensor-product Hermite bases, dx^|alpha| scaling) and 关键设计 2
+// (gradient and Laplacian from the bases' derivatives).  Separable: contract
+// axis 0, then axis 1 (then axis 2), carrying value, d/dx_0 and d2/dx_0^2
+// partial sums.
+#pragma once
+
+#include "hg_device.cuh"
+#include "hg_params.h"
+
+namespace hg {
+
+// Separable 2D blend of one feature: q[corner][alpha].
+__device__ __forceinline__ void blend2(const float (&q)[4][4], const Basis1& b0, const Basis1& b1, float& g,
+                                       float (&dg)[3], float& lap) {
+    g = 0.f, dg[0] = 0.f, dg[1] = 0.f, lap = 0.f;
+#pragma unroll
+    for (int v1 = 0; v1 < 2; ++v1)
+#pragma unroll
+        for (int a1 = 0; a1 < 2; ++a1) {
+            float s = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll
+            for (int v0 = 0; v0 < 2; ++v0)
+#pragma unroll
+                for (int a0 = 0; a0 < 2; ++a0) {
+                    const float c = q[v0 + 2 * v1][a0 + 2 * a1];
+                    s = fmaf(c, b0.w[v0][a0], s);
+                    s1 = fmaf(c, b0.d1[v0][a0], s1);
+                    s2 = fmaf(c, b0.d2[v0][a0], s2);
+                }
+            g = fmaf(s, b1.w[v1][a1], g);
+            dg[0] = fmaf(s1, b1.w[v1][a1], dg[0]);
+            dg[1] = fmaf(s, b1.d1[v1][a1], dg[1]);
+            lap = fmaf(s2, b1.w[v1][a1], lap);
+            lap = fmaf(s, b1.d2[v1][a1], lap);
+        }
+}
+
+// Separable 3D blend of one feature.
+__device__ __forceinline__ void blend3(const float (&q)[8][8], const Basis1& b0, const Basis1& b1,
+                                       const Basis1& b2, float& g, float (&dg)[3], float& lap) {
+    g = 0.f, dg[0] = 0.f, dg[1] = 0.f, dg[2] = 0.f, lap = 0.f;
+#pragma unroll
+    for (int v2 = 0; v2 < 2; ++v2)
+#pragma unroll
+        for (int a2 = 0; a2 < 2; ++a2) {
+            float A = 0.f, B = 0.f, C = 0.f, Dl = 0.f;
+#pragma unroll
+            for (int v1 = 0; v1 < 2; ++v1)
+#pragma unroll
+                for (int a1 = 0; a1 < 2; ++a1) {
+                    float s = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll
+                    for (int v0 = 0; v0 < 2; ++v0)
+#pragma unroll
+                        for (int a0 = 0; a0 < 2; ++a0) {
+                            const float c = q[v0 + 2 * v1 + 4 * v2][a0 + 2 * a1 + 4 * a2];
+                            s = fmaf(c, b0.w[v0][a0], s);
+                            s1 = fmaf(c, b0.d1[v0][a0], s1);
+                            s2 = fmaf(c, b0.d2[v0][a0], s2);
+                        }
+                    A = fmaf(s, b1.w[v1][a1], A);
+                    B = fmaf(s1, b1.w[v1][a1], B);
+                    C = fmaf(s, b1.d1[v1][a1], C);
+                    Dl = fmaf(s2, b1.w[v1][a1], Dl);
+                    Dl = fmaf(s, b1.d2[v1][a1], Dl);
+                }
+            g = fmaf(A, b2.w[v2][a2], g);
+            dg[0] = fmaf(B, b2.w[v2][a2], dg[0]);
+            dg[1] = fmaf(C, b2.w[v2][a2], dg[1]);
+            dg[2] = fmaf(A, b2.d1[v2][a2], dg[2]);
+            lap = fmaf(Dl, b2.w[v2][a2], lap);
+            lap = fmaf(A, b2.d2[v2][a2], lap);
+        }
+}
+
+}  // namespace hg

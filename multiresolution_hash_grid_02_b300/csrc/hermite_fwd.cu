@@ -17,76 +17,13 @@
 
 #include <algorithm>
 
+#include "hermite_blend.cuh"
 #include "hg_device.cuh"
 
 namespace hg {
 namespace {
 
 constexpr int kBlock = 256;
-
-// Separable 2D blend of one feature: q[corner][alpha].
-__device__ __forceinline__ void blend2(const float (&q)[4][4], const Basis1& b0, const Basis1& b1, float& g,
-                                       float (&dg)[3], float& lap) {
-    g = 0.f, dg[0] = 0.f, dg[1] = 0.f, lap = 0.f;
-#pragma unroll
-    for (int v1 = 0; v1 < 2; ++v1)
-#pragma unroll
-        for (int a1 = 0; a1 < 2; ++a1) {
-            float s = 0.f, s1 = 0.f, s2 = 0.f;
-#pragma unroll
-            for (int v0 = 0; v0 < 2; ++v0)
-#pragma unroll
-                for (int a0 = 0; a0 < 2; ++a0) {
-                    const float c = q[v0 + 2 * v1][a0 + 2 * a1];
-                    s = fmaf(c, b0.w[v0][a0], s);
-                    s1 = fmaf(c, b0.d1[v0][a0], s1);
-                    s2 = fmaf(c, b0.d2[v0][a0], s2);
-                }
-            g = fmaf(s, b1.w[v1][a1], g);
-            dg[0] = fmaf(s1, b1.w[v1][a1], dg[0]);
-            dg[1] = fmaf(s, b1.d1[v1][a1], dg[1]);
-            lap = fmaf(s2, b1.w[v1][a1], lap);
-            lap = fmaf(s, b1.d2[v1][a1], lap);
-        }
-}
-
-// Separable 3D blend of one feature.
-__device__ __forceinline__ void blend3(const float (&q)[8][8], const Basis1& b0, const Basis1& b1,
-                                       const Basis1& b2, float& g, float (&dg)[3], float& lap) {
-    g = 0.f, dg[0] = 0.f, dg[1] = 0.f, dg[2] = 0.f, lap = 0.f;
-#pragma unroll
-    for (int v2 = 0; v2 < 2; ++v2)
-#pragma unroll
-        for (int a2 = 0; a2 < 2; ++a2) {
-            float A = 0.f, B = 0.f, C = 0.f, Dl = 0.f;
-#pragma unroll
-            for (int v1 = 0; v1 < 2; ++v1)
-#pragma unroll
-                for (int a1 = 0; a1 < 2; ++a1) {
-                    float s = 0.f, s1 = 0.f, s2 = 0.f;
-#pragma unroll
-                    for (int v0 = 0; v0 < 2; ++v0)
-#pragma unroll
-                        for (int a0 = 0; a0 < 2; ++a0) {
-                            const float c = q[v0 + 2 * v1 + 4 * v2][a0 + 2 * a1 + 4 * a2];
-                            s = fmaf(c, b0.w[v0][a0], s);
-                            s1 = fmaf(c, b0.d1[v0][a0], s1);
-                            s2 = fmaf(c, b0.d2[v0][a0], s2);
-                        }
-                    A = fmaf(s, b1.w[v1][a1], A);
-                    B = fmaf(s1, b1.w[v1][a1], B);
-                    C = fmaf(s, b1.d1[v1][a1], C);
-                    Dl = fmaf(s2, b1.w[v1][a1], Dl);
-                    Dl = fmaf(s, b1.d2[v1][a1], Dl);
-                }
-            g = fmaf(A, b2.w[v2][a2], g);
-            dg[0] = fmaf(B, b2.w[v2][a2], dg[0]);
-            dg[1] = fmaf(C, b2.w[v2][a2], dg[1]);
-            dg[2] = fmaf(A, b2.d1[v2][a2], dg[2]);
-            lap = fmaf(Dl, b2.w[v2][a2], lap);
-            lap = fmaf(A, b2.d2[v2][a2], lap);
-        }
-}
 
 // Separable 2D blend with the full Hessian h = (xx, xy, yy).
 __device__ __forceinline__ void blend2h(const float (&q)[4][4], const Basis1& b0, const Basis1& b1, float& g,
@@ -263,7 +200,7 @@ __global__ void __launch_bounds__(kBlock) hermite_fwd_kernel(const __grid_consta
 
 // Contribution of one packed slot (multi-index alpha, with the weights
 // W0..W2 of its per-axis orders) to the 3D outputs, for both features at
-// once: c[v] is the slot's (feature 0, feature 1) coefficient pair at corner
+// once (the 4D lane-quad forward blends its axis-3 slices with these): c[v] is the slot's (feature 0, feature 1) coefficient pair at corner
 // v = v0 + 2 v1 + 4 v2; o[] accumulates (gamma, d/dx0, d/dx1, d/dx2, lap)
 // pairs.  The same separable order as blend3, restricted to one alpha.
 __device__ __forceinline__ void unit_blend3_f2(const uint64_t (&c)[8], const AxisW2& W0, const AxisW2& W1,
@@ -341,6 +278,104 @@ __device__ __forceinline__ void unit_blend3_f2_hess(const uint64_t (&c)[8], cons
     }
 }
 
+// Lane-pair blend of a packed 3D F = 2 row split by the order along axis 2.
+// After pair_exchange, lane h of a pair holds, for every corner v = v0 + 2 v1
+// + 4 v2, the (feature 0, feature 1) coefficient pairs q[v][i] of the four
+// multi-indices alpha = (i & 1, i >> 1, h): the whole separable contraction
+// over (v0, a0) and (v1, a1) runs inside the lane (axis-0 sums s, s1, s2 for
+// each (v1, a1, v2); axis-1 sums per v2), and axis 2 contributes only its
+// order-h weights w2.  o[] accumulates (gamma, d/dx0, d/dx1, d/dx2, lap)
+// pairs, or with HESS (gamma, d/dx0, d/dx1, d/dx2, xx, xy, xz, yy, yz, zz);
+// gamma and the gradient take the same operations in both variants.  The
+// lane's partial outputs (alpha_2 = h) of the pair add up to the encoding.
+// 148 f32x2 operations per lane (164 with HESS), against 224 for a blend of
+// each slot on its own (3D, 2^21 points, 16 levels: 2.34 -> 2.12 ms).
+template <bool HESS>
+__device__ __forceinline__ void blend3_pair_a2(const uint64_t (&q)[8][4], const Basis1& b0, const Basis1& b1,
+                                               const AxisW& w2, uint64_t (&o)[HESS ? 10 : 5]) {
+#pragma unroll
+    for (int v2 = 0; v2 < 2; ++v2) {
+        uint64_t A, B, C, Dl, D00, D11, E01;
+#pragma unroll
+        for (int v1 = 0; v1 < 2; ++v1)
+#pragma unroll
+            for (int a1 = 0; a1 < 2; ++a1) {
+                uint64_t s, s1, s2;
+#pragma unroll
+                for (int v0 = 0; v0 < 2; ++v0)
+#pragma unroll
+                    for (int a0 = 0; a0 < 2; ++a0) {
+                        const uint64_t c = q[v0 + 2 * v1 + 4 * v2][a0 + 2 * a1];
+                        if (v0 == 0 && a0 == 0) {
+                            s = f2_mul(c, f2_dup(b0.w[0][0]));
+                            s1 = f2_mul(c, f2_dup(b0.d1[0][0]));
+                            s2 = f2_mul(c, f2_dup(b0.d2[0][0]));
+                        } else {
+                            s = f2_fma(c, f2_dup(b0.w[v0][a0]), s);
+                            s1 = f2_fma(c, f2_dup(b0.d1[v0][a0]), s1);
+                            s2 = f2_fma(c, f2_dup(b0.d2[v0][a0]), s2);
+                        }
+                    }
+                const uint64_t w = f2_dup(b1.w[v1][a1]), d1 = f2_dup(b1.d1[v1][a1]), d2 = f2_dup(b1.d2[v1][a1]);
+                if (v1 == 0 && a1 == 0) {
+                    A = f2_mul(s, w);
+                    B = f2_mul(s1, w);
+                    C = f2_mul(s, d1);
+                    if constexpr (HESS) {
+                        D00 = f2_mul(s2, w);
+                        D11 = f2_mul(s, d2);
+                        E01 = f2_mul(s1, d1);
+                    } else {
+                        Dl = f2_fma(s, d2, f2_mul(s2, w));
+                    }
+                } else {
+                    A = f2_fma(s, w, A);
+                    B = f2_fma(s1, w, B);
+                    C = f2_fma(s, d1, C);
+                    if constexpr (HESS) {
+                        D00 = f2_fma(s2, w, D00);
+                        D11 = f2_fma(s, d2, D11);
+                        E01 = f2_fma(s1, d1, E01);
+                    } else {
+                        Dl = f2_fma(s2, w, Dl);
+                        Dl = f2_fma(s, d2, Dl);
+                    }
+                }
+            }
+        const uint64_t w = f2_dup(w2.w[v2]), d1 = f2_dup(w2.d1[v2]), d2 = f2_dup(w2.d2[v2]);
+        o[0] = f2_fma(A, w, o[0]);
+        o[1] = f2_fma(B, w, o[1]);
+        o[2] = f2_fma(C, w, o[2]);
+        o[3] = f2_fma(A, d1, o[3]);
+        if constexpr (HESS) {
+            o[4] = f2_fma(D00, w, o[4]);
+            o[5] = f2_fma(E01, w, o[5]);
+            o[6] = f2_fma(B, d1, o[6]);
+            o[7] = f2_fma(D11, w, o[7]);
+            o[8] = f2_fma(C, d1, o[8]);
+            o[9] = f2_fma(A, d2, o[9]);
+        } else {
+            o[4] = f2_fma(Dl, w, o[4]);
+            o[4] = f2_fma(A, d2, o[4]);
+        }
+    }
+}
+
+// Packed 3D slots (f, fx, fy, fz | fxy, fxz, fyz, fxyz): lane h of a pair
+// loads half h of each corner row.  Swapping fz (lane 0, position 3) with
+// fxy (lane 1, position 0) leaves lane h with the four multi-indices of
+// order h along axis 2, at position i = a0 + 2 a1 -- the layout
+// blend3_pair_a2 reads.
+__device__ __forceinline__ void pair_exchange(unsigned mask, int h, uint64_t (&q)[8][4]) {
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        const uint64_t x = h ? q[v][0] : q[v][3];
+        const uint64_t y = __shfl_xor_sync(mask, x, 1);
+        if (h) q[v][0] = y;
+        else q[v][3] = y;
+    }
+}
+
 // Half-row h of a packed 3D F = 2 row (slots 4h..4h+3, both features) as
 // four (feature 0, feature 1) pairs: one 256-bit load for fp32 rows, one
 // 128-bit load widened exactly for fp16 rows.
@@ -361,10 +396,12 @@ __device__ __forceinline__ void load_half_row(const TT* e, uint64_t (&q)[4]) {
 
 // Lane-pair split for packed 3D F = 2 rows (64 bytes fp32, 32 bytes fp16).
 // Lane h of a pair reads the half h of every corner row with one load, so
-// one warp instruction covers whole rows (one L1 wavefront per row), and
-// blends the four slots of that half.  The two features travel as packed
-// pairs through f32x2 FMAs (the weights are shared).  The encoding is linear
-// in theta, so the pair's partial outputs add up: a reduce-scatter leaves
+// one warp instruction covers whole rows (one L1 wavefront per row); one
+// slot swap per corner (pair_exchange) then gives lane h the multi-indices
+// of order h along axis 2, which it blends with the full separable
+// contraction (blend3_pair_a2).  The two features travel as packed pairs
+// through f32x2 FMAs (the weights are shared).  The encoding is linear in
+// theta, so the pair's partial outputs add up: a reduce-scatter leaves
 // feature h's outputs on lane h, which stores them.
 // Two 256-thread blocks per SM (at most 128 registers): without the bound
 // the full-Hessian variant takes 130 and runs one block per SM (3D, 2^21
@@ -372,7 +409,7 @@ __device__ __forceinline__ void load_half_row(const TT* e, uint64_t (&q)[4]) {
 // 4%, 2.31 -> 2.22 ms).
 template <typename TT, bool HESS>
 __global__ void __launch_bounds__(kBlock, 2) hermite_fwd_pair3_kernel(const __grid_constant__ FwdParams p) {
-    constexpr int D = 3, V = 8, G = 2, S = 4, NO = HESS ? 10 : 5;
+    constexpr int D = 3, V = 8, S = 4, NO = HESS ? 10 : 5;
     const int l = p.c.lvl[blockIdx.y];
     const int64_t n = (static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x) >> 1;
     const int lane = threadIdx.x & 1;
@@ -412,25 +449,13 @@ __global__ void __launch_bounds__(kBlock, 2) hermite_fwd_pair3_kernel(const __gr
         const uint32_t id = vertex_index<D>(g, lv, lv.dense & 1u, p.c.tmask[0]);
         load_half_row<TT>(base + static_cast<int64_t>(id) * p.tab.rs[0], q[v]);
     }
+    const unsigned mask = __activemask();
+    pair_exchange(mask, lane, q);
     uint64_t o[NO];
 #pragma unroll
     for (int k = 0; k < NO; ++k) o[k] = 0ull;  // (+0.0f, +0.0f)
-#pragma unroll
-    for (int u = 0; u < S; ++u) {
-        const AxisW2 W0 = axis_dup(unit_axis<D, G>(B[0], lane, u, 0));
-        const AxisW2 W1 = axis_dup(unit_axis<D, G>(B[1], lane, u, 1));
-        const AxisW2 W2 = axis_dup(unit_axis<D, G>(B[2], lane, u, 2));
-        uint64_t cv[V];
-#pragma unroll
-        for (int v = 0; v < V; ++v) cv[v] = q[v][u];
-        if constexpr (HESS) {
-            unit_blend3_f2_hess(cv, W0, W1, W2, o);
-        } else {
-            unit_blend3_f2(cv, W0, W1, W2, o);
-        }
-    }
+    blend3_pair_a2<HESS>(q, B[0], B[1], axis_pick(B[2], lane), o);
     // reduce-scatter across the pair: lane h keeps feature h
-    const unsigned mask = __activemask();
     float r[NO];
 #pragma unroll
     for (int k = 0; k < NO; ++k) {
@@ -471,8 +496,9 @@ constexpr int kPipeBlock = 128;  // threads of a pipelined CTA: 64 points per ba
 // registers.  Slots are [stage][corner][16-byte chunk][thread], so a warp's
 // copies and reads cover consecutive 16-byte words (no bank conflicts); a
 // lane reads only what it copied, so its own wait suffices.  Lanes past the
-// last point copy the last point's rows and store nothing.  The blend is
-// hermite_fwd_pair3_kernel's, so the outputs are bit-identical.
+// last point copy the last point's rows and store nothing.  The slot swap
+// and the blend are hermite_fwd_pair3_kernel's, so the outputs are
+// bit-identical.
 // Used for fp16 tables, whose half-row is one 16-byte copy: 3D fp16 workload
 // (2^23 points, 10 active levels) 6.55 -> 5.63 ms, full Hessian 7.11 -> 6.95
 // ms.  An fp32 half-row (32 bytes) takes two 16-byte copies, i.e. twice the
@@ -480,7 +506,7 @@ constexpr int kPipeBlock = 128;  // threads of a pipelined CTA: 64 points per ba
 // fp32 workload ran 2.26 -> 4.26 ms, so fp32 stays on the unpipelined kernel.
 template <typename TT, bool HESS>
 __global__ void __launch_bounds__(kPipeBlock) hermite_fwd_pipe3_kernel(const __grid_constant__ FwdParams p) {
-    constexpr int D = 3, V = 8, G = 2, S = 4, NO = HESS ? 10 : 5;
+    constexpr int D = 3, V = 8, S = 4, NO = HESS ? 10 : 5;
     constexpr int CH = S * 2 * static_cast<int>(sizeof(TT)) / 16;  // 16-byte chunks per half-row
     constexpr int PB = kPipeBlock / 2;                                 // points per batch
     extern __shared__ uint4 slots[];                                   // [2][V][CH][kPipeBlock]
@@ -566,23 +592,11 @@ __global__ void __launch_bounds__(kPipeBlock) hermite_fwd_pipe3_kernel(const __g
                 }
             }
         }
+        pair_exchange(0xffffffffu, lane, q);
         uint64_t o[NO];
 #pragma unroll
         for (int k = 0; k < NO; ++k) o[k] = 0ull;  // (+0.0f, +0.0f)
-#pragma unroll
-        for (int u = 0; u < S; ++u) {
-            const AxisW2 W0 = axis_dup(unit_axis<D, G>(B[0], lane, u, 0));
-            const AxisW2 W1 = axis_dup(unit_axis<D, G>(B[1], lane, u, 1));
-            const AxisW2 W2 = axis_dup(unit_axis<D, G>(B[2], lane, u, 2));
-            uint64_t cv[V];
-#pragma unroll
-            for (int v = 0; v < V; ++v) cv[v] = q[v][u];
-            if constexpr (HESS) {
-                unit_blend3_f2_hess(cv, W0, W1, W2, o);
-            } else {
-                unit_blend3_f2(cv, W0, W1, W2, o);
-            }
-        }
+        blend3_pair_a2<HESS>(q, B[0], B[1], axis_pick(B[2], lane), o);
         float r[NO];
 #pragma unroll
         for (int k = 0; k < NO; ++k) {
@@ -870,24 +884,24 @@ cudaError_t launch_pair3(const FwdParams& p, cudaStream_t s) {
 }
 
 // One wave of persistent pipelined CTAs per level (level-major dispatch: the
-// first wave walks level 0's batches while the next level's CTAs wait).
+// first wave walks level 0's batches while the next level's CTAs wait).  The
+// SM count and the occupancy are read for the current device on every call
+// (host-side queries of a few microseconds), so nothing is cached between
+// calls, threads or devices.
 template <typename TT, bool HESS>
 cudaError_t launch_pipe3(const FwdParams& p, cudaStream_t s) {
     constexpr int kSmem = 2 * 8 * (4 * 2 * static_cast<int>(sizeof(TT)) / 16) * kPipeBlock * 16;
-    static int per_sm = 0, sms = 0;  // per instantiation; the device does not change within a process
-    if (per_sm == 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(hermite_fwd_pipe3_kernel<TT, HESS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmem);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hermite_fwd_pipe3_kernel<TT, HESS>, kPipeBlock,
-                                                              kSmem);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) per_sm = 1;
-    }
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(hermite_fwd_pipe3_kernel<TT, HESS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hermite_fwd_pipe3_kernel<TT, HESS>, kPipeBlock,
+                                                          kSmem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
     const int64_t batches = (p.c.n + kPipeBlock / 2 - 1) / (kPipeBlock / 2);
     const int64_t ctas = std::min<int64_t>(batches, static_cast<int64_t>(sms) * per_sm);
     dim3 grid(static_cast<unsigned>(ctas), static_cast<unsigned>(p.c.nlvl));

@@ -256,9 +256,15 @@ int sm_count() {
 // B300: a d-linear level of up to ~100 KB gains several times over direct
 // REDs (a few hundred hot rows serialise in L2), while Hermite levels gain
 // only when tiny -- 3D levels of hundreds of KB run at the full RED rate
-// directly, and the shared-memory pass then costs more than it saves.
+// directly, and the shared-memory pass then costs more than it saves.  2D
+// PINN grid (2^20 points, one level per launch): the 289- and 484-row levels
+// (9 and 15 KB) take 0.12 ms privatised against 0.18 ms direct when the
+// points come in random order, but the 784-row level (25 KB) 0.12 against
+// 0.08 ms; points in stratum order sum their runs in the warp and run faster
+// direct at every level (whole backward 0.66 ms privatising up to 32 KB,
+// 0.56 ms direct).
 constexpr int64_t kPrivMaxBytes = 160 * 1024;
-constexpr int64_t kHermitePrivLevelBytes = 32 * 1024;
+constexpr int64_t kHermitePrivLevelBytes = 16 * 1024;
 
 // Splits the active levels of a backward between the privatised kernel
 // (one-to-one levels whose rows -- part_bytes per row and CTA -- fit in
