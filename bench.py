@@ -1084,6 +1084,30 @@ def run_siren(args):
                 if k["bound"] == "alu" else
                 ("measured live, the larger of the replay of the launch's own row stream and the uniform-random "
                  "L2 rate of the same row pattern")}
+    # the fused forward (encoding formed on chip and fed to the first layer) beside the unfused pair
+    fused = None
+    if w.d in (2, 3) and w.F == 2:
+        fu, fdu, flu = (torch.empty(sh, device="cuda") for sh in ((O, n), (d, O, n), (O, n)))
+
+        def fused_fwd():
+            hg.hg_encode_siren_fwd(desc, n, coords, tviews, sdesc, W1, b1, W2, b2, fu, fdu, flu, stream)
+        for _ in range(args.warmup):
+            fused_fwd()
+        fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in fev:
+            a.record(stream)
+            fused_fwd()
+            b.record(stream)
+        torch.cuda.synchronize()
+        fms = statistics.median(a.elapsed_time(b) for a, b in fev)
+        unf = ms["encode_fwd"] + ms["siren_fwd"]
+        fused = {"ms": fms, "unfused_ms": unf, "speedup": unf / fms,
+                 "achieved_tflops_first_layer": fl / (fms * 1e-3) / 1e12, "peak_fp32_tflops": fp32,
+                 "frac_fp32_first_layer_only": fl / (fms * 1e-3) / 1e12 / fp32,
+                 "hbm_bytes_saved_per_step": 2 * n * (d + 2) * K * 4,
+                 "what": "hg_encode_siren_fwd (one launch: encode every level of a tile of points into shared "
+                         "memory, then the SIREN forward) vs hg_encode_fwd + hg_siren_fwd (gamma, grad gamma, "
+                         "lap gamma written to and read back from HBM); median of the same steps"}
     e2e = None
     if not args.no_e2e and rank == 0:
         e2e = run_e2e_siren(torch, hg, w, desc, sdesc, inputs, sup, tviews, gviews, grad, (W1, b1, W2, b2),
@@ -1100,7 +1124,7 @@ def run_siren(args):
                     "upstream gradients of u, grad u, lap u)",
             "config": describe(w, mask, "feature", siren=True),
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 4 * args.steps, "clocks": clocks,
+            "gpu_launches": 4 * args.steps, "clocks": clocks, "fused_forward": fused,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -317,6 +317,28 @@ hg_status hg_siren_fwd(const hg_siren_desc* desc, int64_t n, const float* gamma,
                        const float* lap, const float* W1, const float* b1, const float* W2, const float* b2,
                        float* u, float* du, float* lapu, hg_stream stream);
 
+/* Fused encoder + SIREN forward [HNGP 整体框架: the encoding feeds the
+ * network; 关键设计 2: the SIREN chain rule]: u, grad u and lap u of the
+ * SIREN at the Hermite encoding of each point, with the encoding (gamma,
+ * grad gamma, lap gamma of every level, as hg_encode_fwd computes them)
+ * formed on chip and fed to the first layer without being written to
+ * memory.  The result equals hg_encode_fwd followed by hg_siren_fwd on its
+ * feature-major outputs.  Grid: desc as for hg_encode_fwd with d = 2 or 3,
+ * F = 2, the packed table layout (see below; 32-byte aligned rows, 16 bytes
+ * for 2D fp16), fp32 or fp16 coefficients; desc->layout is not used (no
+ * encoder output is written).  Inactive levels (level_mask) feed zeros.
+ * SIREN: sdesc->d = desc->d, sdesc->K = L * F (the levels' features
+ * concatenated in level-major, feature-minor order); W1, b1, W2, b2 and the
+ * outputs u [O][n], du [d][O][n], lapu [O][n] (each may be NULL) as for
+ * hg_siren_fwd.  Device pointers owned by the caller; nothing is allocated.
+ * Errors: HG_ERR_INVALID_ARG for a bad desc/sdesc, mismatched d or K, NULL
+ * required pointers or n outside 0..2^31-1; HG_ERR_UNSUPPORTED for d, F or
+ * a table layout outside the above, or a tile that does not fit in shared
+ * memory; HG_ERR_CUDA on a launch failure. */
+hg_status hg_encode_siren_fwd(const hg_grid_desc* desc, int64_t n, const float* coords, const hg_table* tables,
+                              const hg_siren_desc* sdesc, const float* W1, const float* b1, const float* W2,
+                              const float* b2, float* u, float* du, float* lapu, hg_stream stream);
+
 /* Backward: the vector-Jacobian product of hg_siren_fwd with upstream
  * gradients g_u [O][n], g_du [d][O][n], g_lapu [O][n] (NULL = zero).
  * Inputs gamma, dgamma, lap, W1, b1, W2 as for the forward (all required).
@@ -343,8 +365,9 @@ const char* hg_status_string(hg_status status);
 const char* hg_last_error(void);
 
 /* ABI version of this header (bumped on any incompatible change; 2: log2_T
- * has five entries, d may be 4; 3: the SIREN consumer). */
-#define HG_ABI_VERSION 3
+ * has five entries, d may be 4; 3: the SIREN consumer; 4: the fused encoder
+ * + SIREN forward). */
+#define HG_ABI_VERSION 4
 int32_t hg_abi_version(void);
 
 #ifdef __cplusplus

@@ -19,7 +19,7 @@ HG_OK, HG_ERR_INVALID_ARG, HG_ERR_UNSUPPORTED, HG_ERR_CUDA = 0, 1, 2, 3
 HG_F32, HG_F16 = 0, 1
 HG_POINT_MAJOR, HG_FEATURE_MAJOR = 0, 1
 HG_MAX_LEVELS = 32
-HG_ABI_VERSION = 3        # the include/hg.h layout this binding marshals
+HG_ABI_VERSION = 4        # the include/hg.h layout this binding marshals
 
 c_i32, c_i64, c_u32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
 
@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
         "hg_rbf_fwd": [D, c_i64, c_vp, ctypes.c_float, c_i32, T, c_vp, c_vp, c_vp, c_vp],
         "hg_rbf_bwd": [D, c_i64, c_vp, ctypes.c_float, c_i32, c_vp, c_vp, c_vp, G, c_vp],
         "hg_siren_fwd": [S] + [c_i64] + [c_vp] * 11,
+        "hg_encode_siren_fwd": [D, c_i64, c_vp, T, S] + [c_vp] * 8,
         "hg_siren_bwd": [S] + [c_i64] + [c_vp] * 17,
     }
     for name, args in sig.items():
@@ -345,6 +346,17 @@ def hg_siren_fwd(desc: SirenDesc, n: int, gamma, dgamma, lap, W1, b1, W2, b2, u,
                                                                            lapu)], _stream(stream) if n else 0)
     if check:
         _check(st, "hg_siren_fwd")
+    return st
+
+
+def hg_encode_siren_fwd(desc: GridDesc, n: int, coords, tables: Sequence[TableView], sdesc: SirenDesc, W1, b1, W2,
+                        b2, u, du=None, lapu=None, stream=None, check: bool = True) -> int:
+    c, sc = desc.as_c(), sdesc.as_c()
+    st = lib().hg_encode_siren_fwd(ctypes.byref(c), int(n), _addr(coords), _tables_c(tables, hg_table),
+                                   ctypes.byref(sc), *[_addr(a) for a in (W1, b1, W2, b2, u, du, lapu)],
+                                   _stream(stream) if n else 0)
+    if check:
+        _check(st, "hg_encode_siren_fwd")
     return st
 
 

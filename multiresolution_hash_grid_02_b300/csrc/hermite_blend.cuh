@@ -1,4 +1,5 @@
-// Hermite-NGP blends of one (point, level) on one thread.
+// Hermite-NGP blends of one (point, level) on one thread, shared by the
+// generic forward and the fused encoder + SIREN forward.
 //
 // "Hermite-NGP: Gradient-Augmented Hash Encoding for Learning PDEs",
 // 关键设计 1 (tensor-product Hermite bases, dx^|alpha| scaling) and 关键设计 2
@@ -74,6 +75,50 @@ __device__ __forceinline__ void blend3(const float (&q)[8][8], const Basis1& b0,
             lap = fmaf(Dl, b2.w[v2][a2], lap);
             lap = fmaf(A, b2.d2[v2][a2], lap);
         }
+}
+
+// One (point n, level l) of a packed [L][T][2^d][F] table with F = 2, on
+// one thread: the 2^d corner rows read whole (vector loads), then the
+// separable blend of each feature -- the arithmetic of the generic forward's
+// packed path, so the results are bit-identical to it.  g[f], dg[f][j] and
+// lap[f]: gamma, d gamma / d x_j and the Laplacian of feature f.
+template <int D, typename TT>
+__device__ __forceinline__ void encode_item_f2(const FwdParams& p, int64_t n, int l, float (&g)[2],
+                                               float (&dg)[2][3], float (&lap)[2]) {
+    constexpr int V = 1 << D, FC = 2;
+    const Level& lv = p.c.lv[l];
+    uint32_t c[D];
+    float t[D];
+    Basis1 B[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+        locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
+        B[i] = hermite_basis(t[i], lv);
+    }
+    constexpr int ROW = V * FC * static_cast<int>(sizeof(TT));
+    const TT* base = static_cast<const TT*>(p.tab.ptr[0]) + l * p.tab.ls[0];
+    RowRegs<ROW> rows[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        uint32_t gv[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) gv[i] = c[i] + ((v >> i) & 1u);
+        const uint32_t id = vertex_index<D>(gv, lv, lv.dense & 1u, p.c.tmask[0]);
+        load_row<ROW>(base + static_cast<int64_t>(id) * p.tab.rs[0], rows[v]);
+    }
+#pragma unroll
+    for (int f = 0; f < FC; ++f) {
+        float q[V][V];
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+#pragma unroll
+            for (int a = 0; a < V; ++a) q[v][a] = row_elem<TT, ROW>(rows[v], packed_slot<D>(a) * FC + f);
+        if constexpr (D == 2) {
+            blend2(q, B[0], B[1], g[f], dg[f], lap[f]);
+        } else {
+            blend3(q, B[0], B[1], B[2], g[f], dg[f], lap[f]);
+        }
+    }
 }
 
 }  // namespace hg

@@ -837,6 +837,78 @@ hg_status hg_siren_fwd(const hg_siren_desc* desc, int64_t n, const float* gamma,
     return launch_status(hg::launch_siren_fwd(p, ctas, stream), "SIREN forward");
 }
 
+hg_status hg_encode_siren_fwd(const hg_grid_desc* desc, int64_t n, const float* coords, const hg_table* tables,
+                              const hg_siren_desc* sdesc, const float* W1, const float* b1, const float* W2,
+                              const float* b2, float* u, float* du, float* lapu, hg_stream stream) {
+    hg_status st = check_desc(desc, desc ? desc->d + 1 : 0);
+    if (st != HG_OK) return st;
+    if ((st = check_n(n)) != HG_OK) return st;
+    if (!tables) return fail(HG_ERR_INVALID_ARG, "tables is NULL");
+    if (desc->d != 2 && desc->d != 3)
+        return fail(HG_ERR_UNSUPPORTED, "the fused encoder + SIREN forward takes d = 2 or 3 (got %d)", desc->d);
+    if (desc->F != 2) return fail(HG_ERR_UNSUPPORTED, "the fused encoder + SIREN forward takes F = 2 (got %d)", desc->F);
+    hg::SirenParams p;
+    if ((st = siren_plan(sdesc, n, p)) != HG_OK) return st;
+    if (sdesc->d != desc->d)
+        return fail(HG_ERR_INVALID_ARG, "the SIREN's d = %d differs from the grid's d = %d", sdesc->d, desc->d);
+    if (sdesc->K != desc->L * desc->F)
+        return fail(HG_ERR_INVALID_ARG, "the SIREN's K = %d must be L * F = %d", sdesc->K, desc->L * desc->F);
+    const int d = desc->d, F = desc->F, V = 1 << d;
+    const size_t es = dtype_size(desc->dtype);
+    const void* ptrs[5];
+    int64_t ls[5], rs[5];
+    for (int k = 0; k <= d; ++k) {
+        ptrs[k] = tables[k].ptr;
+        ls[k] = tables[k].level_stride;
+        rs[k] = tables[k].row_stride;
+        st = check_view("tables", k, ptrs[k], ls[k], rs[k], static_cast<int64_t>(binom(d, k)) * F,
+                        int64_t(1) << desc->log2_T[k], desc->L, es);
+        if (st != HG_OK) return st;
+    }
+    const size_t row = static_cast<size_t>(V) * F * es;
+    const size_t al = row < 32 ? row : 32;
+    if (!is_packed(desc, ptrs, ls, rs, es) || !aligned(ptrs[0], al) || (static_cast<size_t>(ls[0]) * es) % al != 0)
+        return fail(HG_ERR_UNSUPPORTED, "the fused encoder + SIREN forward needs the packed table layout, "
+                                        "%zu-byte aligned", al);
+    if (!W1 || !b1 || !W2) return fail(HG_ERR_INVALID_ARG, "W1, b1 and W2 must not be NULL");
+    const void* vp[] = {coords, W1, b1, W2, b2, u, du, lapu};
+    for (const void* q : vp)
+        if (q && !aligned(q, 4)) return fail(HG_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
+    if (n == 0 || (!u && !du && !lapu)) return ok();
+    if (!coords) return fail(HG_ERR_INVALID_ARG, "coords must not be NULL");
+    hg::FwdParams e;
+    memset(&e, 0, sizeof(e));
+    if ((st = make_common(desc, d + 1, n, e.c)) != HG_OK) return st;
+    for (int k = 0; k <= d; ++k) {
+        e.tab.ptr[k] = ptrs[k];
+        e.tab.ls[k] = ls[k];
+        e.tab.rs[k] = rs[k];
+    }
+    e.coords = coords;
+    all_levels(e.c);
+    p.W1 = W1;
+    p.b1 = b1;
+    p.W2 = W2;
+    p.b2 = b2;
+    p.u = u;
+    p.du = du;
+    p.lapu = lapu;
+    p.nbuf = 1;  // the tile is computed in place, not copied
+    int dev = 0, sms = 0, smem_max = 0, per_sm = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (ce != cudaSuccess) return fail(HG_ERR_CUDA, "device query failed: %s", cudaGetErrorString(ce));
+    const size_t bytes = hg::siren_smem_bytes(p, false);
+    if (bytes > static_cast<size_t>(smem_max))
+        return fail(HG_ERR_UNSUPPORTED, "a SIREN tile needs %zu bytes of shared memory (at most %d)", bytes, smem_max);
+    ce = static_cast<cudaError_t>(hg::encode_siren_ctas_per_sm(p, desc->dtype, &per_sm));
+    if (ce != cudaSuccess || per_sm < 1) return fail(HG_ERR_CUDA, "fused encoder + SIREN occupancy query failed");
+    const int64_t tiles = (n + p.pts - 1) / p.pts;
+    const int ctas = static_cast<int>(std::min<int64_t>(tiles, static_cast<int64_t>(sms) * per_sm));
+    return launch_status(hg::launch_encode_siren_fwd(p, e, desc->dtype, ctas, stream), "fused encoder + SIREN forward");
+}
+
 hg_status hg_siren_bwd(const hg_siren_desc* desc, int64_t n, const float* gamma, const float* dgamma,
                        const float* lap, const float* W1, const float* b1, const float* W2, const float* g_u,
                        const float* g_du, const float* g_lapu, float* g_gamma, float* g_dgamma, float* g_lap,

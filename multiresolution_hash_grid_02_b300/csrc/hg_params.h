@@ -141,5 +141,9 @@ size_t siren_smem_bytes(const SirenParams& p, bool bwd);
 int launch_siren_fwd(const SirenParams& p, int ctas, void* stream);
 int launch_siren_bwd(const SirenParams& p, int ctas, void* stream);
 int siren_ctas_per_sm(const SirenParams& p, bool bwd, int* ctas);
+// Fused encoder + SIREN forward (d = 2 or 3, packed F = 2 table of dtype `dtype`,
+// one input buffer): CTAs per SM, and the launch of `ctas` persistent CTAs.
+int encode_siren_ctas_per_sm(const SirenParams& p, int dtype, int* ctas);
+int launch_encode_siren_fwd(const SirenParams& p, const FwdParams& e, int dtype, int ctas, void* stream);
 
 }  // namespace hg

@@ -19,6 +19,7 @@
 // and the weight gradients are added to global memory once per CTA.
 #include <cuda_runtime.h>
 
+#include "hermite_blend.cuh"
 #include "hg_device.cuh"
 #include "hg_params.h"
 
@@ -156,6 +157,72 @@ __device__ __forceinline__ void first_layer(const float* W1T, const float* X, in
         for (int e = 0; e < kUnits / 2; ++e) f2_unpack(a2[r][e], acc[r][2 * e], acc[r][2 * e + 1]);
 }
 
+// The forward of one staged tile X ([R][pts][K + 4]) for the thread's point
+// (row pl) and units: the first layer, then u, grad u and lap u reduced over
+// the point's tp threads; the point's first thread stores them.
+template <int D>
+__device__ __forceinline__ void siren_tile_fwd(const SirenParams& p, const float* W1T, const float* b1,
+                                               const float* W2, const float* b2, const float* X, int64_t n0, int pl,
+                                               int q) {
+    constexpr int R = D + 2;
+    const int tp = p.tp, P = p.pts, H = p.H, O = p.O;
+    const float om = p.omega, om2 = om * om;
+    float acc[R][kUnits];
+    first_layer<R>(W1T, X, p.K, H, P, pl, q, tp, acc);
+    float pu[kMaxO], pdu[D][kMaxO], plap[kMaxO];
+#pragma unroll
+    for (int o = 0; o < kMaxO; ++o) {
+        pu[o] = plap[o] = 0.f;
+#pragma unroll
+        for (int i = 0; i < D; ++i) pdu[i][o] = 0.f;
+    }
+#pragma unroll
+    for (int jj = 0; jj < kUnits; ++jj) {
+        const int j = unit_of(q, tp, jj);
+        float a, c;
+        sincosf(om * (acc[0][jj] + b1[j]), &a, &c);
+        float y2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < D; ++i) y2 = fmaf(acc[1 + i][jj], acc[1 + i][jj], y2);
+        const float oc = om * c;
+        const float tl = fmaf(oc, acc[R - 1][jj], -om2 * a * y2);  // omega c s - omega^2 a sum y^2
+#pragma unroll
+        for (int o = 0; o < kMaxO; ++o) {
+            if (o < O) {
+                const float w2 = W2[o * H + j];
+                pu[o] = fmaf(w2, a, pu[o]);
+#pragma unroll
+                for (int i = 0; i < D; ++i) pdu[i][o] = fmaf(w2, oc * acc[1 + i][jj], pdu[i][o]);
+                plap[o] = fmaf(w2, tl, plap[o]);
+            }
+        }
+    }
+    // sum over the tp threads of the point (consecutive lanes)
+    for (int m = 1; m < tp; m <<= 1) {
+#pragma unroll
+        for (int o = 0; o < kMaxO; ++o) {
+            pu[o] += __shfl_xor_sync(0xffffffffu, pu[o], m);
+            plap[o] += __shfl_xor_sync(0xffffffffu, plap[o], m);
+#pragma unroll
+            for (int i = 0; i < D; ++i) pdu[i][o] += __shfl_xor_sync(0xffffffffu, pdu[i][o], m);
+        }
+    }
+    const int64_t n = n0 + pl;
+    if (q == 0 && n < p.n) {
+#pragma unroll
+        for (int o = 0; o < kMaxO; ++o) {
+            if (o < O) {
+                if (p.u) __stcs(p.u + o * p.n + n, pu[o] + b2[o]);
+                if (p.du) {
+#pragma unroll
+                    for (int i = 0; i < D; ++i) __stcs(p.du + (static_cast<int64_t>(i) * O + o) * p.n + n, pdu[i][o]);
+                }
+                if (p.lapu) __stcs(p.lapu + o * p.n + n, plap[o]);
+            }
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2) siren_fwd_kernel(const __grid_constant__ SirenParams p) {
     constexpr int R = D + 2;
@@ -163,14 +230,9 @@ __global__ void __launch_bounds__(kThreads, 2) siren_fwd_kernel(const __grid_con
     float* sm = reinterpret_cast<float*>(smem4);
     const SirenSmem L = siren_layout(p, false);
     stage_weights(p, L, sm, false);
-    const float* W1T = sm + L.w1t;
-    const float* b1 = sm + L.b1;
-    const float* W2 = sm + L.w2;
-    const float* b2 = sm + L.b2;
-    const int tp = p.tp, P = p.pts, H = p.H, O = p.O;
+    const int tp = p.tp, P = p.pts;
     float* Xb[2] = {sm + L.x, sm + L.x + (p.nbuf - 1) * R * P * (p.K + 4)};
     const int pl = threadIdx.x / tp, q = threadIdx.x % tp;
-    const float om = p.omega, om2 = om * om;
     const int64_t tiles = (p.n + P - 1) / P;
     int cur = 0;
     if (static_cast<int64_t>(blockIdx.x) < tiles) issue_tile(p, Xb[0], static_cast<int64_t>(blockIdx.x) * P, R);
@@ -185,62 +247,7 @@ __global__ void __launch_bounds__(kThreads, 2) siren_fwd_kernel(const __grid_con
             cp_async_wait<0>();
         }
         __syncthreads();  // this tile (and the weights) visible to every thread
-        const float* X = Xb[cur];
-        const int64_t n0 = t * P;
-        float acc[R][kUnits];
-        first_layer<R>(W1T, X, p.K, H, P, pl, q, tp, acc);
-        float pu[kMaxO], pdu[D][kMaxO], plap[kMaxO];
-#pragma unroll
-        for (int o = 0; o < kMaxO; ++o) {
-            pu[o] = plap[o] = 0.f;
-#pragma unroll
-            for (int i = 0; i < D; ++i) pdu[i][o] = 0.f;
-        }
-#pragma unroll
-        for (int jj = 0; jj < kUnits; ++jj) {
-            const int j = unit_of(q, tp, jj);
-            float a, c;
-            sincosf(om * (acc[0][jj] + b1[j]), &a, &c);
-            float y2 = 0.f;
-#pragma unroll
-            for (int i = 0; i < D; ++i) y2 = fmaf(acc[1 + i][jj], acc[1 + i][jj], y2);
-            const float oc = om * c;
-            const float tl = fmaf(oc, acc[R - 1][jj], -om2 * a * y2);  // omega c s - omega^2 a sum y^2
-#pragma unroll
-            for (int o = 0; o < kMaxO; ++o) {
-                if (o < O) {
-                    const float w2 = W2[o * H + j];
-                    pu[o] = fmaf(w2, a, pu[o]);
-#pragma unroll
-                    for (int i = 0; i < D; ++i) pdu[i][o] = fmaf(w2, oc * acc[1 + i][jj], pdu[i][o]);
-                    plap[o] = fmaf(w2, tl, plap[o]);
-                }
-            }
-        }
-        // sum over the tp threads of the point (consecutive lanes)
-        for (int m = 1; m < tp; m <<= 1) {
-#pragma unroll
-            for (int o = 0; o < kMaxO; ++o) {
-                pu[o] += __shfl_xor_sync(0xffffffffu, pu[o], m);
-                plap[o] += __shfl_xor_sync(0xffffffffu, plap[o], m);
-#pragma unroll
-                for (int i = 0; i < D; ++i) pdu[i][o] += __shfl_xor_sync(0xffffffffu, pdu[i][o], m);
-            }
-        }
-        const int64_t n = n0 + pl;
-        if (q == 0 && n < p.n) {
-#pragma unroll
-            for (int o = 0; o < kMaxO; ++o) {
-                if (o < O) {
-                    if (p.u) __stcs(p.u + o * p.n + n, pu[o] + b2[o]);
-                    if (p.du) {
-#pragma unroll
-                        for (int i = 0; i < D; ++i) __stcs(p.du + (static_cast<int64_t>(i) * O + o) * p.n + n, pdu[i][o]);
-                    }
-                    if (p.lapu) __stcs(p.lapu + o * p.n + n, plap[o]);
-                }
-            }
-        }
+        siren_tile_fwd<D>(p, sm + L.w1t, sm + L.b1, sm + L.w2, sm + L.b2, Xb[cur], t * P, pl, q);
         __syncthreads();  // this tile's buffer read by every thread
         if (p.nbuf == 1 && tn < tiles) {
             issue_tile(p, Xb[0], tn * P, R);
@@ -249,6 +256,49 @@ __global__ void __launch_bounds__(kThreads, 2) siren_fwd_kernel(const __grid_con
         cur ^= p.nbuf - 1;
     }
     cp_async_wait<0>();
+}
+
+// Fused encoder + SIREN forward ("Hermite-NGP", 整体框架: the encoding feeds
+// the network directly).  Instead of reading gamma, grad gamma and lap gamma
+// back from global memory, each tile's inputs are computed in place: the
+// CTA's threads encode (point, level) items of the tile -- the 2^d corner
+// rows of a packed F = 2 table read whole, the one-thread separable blend --
+// and write each level's two features into the shared-memory tile at
+// columns 2 l, 2 l + 1 (inactive levels and points past n as zeros), then
+// the tile's SIREN forward runs as in siren_fwd_kernel.  The encoder outputs
+// never leave the chip; with all levels' tables resident in L2 (the 2D PINN
+// grid: ~60 MB) the gathers stay on chip too.  One input buffer; the CTAs on
+// an SM (two) overlap one another's encode and contraction.
+template <int D, typename TT>
+__global__ void __launch_bounds__(kThreads, 2) encode_siren_fwd_kernel(const __grid_constant__ SirenParams p,
+                                                                      const __grid_constant__ FwdParams e) {
+    constexpr int R = D + 2;
+    extern __shared__ float4 smem4[];
+    float* sm = reinterpret_cast<float*>(smem4);
+    const SirenSmem L = siren_layout(p, false);
+    stage_weights(p, L, sm, false);
+    const int tp = p.tp, P = p.pts, ld = p.K + 4, levels = e.c.L;
+    float* X = sm + L.x;
+    const int pl = threadIdx.x / tp, q = threadIdx.x % tp;
+    const int64_t tiles = (p.n + P - 1) / P;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int64_t n0 = t * P;
+        for (int i = threadIdx.x; i < P * levels; i += kThreads) {
+            const int pp = i & (P - 1), l = i / P;  // P is a power of two
+            const int64_t n = n0 + pp;
+            float g[2] = {0.f, 0.f}, dg[2][3] = {{0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}}, lp[2] = {0.f, 0.f};
+            if (n < e.c.n && ((e.c.level_mask >> l) & 1u)) encode_item_f2<D, TT>(e, n, l, g, dg, lp);
+            float* x = X + pp * ld + 2 * l;
+            *reinterpret_cast<float2*>(x) = make_float2(g[0], g[1]);
+#pragma unroll
+            for (int j = 0; j < D; ++j)
+                *reinterpret_cast<float2*>(x + (1 + j) * P * ld) = make_float2(dg[0][j], dg[1][j]);
+            *reinterpret_cast<float2*>(x + (D + 1) * P * ld) = make_float2(lp[0], lp[1]);
+        }
+        __syncthreads();  // the tile (and the weights) visible to every thread
+        siren_tile_fwd<D>(p, sm + L.w1t, sm + L.b1, sm + L.w2, sm + L.b2, X, n0, pl, q);
+        __syncthreads();  // every thread done with the tile before the next encode
+    }
 }
 
 // Backward.  Per tile: (1) recompute the first layer, form the pre-activation
@@ -549,6 +599,38 @@ int launch_siren_fwd(const SirenParams& p, int ctas, void* stream) {
 
 int launch_siren_bwd(const SirenParams& p, int ctas, void* stream) {
     return dispatch(p, true, ctas, static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+template <int D, typename TT>
+cudaError_t fused_attr(size_t bytes, int* per_sm, const SirenParams& p, const FwdParams& e, int ctas,
+                       cudaStream_t s, bool launch) {
+    cudaError_t err = cudaFuncSetAttribute(encode_siren_fwd_kernel<D, TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(bytes));
+    if (err != cudaSuccess) return err;
+    if (!launch)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, encode_siren_fwd_kernel<D, TT>, kThreads, bytes);
+    encode_siren_fwd_kernel<D, TT><<<ctas, kThreads, bytes, s>>>(p, e);
+    return cudaGetLastError();
+}
+
+cudaError_t fused_dispatch(const SirenParams& p, const FwdParams& e, int dtype, int* per_sm, int ctas, cudaStream_t s,
+                           bool launch) {
+    const size_t bytes = siren_smem_bytes(p, false);
+    if (p.d == 2)
+        return dtype == HG_F16 ? fused_attr<2, __half>(bytes, per_sm, p, e, ctas, s, launch)
+                               : fused_attr<2, float>(bytes, per_sm, p, e, ctas, s, launch);
+    return dtype == HG_F16 ? fused_attr<3, __half>(bytes, per_sm, p, e, ctas, s, launch)
+                           : fused_attr<3, float>(bytes, per_sm, p, e, ctas, s, launch);
+}
+}  // namespace
+
+int encode_siren_ctas_per_sm(const SirenParams& p, int dtype, int* ctas) {
+    return fused_dispatch(p, FwdParams{}, dtype, ctas, 0, nullptr, false);
+}
+
+int launch_encode_siren_fwd(const SirenParams& p, const FwdParams& e, int dtype, int ctas, void* stream) {
+    return fused_dispatch(p, e, dtype, nullptr, ctas, static_cast<cudaStream_t>(stream), true);
 }
 
 }  // namespace hg

@@ -255,3 +255,33 @@ def test_siren_arguments_are_checked(m):
     assert hg.hg_siren_fwd(good, 0, 0, 0, 0, 0, 0, 0, 0, 0, stream=0, check=False) == E             # still NULL
     assert hg.hg_siren_fwd(good, 0, A, A, A, A, A, A, A, A, stream=0, check=False) == hg.HG_OK
     assert hg.hg_siren_bwd(good, 5, A, A, A, A, A, A, A, A, A, stream=0, check=False) == hg.HG_OK
+
+
+def test_fused_encoder_siren_arguments_are_checked(m):
+    """Grid, SIREN and table checks of the fused encoder + SIREN forward,
+    before any launch."""
+    hg = m.hg
+    E, U, A = hg.HG_ERR_INVALID_ARG, hg.HG_ERR_UNSUPPORTED, 1 << 20
+    desc = m.GridDesc(d=2, L=4, F=2, n_min=4, n_max=32, log2_T=(8, 8, 8))
+    views = hg.packed_views(_FakeTable((4, 256, 4, 2), addr=A), 2)
+    sd = m.SirenDesc(d=2, K=8, H=64)
+
+    def call(desc=desc, n=5, views=views, sd=sd, W1=A, u=A):
+        return hg.hg_encode_siren_fwd(desc, n, A, views, sd, W1, A, A, 0, u, stream=0, check=False)
+
+    assert call(n=0) == hg.HG_OK                                       # nothing to do: no launch
+    assert call(u=0) == hg.HG_OK                                       # no output requested
+    assert call(sd=m.SirenDesc(d=2, K=16, H=64)) == E                  # K must be L * F
+    assert call(sd=m.SirenDesc(d=3, K=8, H=64)) == E                   # d must match the grid
+    assert call(sd=m.SirenDesc(d=2, K=8, H=48)) == E                   # bad SIREN width
+    assert call(W1=0) == E
+    assert call(n=-1) == E
+    d1 = m.GridDesc(d=2, L=8, F=1, n_min=4, n_max=32, log2_T=(8, 8, 8))
+    assert call(desc=d1, views=hg.packed_views(_FakeTable((8, 256, 4, 1), addr=A), 2)) == U   # F = 2 only
+    d4 = m.GridDesc(d=4, L=4, F=2, n_min=2, n_max=8, log2_T=(8, 8, 8, 8, 8))
+    assert call(desc=d4, views=hg.packed_views(_FakeTable((4, 256, 16, 2), addr=A), 4),
+                sd=m.SirenDesc(d=4, K=8, H=64)) == U                   # d = 2 or 3 only
+    sep = m.order_views([_FakeTable((4, 256, k, 2), addr=A + i * (1 << 16)) for i, k in enumerate((1, 2, 1))])
+    assert call(views=sep) == U                                        # packed layout only
+    assert call(views=hg.packed_views(_FakeTable((4, 256, 4, 2), addr=A + 16), 2)) == U   # 32-byte rows unaligned
+    assert hg.hg_last_error() != ""

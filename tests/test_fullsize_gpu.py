@@ -446,3 +446,49 @@ def test_fullsize_siren_consumer():
             mag[k] = mag[k] + r["m" + k]
     for k, t in zip(keys, wg):
         check_close(k, host(t), tot[k], mag[k], rtol=2e-4)
+
+
+def test_fullsize_fused_encoder_siren_pinn():
+    """The fused encoder + SIREN forward on the PINN workload (2^20
+    stratified points, 2D, 16 levels, T = 2^19, fp32; SIREN K = 32, H = 64,
+    O = 1, omega = 30 with the benchmark's seeded weights): every point's u,
+    grad u and lap u against the oracle's encoding followed by its SIREN (the
+    encoder's magnitudes carried into the SIREN's), and bit for bit against
+    the unfused chain on the GPU (encoder outputs through memory, then the
+    SIREN)."""
+    m, hg, W, oracle = _mods()
+    w = W.WORKLOADS[3]
+    inp = W.make(w)
+    n, d, L, F = w.n_points, w.d, w.L, w.F
+    K, H, O = L * F, W.SIREN_H, W.SIREN_O
+    sw = W.siren_weights(np.random.default_rng(w.seed + 2000), K, H, O)
+    res = oracle.level_resolutions(L, w.n_min, w.n_max)
+    desc = _hermite_desc(w, (1 << L) - 1)
+    sdesc = m.SirenDesc(d=d, K=K, H=H, O=O, omega=W.SIREN_OMEGA)
+    coords = torch.from_numpy(inp["coords"]).cuda()
+    table = torch.from_numpy(inp["table"]).cuda()
+    wts = [torch.from_numpy(sw[k]).cuda() for k in ("W1", "b1", "W2", "b2")]
+    u, du, lu = (torch.full(sh, float("nan"), device="cuda") for sh in ((O, n), (d, O, n), (O, n)))
+    hg.hg_encode_siren_fwd(desc, n, coords, m.packed_views(table, d), sdesc, *wts, u, du, lu)
+    g = torch.empty((L, F, n), device="cuda")
+    dg = torch.empty((d, L, F, n), device="cuda")
+    lp = torch.empty((L, F, n), device="cuda")
+    hg.hg_encode_fwd(desc, n, coords, m.packed_views(table, d), g, dg, lp)
+    u2, du2, lu2 = (torch.full(sh, float("nan"), device="cuda") for sh in ((O, n), (d, O, n), (O, n)))
+    hg.hg_siren_fwd(sdesc, n, g, dg, lp, *wts, u2, du2, lu2)
+    torch.cuda.synchronize()
+    got = {k: np.moveaxis(host(t), -1, 0) for k, t in (("u", u), ("du", du), ("lapu", lu))}
+    for a, b in ((u, u2), (du, du2), (lu, lu2)):
+        assert np.array_equal(host(a), host(b))
+    del g, dg, lp, u2, du2, lu2
+    orders = [np.ascontiguousarray(o, np.float64) for o in W.split_orders(np.asarray(inp["table"], np.float64), d)]
+    for lo in range(0, n, CHUNK // 4):
+        hi = min(n, lo + CHUNK // 4)
+        enc = oracle.encode_fwd(d, F, res, w.log2_T, orders, inp["coords"][lo:hi])
+        m_ = hi - lo
+        flat = {k: enc[k].reshape(m_, K) if k in ("gamma", "lap", "mgamma", "mlap") else enc[k].reshape(m_, d, K)
+                for k in ("gamma", "dgamma", "lap", "mgamma", "mdgamma", "mlap")}
+        ref = oracle.siren_fwd(flat["gamma"], flat["dgamma"], flat["lap"], sw["W1"], sw["b1"], sw["W2"], sw["b2"],
+                               W.SIREN_OMEGA, mgamma=flat["mgamma"], mdgamma=flat["mdgamma"], mlap=flat["mlap"])
+        for k in ("u", "du", "lapu"):
+            check_close(f"{k} points {lo}..{hi}", got[k][lo:hi], ref[k], ref["m" + k])

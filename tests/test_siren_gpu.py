@@ -158,3 +158,75 @@ def test_siren_backward_over_the_shared_memory_limit_is_refused():
     buf = torch.zeros(1 << 20, device="cuda")
     st = m.hg.hg_siren_bwd(desc, 16, buf, buf, buf, buf, buf, buf, buf, None, None, buf, check=False)
     assert st == m.hg.HG_ERR_UNSUPPORTED
+
+
+# Fused encoder + SIREN forward (hg_encode_siren_fwd): the Hermite encoding of
+# each point formed on chip and fed to the first layer.
+# (id, d, L, n_min, n_max, log2T, dtype, n, level_mask, H, O, omega)
+FUSED = [
+    ("2d_pinn_grid", 2, 16, 16, 1024, 19, "f32", 3000, None, 64, 1, 30.0),
+    ("2d_f16_mask", 2, 8, 4, 200, 12, "f16", 2049, 0b10110101, 32, 2, 30.0),
+    ("2d_H128_O3", 2, 8, 4, 90, 10, "f32", 700, None, 128, 3, 10.0),
+    ("3d_f32", 3, 8, 4, 64, 12, "f32", 1500, None, 64, 1, 30.0),
+    ("3d_f16_mask", 3, 4, 4, 40, 10, "f16", 777, 0b1011, 64, 1, 30.0),
+    ("2d_one_point", 2, 4, 4, 32, 12, "f32", 1, None, 64, 1, 30.0),
+]
+
+
+def _oracle_chain(oracle, d, F, res, log2T, orders, coords, mask, sw, omega):
+    """The oracle's encoding, then its SIREN, with the encoder's magnitudes
+    carried into the SIREN's (the condition magnitude of the composed
+    evaluation)."""
+    L = len(res)
+    n = coords.shape[0]
+    enc = oracle.encode_fwd(d, F, res, log2T, orders, coords, level_mask=mask)
+    K = L * F
+    flat = {k: enc[k].reshape(n, K) if k in ("gamma", "lap", "mgamma", "mlap") else enc[k].reshape(n, d, K)
+            for k in ("gamma", "dgamma", "lap", "mgamma", "mdgamma", "mlap")}
+    return oracle.siren_fwd(flat["gamma"], flat["dgamma"], flat["lap"], sw["W1"], sw["b1"], sw["W2"], sw["b2"],
+                            omega, mgamma=flat["mgamma"], mdgamma=flat["mdgamma"], mlap=flat["mlap"])
+
+
+@pytest.mark.parametrize("case", FUSED, ids=[c[0] for c in FUSED])
+def test_fused_encoder_siren_forward_parity(case):
+    import multiresolution_hash_grid_02_b300 as m
+    from multiresolution_hash_grid_02_b300 import workloads as W
+    import oracle
+    from test_parity_gpu import _coords
+    cid, d, L, nmin, nmax, log2T, dt, n, mask, H, O, omega = case
+    F, K = 2, L * 2
+    rng = np.random.default_rng(zlib.crc32(cid.encode()))
+    res = oracle.level_resolutions(L, nmin, nmax)
+    coords = _coords(rng, n, d, res)
+    npdt = np.float16 if dt == "f16" else np.float32
+    table = (rng.uniform(-1, 1, (L, 1 << log2T, 1 << d, F)) * 0.05).astype(npdt)
+    sw = W.siren_weights(rng, K, H, O, omega)
+    desc = m.GridDesc(d=d, L=L, F=F, n_min=nmin, n_max=nmax, log2_T=(log2T,) * (d + 1), level_mask=mask,
+                      dtype=m.HG_F16 if dt == "f16" else m.HG_F32, layout=m.HG_FEATURE_MAJOR)
+    sdesc = m.SirenDesc(d=d, K=K, H=H, O=O, omega=omega)
+    t_dev, c_dev = dev(table), dev(coords)
+    wts = [dev(sw[k]) for k in ("W1", "b1", "W2", "b2")]
+    u, du, lu = (torch.full(sh, float("nan"), device="cuda") for sh in ((O, n), (d, O, n), (O, n)))
+    m.hg.hg_encode_siren_fwd(desc, n, c_dev, m.packed_views(t_dev, d), sdesc, *wts, u, du, lu)
+    torch.cuda.synchronize()
+    ref = _oracle_chain(oracle, d, F, res, (log2T,) * (d + 1), W.split_orders(table, d), coords, mask, sw, omega)
+    check_close("u", _pm(host(u)), ref["u"], ref["mu"])
+    check_close("du", _pm(host(du)), ref["du"], ref["mdu"])
+    check_close("lapu", _pm(host(lu)), ref["lapu"], ref["mlapu"])
+    # against the unfused chain on the GPU: the encoder's outputs through memory, then the SIREN
+    g = torch.empty((L, F, n), device="cuda")
+    dg = torch.empty((d, L, F, n), device="cuda")
+    lp = torch.empty((L, F, n), device="cuda")
+    m.hg.hg_encode_fwd(desc, n, c_dev, m.packed_views(t_dev, d), g, dg, lp)
+    u2, du2, lu2 = (torch.full(sh, float("nan"), device="cuda") for sh in ((O, n), (d, O, n), (O, n)))
+    m.hg.hg_siren_fwd(sdesc, n, g, dg, lp, *wts, u2, du2, lu2)
+    torch.cuda.synchronize()
+    if d == 2:
+        # the same 2D encoder arithmetic (one thread per item) and the same SIREN tile: bit for bit
+        for a, b in ((u, u2), (du, du2), (lu, lu2)):
+            assert np.array_equal(host(a), host(b))
+    # outputs not requested are not written
+    u3 = torch.full((O, n), float("nan"), device="cuda")
+    m.hg.hg_encode_siren_fwd(desc, n, c_dev, m.packed_views(t_dev, d), sdesc, *wts, u3)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(u3), host(u))
