@@ -93,15 +93,15 @@ def parse_args():
 
 def kernel_source_hash() -> str:
     """sha256 over the sources of the encoding kernels and the headers they
-    include (the roofline probes' source and header are left out: they do
-    not change the encoding kernels' traffic)."""
+    include (the roofline probes' and the SIREN consumer's sources are left
+    out: they do not change the encoding kernels' traffic)."""
     import glob
     import hashlib
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "multiresolution_hash_grid_02_b300", "csrc")
     files = sorted(f for f in glob.glob(os.path.join(pkg, "*.cu")) + glob.glob(os.path.join(pkg, "*.cuh")) +
                    glob.glob(os.path.join(pkg, "*.h")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
-                   if os.path.basename(f) not in ("probes.cu", "hg_probe.h"))
+                   if os.path.basename(f) not in ("probes.cu", "hg_probe.h", "siren.cu"))
     for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
