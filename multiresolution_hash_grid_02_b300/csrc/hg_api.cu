@@ -494,6 +494,14 @@ hg_status siren_plan(const hg_siren_desc* desc, int64_t n, hg::SirenParams& p) {
     return HG_OK;
 }
 
+// Largest opt-in shared memory per block of the current device.
+hg_status query_smem_max(int& smem_max) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    return e == cudaSuccess ? HG_OK : HG_ERR_CUDA;
+}
+
 // One wave of persistent CTAs for a planned launch (n > 0), and the number of input buffers.
 hg_status siren_grid(hg::SirenParams& p, bool bwd, int& ctas) {
     const int64_t n = p.n;
@@ -833,6 +841,10 @@ hg_status hg_siren_fwd(const hg_siren_desc* desc, int64_t n, const float* gamma,
     p.u = u;
     p.du = du;
     p.lapu = lapu;
+    int smem_max = 0;
+    if (query_smem_max(smem_max) != HG_OK) return fail(HG_ERR_CUDA, "device query failed");
+    if (hg::siren_tc_usable(p, smem_max))
+        return launch_status(hg::launch_siren_fwd_tc(p, stream), "SIREN forward (tensor cores)");
     if ((st = siren_grid(p, false, ctas)) != HG_OK) return st;
     return launch_status(hg::launch_siren_fwd(p, ctas, stream), "SIREN forward");
 }

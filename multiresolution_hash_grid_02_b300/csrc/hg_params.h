@@ -145,5 +145,10 @@ int siren_ctas_per_sm(const SirenParams& p, bool bwd, int* ctas);
 // one input buffer): CTAs per SM, and the launch of `ctas` persistent CTAs.
 int encode_siren_ctas_per_sm(const SirenParams& p, int dtype, int* ctas);
 int launch_encode_siren_fwd(const SirenParams& p, const FwdParams& e, int dtype, int ctas, void* stream);
+// Tensor-core SIREN forward (split tf32 first layer, 128-point tiles, one CTA per SM): whether a shape
+// takes it (d >= 3, H >= 64, (d + 2) H <= 512 TMEM columns, operands within `smem_max` bytes of shared
+// memory), and its launch.
+bool siren_tc_usable(const SirenParams& p, int smem_max);
+int launch_siren_fwd_tc(const SirenParams& p, void* stream);
 
 }  // namespace hg

@@ -22,6 +22,7 @@
 #include "hermite_blend.cuh"
 #include "hg_device.cuh"
 #include "hg_params.h"
+#include "siren_tc.cuh"
 
 namespace hg {
 namespace {
@@ -299,6 +300,254 @@ __global__ void __launch_bounds__(kThreads, 2) encode_siren_fwd_kernel(const __g
         siren_tile_fwd<D>(p, sm + L.w1t, sm + L.b1, sm + L.w2, sm + L.b2, X, n0, pl, q);
         __syncthreads();  // every thread done with the tile before the next encode
     }
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core forward (tcgen05, split tf32; see siren_tc.cuh).  A CTA of 512
+// threads takes tiles of 128 points: the tile's inputs (the encoder's
+// feature-major outputs) are split into tf32 hi/lo parts in shared memory;
+// one thread issues, for every input row r, the three products of
+// Z_r = X_r W1^T (K / 8 MMAs of 128 x H x 8 each) into TMEM columns
+// [r H, (r+1) H); then each thread reads its point's row of Z (TMEM lane =
+// point; the four warps of a lane quadrant take one quarter of the hidden
+// units each) and forms u, grad u and lap u as the CUDA-core forward does.
+// One CTA per SM (the split operands take ~180 KB for d = 3, K = 32); the
+// staging loads are issued in batches so several are in flight per thread.
+// Measured (2^21 points, K = 32, H = 64): 3D 1.45 ms against 1.62 ms on the
+// CUDA cores; 2D 0.74 against 0.69 ms (fewer rows per point, so the
+// staging, not the contraction, dominates) -- hence d >= 3 only.  Staging
+// the raw tile with 4-byte cp.async copies during the previous epilogue was
+// slower (1.76 ms), and so was encoding in place for the fused forward with
+// one CTA per SM (7.6 against 3.3 ms: the gathers cannot be hidden).
+// ---------------------------------------------------------------------------
+constexpr int kTcPts = 128;
+constexpr int kTcThreads = 512;
+constexpr int kTcGroups = kTcThreads / kTcPts;  // warps per TMEM lane quadrant: unit groups
+constexpr int kTcSpin = 1 << 20;  // polls of the completion barrier before giving up
+
+struct TcLayout {
+    int w, x, b1, w2, b2, red, total;  // byte offsets in dynamic shared memory
+};
+
+__host__ __device__ inline int tc_take(int& at, int bytes, int align) {
+    at = (at + align - 1) / align * align;
+    const int here = at;
+    at += bytes;
+    return here;
+}
+
+__host__ __device__ inline TcLayout tc_layout(const SirenParams& p) {
+    const int R = p.d + 2;
+    TcLayout t;
+    int at = 0;
+    t.w = tc_take(at, 2 * p.H * p.K * 4, 1024);           // W1 hi, lo: [H][K] core layout each
+    t.x = tc_take(at, 2 * R * kTcPts * p.K * 4, 1024);     // X_r hi, lo: [128][K] core layout each
+    t.b1 = tc_take(at, p.H * 4, 16);
+    t.w2 = tc_take(at, p.O * p.H * 4, 16);
+    t.b2 = tc_take(at, kMaxO * 4, 16);
+    t.red = tc_take(at, (kTcGroups - 1) * kTcPts * kMaxO * (p.d + 2) * 4, 16);  // other groups' partial outputs
+    t.total = at;
+    return t;
+}
+
+__host__ __device__ inline uint32_t tc_cols(const SirenParams& p) {
+    uint32_t c = 32;
+    while (c < static_cast<uint32_t>((p.d + 2) * p.H)) c <<= 1;
+    return c;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1) siren_fwd_tc_kernel(const __grid_constant__ SirenParams p) {
+    constexpr int R = D + 2;
+    extern __shared__ __align__(1024) unsigned char tsm[];
+    __shared__ __align__(8) uint64_t mbar;
+    __shared__ uint32_t tslot;
+    const TcLayout Lt = tc_layout(p);
+    const int K = p.K, H = p.H, O = p.O;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned char* sw = tsm + Lt.w;
+    unsigned char* sx = tsm + Lt.x;
+    float* b1s = reinterpret_cast<float*>(tsm + Lt.b1);
+    float* w2s = reinterpret_cast<float*>(tsm + Lt.w2);
+    float* b2s = reinterpret_cast<float*>(tsm + Lt.b2);
+    float* red = reinterpret_cast<float*>(tsm + Lt.red);
+    const int wbytes = H * K * 4, xbytes = kTcPts * K * 4;
+    for (int i = tid; i < H * K; i += kTcThreads) {
+        float hi, lo;
+        tc::split_tf32(__ldg(p.W1 + i), hi, lo);
+        const uint32_t o = tc::kmajor_off(i / K, i % K, K);
+        *reinterpret_cast<float*>(sw + o) = hi;
+        *reinterpret_cast<float*>(sw + wbytes + o) = lo;
+    }
+    for (int i = tid; i < H; i += kTcThreads) b1s[i] = __ldg(p.b1 + i);
+    for (int i = tid; i < O * H; i += kTcThreads) w2s[i] = __ldg(p.W2 + i);
+    for (int i = tid; i < kMaxO; i += kTcThreads) b2s[i] = (p.b2 && i < O) ? __ldg(p.b2 + i) : 0.f;
+    if (tid == 0) tc::mbar_init(&mbar, 1);
+    const uint32_t cols = tc_cols(p);
+    if (warp == 0) tc::tmem_alloc(&tslot, cols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = tslot;
+    const uint32_t idesc = tc::idesc_tf32(H);
+    const uint32_t lbo = 128, sbo = static_cast<uint32_t>(K / 4) * 128;
+    const float om = p.omega, om2 = om * om;
+    const int64_t tiles = (p.n + kTcPts - 1) / kTcPts;
+    uint32_t phase = 0;
+    int64_t failed = -1;  // the tile whose products did not complete in time
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int64_t n0 = t * kTcPts;
+        // (1) the tile's inputs, split, into the operand layout (points past n: zeros); the loads of
+        // B items are issued together, so several are in flight per thread
+        {
+            constexpr int B = 4;
+            const int K4 = K / 4, total = R * K4 * kTcPts;
+            for (int i0 = tid; i0 < total; i0 += B * kTcThreads) {
+                float v[B][4];
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    const int i = i0 + b * kTcThreads;
+                    const int m = i & (kTcPts - 1), rc = i / kTcPts;
+                    const int c = rc % K4, r = rc / K4;
+                    const int64_t n = n0 + m;
+                    const float* src = i < total ? p.in[r] : nullptr;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        v[b][q] = (src && n < p.n) ? __ldg(src + static_cast<int64_t>(4 * c + q) * p.n + n) : 0.f;
+                }
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    const int i = i0 + b * kTcThreads;
+                    if (i >= total) break;
+                    const int m = i & (kTcPts - 1), rc = i / kTcPts;
+                    const int c = rc % K4, r = rc / K4;
+                    float4 hi, lo;
+                    tc::split_tf32(v[b][0], hi.x, lo.x);
+                    tc::split_tf32(v[b][1], hi.y, lo.y);
+                    tc::split_tf32(v[b][2], hi.z, lo.z);
+                    tc::split_tf32(v[b][3], hi.w, lo.w);
+                    const uint32_t o = tc::kmajor_off(m, 4 * c, K);
+                    *reinterpret_cast<float4*>(sx + (2 * r) * xbytes + o) = hi;
+                    *reinterpret_cast<float4*>(sx + (2 * r + 1) * xbytes + o) = lo;
+                }
+            }
+        }
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        // (2) Z_r = X_r W1^T for every row: hi*hi, hi*lo, lo*hi
+        if (tid == 0) {
+            for (int r = 0; r < R; ++r) {
+                for (int pass = 0; pass < 3; ++pass) {
+                    const uint32_t xa = tc::smem_u32(sx + (2 * r + (pass == 2 ? 1 : 0)) * xbytes);
+                    const uint32_t wb = tc::smem_u32(sw + (pass == 1 ? wbytes : 0));
+                    for (int s = 0; s < K / 8; ++s)
+                        tc::mma_tf32(tmem + static_cast<uint32_t>(r * H), tc::desc(xa + s * 256, lbo, sbo),
+                                     tc::desc(wb + s * 256, lbo, sbo), idesc, pass > 0 || s > 0);
+                }
+            }
+            tc::commit(&mbar);
+        }
+        const bool done = tc::mbar_wait(&mbar, phase, kTcSpin);
+        phase ^= 1u;
+        if (__syncthreads_or(!done)) {
+            failed = t;
+            break;
+        }
+        tc::fence_after();
+        // (3) epilogue: the thread's point is TMEM lane 32 (warp % 4) + lane; its group's quarter of the units
+        const int quad = warp & 3, grp = warp >> 2, m = quad * 32 + lane;
+        const uint32_t lbase = tmem + ((static_cast<uint32_t>(quad) * 32u) << 16);
+        float pu[kMaxO], pdu[D][kMaxO], plap[kMaxO];
+#pragma unroll
+        for (int o = 0; o < kMaxO; ++o) {
+            pu[o] = plap[o] = 0.f;
+#pragma unroll
+            for (int i = 0; i < D; ++i) pdu[i][o] = 0.f;
+        }
+        const int hq = H / kTcGroups;
+        for (int j0 = grp * hq; j0 < (grp + 1) * hq; j0 += 16) {
+            uint32_t zr[R][16];
+#pragma unroll
+            for (int r = 0; r < R; ++r) tc::tmem_ld16_async(lbase + static_cast<uint32_t>(r * H + j0), zr[r]);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                const int j = j0 + jj;
+                float a, c;
+                sincosf(om * (__uint_as_float(zr[0][jj]) + b1s[j]), &a, &c);
+                float y2 = 0.f;
+#pragma unroll
+                for (int i = 0; i < D; ++i) y2 = fmaf(__uint_as_float(zr[1 + i][jj]), __uint_as_float(zr[1 + i][jj]), y2);
+                const float oc = om * c;
+                const float tl = fmaf(oc, __uint_as_float(zr[R - 1][jj]), -om2 * a * y2);
+#pragma unroll
+                for (int o = 0; o < kMaxO; ++o) {
+                    if (o < O) {
+                        const float w2 = w2s[o * H + j];
+                        pu[o] = fmaf(w2, a, pu[o]);
+#pragma unroll
+                        for (int i = 0; i < D; ++i) pdu[i][o] = fmaf(w2, oc * __uint_as_float(zr[1 + i][jj]), pdu[i][o]);
+                        plap[o] = fmaf(w2, tl, plap[o]);
+                    }
+                }
+            }
+        }
+        // the other groups' partial sums to group 0, which stores the point's outputs (groups in order)
+        if (grp > 0) {
+            float* rp = red + ((grp - 1) * kTcPts + m) * (kMaxO * R);
+#pragma unroll
+            for (int o = 0; o < kMaxO; ++o) {
+                rp[o * R] = pu[o];
+                rp[o * R + 1] = plap[o];
+#pragma unroll
+                for (int i = 0; i < D; ++i) rp[o * R + 2 + i] = pdu[i][o];
+            }
+        }
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        const int64_t n = n0 + m;
+        if (grp == 0 && n < p.n) {
+#pragma unroll
+            for (int g = 0; g < kTcGroups - 1; ++g) {
+                const float* rp = red + (g * kTcPts + m) * (kMaxO * R);
+#pragma unroll
+                for (int o = 0; o < kMaxO; ++o) {
+                    pu[o] += rp[o * R];
+                    plap[o] += rp[o * R + 1];
+#pragma unroll
+                    for (int i = 0; i < D; ++i) pdu[i][o] += rp[o * R + 2 + i];
+                }
+            }
+#pragma unroll
+            for (int o = 0; o < kMaxO; ++o) {
+                if (o < O) {
+                    if (p.u) __stcs(p.u + o * p.n + n, pu[o] + b2s[o]);
+                    if (p.du) {
+#pragma unroll
+                        for (int i = 0; i < D; ++i) __stcs(p.du + (static_cast<int64_t>(i) * O + o) * p.n + n, pdu[i][o]);
+                    }
+                    if (p.lapu) __stcs(p.lapu + o * p.n + n, plap[o]);
+                }
+            }
+        }
+        __syncthreads();  // the reduction buffer and the operands are free for the next tile
+    }
+    if (failed >= 0) {
+        // the products did not complete in time: mark the tile's outputs invalid (NaN), give the tensor
+        // core a bounded while longer to finish before the accumulator memory is released
+        (void)tc::mbar_wait(&mbar, phase ^ 1u, kTcSpin);
+        if (tid < kTcPts) {
+            const int64_t n = failed * kTcPts + tid;
+            if (n < p.n && p.u) p.u[n] = __int_as_float(0x7fc00000);
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) tc::tmem_free(tmem, cols);
 }
 
 // Backward.  Per tile: (1) recompute the first layer, form the pre-activation
@@ -624,6 +873,32 @@ cudaError_t fused_dispatch(const SirenParams& p, const FwdParams& e, int dtype, 
                            : fused_attr<3, float>(bytes, per_sm, p, e, ctas, s, launch);
 }
 }  // namespace
+
+bool siren_tc_usable(const SirenParams& p, int smem_max) {
+    return p.d >= 3 && p.H >= 16 * kTcGroups && (p.d + 2) * p.H <= 512 && p.K % 8 == 0 && p.O <= kMaxO &&
+           tc_layout(p).total + 1024 <= smem_max;
+}
+
+namespace {
+template <int D>
+cudaError_t tc_launch(const SirenParams& p, cudaStream_t s) {
+    const int bytes = tc_layout(p).total;
+    cudaError_t err = cudaFuncSetAttribute(siren_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err != cudaSuccess) return err;
+    int dev = 0, sms = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    const int64_t tiles = (p.n + kTcPts - 1) / kTcPts;
+    const int ctas = static_cast<int>(tiles < sms ? tiles : sms);  // one CTA per SM (shared memory)
+    siren_fwd_tc_kernel<D><<<ctas, kTcThreads, bytes, s>>>(p);
+    return cudaGetLastError();
+}
+}  // namespace
+
+int launch_siren_fwd_tc(const SirenParams& p, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return p.d == 3 ? tc_launch<3>(p, s) : tc_launch<4>(p, s);
+}
 
 int encode_siren_ctas_per_sm(const SirenParams& p, int dtype, int* ctas) {
     return fused_dispatch(p, FwdParams{}, dtype, ctas, 0, nullptr, false);

@@ -170,6 +170,9 @@ FUSED = [
     ("3d_f32", 3, 8, 4, 64, 12, "f32", 1500, None, 64, 1, 30.0),
     ("3d_f16_mask", 3, 4, 4, 40, 10, "f16", 777, 0b1011, 64, 1, 30.0),
     ("2d_one_point", 2, 4, 4, 32, 12, "f32", 1, None, 64, 1, 30.0),
+    # shapes that keep the first layer on the CUDA cores (H < 32; (d + 2) H > 512 TMEM columns)
+    ("2d_H16_cuda_cores", 2, 8, 4, 60, 10, "f32", 900, None, 16, 1, 30.0),
+    ("3d_H128_cuda_cores", 3, 4, 4, 40, 10, "f32", 500, None, 128, 1, 30.0),
 ]
 
 
