@@ -19,7 +19,9 @@
 // per (point, level); taps outside the grid get weight 0 and are not read.
 // The backward is the transposed contraction, accumulated per CTA in a
 // shared-memory tile of its points' neighbourhoods (the page samples
-// stratified points, so a CTA's points are neighbours) before the scatter.
+// stratified points, so a CTA's points are neighbours) before the scatter;
+// in 3D it runs per run of same-cell points and tap row (k1, k2), with the
+// points' separable factors summed in registers (rbf_bwd_cells_kernel).
 #include <cuda_runtime.h>
 
 #include "hg_device.cuh"
@@ -462,6 +464,261 @@ __global__ void __launch_bounds__(kTileBlock, kTileCtas) rbf_bwd_tile_kernel(con
     }
 }
 
+// Cell-run backward, 3D.  The points of a run (consecutive points in one
+// cell) share their K^3 taps, and with the moment form above the gradient
+// of tap (k0, k1, k2) summed over the run's points is
+//   sum_p  w0[k0] Sw[k1,k2] + (w0 delta0)[k0] Sd[k1,k2] + (w0 q0)[k0] Sq[k1,k2],
+// where per point P = w1 w2, Sd = bd0 P, Sq = cl P and
+//   Sw = a0 P + bd1 (w1 delta1) w2 + bd2 w1 (w2 delta2) + cl ((w1 q1) w2 + w1 (w2 q2))
+// (a0 = g_gamma, bd_i = -v g_dgamma_i, cl = v^2 g_lap): the transposed
+// contraction with axis 0 folded in last.  A CTA writes each point's
+// factors to shared memory (axis 0's three weight vectors, the weights and
+// moments of axes 1 and 2, the upstream coefficients), then one thread per
+// (run, k1, k2) sums the K x FC gradients of its taps over the run's points
+// in registers and adds each into the CTA's tile once.  Per point this
+// takes about a sixth of the instructions of a per-point scatter with
+// in-warp run sums (no shuffles; one shared-memory add per tap and run, not
+// per tap and point).  The tile covers the bounding box of the CTA's taps
+// as in rbf_bwd_tile_kernel; when it does not fit, each run's taps are added
+// to the table directly.
+constexpr int kCellBlock = 256;
+constexpr int kCellTileFloats = 6 * 1024;  // 24 KB: the full-grid 3D box of two stratified rows of 128 points
+constexpr int kCellCtas = 3;
+
+template <int K, int FC>
+struct CellRec {
+    static constexpr int a0 = 0;                  // w0[K], (w0 delta0)[K], (w0 q0)[K]
+    static constexpr int a1 = 3 * K;              // w1[K], tau1, var1
+    static constexpr int a2 = a1 + K + 2;         // w2[K], tau2, var2
+    static constexpr int coef = a2 + K + 2;       // a0[FC], bd0[FC], bd1[FC], bd2[FC], cl[FC]
+    static constexpr int key = coef + 5 * FC;     // the cell: first tap of each axis (int32)
+    static constexpr int size = (key + 3 + 3) & ~3;  // floats; a multiple of 4 keeps records 16-byte aligned
+    static_assert((3 * K) % 4 == 0 || (3 * K) % 4 == 2, "axis-0 block: float4s and at most one float2");
+    static_assert(a1 % 2 == 0 && a2 % 2 == 0 && coef % 2 == 0, "float2 fields");
+};
+
+template <int K, int FC>
+constexpr int cell_smem_bytes() {
+    return (kCellBlock * CellRec<K, FC>::size + kCellTileFloats) * static_cast<int>(sizeof(float));
+}
+
+// v[0 .. M) from 16-byte-aligned shared memory, in float4 loads (and one float2).
+template <int M>
+__device__ __forceinline__ void lds_floats(const float* s, float (&v)[M]) {
+#pragma unroll
+    for (int i = 0; i + 4 <= M; i += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(s + i);
+        v[i] = x.x;
+        v[i + 1] = x.y;
+        v[i + 2] = x.z;
+        v[i + 3] = x.w;
+    }
+    if constexpr (M % 4 == 2) {
+        const float2 x = *reinterpret_cast<const float2*>(s + M - 2);
+        v[M - 2] = x.x;
+        v[M - 1] = x.y;
+    }
+}
+
+template <int R, int FC, bool VEC>
+__global__ void __launch_bounds__(kCellBlock, kCellCtas) rbf_bwd_cells_kernel(const __grid_constant__ BwdParams p) {
+    constexpr int K = 2 * R;
+    using Rec = CellRec<K, FC>;
+    constexpr int kItems = K * K;                  // (k1, k2) pairs of a run
+    constexpr int kSlots = kCellBlock / kItems;    // runs in progress at once
+    static_assert(kSlots >= 1, "K^2 <= block");
+    extern __shared__ float4 cell_smem4[];
+    float* rec = reinterpret_cast<float*>(cell_smem4);  // [kCellBlock][Rec::size]
+    float* tile = rec + kCellBlock * Rec::size;         // [kCellTileFloats]
+    __shared__ int32_t box_lo[3], box_hi[3];
+    __shared__ int32_t run_start[kCellBlock + 1];
+    __shared__ int32_t warp_runs[kCellBlock / 32];
+    const int l = p.c.lvl[blockIdx.y];
+    if (!((p.c.level_mask >> l) & 1u)) return;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kCellBlock;
+    const int cnt = static_cast<int>(min(static_cast<int64_t>(kCellBlock), p.c.n - n0));
+    const bool have = t < cnt;
+    const int64_t n = n0 + (have ? t : cnt - 1);
+    const Level& lv = p.c.lv[l];
+    const int F = p.c.F;
+    const int32_t N = static_cast<int32_t>(lv.N);
+    const float v = 2.f * p.eps * p.eps * lv.fN;
+    float* my = rec + t * Rec::size;
+    int32_t* my_key = reinterpret_cast<int32_t*>(my + Rec::key);
+    {
+        RbfAxis<K> A[3];
+        rbf_axes<3, K>(p.coords, n, lv, p.eps * p.eps, A);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            float dl, q;
+            rbf_moments(A[0], k, dl, q);
+            my[Rec::a0 + k] = A[0].w[k];
+            my[Rec::a0 + K + k] = A[0].w[k] * dl;
+            my[Rec::a0 + 2 * K + k] = A[0].w[k] * q;
+            my[Rec::a1 + k] = A[1].w[k];
+            my[Rec::a2 + k] = A[2].w[k];
+        }
+        my[Rec::a1 + K] = A[1].tau;
+        my[Rec::a1 + K + 1] = A[1].var;
+        my[Rec::a2 + K] = A[2].tau;
+        my[Rec::a2 + K + 1] = A[2].var;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) my_key[i] = A[i].first;
+        if (t < 3) {
+            box_lo[t] = INT32_MAX;
+            box_hi[t] = INT32_MIN;
+        }
+    }
+    __syncthreads();
+    // bounding box of the CTA's taps (clipped to the grid), and the runs: a point starts one when its cell
+    // differs from the previous point's
+    bool lead = false;
+    if (have) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            atomicMin(&box_lo[i], max(my_key[i], 0));
+            atomicMax(&box_hi[i], min(my_key[i] + K - 1, N));
+        }
+        lead = t == 0;
+        if (!lead) {
+            const int32_t* prev = reinterpret_cast<const int32_t*>(my - Rec::size + Rec::key);
+            lead = prev[0] != my_key[0] || prev[1] != my_key[1] || prev[2] != my_key[2];
+        }
+    }
+    const uint32_t ball = __ballot_sync(0xffffffffu, lead);
+    if (lane == 0) warp_runs[warp] = __popc(ball);
+    __syncthreads();
+    int before = 0, runs = 0;
+#pragma unroll
+    for (int w = 0; w < kCellBlock / 32; ++w) {
+        const int c = warp_runs[w];
+        before += w < warp ? c : 0;
+        runs += c;
+    }
+    if (lead) run_start[before + __popc(ball & ((1u << lane) - 1u))] = t;
+    if (t == 0) run_start[runs] = cnt;
+    int32_t lo[3], ext[3];
+    int64_t vol = 1;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        lo[i] = box_lo[i];
+        ext[i] = box_hi[i] - box_lo[i] + 1;
+        vol *= ext[i];
+    }
+    const bool tiled = vol * F <= kCellTileFloats;  // the same for the whole CTA
+    if (tiled)
+        for (int32_t i = t; i < static_cast<int32_t>(vol) * F; i += kCellBlock) tile[i] = 0.f;
+    float* gbase = p.grad.ptr[0] + l * p.grad.ls[0];
+    const int64_t rs = p.grad.rs[0];
+    const uint32_t tm = p.c.tmask[0];
+    const int slot = t / kItems, item = t - slot * kItems;
+    const int k1 = item % K, k2 = item / K;
+    for (int f0 = 0; f0 < F; f0 += FC) {
+        // the point's upstream coefficients for this feature chunk (zero past the end)
+#pragma unroll
+        for (int f = 0; f < FC; ++f) {
+            const int64_t lf = static_cast<int64_t>(l) * F + f0 + f;
+            float c[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+            if (have) {
+                if (p.g_gamma) c[0] = __ldg(p.g_gamma + n * p.c.sn + lf * p.c.sf);
+                if (p.g_dgamma) {
+#pragma unroll
+                    for (int j = 0; j < 3; ++j) c[1 + j] = -v * __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf);
+                }
+                if (p.g_lap) c[4] = v * v * __ldg(p.g_lap + n * p.c.sn + lf * p.c.sf);
+            }
+#pragma unroll
+            for (int j = 0; j < 5; ++j) my[Rec::coef + j * FC + f] = c[j];
+        }
+        __syncthreads();
+        if (slot < kSlots) {
+            for (int r = slot; r < runs; r += kSlots) {
+                const int pa = run_start[r], pb = run_start[r + 1];
+                const int32_t* key = reinterpret_cast<const int32_t*>(rec + pa * Rec::size + Rec::key);
+                const int32_t g0 = key[0], g1 = key[1] + k1, g2 = key[2] + k2;
+                if (g1 < 0 || g1 > N || g2 < 0 || g2 > N) continue;  // outside the grid: weight 0, no row
+                float acc[K][FC];
+#pragma unroll
+                for (int k = 0; k < K; ++k)
+#pragma unroll
+                    for (int f = 0; f < FC; ++f) acc[k][f] = 0.f;
+                for (int q = pa; q < pb; ++q) {
+                    const float* pr = rec + q * Rec::size;
+                    float a0[3 * K];
+                    lds_floats<3 * K>(pr + Rec::a0, a0);
+                    const float w1 = pr[Rec::a1 + k1], w2 = pr[Rec::a2 + k2];
+                    const float2 m1 = *reinterpret_cast<const float2*>(pr + Rec::a1 + K);
+                    const float2 m2 = *reinterpret_cast<const float2*>(pr + Rec::a2 + K);
+                    const float dl1 = m1.x - static_cast<float>(k1), q1 = fmaf(dl1, dl1, -m1.y);
+                    const float dl2 = m2.x - static_cast<float>(k2), q2 = fmaf(dl2, dl2, -m2.y);
+                    const float P = w1 * w2, t1 = (w1 * dl1) * w2, t2 = w1 * (w2 * dl2);
+                    const float t3 = fmaf(w1 * q1, w2, w1 * (w2 * q2));
+                    float c[5][FC];
+                    if constexpr (FC == 2) {
+#pragma unroll
+                        for (int j = 0; j < 5; ++j) {
+                            const float2 x = *reinterpret_cast<const float2*>(pr + Rec::coef + 2 * j);
+                            c[j][0] = x.x;
+                            c[j][FC - 1] = x.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 5; ++j) c[j][0] = pr[Rec::coef + j];
+                    }
+#pragma unroll
+                    for (int f = 0; f < FC; ++f) {
+                        const float sw = fmaf(c[4][f], t3, fmaf(c[3][f], t2, fmaf(c[2][f], t1, c[0][f] * P)));
+                        const float sd = c[1][f] * P, sq = c[4][f] * P;
+#pragma unroll
+                        for (int k = 0; k < K; ++k)
+                            acc[k][f] = fmaf(a0[k], sw, fmaf(a0[K + k], sd, fmaf(a0[2 * K + k], sq, acc[k][f])));
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < K; ++k) {
+                    const int32_t gk = g0 + k;
+                    if (gk < 0 || gk > N) continue;
+                    if (tiled) {
+                        const int32_t e = (gk - lo[0]) + ext[0] * ((g1 - lo[1]) + ext[1] * (g2 - lo[2]));
+#pragma unroll
+                        for (int f = 0; f < FC; ++f) atomicAdd(tile + e * F + f0 + f, acc[k][f]);
+                    } else {
+                        float* e = gbase + rbf_row<3>(lv, tm, gk, g1, g2) * rs + f0;
+                        if constexpr (VEC) {
+                            red_add_v2(e, acc[k][0], acc[k][FC - 1]);
+                        } else {
+#pragma unroll
+                            for (int f = 0; f < FC; ++f) red_add_f32(e + f, acc[k][f]);
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (!tiled) return;
+    for (int32_t r = t; r < static_cast<int32_t>(vol); r += kCellBlock) {
+        const int32_t g0 = lo[0] + r % ext[0];
+        const int32_t g1 = lo[1] + (r / ext[0]) % ext[1];
+        const int32_t g2 = lo[2] + r / (ext[0] * ext[1]);
+        float* e = gbase + rbf_row<3>(lv, tm, g0, g1, g2) * rs;
+        const float* a = tile + r * F;
+        for (int f0 = 0; f0 < F; f0 += FC) {
+            bool any = false;
+#pragma unroll
+            for (int f = 0; f < FC; ++f) any = any || a[f0 + f] != 0.f;
+            if (!any) continue;
+            if constexpr (VEC) {
+                red_add_v2(e + f0, a[f0], a[f0 + FC - 1]);
+            } else {
+#pragma unroll
+                for (int f = 0; f < FC; ++f) red_add_f32(e + f0 + f, a[f0 + f]);
+            }
+        }
+    }
+}
+
 template <int D, int R, int FC, typename TT>
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t s) {
     dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
@@ -477,6 +734,15 @@ cudaError_t pick_fwd(const FwdParams& p, int fc, cudaStream_t s) {
 template <int D, int R, int FC, bool VEC>
 cudaError_t launch_bwd(const BwdParams& p, cudaStream_t s) {
     if (p.c.nlvl == 0) return cudaSuccess;
+    if constexpr (D == 3) {
+        constexpr int kSmem = cell_smem_bytes<2 * R, FC>();
+        cudaError_t e = cudaFuncSetAttribute(rbf_bwd_cells_kernel<R, FC, VEC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+        dim3 grid(static_cast<unsigned>((p.c.n + kCellBlock - 1) / kCellBlock), static_cast<unsigned>(p.c.nlvl));
+        rbf_bwd_cells_kernel<R, FC, VEC><<<grid, kCellBlock, kSmem, s>>>(p);
+        return cudaGetLastError();
+    }
     constexpr int kSmem = kTileFloats * static_cast<int>(sizeof(float));
     cudaError_t e = cudaFuncSetAttribute(rbf_bwd_tile_kernel<D, R, FC, VEC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);

@@ -273,7 +273,6 @@ __global__ void __launch_bounds__(kThreads, 2) siren_fwd_kernel(const __grid_con
 template <int D, typename TT>
 __global__ void __launch_bounds__(kThreads, 2) encode_siren_fwd_kernel(const __grid_constant__ SirenParams p,
                                                                       const __grid_constant__ FwdParams e) {
-    constexpr int R = D + 2;
     extern __shared__ float4 smem4[];
     float* sm = reinterpret_cast<float*>(smem4);
     const SirenSmem L = siren_layout(p, false);

@@ -5,8 +5,9 @@ oracle, element by element.
 Cases: d = 2 and 3; rings 1 to 4; kernel widths 0.5 to 2; dense (the page's
 grids) and hashed levels; fp32 and fp16 tables; F = 1, 2, 4; both layouts;
 masks; points at the grid's border (clipped neighbourhoods) and the edge
-coordinates; stratified (coherent) points; coarse levels with many points
-per vertex (the privatised backward).  Tolerance 1e-5 of the oracle's
+coordinates; stratified (coherent) points in 2D and 3D (runs of same-cell
+points, tiles over several rows of strata); coarse levels with many points
+per vertex.  Tolerance 1e-5 of the oracle's
 condition magnitude (every term of the quotient rule in absolute value)."""
 import zlib
 
@@ -41,6 +42,10 @@ CASES = [
     ("2d_F2_coarse_many_points", 2, 2, 2, 4, 8, 10, "f32", 1, 20000, None, 1.0, 3),
     ("3d_F2_coarse_many_points", 3, 2, 2, 2, 5, 10, "f32", 0, 30000, None, 1.0, 2),
     ("3d_one_point", 3, 2, 2, 4, 8, 10, "f32", 1, 1, None, 1.0, 3),
+    # 3D stratified points: runs of same-cell points, tiles of two or more rows of strata
+    ("3d_F2_stratified", 3, 3, 2, 7, 28, 15, "f32", 1, 13824, None, 1.0, 3),
+    ("3d_F1_stratified_hashed_point_major", 3, 2, 1, 5, 20, 12, "f32", 0, 8000, None, 0.8, 2),
+    ("3d_F4_stratified_ring4", 3, 2, 4, 4, 12, 12, "f32", 1, 4096, None, 1.2, 4),
 ]
 
 
