@@ -17,6 +17,8 @@
 // d2/dx_0^2 partial sums, as the Hermite blend -- of the 1D weights and
 // their 1D quotient-rule derivatives (d/dx = N d/dy folded in).  One thread
 // per (point, level); taps outside the grid get weight 0 and are not read.
+// For coherent points a CTA first stages the table rows of its taps'
+// bounding box in shared memory (rbf_fwd_box_kernel).
 // The backward is the transposed contraction, accumulated per CTA in a
 // shared-memory tile of its points' neighbourhoods (the page samples
 // stratified points, so a CTA's points are neighbours) before the scatter;
@@ -150,99 +152,251 @@ __device__ __forceinline__ void rbf_line(const TT* base, int64_t rs, int f0, con
     }
 }
 
+// gamma, d gamma / d x_i and lap gamma of one point and feature chunk from
+// the axis-0 sums of each tap row: line(k1, k2, s, sd, sq) returns, for the
+// row of taps (k1, k2) (k2 = 0 in 2D), s = sum w theta, sd = sum w delta
+// theta and sq = sum w q theta over k0.  The outer axes fold in as the
+// Hermite blend does: in offset units dg_i = sum W delta_i theta and
+// lp = sum W (q_0 + q_1 [+ q_2]) theta with the tap weight W = w_0 w_1 [w_2];
+// the gradient and Laplacian are -v dg and v^2 lp.
+template <int D, int K, int FC, typename Line>
+__device__ __forceinline__ void rbf_contract(const RbfAxis<K> (&A)[D], float v, float (&g)[FC], float (&dg)[3][FC],
+                                             float (&lp)[FC], Line&& line) {
+#pragma unroll
+    for (int f = 0; f < FC; ++f) g[f] = dg[0][f] = dg[1][f] = dg[2][f] = lp[f] = 0.f;
+    if constexpr (D == 2) {
+#pragma unroll
+        for (int k1 = 0; k1 < K; ++k1) {
+            if (!((A[1].valid >> k1) & 1u)) continue;
+            float s[FC], sd[FC], sq[FC], dl1, q1;
+            line(k1, 0, s, sd, sq);
+            rbf_moments(A[1], k1, dl1, q1);
+            const float w1 = A[1].w[k1], wd1 = w1 * dl1;
+#pragma unroll
+            for (int f = 0; f < FC; ++f) {
+                g[f] = fmaf(w1, s[f], g[f]);
+                dg[0][f] = fmaf(w1, sd[f], dg[0][f]);
+                dg[1][f] = fmaf(wd1, s[f], dg[1][f]);
+                lp[f] = fmaf(w1, fmaf(q1, s[f], sq[f]), lp[f]);
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int k2 = 0; k2 < K; ++k2) {
+            if (!((A[D - 1].valid >> k2) & 1u)) continue;
+            float a[FC], b[FC], cc[FC], dl[FC];
+#pragma unroll
+            for (int f = 0; f < FC; ++f) a[f] = b[f] = cc[f] = dl[f] = 0.f;
+#pragma unroll
+            for (int k1 = 0; k1 < K; ++k1) {
+                if (!((A[1].valid >> k1) & 1u)) continue;
+                float s[FC], sd[FC], sq[FC], dl1, q1;
+                line(k1, k2, s, sd, sq);
+                rbf_moments(A[1], k1, dl1, q1);
+                const float w1 = A[1].w[k1], wd1 = w1 * dl1;
+#pragma unroll
+                for (int f = 0; f < FC; ++f) {
+                    a[f] = fmaf(w1, s[f], a[f]);
+                    b[f] = fmaf(w1, sd[f], b[f]);
+                    cc[f] = fmaf(wd1, s[f], cc[f]);
+                    dl[f] = fmaf(w1, fmaf(q1, s[f], sq[f]), dl[f]);
+                }
+            }
+            float dl2, q2;
+            rbf_moments(A[D - 1], k2, dl2, q2);
+            const float w2 = rbf_weight(A[D - 1], k2), wd2 = w2 * dl2;
+#pragma unroll
+            for (int f = 0; f < FC; ++f) {
+                g[f] = fmaf(w2, a[f], g[f]);
+                dg[0][f] = fmaf(w2, b[f], dg[0][f]);
+                dg[1][f] = fmaf(w2, cc[f], dg[1][f]);
+                dg[2][f] = fmaf(wd2, a[f], dg[2][f]);
+                lp[f] = fmaf(w2, fmaf(q2, a[f], dl[f]), lp[f]);
+            }
+        }
+    }
+#pragma unroll
+    for (int f = 0; f < FC; ++f) {
+        lp[f] *= v * v;
+#pragma unroll
+        for (int j = 0; j < 3; ++j) dg[j][f] *= -v;
+    }
+}
+
+template <int D, int FC>
+__device__ __forceinline__ void rbf_store(const FwdParams& p, int64_t n, int l, int f0, const float (&g)[FC],
+                                          const float (&dg)[3][FC], const float (&lp)[FC]) {
+#pragma unroll
+    for (int f = 0; f < FC; ++f) {
+        const int64_t lf = static_cast<int64_t>(l) * p.c.F + f0 + f;
+        __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, g[f]);
+        if (p.dgamma) {
+#pragma unroll
+            for (int j = 0; j < D; ++j) __stcs(p.dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf, dg[j][f]);
+        }
+        if (p.lap) __stcs(p.lap + n * p.c.sn + lf * p.c.sf, lp[f]);
+    }
+}
+
+// One point, every feature chunk, taps gathered from the table (through L1).
+template <int D, int K, int FC, typename TT>
+__device__ __forceinline__ void rbf_fwd_gather(const FwdParams& p, int64_t n, int l, const Level& lv, bool active,
+                                               const RbfAxis<K> (&A)[D]) {
+    const float v = 2.f * p.eps * p.eps * lv.fN;  // d/dx = N d/dy on the weights' derivatives
+    const TT* base = static_cast<const TT*>(p.tab.ptr[0]) + l * p.tab.ls[0];
+    const int64_t rs = p.tab.rs[0];
+    const uint32_t tm = p.c.tmask[0];
+    for (int f0 = 0; f0 < p.c.F; f0 += FC) {
+        float g[FC], dg[3][FC], lp[FC];
+        if (active) {
+            rbf_contract<D, K, FC>(A, v, g, dg, lp,
+                                   [&](int k1, int k2, float (&s)[FC], float (&sd)[FC], float (&sq)[FC]) {
+                                       int32_t g2 = 0;
+                                       if constexpr (D == 3) g2 = A[D - 1].first + k2;
+                                       rbf_line<D, K, FC, TT>(base, rs, f0, lv, tm, A[0], A[1].first + k1, g2, s,
+                                                              sd, sq);
+                                   });
+        } else {
+#pragma unroll
+            for (int f = 0; f < FC; ++f) g[f] = dg[0][f] = dg[1][f] = dg[2][f] = lp[f] = 0.f;
+        }
+        rbf_store<D, FC>(p, n, l, f0, g, dg, lp);
+    }
+}
+
 // Six blocks per SM (at most 40 registers): latency-bound, so occupancy pays -- 3D workload 3.82 ms at
-// two blocks (95 registers), 2.81 ms at four, 2.62 ms at six.
+// two blocks (95 registers), 2.81 ms at four, 2.62 ms at six.  Used when the points are scattered
+// (a CTA's tap box larger than rbf_fwd_box_kernel's tile on most levels).
 template <int D, int R, int FC, typename TT>
 __global__ void __launch_bounds__(kBlock, 6) rbf_fwd_kernel(const __grid_constant__ FwdParams p) {
     constexpr int K = 2 * R;
     const int l = p.c.lvl[blockIdx.y];
     const int64_t n = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
     if (n >= p.c.n) return;
+    const Level& lv = p.c.lv[l];
+    RbfAxis<K> A[D];
+    rbf_axes<D, K>(p.coords, n, lv, p.eps * p.eps, A);
+    rbf_fwd_gather<D, K, FC, TT>(p, n, l, lv, (p.c.level_mask >> l) & 1u, A);
+}
+
+// Box-staged forward for coherent points: a CTA of kBlock consecutive points
+// first copies the rows of its taps' bounding box -- not clipped to the
+// grid; rows outside it are zeros, as their weights are -- into shared
+// memory (fp32), then each point reads tap row (k1, k2) at a fixed offset
+// from its own corner of the box: no hash, no bounds test and no L1 gather
+// per tap, and the axis-0 weights and their moment products are computed
+// once per point instead of once per tap row.  A CTA whose box does not
+// fit gathers from the table as rbf_fwd_kernel does.
+// CTAs per SM: the register budget against latency hiding, measured on the full-size workloads -- 3D
+// (box of 61 x 7 x 6 rows) 1.35 / 1.23 / 1.22 ms at 2 / 3 / 4 (4 spills), 2D 0.244 / 0.262 / 0.289 ms.
+constexpr int kBoxFloats = 6 * 1024;  // 24 KB: two stratified rows of 128 points on the 3D grid's finest level
+template <int D>
+constexpr int box_ctas() { return D == 2 ? 2 : 3; }
+
+template <int D, int R, int FC, typename TT>
+__global__ void __launch_bounds__(kBlock, box_ctas<D>()) rbf_fwd_box_kernel(const __grid_constant__ FwdParams p) {
+    constexpr int K = 2 * R;
+    extern __shared__ float4 box_smem4[];
+    float* box = reinterpret_cast<float*>(box_smem4);
+    __shared__ int32_t box_lo[3], box_hi[3];
+    const int l = p.c.lvl[blockIdx.y];
+    const int t = threadIdx.x;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBlock;
+    const int cnt = static_cast<int>(min(static_cast<int64_t>(kBlock), p.c.n - n0));
+    const bool have = t < cnt;
+    const int64_t n = n0 + (have ? t : cnt - 1);
     const int F = p.c.F;
     const Level& lv = p.c.lv[l];
     const bool active = (p.c.level_mask >> l) & 1u;
     RbfAxis<K> A[D];
     rbf_axes<D, K>(p.coords, n, lv, p.eps * p.eps, A);
-    const float v = 2.f * p.eps * p.eps * lv.fN, v2 = v * v;  // d/dx = N d/dy on the weights' derivatives
+    if (!active) {  // the same for the whole CTA
+        if (have) rbf_fwd_gather<D, K, FC, TT>(p, n, l, lv, false, A);
+        return;
+    }
+    if (t < 3) {
+        box_lo[t] = t < D ? INT32_MAX : 0;
+        box_hi[t] = t < D ? INT32_MIN : 0;
+    }
+    __syncthreads();
+    if (have) {
+#pragma unroll
+        for (int i = 0; i < D; ++i) {
+            atomicMin(&box_lo[i], A[i].first);
+            atomicMax(&box_hi[i], A[i].first + K - 1);
+        }
+    }
+    __syncthreads();
+    int32_t lo[3], ext[3];
+    int64_t vol = 1;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        lo[i] = box_lo[i];
+        ext[i] = box_hi[i] - box_lo[i] + 1;
+        vol *= ext[i];
+    }
+    if (vol * F > kBoxFloats) {  // the same for the whole CTA
+        if (have) rbf_fwd_gather<D, K, FC, TT>(p, n, l, lv, true, A);
+        return;
+    }
     const TT* base = static_cast<const TT*>(p.tab.ptr[0]) + l * p.tab.ls[0];
     const int64_t rs = p.tab.rs[0];
     const uint32_t tm = p.c.tmask[0];
+    const int32_t N = static_cast<int32_t>(lv.N);
+    for (int32_t r = t; r < static_cast<int32_t>(vol); r += kBlock) {
+        const int32_t g0 = lo[0] + r % ext[0];
+        const int32_t g1 = lo[1] + (r / ext[0]) % ext[1];
+        const int32_t g2 = lo[2] + r / (ext[0] * ext[1]);
+        const bool in = g0 >= 0 && g0 <= N && g1 >= 0 && g1 <= N && (D == 2 || (g2 >= 0 && g2 <= N));
+        float* dst = box + r * F;
+        if (in) {
+            const TT* src = base + rbf_row<D>(lv, tm, g0, g1, g2) * rs;
+            for (int f = 0; f < F; ++f) dst[f] = to_f32<TT>(__ldg(src + f));
+        } else {
+            for (int f = 0; f < F; ++f) dst[f] = 0.f;
+        }
+    }
+    __syncthreads();
+    if (!have) return;
+    float w0[K], wd0[K], wq0[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        float dl, q;
+        rbf_moments(A[0], k, dl, q);
+        w0[k] = A[0].w[k];
+        wd0[k] = w0[k] * dl;
+        wq0[k] = w0[k] * q;
+    }
+    int32_t o2 = 0;
+    if constexpr (D == 3) o2 = A[D - 1].first - lo[2];
+    const float* corner = box + (A[0].first - lo[0] + ext[0] * (A[1].first - lo[1] + ext[1] * o2)) * F;
+    const int32_t s1 = ext[0] * F, s2 = ext[0] * ext[1] * F;  // floats between tap rows along axes 1 and 2
+    const float v = 2.f * p.eps * p.eps * lv.fN;
     for (int f0 = 0; f0 < F; f0 += FC) {
         float g[FC], dg[3][FC], lp[FC];
+        rbf_contract<D, K, FC>(A, v, g, dg, lp, [&](int k1, int k2, float (&s)[FC], float (&sd)[FC], float (&sq)[FC]) {
+            const float* row = corner + k1 * s1 + k2 * s2 + f0;
 #pragma unroll
-        for (int f = 0; f < FC; ++f) g[f] = dg[0][f] = dg[1][f] = dg[2][f] = lp[f] = 0.f;
-        // sums in offset units: dg_i = sum W delta_i theta, lp = sum W (q_0 + q_1 [+ q_2]) theta with the
-        // tap weight W = w_0 w_1 [w_2]; the gradient and Laplacian are -v dg and v^2 lp
-        if (active) {
-            if constexpr (D == 2) {
+            for (int f = 0; f < FC; ++f) s[f] = sd[f] = sq[f] = 0.f;
 #pragma unroll
-                for (int k1 = 0; k1 < K; ++k1) {
-                    if (!((A[1].valid >> k1) & 1u)) continue;
-                    float s[FC], sd[FC], sq[FC], dl1, q1;
-                    rbf_line<2, K, FC, TT>(base, rs, f0, lv, tm, A[0], A[1].first + k1, 0, s, sd, sq);
-                    rbf_moments(A[1], k1, dl1, q1);
-                    const float w1 = A[1].w[k1], wd1 = w1 * dl1;
-#pragma unroll
-                    for (int f = 0; f < FC; ++f) {
-                        g[f] = fmaf(w1, s[f], g[f]);
-                        dg[0][f] = fmaf(w1, sd[f], dg[0][f]);
-                        dg[1][f] = fmaf(wd1, s[f], dg[1][f]);
-                        lp[f] = fmaf(w1, fmaf(q1, s[f], sq[f]), lp[f]);
-                    }
+            for (int k = 0; k < K; ++k) {
+                float x[FC];
+                if constexpr (FC == 2) {
+                    const float2 y = *reinterpret_cast<const float2*>(row + k * F);
+                    x[0] = y.x;
+                    x[FC - 1] = y.y;
+                } else {
+                    x[0] = row[k * F];
                 }
-            } else {
-#pragma unroll 1
-                for (int k2 = 0; k2 < K; ++k2) {
-                    if (!((A[2].valid >> k2) & 1u)) continue;
-                    float a[FC], b[FC], cc[FC], dl[FC];
 #pragma unroll
-                    for (int f = 0; f < FC; ++f) a[f] = b[f] = cc[f] = dl[f] = 0.f;
-#pragma unroll
-                    for (int k1 = 0; k1 < K; ++k1) {
-                        if (!((A[1].valid >> k1) & 1u)) continue;
-                        float s[FC], sd[FC], sq[FC], dl1, q1;
-                        rbf_line<3, K, FC, TT>(base, rs, f0, lv, tm, A[0], A[1].first + k1, A[2].first + k2, s, sd,
-                                               sq);
-                        rbf_moments(A[1], k1, dl1, q1);
-                        const float w1 = A[1].w[k1], wd1 = w1 * dl1;
-#pragma unroll
-                        for (int f = 0; f < FC; ++f) {
-                            a[f] = fmaf(w1, s[f], a[f]);
-                            b[f] = fmaf(w1, sd[f], b[f]);
-                            cc[f] = fmaf(wd1, s[f], cc[f]);
-                            dl[f] = fmaf(w1, fmaf(q1, s[f], sq[f]), dl[f]);
-                        }
-                    }
-                    float dl2, q2;
-                    rbf_moments(A[2], k2, dl2, q2);
-                    const float w2 = rbf_weight(A[2], k2), wd2 = w2 * dl2;
-#pragma unroll
-                    for (int f = 0; f < FC; ++f) {
-                        g[f] = fmaf(w2, a[f], g[f]);
-                        dg[0][f] = fmaf(w2, b[f], dg[0][f]);
-                        dg[1][f] = fmaf(w2, cc[f], dg[1][f]);
-                        dg[2][f] = fmaf(wd2, a[f], dg[2][f]);
-                        lp[f] = fmaf(w2, fmaf(q2, a[f], dl[f]), lp[f]);
-                    }
+                for (int f = 0; f < FC; ++f) {
+                    s[f] = fmaf(w0[k], x[f], s[f]);
+                    sd[f] = fmaf(wd0[k], x[f], sd[f]);
+                    sq[f] = fmaf(wq0[k], x[f], sq[f]);
                 }
             }
-        }
-#pragma unroll
-        for (int f = 0; f < FC; ++f) {
-            lp[f] *= v2;
-#pragma unroll
-            for (int j = 0; j < 3; ++j) dg[j][f] *= -v;
-        }
-#pragma unroll
-        for (int f = 0; f < FC; ++f) {
-            const int64_t lf = static_cast<int64_t>(l) * F + f0 + f;
-            __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, g[f]);
-            if (p.dgamma) {
-#pragma unroll
-                for (int j = 0; j < D; ++j) __stcs(p.dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf, dg[j][f]);
-            }
-            if (p.lap) __stcs(p.lap + n * p.c.sn + lf * p.c.sf, lp[f]);
-        }
+        });
+        rbf_store<D, FC>(p, n, l, f0, g, dg, lp);
     }
 }
 
@@ -722,7 +876,11 @@ __global__ void __launch_bounds__(kCellBlock, kCellCtas) rbf_bwd_cells_kernel(co
 template <int D, int R, int FC, typename TT>
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t s) {
     dim3 grid(static_cast<unsigned>((p.c.n + kBlock - 1) / kBlock), static_cast<unsigned>(p.c.nlvl));
-    rbf_fwd_kernel<D, R, FC, TT><<<grid, kBlock, 0, s>>>(p);
+    constexpr int kSmem = kBoxFloats * static_cast<int>(sizeof(float));
+    cudaError_t e = cudaFuncSetAttribute(rbf_fwd_box_kernel<D, R, FC, TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmem);
+    if (e != cudaSuccess) return e;
+    rbf_fwd_box_kernel<D, R, FC, TT><<<grid, kBlock, kSmem, s>>>(p);
     return cudaGetLastError();
 }
 
