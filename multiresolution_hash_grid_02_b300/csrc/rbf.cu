@@ -21,9 +21,9 @@
 // bounding box in shared memory (rbf_fwd_box_kernel).
 // The backward is the transposed contraction, accumulated per CTA in a
 // shared-memory tile of its points' neighbourhoods (the page samples
-// stratified points, so a CTA's points are neighbours) before the scatter;
-// in 3D it runs per run of same-cell points and tap row (k1, k2), with the
-// points' separable factors summed in registers (rbf_bwd_cells_kernel).
+// stratified points, so a CTA's points are neighbours) before the scatter,
+// one thread per run of same-cell points and tap row, with the points'
+// separable factors summed in registers (rbf_bwd_cells_kernel).
 #include <cuda_runtime.h>
 
 #include "hg_device.cuh"
@@ -264,21 +264,6 @@ __device__ __forceinline__ void rbf_fwd_gather(const FwdParams& p, int64_t n, in
     }
 }
 
-// Six blocks per SM (at most 40 registers): latency-bound, so occupancy pays -- 3D workload 3.82 ms at
-// two blocks (95 registers), 2.81 ms at four, 2.62 ms at six.  Used when the points are scattered
-// (a CTA's tap box larger than rbf_fwd_box_kernel's tile on most levels).
-template <int D, int R, int FC, typename TT>
-__global__ void __launch_bounds__(kBlock, 6) rbf_fwd_kernel(const __grid_constant__ FwdParams p) {
-    constexpr int K = 2 * R;
-    const int l = p.c.lvl[blockIdx.y];
-    const int64_t n = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
-    if (n >= p.c.n) return;
-    const Level& lv = p.c.lv[l];
-    RbfAxis<K> A[D];
-    rbf_axes<D, K>(p.coords, n, lv, p.eps * p.eps, A);
-    rbf_fwd_gather<D, K, FC, TT>(p, n, l, lv, (p.c.level_mask >> l) & 1u, A);
-}
-
 // Box-staged forward for coherent points: a CTA of kBlock consecutive points
 // first copies the rows of its taps' bounding box -- not clipped to the
 // grid; rows outside it are zeros, as their weights are -- into shared
@@ -286,7 +271,10 @@ __global__ void __launch_bounds__(kBlock, 6) rbf_fwd_kernel(const __grid_constan
 // from its own corner of the box: no hash, no bounds test and no L1 gather
 // per tap, and the axis-0 weights and their moment products are computed
 // once per point instead of once per tap row.  A CTA whose box does not
-// fit gathers from the table as rbf_fwd_kernel does.
+// fit (scattered points) gathers each tap row from the table through L1;
+// that path is latency-bound and runs at this kernel's occupancy (a
+// gather-only kernel measured 3.82 / 2.81 / 2.62 ms on the 3D workload at
+// two / four / six blocks per SM, against 1.23 ms for the box path).
 // CTAs per SM: the register budget against latency hiding, measured on the full-size workloads -- 3D
 // (box of 61 x 7 x 6 rows) 1.35 / 1.23 / 1.22 ms at 2 / 3 / 4 (4 spills), 2D 0.244 / 0.262 / 0.289 ms.
 constexpr int kBoxFloats = 6 * 1024;  // 24 KB: two stratified rows of 128 points on the 3D grid's finest level
@@ -400,260 +388,49 @@ __global__ void __launch_bounds__(kBlock, box_ctas<D>()) rbf_fwd_box_kernel(cons
     }
 }
 
-// Transposed contraction of one (point, level, feature chunk): the
-// coefficient gradient of every tap of the ring box, handed to
-// add(g0, g1, g2, in, values) with the tap's vertex coordinates (g2 = 0 in
-// 2D) and whether it lies inside the grid (taps outside weigh 0 and must not
-// be written).  The loops are the same for every lane of a warp, so add()
-// may use warp shuffles.  With the moment form of the weights' derivatives
-// the gradient of tap (k0, k1[, k2]) is W (g_gamma - v sum_i g_dgamma_i
-// delta_i + v^2 g_lap sum_i q_i), W = w_0 w_1 [w_2], folded in axis by axis
-// from the outside.
-template <int D, int R, int FC, typename Add>
-__device__ __forceinline__ void rbf_point_bwd(const BwdParams& p, int64_t n, int l, int f0, const RbfAxis<2 * R> (&A)[D],
-                                              const Level& lv, Add&& add) {
-    constexpr int K = 2 * R;
-    const int F = p.c.F;
-    const float v = 2.f * p.eps * p.eps * lv.fN;
-    float a0[FC], bd[3][FC], cl[FC];  // g_gamma, -v g_dgamma_i, v^2 g_lap
-#pragma unroll
-    for (int f = 0; f < FC; ++f) {
-        const int64_t lf = static_cast<int64_t>(l) * F + f0 + f;
-        a0[f] = p.g_gamma ? __ldg(p.g_gamma + n * p.c.sn + lf * p.c.sf) : 0.f;
-        cl[f] = p.g_lap ? v * v * __ldg(p.g_lap + n * p.c.sn + lf * p.c.sf) : 0.f;
-#pragma unroll
-        for (int j = 0; j < 3; ++j)
-            bd[j][f] = (p.g_dgamma && j < D) ? -v * __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf) : 0.f;
-    }
-    // one row of taps along axis 0: weight beta w_0 and factor alpha + bd_0 delta_0 + cl q_0
-    auto line = [&](int32_t g1, int32_t g2, bool row_in, float beta, const float (&alpha)[FC]) {
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-            float dl, q, val[FC];
-            rbf_moments(A[0], k, dl, q);
-            const float bw = beta * A[0].w[k];
-#pragma unroll
-            for (int f = 0; f < FC; ++f) val[f] = bw * fmaf(cl[f], q, fmaf(bd[0][f], dl, alpha[f]));
-            add(A[0].first + k, g1, g2, row_in && ((A[0].valid >> k) & 1u), val);
-        }
-    };
-    if constexpr (D == 2) {
-#pragma unroll 1
-        for (int k1 = 0; k1 < K; ++k1) {
-            float dl1, q1, al[FC];
-            rbf_moments(A[1], k1, dl1, q1);
-#pragma unroll
-            for (int f = 0; f < FC; ++f) al[f] = fmaf(cl[f], q1, fmaf(bd[1][f], dl1, a0[f]));
-            line(A[1].first + k1, 0, (A[1].valid >> k1) & 1u, rbf_weight(A[1], k1), al);
-        }
-    } else {
-#pragma unroll 1
-        for (int k2 = 0; k2 < K; ++k2) {
-            float dl2, q2, al2[FC];
-            rbf_moments(A[2], k2, dl2, q2);
-            const float w2 = rbf_weight(A[2], k2);
-            const bool in2 = (A[2].valid >> k2) & 1u;
-#pragma unroll
-            for (int f = 0; f < FC; ++f) al2[f] = fmaf(cl[f], q2, fmaf(bd[2][f], dl2, a0[f]));
-#pragma unroll
-            for (int k1 = 0; k1 < K; ++k1) {
-                float dl1, q1, al[FC];
-                rbf_moments(A[1], k1, dl1, q1);
-#pragma unroll
-                for (int f = 0; f < FC; ++f) al[f] = fmaf(cl[f], q1, fmaf(bd[1][f], dl1, al2[f]));
-                line(A[1].first + k1, A[2].first + k2, in2 && ((A[1].valid >> k1) & 1u), w2 * A[1].w[k1], al);
-            }
-        }
-    }
-}
-
-// Runs of consecutive lanes whose points lie in the same cell (so have the
-// same taps): their contributions are summed in the warp and added by the
-// run's first lane.  `key` differs between lanes in different cells.
-struct LaneRuns {
-    uint32_t end;  // one past the last lane of this lane's run
-    int span;      // the warp's longest run
-    bool lead;     // first lane of its run
-};
-
-template <int D, int K>
-__device__ __forceinline__ LaneRuns lane_runs(const RbfAxis<K> (&A)[D], bool unique) {
-    const uint32_t lane = threadIdx.x & 31u;
-    int32_t key[3] = {A[0].first, A[1].first, D == 3 ? A[D - 1].first : 0};
-    if (unique) key[2] = INT32_MIN + static_cast<int32_t>(lane);  // no tap's coordinate: a run of its own
-    bool same = lane > 0;
-#pragma unroll
-    for (int i = 0; i < 3; ++i) same = (__shfl_up_sync(0xffffffffu, key[i], 1) == key[i]) && same;
-    LaneRuns r;
-    r.lead = !same;
-    const uint32_t starts = __ballot_sync(0xffffffffu, r.lead);
-    const uint32_t above = lane == 31u ? 0u : starts & (0xffffffffu << (lane + 1u));
-    r.end = above ? static_cast<uint32_t>(__ffs(above) - 1) : 32u;
-    r.span = static_cast<int>(__reduce_max_sync(0xffffffffu, r.lead ? r.end - lane : 0u));
-    return r;
-}
-
-// Sum of v over the lane's run, complete in the run's first lane.
-template <int FC>
-__device__ __forceinline__ void run_sum(const LaneRuns& r, float (&v)[FC]) {
-    const uint32_t lane = threadIdx.x & 31u;
-    for (int o = 1; o < r.span; o <<= 1) {
-#pragma unroll
-        for (int f = 0; f < FC; ++f) {
-            const float t = __shfl_down_sync(0xffffffffu, v[f], o);
-            if (lane + o < r.end) v[f] += t;
-        }
-    }
-}
-
-constexpr int kTileBlock = 256;  // 8 warps: the lane interleave below relies on it
-static_assert(kTileBlock == 8 * 32, "eight warps of 32 lanes");
-// Tile capacity (floats, 48 KB of shared memory) and CTAs per SM.
-constexpr int kTileFloats = 12 * 1024;
-constexpr int kTileCtas = 4;
-
-// Tiled backward for coherent points (the page's structured sampling): a CTA
-// takes kTileBlock consecutive points of one level, finds the bounding box
-// of their tap neighbourhoods (a block reduction of their cells), and when
-// the box's rows fit the tile it accumulates every contribution in a
-// shared-memory tile of that box and then adds each touched row into the
-// table once -- consecutive stratified points share most of their taps, so
-// this replaces tens of REDs on the same rows by one.  A CTA whose box does
-// not fit (scattered points on a fine level) scatters directly.
-// The shared-memory adds are latency-bound, so occupancy pays: 3D workload 13.3 ms at two blocks per SM
-// (96 KB tiles, 110 registers), 7.4 ms at four (48 KB, 64 registers); five (40 KB) spill at 48
-// registers and take 7.7 ms, three 8.2 ms.  Summing the runs of same-cell lanes in the warp before the
-// adds: 7.4 -> 6.9 ms (2D 0.67 -> 0.50 ms; interleaving the points over the lanes instead, so that the
-// lanes of one add sit in different cells, gives 7.0 and 0.62 ms).
-template <int D, int R, int FC, bool VEC>
-__global__ void __launch_bounds__(kTileBlock, kTileCtas) rbf_bwd_tile_kernel(const __grid_constant__ BwdParams p) {
-    extern __shared__ float tile[];
-    __shared__ int32_t box_lo[3], box_hi[3];
-    const int l = p.c.lvl[blockIdx.y];
-    if (!((p.c.level_mask >> l) & 1u)) return;
-    // consecutive points per warp: lanes in one cell form runs whose contributions are summed in the warp
-    // first, so one lane per run adds them (a lane past the end works on the last point and adds nothing)
-    const int64_t n = static_cast<int64_t>(blockIdx.x) * kTileBlock + threadIdx.x;
-    const bool have = n < p.c.n;
-    const int64_t nc = have ? n : p.c.n - 1;
-    const Level& lv = p.c.lv[l];
-    const int F = p.c.F;
-    RbfAxis<2 * R> A[D];
-    rbf_axes<D, 2 * R>(p.coords, nc, lv, p.eps * p.eps, A);
-    // bounding box of the CTA's taps, clipped to the grid
-    if (threadIdx.x < 3) {
-        box_lo[threadIdx.x] = INT32_MAX;
-        box_hi[threadIdx.x] = INT32_MIN;
-    }
-    __syncthreads();
-    if (have) {
-#pragma unroll
-        for (int i = 0; i < D; ++i) {
-            atomicMin(&box_lo[i], max(A[i].first, 0));
-            atomicMax(&box_hi[i], min(A[i].first + 2 * R - 1, static_cast<int32_t>(lv.N)));
-        }
-    }
-    __syncthreads();
-    if (!have) A[0].valid = 0u;
-    const LaneRuns run = lane_runs<D>(A, !have);
-    int32_t lo[3] = {0, 0, 0}, ext[3] = {1, 1, 1};
-    int64_t vol = 1;
-#pragma unroll
-    for (int i = 0; i < D; ++i) {
-        lo[i] = box_lo[i];
-        ext[i] = box_hi[i] - box_lo[i] + 1;
-        vol *= ext[i];
-    }
-    float* base = p.grad.ptr[0] + l * p.grad.ls[0];
-    const uint32_t tm = p.c.tmask[0];
-    if (vol * F > kTileFloats) {  // the same branch for the whole CTA: scatter directly
-        for (int f0 = 0; f0 < F; f0 += FC) {
-            rbf_point_bwd<D, R, FC>(p, nc, l, f0, A, lv,
-                                    [&](int32_t g0, int32_t g1, int32_t g2, bool in, float (&v)[FC]) {
-                run_sum<FC>(run, v);
-                if (!(run.lead && in)) return;
-                float* e = base + rbf_row<D>(lv, tm, g0, g1, g2) * p.grad.rs[0] + f0;
-                if constexpr (VEC) {
-                    red_add_v2(e, v[0], v[FC - 1]);
-                } else {
-#pragma unroll
-                    for (int f = 0; f < FC; ++f) red_add_f32(e + f, v[f]);
-                }
-            });
-        }
-        return;
-    }
-    const int32_t vals = static_cast<int32_t>(vol) * F;
-    for (int32_t i = threadIdx.x; i < vals; i += kTileBlock) tile[i] = 0.f;
-    __syncthreads();
-    for (int f0 = 0; f0 < F; f0 += FC) {
-        rbf_point_bwd<D, R, FC>(p, nc, l, f0, A, lv, [&](int32_t g0, int32_t g1, int32_t g2, bool in, float (&v)[FC]) {
-            run_sum<FC>(run, v);
-            if (!(run.lead && in)) return;
-            const int32_t r = (g0 - lo[0]) + ext[0] * ((g1 - lo[1]) + ext[1] * (D == 3 ? g2 - lo[2] : 0));
-            float* a = tile + r * F + f0;
-#pragma unroll
-            for (int f = 0; f < FC; ++f) atomicAdd(a + f, v[f]);
-        });
-    }
-    __syncthreads();
-    for (int32_t r = threadIdx.x; r < static_cast<int32_t>(vol); r += kTileBlock) {
-        const int32_t g0 = lo[0] + r % ext[0];
-        const int32_t g1 = lo[1] + (r / ext[0]) % ext[1];
-        const int32_t g2 = D == 3 ? lo[2] + r / (ext[0] * ext[1]) : 0;
-        float* e = base + rbf_row<D>(lv, tm, g0, g1, g2) * p.grad.rs[0];
-        const float* a = tile + r * F;
-        for (int f0 = 0; f0 < F; f0 += FC) {
-            bool any = false;
-#pragma unroll
-            for (int f = 0; f < FC; ++f) any = any || a[f0 + f] != 0.f;
-            if (!any) continue;
-            if constexpr (VEC) {
-                red_add_v2(e + f0, a[f0], a[f0 + FC - 1]);
-            } else {
-#pragma unroll
-                for (int f = 0; f < FC; ++f) red_add_f32(e + f0 + f, a[f0 + f]);
-            }
-        }
-    }
-}
-
-// Cell-run backward, 3D.  The points of a run (consecutive points in one
-// cell) share their K^3 taps, and with the moment form above the gradient
-// of tap (k0, k1, k2) summed over the run's points is
+// Cell-run backward.  The points of a run (consecutive points in one cell)
+// share their K^d taps, and with the moment form above the gradient of tap
+// (k0, k1, k2) summed over the run's points is
 //   sum_p  w0[k0] Sw[k1,k2] + (w0 delta0)[k0] Sd[k1,k2] + (w0 q0)[k0] Sq[k1,k2],
 // where per point P = w1 w2, Sd = bd0 P, Sq = cl P and
 //   Sw = a0 P + bd1 (w1 delta1) w2 + bd2 w1 (w2 delta2) + cl ((w1 q1) w2 + w1 (w2 q2))
-// (a0 = g_gamma, bd_i = -v g_dgamma_i, cl = v^2 g_lap): the transposed
-// contraction with axis 0 folded in last.  A CTA writes each point's
+// (a0 = g_gamma, bd_i = -v g_dgamma_i, cl = v^2 g_lap; in 2D w2 = 1 and
+// delta2 = q2 = 0): the transposed contraction with axis 0 folded in last.  A CTA writes each point's
 // factors to shared memory (axis 0's three weight vectors, the weights and
 // moments of axes 1 and 2, the upstream coefficients), then one thread per
-// (run, k1, k2) sums the K x FC gradients of its taps over the run's points
+// (run, k1, k2) -- kCellRows rows k1 of one k2 -- sums the K x FC gradients
+// of its taps over the run's points
 // in registers and adds each into the CTA's tile once.  Per point this
-// takes about a sixth of the instructions of a per-point scatter with
-// in-warp run sums (no shuffles; one shared-memory add per tap and run, not
-// per tap and point).  The tile covers the bounding box of the CTA's taps
-// as in rbf_bwd_tile_kernel; when it does not fit, each run's taps are added
-// to the table directly.
+// takes about a sixth of the instructions of a per-point scatter with the
+// runs summed by warp shuffles (3D: 6.9 -> 2.6 ms; 2D: 0.49 -> 0.42 ms), and
+// one shared-memory add per tap and run instead of per tap and point.  The
+// tile covers the bounding box of the CTA's taps (clipped to the grid); each
+// touched row is added to the table once.  When it does not fit (scattered
+// points on a fine level), each run's taps are added to the table directly.
+// Any point order is correct; a random one gives runs of one point.
 constexpr int kCellBlock = 256;
 constexpr int kCellTileFloats = 6 * 1024;  // 24 KB: the full-grid 3D box of two stratified rows of 128 points
 constexpr int kCellCtas = 3;
+// Tap rows k1 per thread: more rows share the point's shared-memory loads but leave fewer threads per
+// run.  Measured on the full-size workloads at one / two / three rows: 3D 2.61 / 2.78 / 2.99 ms, 2D
+// 0.42 / 0.46 / 0.47 ms.
+constexpr int kCellRows = 1;
 
-template <int K, int FC>
+template <int D, int K, int FC>
 struct CellRec {
     static constexpr int a0 = 0;                  // w0[K], (w0 delta0)[K], (w0 q0)[K]
     static constexpr int a1 = 3 * K;              // w1[K], tau1, var1
-    static constexpr int a2 = a1 + K + 2;         // w2[K], tau2, var2
-    static constexpr int coef = a2 + K + 2;       // a0[FC], bd0[FC], bd1[FC], bd2[FC], cl[FC]
+    static constexpr int a2 = a1 + K + 2;         // 3D: w2[K], tau2, var2
+    static constexpr int coef = a1 + (D - 1) * (K + 2);  // a0[FC], bd0[FC], bd1[FC], bd2[FC], cl[FC]
     static constexpr int key = coef + 5 * FC;     // the cell: first tap of each axis (int32)
     static constexpr int size = (key + 3 + 3) & ~3;  // floats; a multiple of 4 keeps records 16-byte aligned
     static_assert((3 * K) % 4 == 0 || (3 * K) % 4 == 2, "axis-0 block: float4s and at most one float2");
     static_assert(a1 % 2 == 0 && a2 % 2 == 0 && coef % 2 == 0, "float2 fields");
 };
 
-template <int K, int FC>
+template <int D, int K, int FC>
 constexpr int cell_smem_bytes() {
-    return (kCellBlock * CellRec<K, FC>::size + kCellTileFloats) * static_cast<int>(sizeof(float));
+    return (kCellBlock * CellRec<D, K, FC>::size + kCellTileFloats) * static_cast<int>(sizeof(float));
 }
 
 // v[0 .. M) from 16-byte-aligned shared memory, in float4 loads (and one float2).
@@ -674,13 +451,14 @@ __device__ __forceinline__ void lds_floats(const float* s, float (&v)[M]) {
     }
 }
 
-template <int R, int FC, bool VEC>
+template <int D, int R, int FC, bool VEC>
 __global__ void __launch_bounds__(kCellBlock, kCellCtas) rbf_bwd_cells_kernel(const __grid_constant__ BwdParams p) {
     constexpr int K = 2 * R;
-    using Rec = CellRec<K, FC>;
-    constexpr int kItems = K * K;                  // (k1, k2) pairs of a run
-    constexpr int kSlots = kCellBlock / kItems;    // runs in progress at once
-    static_assert(kSlots >= 1, "K^2 <= block");
+    using Rec = CellRec<D, K, FC>;
+    constexpr int J = K % kCellRows == 0 ? kCellRows : 1;  // tap rows of a thread: k1, k1 + K/J, ...
+    constexpr int kItems = (K / J) * (D == 3 ? K : 1);       // threads per run
+    constexpr int kSlots = kCellBlock / kItems;              // runs in progress at once
+    static_assert(kSlots >= 1, "a run's threads fit the block");
     extern __shared__ float4 cell_smem4[];
     float* rec = reinterpret_cast<float*>(cell_smem4);  // [kCellBlock][Rec::size]
     float* tile = rec + kCellBlock * Rec::size;         // [kCellTileFloats]
@@ -701,8 +479,8 @@ __global__ void __launch_bounds__(kCellBlock, kCellCtas) rbf_bwd_cells_kernel(co
     float* my = rec + t * Rec::size;
     int32_t* my_key = reinterpret_cast<int32_t*>(my + Rec::key);
     {
-        RbfAxis<K> A[3];
-        rbf_axes<3, K>(p.coords, n, lv, p.eps * p.eps, A);
+        RbfAxis<K> A[D];
+        rbf_axes<D, K>(p.coords, n, lv, p.eps * p.eps, A);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             float dl, q;
@@ -711,17 +489,20 @@ __global__ void __launch_bounds__(kCellBlock, kCellCtas) rbf_bwd_cells_kernel(co
             my[Rec::a0 + K + k] = A[0].w[k] * dl;
             my[Rec::a0 + 2 * K + k] = A[0].w[k] * q;
             my[Rec::a1 + k] = A[1].w[k];
-            my[Rec::a2 + k] = A[2].w[k];
+            if constexpr (D == 3) my[Rec::a2 + k] = A[D - 1].w[k];
         }
         my[Rec::a1 + K] = A[1].tau;
         my[Rec::a1 + K + 1] = A[1].var;
-        my[Rec::a2 + K] = A[2].tau;
-        my[Rec::a2 + K + 1] = A[2].var;
-#pragma unroll
-        for (int i = 0; i < 3; ++i) my_key[i] = A[i].first;
-        if (t < 3) {
-            box_lo[t] = INT32_MAX;
-            box_hi[t] = INT32_MIN;
+        if constexpr (D == 3) {
+            my[Rec::a2 + K] = A[D - 1].tau;
+            my[Rec::a2 + K + 1] = A[D - 1].var;
+        }
+        my_key[0] = A[0].first;
+        my_key[1] = A[1].first;
+        my_key[2] = D == 3 ? A[D - 1].first : 0;
+        if (t < 3) {  // an absent axis 2 spans the single index 0
+            box_lo[t] = t < D ? INT32_MAX : 0;
+            box_hi[t] = t < D ? INT32_MIN : 0;
         }
     }
     __syncthreads();
@@ -730,7 +511,7 @@ __global__ void __launch_bounds__(kCellBlock, kCellCtas) rbf_bwd_cells_kernel(co
     bool lead = false;
     if (have) {
 #pragma unroll
-        for (int i = 0; i < 3; ++i) {
+        for (int i = 0; i < D; ++i) {
             atomicMin(&box_lo[i], max(my_key[i], 0));
             atomicMax(&box_hi[i], min(my_key[i] + K - 1, N));
         }
@@ -767,7 +548,7 @@ __global__ void __launch_bounds__(kCellBlock, kCellCtas) rbf_bwd_cells_kernel(co
     const int64_t rs = p.grad.rs[0];
     const uint32_t tm = p.c.tmask[0];
     const int slot = t / kItems, item = t - slot * kItems;
-    const int k1 = item % K, k2 = item / K;
+    const int k1 = item % (K / J), k2 = item / (K / J);
     for (int f0 = 0; f0 < F; f0 += FC) {
         // the point's upstream coefficients for this feature chunk (zero past the end)
 #pragma unroll
@@ -778,7 +559,7 @@ __global__ void __launch_bounds__(kCellBlock, kCellCtas) rbf_bwd_cells_kernel(co
                 if (p.g_gamma) c[0] = __ldg(p.g_gamma + n * p.c.sn + lf * p.c.sf);
                 if (p.g_dgamma) {
 #pragma unroll
-                    for (int j = 0; j < 3; ++j) c[1 + j] = -v * __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf);
+                    for (int j = 0; j < D; ++j) c[1 + j] = -v * __ldg(p.g_dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf);
                 }
                 if (p.g_lap) c[4] = v * v * __ldg(p.g_lap + n * p.c.sn + lf * p.c.sf);
             }
@@ -790,60 +571,93 @@ __global__ void __launch_bounds__(kCellBlock, kCellCtas) rbf_bwd_cells_kernel(co
             for (int r = slot; r < runs; r += kSlots) {
                 const int pa = run_start[r], pb = run_start[r + 1];
                 const int32_t* key = reinterpret_cast<const int32_t*>(rec + pa * Rec::size + Rec::key);
-                const int32_t g0 = key[0], g1 = key[1] + k1, g2 = key[2] + k2;
-                if (g1 < 0 || g1 > N || g2 < 0 || g2 > N) continue;  // outside the grid: weight 0, no row
-                float acc[K][FC];
+                const int32_t g0 = key[0], g2 = key[2] + k2;
+                bool in1[J], any = false;
 #pragma unroll
-                for (int k = 0; k < K; ++k)
+                for (int j = 0; j < J; ++j) {
+                    const int32_t g1 = key[1] + k1 + j * (K / J);
+                    in1[j] = g1 >= 0 && g1 <= N;
+                    any = any || in1[j];
+                }
+                if (!any || g2 < 0 || g2 > N) continue;  // outside the grid: weight 0, no row
+                float acc[J][K][FC];
 #pragma unroll
-                    for (int f = 0; f < FC; ++f) acc[k][f] = 0.f;
+                for (int j = 0; j < J; ++j)
+#pragma unroll
+                    for (int k = 0; k < K; ++k)
+#pragma unroll
+                        for (int f = 0; f < FC; ++f) acc[j][k][f] = 0.f;
+#pragma unroll 1
                 for (int q = pa; q < pb; ++q) {
                     const float* pr = rec + q * Rec::size;
                     float a0[3 * K];
                     lds_floats<3 * K>(pr + Rec::a0, a0);
-                    const float w1 = pr[Rec::a1 + k1], w2 = pr[Rec::a2 + k2];
                     const float2 m1 = *reinterpret_cast<const float2*>(pr + Rec::a1 + K);
-                    const float2 m2 = *reinterpret_cast<const float2*>(pr + Rec::a2 + K);
-                    const float dl1 = m1.x - static_cast<float>(k1), q1 = fmaf(dl1, dl1, -m1.y);
-                    const float dl2 = m2.x - static_cast<float>(k2), q2 = fmaf(dl2, dl2, -m2.y);
-                    const float P = w1 * w2, t1 = (w1 * dl1) * w2, t2 = w1 * (w2 * dl2);
-                    const float t3 = fmaf(w1 * q1, w2, w1 * (w2 * q2));
+                    float w2 = 1.f, wd2 = 0.f, wq2 = 0.f;
+                    if constexpr (D == 3) {
+                        w2 = pr[Rec::a2 + k2];
+                        const float2 m2 = *reinterpret_cast<const float2*>(pr + Rec::a2 + K);
+                        const float dl2 = m2.x - static_cast<float>(k2), q2 = fmaf(dl2, dl2, -m2.y);
+                        wd2 = w2 * dl2;
+                        wq2 = w2 * q2;
+                    }
                     float c[5][FC];
                     if constexpr (FC == 2) {
 #pragma unroll
-                        for (int j = 0; j < 5; ++j) {
-                            const float2 x = *reinterpret_cast<const float2*>(pr + Rec::coef + 2 * j);
-                            c[j][0] = x.x;
-                            c[j][FC - 1] = x.y;
+                        for (int i = 0; i < 5; ++i) {
+                            const float2 x = *reinterpret_cast<const float2*>(pr + Rec::coef + 2 * i);
+                            c[i][0] = x.x;
+                            c[i][FC - 1] = x.y;
                         }
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 5; ++j) c[j][0] = pr[Rec::coef + j];
+                        for (int i = 0; i < 5; ++i) c[i][0] = pr[Rec::coef + i];
                     }
 #pragma unroll
-                    for (int f = 0; f < FC; ++f) {
-                        const float sw = fmaf(c[4][f], t3, fmaf(c[3][f], t2, fmaf(c[2][f], t1, c[0][f] * P)));
-                        const float sd = c[1][f] * P, sq = c[4][f] * P;
+                    for (int j = 0; j < J; ++j) {
+                        const int kk = k1 + j * (K / J);
+                        const float w1 = pr[Rec::a1 + kk];
+                        const float dl1 = m1.x - static_cast<float>(kk), q1 = fmaf(dl1, dl1, -m1.y);
+                        float P = w1, t1 = w1 * dl1, t2 = 0.f, t3 = w1 * q1;
+                        if constexpr (D == 3) {
+                            P = w1 * w2;
+                            t1 = (w1 * dl1) * w2;
+                            t2 = w1 * wd2;
+                            t3 = fmaf(w1 * q1, w2, w1 * wq2);
+                        }
 #pragma unroll
-                        for (int k = 0; k < K; ++k)
-                            acc[k][f] = fmaf(a0[k], sw, fmaf(a0[K + k], sd, fmaf(a0[2 * K + k], sq, acc[k][f])));
+                        for (int f = 0; f < FC; ++f) {
+                            float sw = fmaf(c[2][f], t1, c[0][f] * P);
+                            if constexpr (D == 3) sw = fmaf(c[3][f], t2, sw);
+                            sw = fmaf(c[4][f], t3, sw);
+                            const float sd = c[1][f] * P, sq = c[4][f] * P;
+#pragma unroll
+                            for (int k = 0; k < K; ++k)
+                                acc[j][k][f] =
+                                    fmaf(a0[k], sw, fmaf(a0[K + k], sd, fmaf(a0[2 * K + k], sq, acc[j][k][f])));
+                        }
                     }
                 }
 #pragma unroll
-                for (int k = 0; k < K; ++k) {
-                    const int32_t gk = g0 + k;
-                    if (gk < 0 || gk > N) continue;
-                    if (tiled) {
-                        const int32_t e = (gk - lo[0]) + ext[0] * ((g1 - lo[1]) + ext[1] * (g2 - lo[2]));
+                for (int j = 0; j < J; ++j) {
+                    if (!in1[j]) continue;
+                    const int32_t g1 = key[1] + k1 + j * (K / J);
 #pragma unroll
-                        for (int f = 0; f < FC; ++f) atomicAdd(tile + e * F + f0 + f, acc[k][f]);
-                    } else {
-                        float* e = gbase + rbf_row<3>(lv, tm, gk, g1, g2) * rs + f0;
-                        if constexpr (VEC) {
-                            red_add_v2(e, acc[k][0], acc[k][FC - 1]);
+                    for (int k = 0; k < K; ++k) {
+                        const int32_t gk = g0 + k;
+                        if (gk < 0 || gk > N) continue;
+                        if (tiled) {
+                            const int32_t e = (gk - lo[0]) + ext[0] * ((g1 - lo[1]) + ext[1] * (g2 - lo[2]));
+#pragma unroll
+                            for (int f = 0; f < FC; ++f) atomicAdd(tile + e * F + f0 + f, acc[j][k][f]);
                         } else {
+                            float* e = gbase + rbf_row<D>(lv, tm, gk, g1, g2) * rs + f0;
+                            if constexpr (VEC) {
+                                red_add_v2(e, acc[j][k][0], acc[j][k][FC - 1]);
+                            } else {
 #pragma unroll
-                            for (int f = 0; f < FC; ++f) red_add_f32(e + f, acc[k][f]);
+                                for (int f = 0; f < FC; ++f) red_add_f32(e + f, acc[j][k][f]);
+                            }
                         }
                     }
                 }
@@ -856,7 +670,7 @@ __global__ void __launch_bounds__(kCellBlock, kCellCtas) rbf_bwd_cells_kernel(co
         const int32_t g0 = lo[0] + r % ext[0];
         const int32_t g1 = lo[1] + (r / ext[0]) % ext[1];
         const int32_t g2 = lo[2] + r / (ext[0] * ext[1]);
-        float* e = gbase + rbf_row<3>(lv, tm, g0, g1, g2) * rs;
+        float* e = gbase + rbf_row<D>(lv, tm, g0, g1, g2) * rs;
         const float* a = tile + r * F;
         for (int f0 = 0; f0 < F; f0 += FC) {
             bool any = false;
@@ -892,21 +706,12 @@ cudaError_t pick_fwd(const FwdParams& p, int fc, cudaStream_t s) {
 template <int D, int R, int FC, bool VEC>
 cudaError_t launch_bwd(const BwdParams& p, cudaStream_t s) {
     if (p.c.nlvl == 0) return cudaSuccess;
-    if constexpr (D == 3) {
-        constexpr int kSmem = cell_smem_bytes<2 * R, FC>();
-        cudaError_t e = cudaFuncSetAttribute(rbf_bwd_cells_kernel<R, FC, VEC>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e != cudaSuccess) return e;
-        dim3 grid(static_cast<unsigned>((p.c.n + kCellBlock - 1) / kCellBlock), static_cast<unsigned>(p.c.nlvl));
-        rbf_bwd_cells_kernel<R, FC, VEC><<<grid, kCellBlock, kSmem, s>>>(p);
-        return cudaGetLastError();
-    }
-    constexpr int kSmem = kTileFloats * static_cast<int>(sizeof(float));
-    cudaError_t e = cudaFuncSetAttribute(rbf_bwd_tile_kernel<D, R, FC, VEC>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    constexpr int kSmem = cell_smem_bytes<D, 2 * R, FC>();
+    cudaError_t e = cudaFuncSetAttribute(rbf_bwd_cells_kernel<D, R, FC, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmem);
     if (e != cudaSuccess) return e;
-    dim3 grid(static_cast<unsigned>((p.c.n + kTileBlock - 1) / kTileBlock), static_cast<unsigned>(p.c.nlvl));
-    rbf_bwd_tile_kernel<D, R, FC, VEC><<<grid, kTileBlock, kSmem, s>>>(p);
+    dim3 grid(static_cast<unsigned>((p.c.n + kCellBlock - 1) / kCellBlock), static_cast<unsigned>(p.c.nlvl));
+    rbf_bwd_cells_kernel<D, R, FC, VEC><<<grid, kCellBlock, kSmem, s>>>(p);
     return cudaGetLastError();
 }
 
