@@ -487,8 +487,6 @@ hg_status siren_plan(const hg_siren_desc* desc, int64_t n, hg::SirenParams& p) {
     p.tp = desc->H / 16;
     p.nbuf = 1;
     p.pts = 256 / p.tp;
-    const int nb = (desc->H / 4) * (desc->K / 4);
-    p.groups = nb >= 256 ? 1 : 256 / nb;
     p.n = n;
     p.omega = desc->omega;
     return HG_OK;
@@ -955,6 +953,7 @@ hg_status hg_siren_bwd(const hg_siren_desc* desc, int64_t n, const float* gamma,
     p.gb1 = gb1;
     p.gW2 = gW2;
     p.gb2 = gb2;
+    hg::siren_bwd_tiles(p);
     if ((st = siren_grid(p, true, ctas)) != HG_OK) return st;
     return launch_status(hg::launch_siren_bwd(p, ctas, stream), "SIREN backward");
 }

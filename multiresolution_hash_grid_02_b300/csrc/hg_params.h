@@ -120,9 +120,8 @@ int launch_replay(const ReplayParams& p, bool red, void* stream);
 // 1..d = d gamma / d x_i, d + 1 = lap gamma (each feature-major, [K][n]).
 struct SirenParams {
     int32_t d, K, H, O;
-    int32_t tp;          // threads per point (H / 16; each owns 16 hidden units)
-    int32_t pts;         // points per tile (256 / tp)
-    int32_t groups;      // splits of the first-layer weight-gradient reduction over a tile
+    int32_t tp;          // threads per point (forward H / 16, backward H / 8: 16 or 8 hidden units each)
+    int32_t pts;         // points per tile (CTA threads / tp)
     int32_t nbuf;        // input tile buffers: 2 = the next tile loads while this one computes
     int64_t n;
     float omega;
@@ -137,6 +136,8 @@ struct SirenParams {
     float *gW1, *gb1, *gW2, *gb2;
 };
 // Dynamic shared memory of one CTA, and the launch (persistent CTAs, at most `ctas`).
+// siren_bwd_tiles sets the backward's tp and pts (its CTAs are twice the forward's).
+void siren_bwd_tiles(SirenParams& p);
 size_t siren_smem_bytes(const SirenParams& p, bool bwd);
 int launch_siren_fwd(const SirenParams& p, int ctas, void* stream);
 int launch_siren_bwd(const SirenParams& p, int ctas, void* stream);

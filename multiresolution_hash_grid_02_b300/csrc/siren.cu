@@ -15,7 +15,7 @@
 // for tf32 or bf16 tensor cores.  A CTA of 256 threads takes a tile of `pts`
 // points staged in shared memory; tp = H / 16 threads share a point, each
 // owning 16 hidden units, so every weight read from shared memory feeds d + 2
-// FMAs.  CTAs are persistent (one wave): the weights are staged once per CTA
+// FMAs (the backward: 512 threads of 8 units).  CTAs are persistent (one wave): the weights are staged once per CTA
 // and the weight gradients are added to global memory once per CTA.
 #include <cuda_runtime.h>
 
@@ -33,7 +33,7 @@ constexpr int kMaxO = 4;
 
 // Shared-memory layout of a CTA, in floats; every region starts on 16 bytes.
 struct SirenSmem {
-    int w1t, b1, w2, b2, x, w1, g, gw1, gw2, gb1, gb2, total;
+    int w1t, b1, w2, b2, x, w1, g, gw2, gb1, gb2, total;
 };
 
 __host__ __device__ inline int take(int& at, int n) {
@@ -53,28 +53,28 @@ __host__ __device__ inline SirenSmem siren_layout(const SirenParams& p, bool bwd
     m.x = take(at, p.nbuf * R * p.pts * (p.K + 4));  // inputs [nbuf][R][pts][K + 4] (padding: no bank conflicts)
     if (bwd) {
         m.w1 = take(at, p.H * p.K);          // W1 as given, [H][K]: the input gradients
-        m.g = take(at, R * p.pts * (p.H + 4));  // pre-activation gradients [R][pts][H + 4]
-        m.gw1 = take(at, p.groups * p.H * p.K);
+        // pre-activation gradients [R][pts][H + 4]; after the last tile the CTA's W1 gradient [H][K]
+        m.g = take(at, max(R * p.pts * (p.H + 4), p.H * p.K));
         m.gw2 = take(at, p.O * p.H);
         m.gb1 = take(at, p.H);
         m.gb2 = take(at, p.O);
     } else {
-        m.w1 = m.g = m.gw1 = m.gw2 = m.gb1 = m.gb2 = -1;
+        m.w1 = m.g = m.gw2 = m.gb1 = m.gb2 = -1;
     }
     m.total = at;
     return m;
 }
 
 // Weights into shared memory (W1 transposed for the forward contraction).
-__device__ void stage_weights(const SirenParams& p, const SirenSmem& L, float* sm, bool bwd) {
-    for (int i = threadIdx.x; i < p.H * p.K; i += kThreads) {
+__device__ void stage_weights(const SirenParams& p, const SirenSmem& L, float* sm, bool bwd, int nt = kThreads) {
+    for (int i = threadIdx.x; i < p.H * p.K; i += nt) {
         const float w = __ldg(p.W1 + i);
         sm[L.w1t + (i % p.K) * p.H + i / p.K] = w;
         if (bwd) sm[L.w1 + i] = w;
     }
-    for (int i = threadIdx.x; i < p.H; i += kThreads) sm[L.b1 + i] = __ldg(p.b1 + i);
-    for (int i = threadIdx.x; i < p.O * p.H; i += kThreads) sm[L.w2 + i] = __ldg(p.W2 + i);
-    for (int i = threadIdx.x; i < p.O; i += kThreads) sm[L.b2 + i] = p.b2 ? __ldg(p.b2 + i) : 0.f;
+    for (int i = threadIdx.x; i < p.H; i += nt) sm[L.b1 + i] = __ldg(p.b1 + i);
+    for (int i = threadIdx.x; i < p.O * p.H; i += nt) sm[L.w2 + i] = __ldg(p.W2 + i);
+    for (int i = threadIdx.x; i < p.O; i += nt) sm[L.b2 + i] = p.b2 ? __ldg(p.b2 + i) : 0.f;
 }
 
 __device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid) {
@@ -91,10 +91,10 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // points past n and NULL rows are zero-filled.  A thread takes four
 // consecutive features of one point (lanes: consecutive points, so the reads
 // are coalesced).
-__device__ void issue_tile(const SirenParams& p, float* X, int64_t n0, int R) {
+__device__ void issue_tile(const SirenParams& p, float* X, int64_t n0, int R, int nt = kThreads) {
     const int P = p.pts, K4 = p.K / 4;
     const int total = R * K4 * P;
-    for (int i = threadIdx.x; i < total; i += kThreads) {
+    for (int i = threadIdx.x; i < total; i += nt) {
         const int pp = i & (P - 1), rk = i / P;  // P is a power of two
         const int k = 4 * (rk % K4), r = rk / K4;
         const int64_t n = n0 + pp;
@@ -120,14 +120,14 @@ __device__ __forceinline__ float lane4(const float4& v, int i) {
 // acc[r][jj] = sum_k W1[unit_of(q, tp, jj)][k] X[r][pl][k], k ascending.  The
 // contraction runs on f32x2 pairs of units (two round-to-nearest FMAs per
 // instruction, the same sums), which halves the issued FMA instructions.
-template <int R>
+template <int R, int U = kUnits>
 __device__ __forceinline__ void first_layer(const float* W1T, const float* X, int K, int H, int P, int pl, int q,
-                                            int tp, float (&acc)[R][kUnits]) {
-    uint64_t a2[R][kUnits / 2];
+                                            int tp, float (&acc)[R][U]) {
+    uint64_t a2[R][U / 2];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int e = 0; e < kUnits / 2; ++e) a2[r][e] = 0;
+        for (int e = 0; e < U / 2; ++e) a2[r][e] = 0;
     const int ld = K + 4;
     const float* xp = X + pl * ld;
     for (int k = 0; k < K; k += 4) {
@@ -137,9 +137,9 @@ __device__ __forceinline__ void first_layer(const float* W1T, const float* X, in
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const float* wrow = W1T + (k + kk) * H + 4 * q;
-            uint64_t w[kUnits / 2];
+            uint64_t w[U / 2];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
+            for (int v = 0; v < U / 4; ++v) {
                 const float4 wq = *reinterpret_cast<const float4*>(wrow + 4 * tp * v);
                 w[2 * v] = f2_pack(wq.x, wq.y);
                 w[2 * v + 1] = f2_pack(wq.z, wq.w);
@@ -148,14 +148,14 @@ __device__ __forceinline__ void first_layer(const float* W1T, const float* X, in
             for (int r = 0; r < R; ++r) {
                 const uint64_t xv = f2_dup(lane4(xr[r], kk));
 #pragma unroll
-                for (int e = 0; e < kUnits / 2; ++e) a2[r][e] = f2_fma(w[e], xv, a2[r][e]);
+                for (int e = 0; e < U / 2; ++e) a2[r][e] = f2_fma(w[e], xv, a2[r][e]);
             }
         }
     }
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int e = 0; e < kUnits / 2; ++e) f2_unpack(a2[r][e], acc[r][2 * e], acc[r][2 * e + 1]);
+        for (int e = 0; e < U / 2; ++e) f2_unpack(a2[r][e], acc[r][2 * e], acc[r][2 * e + 1]);
 }
 
 // The forward of one staged tile X ([R][pts][K + 4]) for the thread's point
@@ -550,29 +550,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) siren_fwd_tc_kernel(const __gri
 }
 
 // Backward.  Per tile: (1) recompute the first layer, form the pre-activation
-// gradients g_z = d/dz, g_y_i = d/dy_i, g_s = d/ds of the thread's 16 units
-// into shared memory ([R][pts][H + 4]; rows z, y_1 .. y_d, s), and sum the
+// gradients g_z = d/dz, g_y_i = d/dy_i, g_s = d/ds of the thread's units into
+// shared memory ([R][pts][H + 4]; rows z, y_1 .. y_d, s), and sum the
 // output-layer and bias gradients over the warp's points; (2) input gradients
-// g_in[r][k] = sum_j W1[j][k] G[r][j] per point; (3) first-layer weight
-// gradient gW1[j][k] += sum_{r, point} G[r][j] X[r][k], each 4 x 4 block of it
-// owned by one thread of each of `groups` splits of the tile's rows.
+// g_in[r][k] = sum_j W1[j][k] G[r][j] per point, four features per thread at
+// a time; (3) first-layer weight gradient gW1[j][k] += sum_{r, point}
+// G[r][j] X[r][k]: each 4 x 4 block of it is owned by `groups` threads, each
+// summing a share of the tile's R * pts rows into registers that persist
+// across the CTA's tiles, and the blocks are summed in shared memory and
+// added to global memory once per CTA.
+// 512 threads, 8 hidden units each (tp = H / 8): 16 warps per SM at one CTA
+// per SM (the tiles' shared memory allows one) against 8 with 256 threads of
+// 16 units, whose 231 registers also allowed no more.
+constexpr int kBwdThreads = 512;
+constexpr int kBwdUnits = 8;
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_constant__ SirenParams p) {
-    constexpr int R = D + 2;
+__global__ void __launch_bounds__(kBwdThreads, 1) siren_bwd_kernel(const __grid_constant__ SirenParams p) {
+    constexpr int R = D + 2, U = kBwdUnits, NT = kBwdThreads;
     extern __shared__ float4 smem4[];
     float* sm = reinterpret_cast<float*>(smem4);
     const SirenSmem L = siren_layout(p, true);
-    stage_weights(p, L, sm, true);
-    for (int i = threadIdx.x; i < p.groups * p.H * p.K; i += kThreads) sm[L.gw1 + i] = 0.f;
-    for (int i = threadIdx.x; i < p.O * p.H; i += kThreads) sm[L.gw2 + i] = 0.f;
-    for (int i = threadIdx.x; i < p.H; i += kThreads) sm[L.gb1 + i] = 0.f;
-    for (int i = threadIdx.x; i < p.O; i += kThreads) sm[L.gb2 + i] = 0.f;
+    stage_weights(p, L, sm, true, NT);
+    for (int i = threadIdx.x; i < p.O * p.H; i += NT) sm[L.gw2 + i] = 0.f;
+    for (int i = threadIdx.x; i < p.H; i += NT) sm[L.gb1 + i] = 0.f;
+    for (int i = threadIdx.x; i < p.O; i += NT) sm[L.gb2 + i] = 0.f;
     const float* W1T = sm + L.w1t;
     const float* W1 = sm + L.w1;
     const float* b1 = sm + L.b1;
     const float* W2 = sm + L.w2;
     float* G = sm + L.g;
-    float* gW1s = sm + L.gw1;
     float* gW2s = sm + L.gw2;
     float* gb1s = sm + L.gb1;
     float* gb2s = sm + L.gb2;
@@ -585,20 +592,22 @@ __global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_con
     bool want_in = false;
 #pragma unroll
     for (int r = 0; r < R; ++r) want_in = want_in || p.g_in[r];
-    // first-layer weight-gradient ownership: 4 x 4 blocks; `groups` threads share a block, each
-    // summing a contiguous share of the tile's R * pts rows
-    const int nb = (H / 4) * (K / 4);
-    const int grp = nb >= kThreads ? 0 : threadIdx.x / nb;
-    const int rows = R * P, share = (rows + p.groups - 1) / p.groups;
+    // first-layer weight-gradient ownership: block b (4 units x 4 features), group grp of `groups`
+    const int nb = (H / 4) * (K / 4), groups = NT / nb;  // nb <= 512 (H <= 128, K <= 64)
+    const int grp = threadIdx.x / nb, b = threadIdx.x % nb;
+    const bool owner = p.gW1 && grp < groups;
+    const int bj = 4 * (b / (K / 4)), bk = 4 * (b % (K / 4));
+    const int rows = R * P, share = (rows + groups - 1) / groups;
     const int m0 = grp * share, m1 = min(rows, m0 + share);
+    uint64_t a3[4][2] = {};  // the block's sums, f32x2 pairs over k
     const int64_t tiles = (p.n + P - 1) / P;
     int cur = 0;
-    if (static_cast<int64_t>(blockIdx.x) < tiles) issue_tile(p, Xb[0], static_cast<int64_t>(blockIdx.x) * P, R);
+    if (static_cast<int64_t>(blockIdx.x) < tiles) issue_tile(p, Xb[0], static_cast<int64_t>(blockIdx.x) * P, R, NT);
     cp_async_commit();
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const int64_t tn = t + gridDim.x;
         if (p.nbuf == 2) {  // the next tile's copy flies while this one computes
-            if (tn < tiles) issue_tile(p, Xb[cur ^ 1], tn * P, R);
+            if (tn < tiles) issue_tile(p, Xb[cur ^ 1], tn * P, R, NT);
             cp_async_commit();
         }
         const float* X = Xb[cur];
@@ -622,11 +631,11 @@ __global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_con
         __syncthreads();  // this tile (and the weights) visible to every thread
         // (1) pre-activation gradients
         {
-            float acc[R][kUnits];
-            first_layer<R>(W1T, X, K, H, P, pl, q, tp, acc);
+            float acc[R][U];
+            first_layer<R, U>(W1T, X, K, H, P, pl, q, tp, acc);
             float* Gp = G + pl * gld;
 #pragma unroll
-            for (int jj = 0; jj < kUnits; ++jj) {
+            for (int jj = 0; jj < U; ++jj) {
                 const int j = unit_of(q, tp, jj);
                 float a, c;
                 sincosf(om * (acc[0][jj] + b1[j]), &a, &c);
@@ -636,21 +645,21 @@ __global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_con
                 for (int i = 0; i < D; ++i) y2 = fmaf(acc[1 + i][jj], acc[1 + i][jj], y2);
                 const float s = acc[R - 1][jj];
                 // adjoints of a, omega c y_i and the Laplacian's bracket through W2
-                float U = 0.f, Pl = 0.f, Dv[D];
+                float Uo = 0.f, Pl = 0.f, Dv[D];
 #pragma unroll
                 for (int i = 0; i < D; ++i) Dv[i] = 0.f;
 #pragma unroll
                 for (int o = 0; o < kMaxO; ++o) {
                     if (o < O) {
                         const float w2 = W2[o * H + j];
-                        U = fmaf(w2, gu[o], U);
+                        Uo = fmaf(w2, gu[o], Uo);
                         Pl = fmaf(w2, glu[o], Pl);
 #pragma unroll
                         for (int i = 0; i < D; ++i) Dv[i] = fmaf(w2, gdu[i][o], Dv[i]);
                     }
                 }
-                const float ga = fmaf(-om2 * Pl, y2, U);  // d/da
-                float gc = Pl * s;                         // d/dc, over omega
+                const float ga = fmaf(-om2 * Pl, y2, Uo);  // d/da
+                float gc = Pl * s;                          // d/dc, over omega
 #pragma unroll
                 for (int i = 0; i < D; ++i) gc = fmaf(Dv[i], acc[1 + i][jj], gc);
                 gc *= om;
@@ -691,101 +700,89 @@ __global__ void __launch_bounds__(kThreads, 1) siren_bwd_kernel(const __grid_con
             }
         }
         __syncthreads();
-        // (2) input gradients of the thread's point, 8 features at a time
+        // (2) input gradients of the thread's point, 4 features at a time
         if (want_in) {
-            for (int kc = 8 * q; kc < K; kc += 8 * tp) {
-                uint64_t a2[R][4];  // f32x2 pairs of features
+            for (int kc = 4 * q; kc < K; kc += 4 * tp) {
+                uint64_t a2[R][2];  // f32x2 pairs of features
 #pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) a2[r][e] = 0;
+                for (int r = 0; r < R; ++r) a2[r][0] = a2[r][1] = 0;
                 for (int j = 0; j < H; j += 4) {
                     float4 g4[R];
 #pragma unroll
                     for (int r = 0; r < R; ++r) g4[r] = *reinterpret_cast<const float4*>(G + (r * P + pl) * gld + j);
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
-                        const float4* wv = reinterpret_cast<const float4*>(W1 + (j + jj) * K + kc);
-                        const float4 wa = wv[0], wb = wv[1];
-                        const uint64_t w[4] = {f2_pack(wa.x, wa.y), f2_pack(wa.z, wa.w), f2_pack(wb.x, wb.y),
-                                               f2_pack(wb.z, wb.w)};
+                        const float4 wa = *reinterpret_cast<const float4*>(W1 + (j + jj) * K + kc);
+                        const uint64_t w0 = f2_pack(wa.x, wa.y), w1 = f2_pack(wa.z, wa.w);
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const uint64_t gv = f2_dup(lane4(g4[r], jj));
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) a2[r][e] = f2_fma(gv, w[e], a2[r][e]);
+                            a2[r][0] = f2_fma(gv, w0, a2[r][0]);
+                            a2[r][1] = f2_fma(gv, w1, a2[r][1]);
                         }
                     }
                 }
-                float acc2[R][8];
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) f2_unpack(a2[r][e], acc2[r][2 * e], acc2[r][2 * e + 1]);
                 if (have) {
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         if (p.g_in[r]) {
+                            float v[4];
+                            f2_unpack(a2[r][0], v[0], v[1]);
+                            f2_unpack(a2[r][1], v[2], v[3]);
 #pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) __stcs(p.g_in[r] + (kc + kk) * p.n + n, acc2[r][kk]);
+                            for (int kk = 0; kk < 4; ++kk) __stcs(p.g_in[r] + (kc + kk) * p.n + n, v[kk]);
                         }
                     }
                 }
             }
         }
-        // (3) first-layer weight gradient
-        if (p.gW1 && grp < p.groups) {
-            for (int b = nb >= kThreads ? threadIdx.x : threadIdx.x % nb; b < nb; b += kThreads) {
-                const int j = 4 * (b / (K / 4)), k = 4 * (b % (K / 4));
-                uint64_t a3[4][2] = {};  // f32x2 pairs over k
-                for (int m = m0; m < m1; ++m) {
-                    const float4 g4 = *reinterpret_cast<const float4*>(G + m * gld + j);
-                    const float4 x4 = *reinterpret_cast<const float4*>(X + m * xld + k);
-                    const uint64_t x01 = f2_pack(x4.x, x4.y), x23 = f2_pack(x4.z, x4.w);
-#pragma unroll
-                    for (int aa = 0; aa < 4; ++aa) {
-                        const uint64_t gv = f2_dup(lane4(g4, aa));
-                        a3[aa][0] = f2_fma(gv, x01, a3[aa][0]);
-                        a3[aa][1] = f2_fma(gv, x23, a3[aa][1]);
-                    }
-                }
-                float acc3[4][4];
+        // (3) first-layer weight gradient: this thread's block over its share of the tile's rows
+        if (owner) {
+            for (int m = m0; m < m1; ++m) {
+                const float4 g4 = *reinterpret_cast<const float4*>(G + m * gld + bj);
+                const float4 x4 = *reinterpret_cast<const float4*>(X + m * xld + bk);
+                const uint64_t x01 = f2_pack(x4.x, x4.y), x23 = f2_pack(x4.z, x4.w);
 #pragma unroll
                 for (int aa = 0; aa < 4; ++aa) {
-                    f2_unpack(a3[aa][0], acc3[aa][0], acc3[aa][1]);
-                    f2_unpack(a3[aa][1], acc3[aa][2], acc3[aa][3]);
+                    const uint64_t gv = f2_dup(lane4(g4, aa));
+                    a3[aa][0] = f2_fma(gv, x01, a3[aa][0]);
+                    a3[aa][1] = f2_fma(gv, x23, a3[aa][1]);
                 }
-                float* dst = gW1s + (grp * H + j) * K + k;
-#pragma unroll
-                for (int aa = 0; aa < 4; ++aa)
-#pragma unroll
-                    for (int bb = 0; bb < 4; ++bb) dst[aa * K + bb] += acc3[aa][bb];
-                if (nb < kThreads) break;  // one block per thread of a group
             }
         }
         __syncthreads();  // this tile's X and G read by every thread
         if (p.nbuf == 1 && tn < tiles) {
-            issue_tile(p, Xb[0], tn * P, R);
+            issue_tile(p, Xb[0], tn * P, R, NT);
             cp_async_commit();
         }
         cur ^= p.nbuf - 1;
     }
     cp_async_wait<0>();
     __syncthreads();
-    // the CTA's weight gradients, added once
+    // the CTA's weight gradients, added once; the groups' blocks are summed in the (now free) G region
     if (p.gW1) {
-        for (int e = threadIdx.x; e < H * K; e += kThreads) {
-            float v = 0.f;
-            for (int g = 0; g < p.groups; ++g) v += gW1s[g * H * K + e];
-            atomicAdd(p.gW1 + e, v);
+        float* gW1s = G;  // [H][K]
+        for (int e = threadIdx.x; e < H * K; e += NT) gW1s[e] = 0.f;
+        __syncthreads();
+        if (owner) {
+#pragma unroll
+            for (int aa = 0; aa < 4; ++aa) {
+                float v[4];
+                f2_unpack(a3[aa][0], v[0], v[1]);
+                f2_unpack(a3[aa][1], v[2], v[3]);
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) atomicAdd(gW1s + (bj + aa) * K + bk + bb, v[bb]);
+            }
         }
+        __syncthreads();
+        for (int e = threadIdx.x; e < H * K; e += NT) atomicAdd(p.gW1 + e, gW1s[e]);
     }
     if (p.gW2)
-        for (int e = threadIdx.x; e < O * H; e += kThreads) atomicAdd(p.gW2 + e, gW2s[e]);
+        for (int e = threadIdx.x; e < O * H; e += NT) atomicAdd(p.gW2 + e, gW2s[e]);
     if (p.gb1)
-        for (int e = threadIdx.x; e < H; e += kThreads) atomicAdd(p.gb1 + e, gb1s[e]);
+        for (int e = threadIdx.x; e < H; e += NT) atomicAdd(p.gb1 + e, gb1s[e]);
     if (p.gb2)
-        for (int e = threadIdx.x; e < O; e += kThreads) atomicAdd(p.gb2 + e, gb2s[e]);
+        for (int e = threadIdx.x; e < O; e += NT) atomicAdd(p.gb2 + e, gb2s[e]);
 }
 
 template <int D>
@@ -800,7 +797,7 @@ template <int D>
 cudaError_t occupancy(bool bwd, size_t bytes, int* blocks) {
     cudaError_t e = set_smem<D>(bwd, bytes);
     if (e != cudaSuccess) return e;
-    return bwd ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, siren_bwd_kernel<D>, kThreads, bytes)
+    return bwd ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, siren_bwd_kernel<D>, kBwdThreads, bytes)
                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, siren_fwd_kernel<D>, kThreads, bytes);
 }
 
@@ -810,7 +807,7 @@ cudaError_t launch(const SirenParams& p, bool bwd, int ctas, cudaStream_t s) {
     cudaError_t e = set_smem<D>(bwd, bytes);
     if (e != cudaSuccess) return e;
     if (bwd)
-        siren_bwd_kernel<D><<<ctas, kThreads, bytes, s>>>(p);
+        siren_bwd_kernel<D><<<ctas, kBwdThreads, bytes, s>>>(p);
     else
         siren_fwd_kernel<D><<<ctas, kThreads, bytes, s>>>(p);
     return cudaGetLastError();
@@ -826,6 +823,11 @@ cudaError_t dispatch(const SirenParams& p, bool bwd, int ctas, cudaStream_t s) {
 }
 
 }  // namespace
+
+void siren_bwd_tiles(SirenParams& p) {
+    p.tp = p.H / kBwdUnits;
+    p.pts = kBwdThreads / p.tp;
+}
 
 size_t siren_smem_bytes(const SirenParams& p, bool bwd) {
     return static_cast<size_t>(siren_layout(p, bwd).total) * sizeof(float);
