@@ -91,17 +91,22 @@ def parse_args():
 # DRAM traffic recorded from an ncu capture, valid while the kernels are unchanged
 # ---------------------------------------------------------------------------
 
+# Sources of kernels whose DRAM traffic is not recorded: the roofline probes, the SIREN consumer and
+# the other encodings (d-linear, INGP-FD, Gaussian-RBF) -- a change there leaves the Hermite kernels'
+# recorded traffic valid.
+UNRECORDED_SOURCES = ("probes.cu", "hg_probe.h", "siren.cu", "siren_tc.cuh", "linear.cu", "linear_fd.cu", "rbf.cu")
+
+
 def kernel_source_hash() -> str:
-    """sha256 over the sources of the encoding kernels and the headers they
-    include (the roofline probes' and the SIREN consumer's sources are left
-    out: they do not change the encoding kernels' traffic)."""
+    """sha256 over the sources of the Hermite encoding kernels, their launch
+    code and the headers they include (UNRECORDED_SOURCES left out)."""
     import glob
     import hashlib
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "multiresolution_hash_grid_02_b300", "csrc")
     files = sorted(f for f in glob.glob(os.path.join(pkg, "*.cu")) + glob.glob(os.path.join(pkg, "*.cuh")) +
                    glob.glob(os.path.join(pkg, "*.h")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
-                   if os.path.basename(f) not in ("probes.cu", "hg_probe.h", "siren.cu"))
+                   if os.path.basename(f) not in UNRECORDED_SOURCES)
     for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
