@@ -39,6 +39,38 @@ __device__ __forceinline__ void blend2(const float (&q)[4][4], const Basis1& b0,
         }
 }
 
+// blend2 for both features at once: q[corner][alpha] holds the (feature 0,
+// feature 1) coefficient pairs, o[] accumulates (gamma, d/dx0, d/dx1, lap)
+// pairs.  Each f32x2 operation is the scalar blend2's operation on both
+// features (the same order, the same roundings), so the results are
+// bit-identical to blend2's, with half the FMA instructions.
+__device__ __forceinline__ void blend2_f2(const uint64_t (&q)[4][4], const Basis1& b0, const Basis1& b1,
+                                          uint64_t (&o)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = 0ull;  // (+0.0f, +0.0f)
+#pragma unroll
+    for (int v1 = 0; v1 < 2; ++v1)
+#pragma unroll
+        for (int a1 = 0; a1 < 2; ++a1) {
+            uint64_t s = 0ull, s1 = 0ull, s2 = 0ull;
+#pragma unroll
+            for (int v0 = 0; v0 < 2; ++v0)
+#pragma unroll
+                for (int a0 = 0; a0 < 2; ++a0) {
+                    const uint64_t c = q[v0 + 2 * v1][a0 + 2 * a1];
+                    s = f2_fma(c, f2_dup(b0.w[v0][a0]), s);
+                    s1 = f2_fma(c, f2_dup(b0.d1[v0][a0]), s1);
+                    s2 = f2_fma(c, f2_dup(b0.d2[v0][a0]), s2);
+                }
+            const uint64_t w = f2_dup(b1.w[v1][a1]);
+            o[0] = f2_fma(s, w, o[0]);
+            o[1] = f2_fma(s1, w, o[1]);
+            o[2] = f2_fma(s, f2_dup(b1.d1[v1][a1]), o[2]);
+            o[3] = f2_fma(s2, w, o[3]);
+            o[3] = f2_fma(s, f2_dup(b1.d2[v1][a1]), o[3]);
+        }
+}
+
 // Separable 3D blend of one feature.
 __device__ __forceinline__ void blend3(const float (&q)[8][8], const Basis1& b0, const Basis1& b1,
                                        const Basis1& b2, float& g, float (&dg)[3], float& lap) {
@@ -79,8 +111,9 @@ __device__ __forceinline__ void blend3(const float (&q)[8][8], const Basis1& b0,
 
 // One (point n, level l) of a packed [L][T][2^d][F] table with F = 2, on
 // one thread: the 2^d corner rows read whole (vector loads), then the
-// separable blend of each feature -- the arithmetic of the generic forward's
-// packed path, so the results are bit-identical to it.  g[f], dg[f][j] and
+// separable blend of each feature (2D: both features at once, blend2_f2) --
+// the arithmetic of the generic forward's packed path, so the results are
+// bit-identical to it.  g[f], dg[f][j] and
 // lap[f]: gamma, d gamma / d x_j and the Laplacian of feature f.
 template <int D, typename TT>
 __device__ __forceinline__ void encode_item_f2(const FwdParams& p, int64_t n, int l, float (&g)[2],
@@ -106,16 +139,28 @@ __device__ __forceinline__ void encode_item_f2(const FwdParams& p, int64_t n, in
         const uint32_t id = vertex_index<D>(gv, lv, lv.dense & 1u, p.c.tmask[0]);
         load_row<ROW>(base + static_cast<int64_t>(id) * p.tab.rs[0], rows[v]);
     }
-#pragma unroll
-    for (int f = 0; f < FC; ++f) {
-        float q[V][V];
+    if constexpr (D == 2) {
+        uint64_t q[V][V], o[4];
 #pragma unroll
         for (int v = 0; v < V; ++v)
 #pragma unroll
-            for (int a = 0; a < V; ++a) q[v][a] = row_elem<TT, ROW>(rows[v], packed_slot<D>(a) * FC + f);
-        if constexpr (D == 2) {
-            blend2(q, B[0], B[1], g[f], dg[f], lap[f]);
-        } else {
+            for (int a = 0; a < V; ++a)
+                q[v][a] = f2_pack(row_elem<TT, ROW>(rows[v], packed_slot<D>(a) * FC),
+                                  row_elem<TT, ROW>(rows[v], packed_slot<D>(a) * FC + 1));
+        blend2_f2(q, B[0], B[1], o);
+        f2_unpack(o[0], g[0], g[1]);
+        f2_unpack(o[1], dg[0][0], dg[1][0]);
+        f2_unpack(o[2], dg[0][1], dg[1][1]);
+        f2_unpack(o[3], lap[0], lap[1]);
+        dg[0][2] = dg[1][2] = 0.f;
+    } else {
+#pragma unroll
+        for (int f = 0; f < FC; ++f) {
+            float q[V][V];
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+#pragma unroll
+                for (int a = 0; a < V; ++a) q[v][a] = row_elem<TT, ROW>(rows[v], packed_slot<D>(a) * FC + f);
             blend3(q, B[0], B[1], B[2], g[f], dg[f], lap[f]);
         }
     }

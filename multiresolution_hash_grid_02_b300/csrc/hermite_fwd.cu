@@ -138,61 +138,95 @@ __global__ void __launch_bounds__(kBlock) hermite_fwd_kernel(const __grid_consta
         for (int k = 0; k < NK; ++k) idx[k][v] = vertex_index<D>(g, lv, (lv.dense >> k) & 1u, p.c.tmask[k]);
     }
 
-    for (int f0 = 0; f0 < F; f0 += FC) {
-        float q[FC][V][V];
+    if constexpr (D == 2 && VEC && FC == 2 && !HESS) {
+        // packed 2D rows, both features per f32x2 operation (blend2_f2: bit-identical to blend2)
+        float g[2] = {0.f, 0.f}, dg[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, lap[2] = {0.f, 0.f};
         if (active) {
-            if constexpr (VEC) {
-                constexpr int ROW = V * FC * static_cast<int>(sizeof(TT));
-                const TT* base = static_cast<const TT*>(p.tab.ptr[0]) + l * p.tab.ls[0];
-                RowRegs<ROW> rows[V];
+            constexpr int ROW = V * FC * static_cast<int>(sizeof(TT));
+            const TT* base = static_cast<const TT*>(p.tab.ptr[0]) + l * p.tab.ls[0];
+            RowRegs<ROW> rows[V];
 #pragma unroll
-                for (int v = 0; v < V; ++v) load_row<ROW>(base + static_cast<int64_t>(idx[0][v]) * p.tab.rs[0], rows[v]);
+            for (int v = 0; v < V; ++v) load_row<ROW>(base + static_cast<int64_t>(idx[0][v]) * p.tab.rs[0], rows[v]);
+            uint64_t q2[V][V], o[4];
 #pragma unroll
-                for (int v = 0; v < V; ++v)
+            for (int v = 0; v < V; ++v)
 #pragma unroll
-                    for (int a = 0; a < V; ++a)
-#pragma unroll
-                        for (int f = 0; f < FC; ++f) q[f][v][a] = row_elem<TT, ROW>(rows[v], packed_slot<D>(a) * FC + f);
-            } else {
-#pragma unroll
-                for (int v = 0; v < V; ++v)
-#pragma unroll
-                    for (int a = 0; a < V; ++a) {
-                        const int k = alpha_order(a);
-                        const TT* e = static_cast<const TT*>(p.tab.ptr[k]) + l * p.tab.ls[k] +
-                                      static_cast<int64_t>(idx[k][v]) * p.tab.rs[k] + bucket_slot<D>(a) * F + f0;
-#pragma unroll
-                        for (int f = 0; f < FC; ++f) q[f][v][a] = to_f32<TT>(e[f]);
-                    }
-            }
+                for (int a = 0; a < V; ++a)
+                    q2[v][a] = f2_pack(row_elem<TT, ROW>(rows[v], packed_slot<D>(a) * FC),
+                                       row_elem<TT, ROW>(rows[v], packed_slot<D>(a) * FC + 1));
+            blend2_f2(q2, B[0], B[1], o);
+            f2_unpack(o[0], g[0], g[1]);
+            f2_unpack(o[1], dg[0][0], dg[1][0]);
+            f2_unpack(o[2], dg[0][1], dg[1][1]);
+            f2_unpack(o[3], lap[0], lap[1]);
         }
 #pragma unroll
-        for (int f = 0; f < FC; ++f) {
-            float g = 0.f, dg[3] = {0.f, 0.f, 0.f}, lap = 0.f, h[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (active) {
-                if constexpr (HESS) {
-                    if constexpr (D == 2) {
-                        blend2h(q[f], B[0], B[1], g, dg, h);
-                    } else {
-                        blend3h(q[f], B[0], B[1], B[D - 1], g, dg, h);
-                    }
-                } else if constexpr (D == 2) {
-                    blend2(q[f], B[0], B[1], g, dg, lap);
-                } else {
-                    blend3(q[f], B[0], B[1], B[D - 1], g, dg, lap);
-                }
-            }
-            const int64_t lf = static_cast<int64_t>(l) * F + f0 + f;
-            __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, g);
+        for (int f = 0; f < 2; ++f) {
+            const int64_t lf = static_cast<int64_t>(l) * F + f;
+            __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, g[f]);
             if (p.dgamma) {
 #pragma unroll
-                for (int j = 0; j < D; ++j) __stcs(p.dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf, dg[j]);
+                for (int j = 0; j < D; ++j) __stcs(p.dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf, dg[f][j]);
             }
-            if constexpr (HESS) {
+            if (p.lap) __stcs(p.lap + n * p.c.sn + lf * p.c.sf, lap[f]);
+        }
+    } else {
+        for (int f0 = 0; f0 < F; f0 += FC) {
+            float q[FC][V][V];
+            if (active) {
+                if constexpr (VEC) {
+                    constexpr int ROW = V * FC * static_cast<int>(sizeof(TT));
+                    const TT* base = static_cast<const TT*>(p.tab.ptr[0]) + l * p.tab.ls[0];
+                    RowRegs<ROW> rows[V];
 #pragma unroll
-                for (int k = 0; k < P; ++k) __stcs(p.hess + n * p.c.hsn + k * p.c.hsq + lf * p.c.hsf, h[k]);
-            } else if (p.lap) {
-                __stcs(p.lap + n * p.c.sn + lf * p.c.sf, lap);
+                    for (int v = 0; v < V; ++v) load_row<ROW>(base + static_cast<int64_t>(idx[0][v]) * p.tab.rs[0], rows[v]);
+#pragma unroll
+                    for (int v = 0; v < V; ++v)
+#pragma unroll
+                        for (int a = 0; a < V; ++a)
+#pragma unroll
+                            for (int f = 0; f < FC; ++f) q[f][v][a] = row_elem<TT, ROW>(rows[v], packed_slot<D>(a) * FC + f);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < V; ++v)
+#pragma unroll
+                        for (int a = 0; a < V; ++a) {
+                            const int k = alpha_order(a);
+                            const TT* e = static_cast<const TT*>(p.tab.ptr[k]) + l * p.tab.ls[k] +
+                                          static_cast<int64_t>(idx[k][v]) * p.tab.rs[k] + bucket_slot<D>(a) * F + f0;
+#pragma unroll
+                            for (int f = 0; f < FC; ++f) q[f][v][a] = to_f32<TT>(e[f]);
+                        }
+                }
+            }
+#pragma unroll
+            for (int f = 0; f < FC; ++f) {
+                float g = 0.f, dg[3] = {0.f, 0.f, 0.f}, lap = 0.f, h[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (active) {
+                    if constexpr (HESS) {
+                        if constexpr (D == 2) {
+                            blend2h(q[f], B[0], B[1], g, dg, h);
+                        } else {
+                            blend3h(q[f], B[0], B[1], B[D - 1], g, dg, h);
+                        }
+                    } else if constexpr (D == 2) {
+                        blend2(q[f], B[0], B[1], g, dg, lap);
+                    } else {
+                        blend3(q[f], B[0], B[1], B[D - 1], g, dg, lap);
+                    }
+                }
+                const int64_t lf = static_cast<int64_t>(l) * F + f0 + f;
+                __stcs(p.gamma + n * p.c.sn + lf * p.c.sf, g);
+                if (p.dgamma) {
+#pragma unroll
+                    for (int j = 0; j < D; ++j) __stcs(p.dgamma + n * p.c.dsn + j * p.c.dsj + lf * p.c.dsf, dg[j]);
+                }
+                if constexpr (HESS) {
+#pragma unroll
+                    for (int k = 0; k < P; ++k) __stcs(p.hess + n * p.c.hsn + k * p.c.hsq + lf * p.c.hsf, h[k]);
+                } else if (p.lap) {
+                    __stcs(p.lap + n * p.c.sn + lf * p.c.sf, lap);
+                }
             }
         }
     }
