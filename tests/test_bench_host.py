@@ -141,6 +141,34 @@ def test_ncu_log_parser_and_traffic_staleness(tmp_path, monkeypatch):
     assert bench.traffic_key(bench_workload(4), None, True) == "3d_hermite+hessian"
 
 
+def test_traffic_hash_covers_the_hermite_sources_only(tmp_path, monkeypatch):
+    """The recorded DRAM traffic stays valid across edits of kernels whose
+    traffic is not recorded (the other encodings, the SIREN, the probes) and
+    is invalidated by an edit of the Hermite kernels or their shared headers."""
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = tmp_path / "multiresolution_hash_grid_02_b300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "include").mkdir()
+    names = ["hermite_fwd.cu", "hermite_bwd.cu", "hg_device.cuh", "hg_params.h", "hg_api.cu"] + \
+        list(bench.UNRECORDED_SOURCES)
+    for nm in names:
+        (csrc if nm != "hg_probe.h" else tmp_path / "include").joinpath(nm).write_text(nm)
+    (tmp_path / "include" / "hg.h").write_text("hg.h")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    for nm in bench.UNRECORDED_SOURCES:
+        f = (csrc if nm != "hg_probe.h" else tmp_path / "include") / nm
+        f.write_text(nm + " edited")
+        assert bench.kernel_source_hash() == h0, nm
+    for f in (csrc / "hermite_fwd.cu", csrc / "hg_params.h", tmp_path / "include" / "hg.h"):
+        old = f.read_text()
+        f.write_text(old + " edited")
+        assert bench.kernel_source_hash() != h0, f.name
+        f.write_text(old)
+    assert bench.kernel_source_hash() == h0
+
+
 def test_reference_arm_fd_line():
     """The reference arm runs the INGP-FD workload's oracle step."""
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "7",
