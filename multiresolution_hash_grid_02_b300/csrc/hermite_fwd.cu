@@ -469,9 +469,10 @@ __global__ void __launch_bounds__(kBlock, 2) hermite_fwd_pair3_kernel(const __gr
     uint32_t c[D];
     float t[D];
     Basis1 B[D];
+    const uint64_t keep = l2_evict_last_policy();  // the coordinates, re-read by every level's pass
 #pragma unroll
     for (int i = 0; i < D; ++i) {
-        locate(__ldg(p.coords + n * D + i), lv, c[i], t[i]);
+        locate(ldg_hint(p.coords + n * D + i, keep), lv, c[i], t[i]);
         B[i] = hermite_basis(t[i], lv);
     }
     // half-row h of corner v: 4 slots x (f0, f1) = four 64-bit pairs

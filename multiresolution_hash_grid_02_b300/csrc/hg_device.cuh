@@ -288,6 +288,28 @@ __device__ __forceinline__ void ld_nc_v4b64(const void* p, uint64_t (&r)[4]) {
     asm("ld.global.nc.v4.b64 {%0,%1,%2,%3}, [%4];" : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]) : "l"(p));
 }
 
+// L2 eviction priorities for read-only loads (createpolicy + L2::cache_hint).
+// Every level's pass re-reads the points' coordinates while its own stream
+// (a level's upstream gradients or outputs, its table) passes through the
+// L2: loaded evict-last, the coordinates stay resident from one pass to the
+// next instead of coming back from DRAM once per level; the upstream
+// gradients, read once, are loaded evict-first.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ float ldg_hint(const float* p, uint64_t pol) {
+    float v;
+    asm("ld.global.nc.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
+    return v;
+}
+
 }  // namespace hg
 
 namespace hg {
