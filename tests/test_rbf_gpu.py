@@ -6,8 +6,9 @@ Cases: d = 2 and 3; rings 1 to 4; kernel widths 0.5 to 2; dense (the page's
 grids) and hashed levels; fp32 and fp16 tables; F = 1, 2, 4; both layouts;
 masks; points at the grid's border (clipped neighbourhoods) and the edge
 coordinates; stratified (coherent) points in 2D and 3D (runs of same-cell
-points, tiles over several rows of strata); coarse levels with many points
-per vertex.  Tolerance 1e-5 of the oracle's
+points, tiles over several rows of strata) and the same points shuffled (runs
+of one point, tap boxes too large for a CTA's tile); coarse levels with many
+points per vertex.  Tolerance 1e-5 of the oracle's
 condition magnitude (every term of the quotient rule in absolute value)."""
 import zlib
 
@@ -46,6 +47,8 @@ CASES = [
     ("3d_F2_stratified", 3, 3, 2, 7, 28, 15, "f32", 1, 13824, None, 1.0, 3),
     ("3d_F1_stratified_hashed_point_major", 3, 2, 1, 5, 20, 12, "f32", 0, 8000, None, 0.8, 2),
     ("3d_F4_stratified_ring4", 3, 2, 4, 4, 12, 12, "f32", 1, 4096, None, 1.2, 4),
+    ("3d_F2_stratified_shuffled", 3, 3, 2, 7, 28, 15, "f32", 1, 13824, None, 1.0, 3),
+    ("2d_F2_stratified_shuffled", 2, 3, 2, 16, 64, 13, "f32", 1, 16384, None, 1.0, 3),
 ]
 
 
@@ -56,6 +59,8 @@ def _build(case, seed=0):
     rng = np.random.default_rng(zlib.crc32(cid.encode()) + seed)
     res = oracle.level_resolutions(L, nmin, nmax)
     x = _coords(rng, n, d, res, stratified="stratified" in cid)
+    if "shuffled" in cid:  # the same strata in a random order: runs of one point, boxes past the tile
+        x = np.ascontiguousarray(x[rng.permutation(n)])
     npdt = np.float16 if dt == "f16" else np.float32
     table = (rng.random((L, 1 << log2T, F), dtype=np.float32) * 2 - 1).astype(npdt)
     desc = m.GridDesc(d=d, L=L, F=F, n_min=nmin, n_max=nmax, log2_T=(log2T,), level_mask=mask,
